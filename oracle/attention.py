@@ -1,0 +1,137 @@
+"""Dense softmax decode-attention oracle (test infrastructure only; see ``oracle``).
+
+"Week 3 Day 3: Paged KV Cache" (tiny-llm), section "Correctness Checkpoint:
+Gather Pages for Dense Attention", keeps the pages as the source of truth,
+gathers a request's rows back into dense K/V in logical order and feeds them
+to the plain dense attention equation. The pages never print that equation,
+so this module takes the textbook scaled-dot-product form, computed in
+float64 on rows that are widened exactly from their stored type:
+
+    s_t = scale * <q_h, k_t>          for the gathered positions t
+    p   = softmax(s)                  (shifted by max(s) before exp)
+    out = sum_t p_t * v_t
+
+Which positions: "A Paged KV Cache and Sliding-Window Attention" (chapter
+15, section "The model") lets a step with context ``L`` and window ``W``
+attend the new token and at most ``W - 1`` earlier ones, i.e. positions
+``L - min(L, W) … L - 1``. With the new token stored before the attention
+runs, that is ``lo = max(0, L - W)`` up to ``L``; no window (``W`` absent or
+``<= 0``) means ``lo = 0``.
+
+Grouped-query heads: query head ``h`` reads KV head ``h // (Hq // Hkv)``
+(contiguous groups); the pages do not state a mapping, this is the plain one.
+
+Rows are read LITERALLY through the tables: a block table maps position
+``t`` to slot ``table[t // P] * P + t % P`` ("PagedAttention block
+allocator", section "Sequence block table"); a raw-location table maps it to
+``table[t]`` (mini-sglang code series, part 4). A negative entry is a
+released page and reading it is an error, never a mask.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+
+def window_lo(L: int, W) -> int:
+    """First position a step with context ``L`` attends under window ``W``."""
+    if W is None or W <= 0:
+        return 0
+    return max(0, L - W)
+
+
+def attention_one(q, K, V, scale: float):
+    """One query row against ``n >= 1`` key/value rows, float64.
+
+    q: [D]; K, V: [n, D]. Returns [D].
+    """
+    q = np.asarray(q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    V = np.asarray(V, dtype=np.float64)
+    if K.shape[0] == 0:
+        raise ValueError("attention over zero rows")
+    s = scale * (K @ q)
+    s = s - s.max()
+    w = np.exp(s)
+    return (w @ V) / w.sum()
+
+
+def decode_attention(q, K, V, scale: float):
+    """All query heads of one request.
+
+    q: [Hq, D]; K, V: [n, Hkv, D] in logical order. Returns [Hq, D] float64.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    Hq = q.shape[0]
+    Hkv = K.shape[1]
+    if Hq % Hkv:
+        raise ValueError("Hq must be a multiple of Hkv")
+    G = Hq // Hkv
+    out = np.empty_like(q)
+    for h in range(Hq):
+        g = h // G
+        out[h] = attention_one(q[h], K[:, g, :], V[:, g, :], scale)
+    return out
+
+
+def gather_block(table_row, P: int, lo: int, hi: int) -> list:
+    """Slots of positions ``lo <= t < hi`` through a block-table row."""
+    slots = []
+    for t in range(lo, hi):
+        page = int(table_row[t // P])
+        if page < 0:
+            raise IndexError(f"position {t} lies in a released page")
+        slots.append(page * P + t % P)
+    return slots
+
+
+def gather_raw(raw_row, lo: int, hi: int) -> list:
+    """Slots of positions ``lo <= t < hi`` through a raw-location row."""
+    slots = []
+    for t in range(lo, hi):
+        s = int(raw_row[t])
+        if s < 0:
+            raise IndexError(f"position {t} lies in a released page")
+        slots.append(s)
+    return slots
+
+
+class SlotStore:
+    """One layer of the KV pool viewed as flat token slots (``page * P + offset``).
+
+    Only slots that were written exist; reading any other slot is an error.
+    ``store_cache`` follows the mini-sglang code series, part 4, section "KV
+    버퍼는 6축인데, 쓸 때는 3축이다": row ``i`` of ``k`` and ``v`` goes to slot
+    ``out_loc[i]``.
+    """
+
+    def __init__(self):
+        self.k = {}
+        self.v = {}
+
+    def store_cache(self, out_loc, k, v) -> None:
+        for i, s in enumerate(out_loc):
+            self.k[int(s)] = np.array(k[i], dtype=np.float64)
+            self.v[int(s)] = np.array(v[i], dtype=np.float64)
+
+    def copy_page(self, src: int, dst: int, P: int) -> None:
+        """Copy-on-write: the whole page ``src`` into page ``dst``."""
+        for j in range(P):
+            s, d = src * P + j, dst * P + j
+            if s in self.k:
+                self.k[d] = self.k[s].copy()
+                self.v[d] = self.v[s].copy()
+            else:
+                self.k.pop(d, None)
+                self.v.pop(d, None)
+
+    def gather(self, slots):
+        K = np.stack([self.k[s] for s in slots])
+        V = np.stack([self.v[s] for s in slots])
+        return K, V
+
+
+def attend_request(store: SlotStore, q, slots, scale: float):
+    """Decode attention of one request over the given slots (logical order)."""
+    K, V = store.gather(slots)
+    return decode_attention(q, K, V, scale)

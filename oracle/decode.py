@@ -1,0 +1,73 @@
+"""One layer's decode loop over the oracle's tables (test infrastructure only).
+
+Order of one step, for every request of the batch (reading of "A Paged KV
+Cache and Sliding-Window Attention", chapter 15, section "The model", with
+the attention moved after a separate store):
+
+1. append the new token to the request's block table (a fresh page on a page
+   boundary, lazy copy-on-write of a shared tail page) -> its slot;
+2. copy every copied-on-write page, then store the new K/V rows at their
+   slots (mini-sglang code series, part 4: ``store_cache`` with ``out_loc``);
+3. attend positions ``max(0, L - W) .. L - 1`` (``L`` = length after the
+   append) read through the table;
+4. trim the request to ``keep_from = L + 1 - W`` so that the page holding the
+   first row the NEXT step needs is kept.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+from .attention import SlotStore, attend_request, gather_block, gather_raw, window_lo
+
+
+class BlockDecoder:
+    """Decode loop in block-table mode (one layer)."""
+
+    def __init__(self, pt, window, scale: float):
+        self.pt = pt
+        self.P = pt.page
+        self.window = window
+        self.scale = scale
+        self.store = SlotStore()
+
+    def prefill(self, rid, k, v) -> list:
+        """Append ``len(k)`` rows to request ``rid`` (no attention); returns slots."""
+        slots = []
+        for i in range(len(k)):
+            r = self.pt.append(rid)
+            if r["cow"] is not None:
+                self.store.copy_page(r["cow"][0], r["cow"][1], self.P)
+            slots.append(r["slot"])
+            self.store.store_cache([r["slot"]], k[i:i + 1], v[i:i + 1])
+            if self.window is not None and self.window > 0:
+                self.pt.trim(rid, max(0, self.pt.length[rid] + 1 - self.window))
+        return slots
+
+    def step(self, rids, q, k_new, v_new):
+        """One decode step. Returns (slots, copy-on-write pairs, outputs [B, Hq, D])."""
+        slots, cows = [], []
+        for rid in rids:
+            r = self.pt.append(rid)
+            if r["cow"] is not None:
+                cows.append(r["cow"])
+            slots.append(r["slot"])
+        for src, dst in cows:
+            self.store.copy_page(src, dst, self.P)
+        self.store.store_cache(slots, k_new, v_new)
+        outs = []
+        for i, rid in enumerate(rids):
+            L = self.pt.length[rid]
+            lo = window_lo(L, self.window)
+            s = gather_block(self.pt.block_row(rid), self.P, lo, L)
+            outs.append(attend_request(self.store, q[i], s, self.scale))
+        if self.window is not None and self.window > 0:
+            for rid in rids:
+                self.pt.trim(rid, max(0, self.pt.length[rid] + 1 - self.window))
+        return slots, cows, np.stack(outs)
+
+
+def attend_raw(store: SlotStore, raw_row, q, L: int, window, scale: float):
+    """Decode attention of one request through a raw-location table row."""
+    lo = window_lo(L, window)
+    return attend_request(store, q, gather_raw(raw_row, lo, L), scale)

@@ -1,0 +1,222 @@
+"""Seeded synthetic inputs for the paged decode-attention workloads.
+
+This module is the ONLY code that both the CUDA path (tests, bench) and the
+CPU oracle consume. It holds none of the method's arithmetic: it produces
+random values, lengths and permutations, nothing else.
+
+Values
+------
+Every Q/K/V element is a pure function of ``(seed, stream, element index)``
+(a counter-based generator), so any subset of rows can be produced on any
+device, in any order, bit-identically. The recipe:
+
+1. ``h = mix32(lo ^ mix32((hi + key) mod 2^32))`` where ``lo``/``hi`` are the
+   low/high 32 bits of the element index, ``key`` mixes seed and stream, and
+   ``mix32`` is the "lowbias32" integer hash published by C. Wellons (hash
+   prospector): ``x ^= x>>16; x *= 0x7feb352d; x ^= x>>15; x *= 0x846ca68b;
+   x ^= x>>16`` (mod 2^32).
+2. The three low bytes of ``h`` are summed (Irwin-Hall with three terms),
+   centred and scaled: ``(b0 + b1 + b2 - 382) / 128``. The result has mean
+   ~0.004, standard deviation 1.000 and support [-2.98, 3.0]: a bounded
+   stand-in for N(0, 1) that is exact in float32.
+3. bf16 workloads round that float32 value to bf16 (round to nearest even).
+
+All integer steps run in int64 tensors holding 32-bit values, with the
+32-bit products split in 16-bit halves so that no step overflows; torch
+gives the same bits on CPU and CUDA.
+
+Element indices
+---------------
+``K/V``: ``((((layer*2 + kv)*2^12 + request)*2^20 + position)*2^6 + head)*2^9 + d``
+``Q``:   ``((((step*2^6 + layer)*2^12 + request)*2^6 + head)*2^9 + d``
+
+Lengths and permutations come from ``numpy.random.RandomState`` (whose
+stream numpy keeps frozen across versions).
+"""
+
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+_M32 = 0xFFFFFFFF
+STREAM_K, STREAM_V, STREAM_Q = 1, 2, 3
+
+
+def _mul32_t(x: torch.Tensor, c: int) -> torch.Tensor:
+    lo, hi = c & 0xFFFF, c >> 16
+    return (x * lo + (((x * hi) & 0xFFFF) << 16)) & _M32
+
+
+def _mix32_t(x: torch.Tensor) -> torch.Tensor:
+    x = x ^ (x >> 16)
+    x = _mul32_t(x, 0x7FEB352D)
+    x = x ^ (x >> 15)
+    x = _mul32_t(x, 0x846CA68B)
+    return x ^ (x >> 16)
+
+
+def _mix32_i(x: int) -> int:
+    x &= _M32
+    x ^= x >> 16
+    x = (x * 0x7FEB352D) & _M32
+    x ^= x >> 15
+    x = (x * 0x846CA68B) & _M32
+    return x ^ (x >> 16)
+
+
+def hash_normal(seed: int, stream: int, idx: torch.Tensor) -> torch.Tensor:
+    """float32 approximately-N(0,1) value for each int64 element index."""
+    key = _mix32_i(_mix32_i(seed * 0x9E3779B9 + 0x632BE5AB) ^ (stream * 0x85EBCA77))
+    lo = idx & _M32
+    hi = idx >> 32
+    h = _mix32_t(lo ^ _mix32_t((hi + key) & _M32))
+    s = (h & 255) + ((h >> 8) & 255) + ((h >> 16) & 255) - 382
+    return s.to(torch.float32) * (1.0 / 128.0)
+
+
+def _as_index(x, device) -> torch.Tensor:
+    return torch.as_tensor(x, dtype=torch.int64, device=device).reshape(-1)
+
+
+def kv_rows(seed: int, layer: int, rid, pos, Hkv: int, D: int,
+            dtype=torch.bfloat16, device="cpu"):
+    """K and V rows ``[n, Hkv, D]`` of tokens ``(rid[i], pos[i])`` in ``layer``.
+
+    ``rid`` and ``pos`` are equal-length integer sequences (or one of them a
+    scalar). Values depend only on (seed, layer, request, position, head, d).
+    """
+    rid = _as_index(rid, device)
+    pos = _as_index(pos, device)
+    rid, pos = torch.broadcast_tensors(rid, pos)
+    assert Hkv <= 64 and D <= 512 and layer < 64
+    h = torch.arange(Hkv, dtype=torch.int64, device=device).view(1, Hkv, 1)
+    d = torch.arange(D, dtype=torch.int64, device=device).view(1, 1, D)
+    out = []
+    for kv, stream in ((0, STREAM_K), (1, STREAM_V)):
+        base = ((layer * 2 + kv) * 4096 + rid) * (1 << 20) + pos
+        idx = ((base.view(-1, 1, 1) * 64 + h) * 512) + d
+        out.append(hash_normal(seed, stream, idx).to(dtype))
+    return out[0], out[1]
+
+
+def q_rows(seed: int, step: int, layer: int, rid, Hq: int, D: int,
+           dtype=torch.bfloat16, device="cpu"):
+    """Query rows ``[n, Hq, D]`` of requests ``rid`` at decode step ``step``."""
+    rid = _as_index(rid, device)
+    assert Hq <= 64 and D <= 512 and layer < 64
+    h = torch.arange(Hq, dtype=torch.int64, device=device).view(1, Hq, 1)
+    d = torch.arange(D, dtype=torch.int64, device=device).view(1, 1, D)
+    base = (step * 64 + layer) * 4096 + rid
+    idx = ((base.view(-1, 1, 1) * 64 + h) * 512) + d
+    return hash_normal(seed, STREAM_Q, idx).to(dtype)
+
+
+def permutation(seed: int, n: int) -> np.ndarray:
+    return np.random.RandomState(seed).permutation(n).astype(np.int64)
+
+
+def free_stack_for_order(order) -> list:
+    """Free-list stack (top = end) that hands pages out in ``order``."""
+    return [int(p) for p in reversed(list(order))]
+
+
+# ---------------------------------------------------------------------------
+# The five workloads. Each is a plain description: shapes, lengths and the
+# initial free-list order; building tables from them is the method's job.
+# ---------------------------------------------------------------------------
+
+@dataclass
+class Workload:
+    name: str
+    dtype: str                 # "f32" or "bf16"
+    Hq: int
+    Hkv: int
+    D: int
+    P: int
+    layers: int
+    num_pages: int             # managed pages (the pool may add a dummy page)
+    free_order: list           # free-list stack, top = end
+    lengths: list              # context length of each request before the first decode step
+    window: int = 0            # <= 0: none
+    scale: float = 0.0
+    table_mode: str = "block"  # "block" or "raw"
+    extra: dict = field(default_factory=dict)
+
+
+def tiny(seed: int = 0, window=None) -> Workload:
+    """1 layer, fp32, 2 q / 2 kv heads, head_dim 16, page 4, 64 pages; 4 requests
+    decode 32 tokens each from empty; windows none / 8 / 4."""
+    n_pages = 64
+    return Workload("tiny", "f32", 2, 2, 16, 4, 1, n_pages,
+                    free_stack_for_order(permutation(seed * 7919 + 11, n_pages)),
+                    [0, 0, 0, 0], window=0 if window is None else window,
+                    scale=1.0 / math.sqrt(16), extra={"steps": 32})
+
+
+def gqa_decode(seed: int = 0) -> Workload:
+    """bf16, 32 q / 8 kv heads, head_dim 128, page 16, batch 64, context
+    lengths uniform in [512, 4096], pool = pages needed + 10%, block tables a
+    seeded random permutation of the pages, no window."""
+    P, B = 16, 64
+    rs = np.random.RandomState(seed * 7919 + 2)
+    lengths = rs.randint(512, 4096 + 1, size=B).tolist()
+    need = sum(-(-L // P) for L in lengths)
+    n_pages = int(math.ceil(need * 1.1))
+    order = np.random.RandomState(seed * 7919 + 3).permutation(n_pages)
+    return Workload("gqa_decode", "bf16", 32, 8, 128, P, 1, n_pages,
+                    free_stack_for_order(order), lengths, scale=1.0 / math.sqrt(128))
+
+
+def sliding_window(seed: int = 0) -> Workload:
+    """bf16, 32 q / 8 kv heads, head_dim 128, page 16, batch 32, W = 4096,
+    context lengths uniform in [8192, 32768]; pages older than the window are
+    released (front holes), at most ceil((W-1)/16)+1 live pages per request."""
+    P, B, W = 16, 32, 4096
+    rs = np.random.RandomState(seed * 7919 + 4)
+    lengths = rs.randint(8192, 32768 + 1, size=B).tolist()
+    live = -(-(W - 1) // P) + 1
+    n_pages = int(math.ceil(B * live * 1.1))
+    order = np.random.RandomState(seed * 7919 + 5).permutation(n_pages)
+    return Workload("sliding_window", "bf16", 32, 8, 128, P, 1, n_pages,
+                    free_stack_for_order(order), lengths, window=W,
+                    scale=1.0 / math.sqrt(128))
+
+
+def prefix_sharing(seed: int = 0) -> Workload:
+    """bf16, 32 q / 8 kv heads, head_dim 128, page 16: 8 prompts of 2050 tokens,
+    each forked 16 times (128 requests); private suffixes uniform in [16, 512]."""
+    P, n_prompts, forks, prompt_len = 16, 8, 16, 2050
+    rs = np.random.RandomState(seed * 7919 + 6)
+    suffix = rs.randint(16, 512 + 1, size=n_prompts * forks).tolist()
+    shared = n_prompts * -(-prompt_len // P)
+    private = sum(-(-(prompt_len + s + 256) // P) - prompt_len // P for s in suffix)
+    n_pages = int(math.ceil((shared + private) * 1.1))
+    order = np.random.RandomState(seed * 7919 + 7).permutation(n_pages)
+    lengths = [prompt_len + s for s in suffix]
+    return Workload("prefix_sharing", "bf16", 32, 8, 128, P, 1, n_pages,
+                    free_stack_for_order(order), lengths, scale=1.0 / math.sqrt(128),
+                    extra={"n_prompts": n_prompts, "forks": forks,
+                           "prompt_len": prompt_len, "suffix": suffix})
+
+
+def large_batch(seed: int = 0, P: int = 16, headroom: int = 256) -> Workload:
+    """mini-sglang layout: bf16, 64 q / 8 kv heads, head_dim 128, batch 256,
+    32 layers, context lengths lognormal (median 1024, sigma 0.8) capped at
+    16384 (minus ``headroom`` decode steps), raw token-location page table of
+    shape (257, align32(16384)), run at page 16 and page 1."""
+    B, max_seq = 256, 16384
+    rs = np.random.RandomState(seed * 7919 + 8)
+    draw = rs.lognormal(mean=math.log(1024.0), sigma=0.8, size=B)
+    lengths = [int(min(max_seq - headroom, max(1, math.floor(x + 0.5)))) for x in draw]
+    need = sum(-(-(L + headroom) // P) for L in lengths)
+    n_pages = int(math.ceil(need * 1.1))
+    order = np.random.RandomState(seed * 7919 + 9 + P).permutation(n_pages)
+    return Workload(f"large_batch_p{P}", "bf16", 64, 8, 128, P, 32, n_pages,
+                    free_stack_for_order(order), lengths, scale=1.0 / math.sqrt(128),
+                    table_mode="raw",
+                    extra={"max_running_req": B, "max_seq_len": max_seq,
+                           "headroom": headroom})
