@@ -1,0 +1,246 @@
+/*
+ * pagedkv.h -- C ABI of libpagedkv: the data-parallel hot path of a paged
+ * KV cache on GB300 (sm_103a).
+ *
+ * What the library computes comes from four pages:
+ *  - "A Paged KV Cache and Sliding-Window Attention" (silicon_compiler_from_
+ *    scratch, chapter 15), section "The model": fixed-size pages from a
+ *    shared pool, a block table per request, a LIFO free list, reference
+ *    counts, fork, lazy copy-on-write and the window trim; Figure 15.1 (the
+ *    released pages leave holes at the front of the table).
+ *  - "PagedAttention block allocator" (llm-systems-cookbook), section
+ *    "Sequence block table": position t lives in logical page t / P at
+ *    offset t % P.
+ *  - mini-sglang code series, part 4 (jaehun.me): the 6-axis KV buffer
+ *    (2, layers, num_pages, page_size, kv_heads, head_dim), store_cache
+ *    writing rows at flat token locations ``out_loc``, the raw-location page
+ *    table, the page->token expansion and the one-scatter table write, the
+ *    dummy request row and dummy page.
+ *  - "Week 3 Day 3: Paged KV Cache" (tiny-llm), sections "Tail-Append Logic"
+ *    and "Make write cost proportional to the appended slice" (a device write
+ *    sized to the new rows) and "Correctness Checkpoint: Gather Pages for
+ *    Dense Attention" (attention over the rows gathered in logical order).
+ *
+ * Conventions for every call
+ *  - Return value: KVP_OK (0) or a negative KVP_ERR_* code. No exception or
+ *    abort crosses the ABI.
+ *  - Host-side argument checks run before any launch; a call that fails them
+ *    launches nothing and changes nothing.
+ *  - Device pointers (KV buffer, tables, q/k/v, outputs, workspace, the error
+ *    word) are OWNED BY THE CALLER; the library never allocates or frees
+ *    them. Host pointers are read or written only during the call.
+ *  - ``stream`` is a cudaStream_t (NULL = the legacy default stream). Device
+ *    calls are asynchronous on it; the caller orders them (page_table_write,
+ *    copy_pages, store_cache, then paged_decode_attention for one step).
+ *  - Errors found ON THE DEVICE (a negative or out-of-range table entry,
+ *    slot or length, or a bounded internal wait that ran out) are recorded in
+ *    the pool's device error word (first error wins) and the offending row
+ *    is skipped; kvp_sync_error() reads and clears it. Kernels never trap.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVP_OK 0
+#define KVP_ERR_INVALID_ARG (-1) /* bad argument; nothing launched            */
+#define KVP_ERR_CUDA (-2)        /* a CUDA runtime call failed                */
+#define KVP_ERR_OUT_OF_PAGES (-3)/* host bookkeeping: no free page, no change */
+#define KVP_ERR_BAD_INDEX (-4)   /* device: table entry/slot/length invalid   */
+#define KVP_ERR_TIMEOUT (-5)     /* device: a bounded wait ran out            */
+
+enum kvp_dtype { KVP_F32 = 0, KVP_BF16 = 1 };
+enum kvp_table_mode {
+  KVP_BLOCK_TABLE = 0,   /* table[row][logical page] = physical page, -1 hole */
+  KVP_RAW_LOCATIONS = 1  /* table[row][position] = flat token slot, -1 hole   */
+};
+
+typedef struct kvp_pool kvp_pool;
+
+/* ------------------------------------------------------------------------
+ * kv_pool_create: describe a caller-owned KV buffer (mini-sglang part 4,
+ * section "KV 버퍼는 6축인데, 쓸 때는 3축이다").
+ *   kv_buffer   device, (2, num_layers, num_pages, page_size, kv_heads,
+ *               head_dim) elements of ``dtype``, C-contiguous; index 0 of
+ *               the first axis is K, 1 is V. Must be 16-byte aligned.
+ *               A flat token slot s = page * page_size + offset addresses
+ *               row s of the (num_pages * page_size, kv_heads, head_dim)
+ *               view of one layer's K or V. num_pages counts EVERY page of
+ *               the buffer, including a dummy page the caller keeps back.
+ *   error_word  device int32, zero-initialised, caller-owned; receives the
+ *               first device-detected error of calls on this pool.
+ *   out         receives an opaque descriptor (host memory owned by the
+ *               library until kv_pool_destroy).
+ * kv_heads * head_dim * sizeof(dtype) must be a multiple of 16 bytes.
+ * Errors: INVALID_ARG (null pointer, non-positive size, misalignment),
+ * CUDA (device query failed).
+ * ---------------------------------------------------------------------- */
+int kv_pool_create(int num_pages, int page_size, int kv_heads, int head_dim,
+                   int dtype, int num_layers, void* kv_buffer,
+                   int32_t* error_word, kvp_pool** out);
+int kv_pool_destroy(kvp_pool* pool);
+
+/* ------------------------------------------------------------------------
+ * store_cache: K[layer][out_loc[i]] = k[i], V[layer][out_loc[i]] = v[i] for
+ * i < n (mini-sglang part 4: store_cache(k_cache, v_cache, indices=out_loc,
+ * k, v); tiny-llm week 3 day 3: the write covers only the new rows).
+ *   k, v     device, [n, kv_heads, head_dim] of the pool's dtype, contiguous.
+ *   out_loc  device int32 [n], flat token slots. Duplicate slots within one
+ *            call are a caller error except in a dummy page (the last write
+ *            is then unspecified).
+ * A slot outside [0, num_pages*page_size) sets KVP_ERR_BAD_INDEX on the
+ * device and that row is skipped. n == 0 launches nothing.
+ * ---------------------------------------------------------------------- */
+int store_cache(const kvp_pool* pool, int layer, const void* k, const void* v,
+                const int32_t* out_loc, int n, void* stream);
+
+/* ------------------------------------------------------------------------
+ * page_table_write: the device-side table write for newly allocated (or
+ * released, or copied-on-write) pages (mini-sglang part 4, section "할당은
+ * 페이지로, 기록은 토큰으로": host-built (row, position) lists, one scatter;
+ * its page->token expansion is done here on the device).
+ * For i < n and j < expand:
+ *     table[rows[i]][cols[i]*expand + j] = vals[i] < 0 ? -1
+ *                                                    : vals[i]*expand + j
+ *   expand = 1          block-table mode: cols = logical page, vals = page.
+ *   expand = page_size  raw-location mode: cols/vals in PAGE units, written
+ *                       as page_size token locations each.
+ *   table    device int32 [table_rows_total, table_cols], row-major.
+ *   rows, cols, vals  device int32 [n].
+ *   error_word        device int32 or NULL; an entry outside the table sets
+ *                     KVP_ERR_BAD_INDEX there and is skipped.
+ * ---------------------------------------------------------------------- */
+int page_table_write(int32_t* table, int table_rows_total, int table_cols,
+                     const int32_t* rows, const int32_t* cols,
+                     const int32_t* vals, int n, int expand,
+                     int32_t* error_word, void* stream);
+
+/* ------------------------------------------------------------------------
+ * copy_pages: copy-on-write (chapter 15, section "The model": a shared tail
+ * page is copied whole before a private write). For i < n, every layer, K
+ * and V: page dst[i] <- page src[i]. src/dst device int32 [n]; a page
+ * outside [0, num_pages) sets KVP_ERR_BAD_INDEX and is skipped. Pairs must
+ * not overlap (no page is both a source and a destination).
+ * ---------------------------------------------------------------------- */
+int copy_pages(const kvp_pool* pool, const int32_t* src, const int32_t* dst,
+               int n, void* stream);
+
+/* ------------------------------------------------------------------------
+ * paged_decode_attention: one decode step of attention for ``batch``
+ * requests, one query token each, reading K/V in place through the table.
+ * For request b and query head h (GQA: KV head h / (num_q_heads/kv_heads)):
+ *     L  = context_lens[b]            (includes the token stored this step)
+ *     lo = window > 0 ? max(0, L - window) : 0
+ *     s_t = scale * <q[b][h], K[slot(b,t)][h/G]>       for lo <= t < L
+ *     out[b][h] = sum_t softmax(s)_t * V[slot(b,t)][h/G]
+ * slot(b,t): block mode table[r][t/P]*P + t%P, raw mode table[r][t], with
+ * r = table_rows ? table_rows[b] : b (the mini-sglang table_idx).
+ * Sources: chapter 15, section "The model" (the window: the new token and at
+ * most W-1 earlier ones); tiny-llm week 3 day 3, section "Correctness
+ * Checkpoint" (dense attention over the gathered rows, here read in place).
+ *   q            device [batch, num_q_heads, head_dim], pool dtype.
+ *   table        device int32 [table_rows_total, table_cols].
+ *   context_lens device int32 [batch]; 1 <= L <= table capacity.
+ *   out          device [batch, num_q_heads, head_dim], pool dtype (bf16
+ *                results are rounded to nearest even from fp32).
+ *   workspace    device, >= paged_decode_attention_workspace_size() bytes,
+ *                256-byte aligned; scratch for the work plan and split-K
+ *                partials. Its contents need no initialisation and are
+ *                clobbered.
+ * Device-detected errors (L out of range, hole or out-of-range entry in the
+ * attended range) set KVP_ERR_BAD_INDEX; an invalid request's output is
+ * zero-filled.
+ * ---------------------------------------------------------------------- */
+int paged_decode_attention_workspace_size(const kvp_pool* pool, int batch,
+                                          int num_q_heads, size_t* bytes);
+int paged_decode_attention(const kvp_pool* pool, int layer, const void* q,
+                           int batch, int num_q_heads, const int32_t* table,
+                           int table_rows_total, int table_cols,
+                           int table_mode, const int32_t* table_rows,
+                           const int32_t* context_lens, int window,
+                           float scale, void* out, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * gather_indices: the slots paged_decode_attention would read, for
+ * bit-exact checks of the index arithmetic ("PagedAttention block
+ * allocator", section "Sequence block table"; chapter 15 Figure 15.1).
+ * slots_out device int32 [batch, max_tokens]: row b holds slot(b, lo+i) for
+ * i < L-lo and -1 after. L - lo > max_tokens, or an invalid entry, sets
+ * KVP_ERR_BAD_INDEX (the entry is written as -1).
+ * ---------------------------------------------------------------------- */
+int gather_indices(const kvp_pool* pool, const int32_t* table,
+                   int table_rows_total, int table_cols, int table_mode,
+                   const int32_t* table_rows, const int32_t* context_lens,
+                   int batch, int window, int32_t* slots_out, int max_tokens,
+                   void* stream);
+
+/* kvp_sync_error: wait for ``stream``, read the pool's device error word
+ * into *err (0 = none) and clear it. */
+int kvp_sync_error(const kvp_pool* pool, void* stream, int* err);
+
+/* ========================================================================
+ * Host bookkeeping (pure host C++; no CUDA). Chapter 15, section "The
+ * model", restated: LIFO free list, reference counts, block tables indexed
+ * by absolute logical page, fork, lazy copy-on-write, window trim, release.
+ * Request ids are table rows in [0, max_requests).
+ * Every call that can run out of pages checks first and changes nothing on
+ * KVP_ERR_OUT_OF_PAGES (chapter 15, section "Tests", item 2).
+ * ====================================================================== */
+typedef struct kvp_host kvp_host;
+
+/* free_stack: the initial free list as a stack, free_stack[num_pages-1] is
+ * handed out first; NULL means num_pages-1 .. 0 (page 0 first). */
+int kvp_host_create(int num_pages, int page_size, int max_requests,
+                    const int32_t* free_stack, kvp_host** out);
+int kvp_host_destroy(kvp_host* h);
+int kvp_host_new(kvp_host* h, int rid);
+int kvp_host_release(kvp_host* h, int rid);
+
+/* Fork: dst shares every page of src (one more reference each, no data
+ * copied). Emits the table writes (dst, logical page, page or -1) that make
+ * the device row of dst equal to that of src; capacity tw_cap must cover
+ * every logical page of src, count in *n_tw. On a short buffer returns
+ * KVP_ERR_INVALID_ARG and changes nothing. */
+int kvp_host_fork(kvp_host* h, int src, int dst, int32_t* tw_rows,
+                  int32_t* tw_cols, int32_t* tw_vals, int tw_cap, int* n_tw);
+
+/* Append one token to each of rids[0..n) in order (one token per entry; a
+ * request may appear several times). Outputs (host arrays):
+ *   slots[n]                 flat slot of each new token;
+ *   tw_rows/tw_cols/tw_vals  table writes (row, logical page, page) for new
+ *                            pages and copy-on-write replacements; capacity
+ *                            tw_cap >= n suffices; count in *n_tw;
+ *   cow_src/cow_dst          copy-on-write page pairs, capacity >= n; count
+ *                            in *n_cow.
+ * If the pool cannot serve the whole batch, returns KVP_ERR_OUT_OF_PAGES and
+ * changes nothing. */
+int kvp_host_append(kvp_host* h, const int32_t* rids, int n, int32_t* slots,
+                    int32_t* tw_rows, int32_t* tw_cols, int32_t* tw_vals,
+                    int tw_cap, int* n_tw, int32_t* cow_src,
+                    int32_t* cow_dst, int* n_cow);
+
+/* Release the front pages of request rid that hold only positions below
+ * keep_from (page ``dropped`` goes while (dropped+1)*P <= keep_from). Emits
+ * (rid, logical page, -1) table writes; capacity tw_cap, count in *n_tw. */
+int kvp_host_trim(kvp_host* h, int rid, int keep_from, int32_t* tw_rows,
+                  int32_t* tw_cols, int32_t* tw_vals, int tw_cap, int* n_tw);
+
+/* Queries. kvp_host_block_row writes dropped+live entries (-1 for released
+ * pages) to out (capacity cap) and the count to *n. */
+int kvp_host_used(const kvp_host* h, int* used);
+int kvp_host_length(const kvp_host* h, int rid, int* length, int* dropped);
+int kvp_host_block_row(const kvp_host* h, int rid, int32_t* out, int cap,
+                       int* n);
+int kvp_host_refcounts(const kvp_host* h, int32_t* out, int cap);
+int kvp_host_free_list(const kvp_host* h, int32_t* out, int cap, int* n);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PAGEDKV_H */

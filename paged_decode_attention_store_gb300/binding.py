@@ -1,0 +1,322 @@
+"""Thin Python binding of libpagedkv (argument marshalling only).
+
+Same names as the C ABI in ``include/pagedkv.h``. Device arguments are torch
+CUDA tensors (PyTorch supplies device memory and streams); every step of the
+path runs in the library's kernels. A missing library or a non-zero status
+raises: there is no fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpagedkv.so")
+
+KVP_OK = 0
+KVP_ERR_INVALID_ARG = -1
+KVP_ERR_CUDA = -2
+KVP_ERR_OUT_OF_PAGES = -3
+KVP_ERR_BAD_INDEX = -4
+KVP_ERR_TIMEOUT = -5
+
+KVP_F32, KVP_BF16 = 0, 1
+KVP_BLOCK_TABLE, KVP_RAW_LOCATIONS = 0, 1
+
+_ERR_NAMES = {
+    KVP_ERR_INVALID_ARG: "KVP_ERR_INVALID_ARG",
+    KVP_ERR_CUDA: "KVP_ERR_CUDA",
+    KVP_ERR_OUT_OF_PAGES: "KVP_ERR_OUT_OF_PAGES",
+    KVP_ERR_BAD_INDEX: "KVP_ERR_BAD_INDEX",
+    KVP_ERR_TIMEOUT: "KVP_ERR_TIMEOUT",
+}
+
+# Every symbol the header declares, with its C signature.
+_vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+_ip = ctypes.POINTER(ctypes.c_int)
+_szp = ctypes.POINTER(ctypes.c_size_t)
+SIGNATURES = {
+    "kv_pool_create": [_i, _i, _i, _i, _i, _i, _vp, _vp, ctypes.POINTER(_vp)],
+    "kv_pool_destroy": [_vp],
+    "store_cache": [_vp, _i, _vp, _vp, _vp, _i, _vp],
+    "page_table_write": [_vp, _i, _i, _vp, _vp, _vp, _i, _i, _vp, _vp],
+    "copy_pages": [_vp, _vp, _vp, _i, _vp],
+    "paged_decode_attention_workspace_size": [_vp, _i, _i, _szp],
+    "paged_decode_attention": [_vp, _i, _vp, _i, _i, _vp, _i, _i, _i, _vp, _vp, _i, _f, _vp, _vp, _sz, _vp],
+    "gather_indices": [_vp, _vp, _i, _i, _i, _vp, _vp, _i, _i, _vp, _i, _vp],
+    "kvp_sync_error": [_vp, _vp, _ip],
+    "kvp_host_create": [_i, _i, _i, _vp, ctypes.POINTER(_vp)],
+    "kvp_host_destroy": [_vp],
+    "kvp_host_new": [_vp, _i],
+    "kvp_host_fork": [_vp, _i, _i, _vp, _vp, _vp, _i, _ip],
+    "kvp_host_release": [_vp, _i],
+    "kvp_host_append": [_vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _ip, _vp, _vp, _ip],
+    "kvp_host_trim": [_vp, _i, _i, _vp, _vp, _vp, _i, _ip],
+    "kvp_host_used": [_vp, _ip],
+    "kvp_host_length": [_vp, _i, _ip, _ip],
+    "kvp_host_block_row": [_vp, _i, _vp, _i, _ip],
+    "kvp_host_refcounts": [_vp, _vp, _i],
+    "kvp_host_free_list": [_vp, _vp, _i, _ip],
+}
+
+_lib = None
+
+
+class KvpError(RuntimeError):
+    def __init__(self, code, what):
+        super().__init__(f"{what}: {_ERR_NAMES.get(code, code)}")
+        self.code = code
+
+
+class OutOfPages(KvpError):
+    pass
+
+
+def lib():
+    """Load libpagedkv.so (built by ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()')")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, args in SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _check(code, what):
+    if code == KVP_ERR_OUT_OF_PAGES:
+        raise OutOfPages(code, what)
+    if code != KVP_OK:
+        raise KvpError(code, what)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dev(t, dtype=None, name="tensor"):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+_TORCH_DTYPE = {KVP_F32: torch.float32, KVP_BF16: torch.bfloat16}
+
+
+class Pool:
+    """A kvp_pool over a caller-owned KV buffer (kept alive here)."""
+
+    def __init__(self, kv_buffer, page_size, dtype, error_word=None):
+        _dev(kv_buffer, name="kv_buffer")
+        if kv_buffer.dim() != 6 or kv_buffer.shape[0] != 2 or kv_buffer.shape[3] != page_size:
+            raise ValueError("kv_buffer must be (2, layers, num_pages, page_size, kv_heads, head_dim)")
+        if kv_buffer.dtype != _TORCH_DTYPE[dtype]:
+            raise TypeError("kv_buffer dtype does not match")
+        _, self.num_layers, self.num_pages, self.page_size, self.kv_heads, self.head_dim = kv_buffer.shape
+        self.dtype = dtype
+        self.kv_buffer = kv_buffer
+        self.error_word = (torch.zeros(1, dtype=torch.int32, device=kv_buffer.device)
+                           if error_word is None else _dev(error_word, torch.int32, "error_word"))
+        h = ctypes.c_void_p()
+        _check(lib().kv_pool_create(self.num_pages, page_size, self.kv_heads, self.head_dim, dtype,
+                                    self.num_layers, _ptr(kv_buffer), _ptr(self.error_word), ctypes.byref(h)),
+               "kv_pool_create")
+        self.handle = h
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h is not None and _lib is not None:
+            _lib.kv_pool_destroy(h)
+            self.handle = None
+
+
+def kv_pool_create(num_pages, page_size, kv_heads, head_dim, dtype, num_layers, kv_buffer=None, device="cuda"):
+    """Describe (allocating with torch when ``kv_buffer`` is None) a KV buffer."""
+    if kv_buffer is None:
+        kv_buffer = torch.empty((2, num_layers, num_pages, page_size, kv_heads, head_dim),
+                                dtype=_TORCH_DTYPE[dtype], device=device)
+    return Pool(kv_buffer, page_size, dtype)
+
+
+def store_cache(pool, layer, k, v, out_loc, stream=None):
+    _dev(k, _TORCH_DTYPE[pool.dtype], "k")
+    _dev(v, _TORCH_DTYPE[pool.dtype], "v")
+    _dev(out_loc, torch.int32, "out_loc")
+    n = out_loc.numel()
+    if k.numel() != n * pool.kv_heads * pool.head_dim or v.numel() != k.numel():
+        raise ValueError("k/v must be [n, kv_heads, head_dim]")
+    _check(lib().store_cache(pool.handle, layer, _ptr(k), _ptr(v), _ptr(out_loc), n, _stream(stream)), "store_cache")
+
+
+def page_table_write(table, rows, cols, vals, expand=1, error_word=None, stream=None):
+    _dev(table, torch.int32, "table")
+    for t, nm in ((rows, "rows"), (cols, "cols"), (vals, "vals")):
+        _dev(t, torch.int32, nm)
+    n = rows.numel()
+    if cols.numel() != n or vals.numel() != n:
+        raise ValueError("rows, cols and vals must have the same length")
+    _check(lib().page_table_write(_ptr(table), table.shape[0], table.shape[1], _ptr(rows), _ptr(cols), _ptr(vals),
+                                  n, expand, _ptr(error_word), _stream(stream)), "page_table_write")
+
+
+def copy_pages(pool, src, dst, stream=None):
+    _dev(src, torch.int32, "src")
+    _dev(dst, torch.int32, "dst")
+    if src.numel() != dst.numel():
+        raise ValueError("src and dst must have the same length")
+    _check(lib().copy_pages(pool.handle, _ptr(src), _ptr(dst), src.numel(), _stream(stream)), "copy_pages")
+
+
+def paged_decode_attention_workspace_size(pool, batch, num_q_heads):
+    n = ctypes.c_size_t()
+    _check(lib().paged_decode_attention_workspace_size(pool.handle, batch, num_q_heads, ctypes.byref(n)),
+           "paged_decode_attention_workspace_size")
+    return n.value
+
+
+def alloc_workspace(pool, batch, num_q_heads, device="cuda"):
+    nbytes = paged_decode_attention_workspace_size(pool, batch, num_q_heads)
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def paged_decode_attention(pool, layer, q, table, table_mode, context_lens, window, scale, out, workspace,
+                           table_rows=None, stream=None):
+    dt = _TORCH_DTYPE[pool.dtype]
+    _dev(q, dt, "q")
+    _dev(out, dt, "out")
+    _dev(table, torch.int32, "table")
+    _dev(context_lens, torch.int32, "context_lens")
+    if table_rows is not None:
+        _dev(table_rows, torch.int32, "table_rows")
+    B, Hq = q.shape[0], q.shape[1]
+    if out.shape != q.shape or context_lens.numel() != B:
+        raise ValueError("q/out must be [B, Hq, D] and context_lens [B]")
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (_ptr(workspace), workspace.numel() * workspace.element_size())
+    _check(lib().paged_decode_attention(pool.handle, layer, _ptr(q), B, Hq, _ptr(table), table.shape[0],
+                                        table.shape[1], table_mode, _ptr(table_rows), _ptr(context_lens),
+                                        int(window or 0), float(scale), _ptr(out), ws_ptr, ws_bytes,
+                                        _stream(stream)), "paged_decode_attention")
+
+
+def gather_indices(pool, table, table_mode, context_lens, window, slots_out, table_rows=None, stream=None):
+    _dev(table, torch.int32, "table")
+    _dev(context_lens, torch.int32, "context_lens")
+    _dev(slots_out, torch.int32, "slots_out")
+    B = context_lens.numel()
+    _check(lib().gather_indices(pool.handle, _ptr(table), table.shape[0], table.shape[1], table_mode,
+                                _ptr(table_rows), _ptr(context_lens), B, int(window or 0), _ptr(slots_out),
+                                slots_out.shape[1], _stream(stream)), "gather_indices")
+
+
+def kvp_sync_error(pool, stream=None):
+    e = ctypes.c_int()
+    _check(lib().kvp_sync_error(pool.handle, _stream(stream), ctypes.byref(e)), "kvp_sync_error")
+    return e.value
+
+
+# ---------------------------------------------------------------------------
+# Host bookkeeping (pure C++, usable without a GPU).
+# ---------------------------------------------------------------------------
+def _i32(n):
+    return (ctypes.c_int32 * max(1, n))()
+
+
+class HostPageTable:
+    """kvp_host_*: refcounted LIFO free list, block tables with -1 holes,
+    fork, lazy copy-on-write, window trim; emits device table writes."""
+
+    def __init__(self, num_pages, page_size, max_requests, free_stack=None):
+        self.num_pages, self.page_size, self.max_requests = num_pages, page_size, max_requests
+        h = ctypes.c_void_p()
+        fs = None
+        if free_stack is not None:
+            fs = (ctypes.c_int32 * num_pages)(*[int(x) for x in free_stack])
+        _check(lib().kvp_host_create(num_pages, page_size, max_requests, fs, ctypes.byref(h)), "kvp_host_create")
+        self.handle = h
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h is not None and _lib is not None:
+            _lib.kvp_host_destroy(h)
+            self.handle = None
+
+    def new(self, rid):
+        _check(lib().kvp_host_new(self.handle, rid), "kvp_host_new")
+
+    def fork(self, src, dst):
+        """Share every page of ``src`` with ``dst``; returns the table writes for dst's row."""
+        cap = self.length(src)[0] // self.page_size + 2
+        tr, tc, tv = _i32(cap), _i32(cap), _i32(cap)
+        n = ctypes.c_int()
+        _check(lib().kvp_host_fork(self.handle, src, dst, tr, tc, tv, cap, ctypes.byref(n)), "kvp_host_fork")
+        return list(zip(tr[:n.value], tc[:n.value], tv[:n.value]))
+
+    def release(self, rid):
+        _check(lib().kvp_host_release(self.handle, rid), "kvp_host_release")
+
+    def append(self, rids):
+        """One token for each entry of ``rids`` -> (slots, table writes, cow pairs) as Python lists."""
+        rids = [int(r) for r in rids]
+        n = len(rids)
+        r = (ctypes.c_int32 * max(1, n))(*rids)
+        slots, tr, tc, tv, cs, cd = _i32(n), _i32(n), _i32(n), _i32(n), _i32(n), _i32(n)
+        ntw, ncow = ctypes.c_int(), ctypes.c_int()
+        _check(lib().kvp_host_append(self.handle, r, n, slots, tr, tc, tv, n, ctypes.byref(ntw), cs, cd,
+                                     ctypes.byref(ncow)), "kvp_host_append")
+        writes = list(zip(tr[:ntw.value], tc[:ntw.value], tv[:ntw.value]))
+        cows = list(zip(cs[:ncow.value], cd[:ncow.value]))
+        return list(slots[:n]), writes, cows
+
+    def trim(self, rid, keep_from):
+        cap = max(1, self.length(rid)[0] // self.page_size + 1)
+        tr, tc, tv = _i32(cap), _i32(cap), _i32(cap)
+        n = ctypes.c_int()
+        _check(lib().kvp_host_trim(self.handle, rid, int(keep_from), tr, tc, tv, cap, ctypes.byref(n)),
+               "kvp_host_trim")
+        return list(zip(tr[:n.value], tc[:n.value], tv[:n.value]))
+
+    def used(self):
+        u = ctypes.c_int()
+        _check(lib().kvp_host_used(self.handle, ctypes.byref(u)), "kvp_host_used")
+        return u.value
+
+    def length(self, rid):
+        L, d = ctypes.c_int(), ctypes.c_int()
+        _check(lib().kvp_host_length(self.handle, rid, ctypes.byref(L), ctypes.byref(d)), "kvp_host_length")
+        return L.value, d.value
+
+    def block_row(self, rid):
+        L, _ = self.length(rid)
+        cap = L // self.page_size + 2
+        out = _i32(cap)
+        n = ctypes.c_int()
+        _check(lib().kvp_host_block_row(self.handle, rid, out, cap, ctypes.byref(n)), "kvp_host_block_row")
+        return list(out[:n.value])
+
+    def refcounts(self):
+        out = _i32(self.num_pages)
+        _check(lib().kvp_host_refcounts(self.handle, out, self.num_pages), "kvp_host_refcounts")
+        return list(out[:self.num_pages])
+
+    def free_list(self):
+        out = _i32(self.num_pages)
+        n = ctypes.c_int()
+        _check(lib().kvp_host_free_list(self.handle, out, self.num_pages, ctypes.byref(n)), "kvp_host_free_list")
+        return list(out[:n.value])

@@ -1,0 +1,188 @@
+"""Drive the product path and the oracle side by side on one workload.
+
+``ProductSession`` uses only the library (host bookkeeping in C++, device
+writes and attention through the C ABI); ``OracleSession`` uses only
+``oracle/``. Both take the same seeded inputs from the workload generator:
+the product generates its K/V/Q rows on the GPU, the oracle on the CPU (the
+generator is bit-identical on both devices).
+"""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+import oracle.attention as OA
+from oracle.pagetable import PageTable
+from oracle.raw_locations import RawLocationTable, align32
+from paged_decode_attention_store_gb300 import workloads as wl
+
+TORCH_DT = {"bf16": torch.bfloat16, "f32": torch.float32}
+
+
+class ProductSession:
+    def __init__(self, kb, w, device, max_requests, cols=None, mode="block", layers=None, seed=0):
+        self.kb, self.w, self.dev, self.mode, self.seed = kb, w, device, mode, seed
+        self.P = w.P
+        self.layers = layers or w.layers
+        self.dt = TORCH_DT[w.dtype]
+        kdt = kb.KVP_BF16 if w.dtype == "bf16" else kb.KVP_F32
+        extra = 1 if mode == "raw" else 0  # the dummy page of the raw-location layout
+        self.kv = torch.zeros((2, self.layers, w.num_pages + extra, w.P, w.Hkv, w.D), dtype=self.dt, device=device)
+        self.pool = kb.Pool(self.kv, w.P, kdt)
+        self.host = kb.HostPageTable(w.num_pages, w.P, max_requests, w.free_order)
+        self.max_requests = max_requests
+        if mode == "block":
+            cols = cols or 1
+            self.table = torch.full((max_requests, cols), -1, dtype=torch.int32, device=device)
+        else:
+            cols = align32(min(cols or w.num_pages * w.P, w.num_pages * w.P))
+            self.table = torch.zeros((max_requests + 1, cols), dtype=torch.int32, device=device)
+            self.table[max_requests].fill_(w.num_pages * w.P)
+        self.ws = None
+        self.n_copies = 0
+
+    def _i32(self, xs):
+        return torch.tensor(list(xs), dtype=torch.int32, device=self.dev)
+
+    def _write(self, writes):
+        if not writes:
+            return
+        r, c, v = zip(*writes)
+        self.kb.page_table_write(self.table, self._i32(r), self._i32(c), self._i32(v),
+                                 expand=self.P if self.mode == "raw" else 1, error_word=self.pool.error_word)
+
+    def new(self, rid):
+        self.host.new(rid)
+
+    def fork(self, src, dst):
+        self._write(self.host.fork(src, dst))
+
+    def release(self, rid):
+        self.host.release(rid)
+
+    def append(self, rids, positions):
+        """Append one token per entry; K/V of (rid, position) come from the generator."""
+        slots, writes, cows = self.host.append(rids)
+        self._write(writes)
+        if cows:
+            s, d = zip(*cows)
+            self.kb.copy_pages(self.pool, self._i32(s), self._i32(d))
+            self.n_copies += len(cows)
+        out_loc = self._i32(slots)
+        for layer in range(self.layers):
+            k, v = wl.kv_rows(self.seed, layer, rids, positions, self.w.Hkv, self.w.D, dtype=self.dt, device=self.dev)
+            self.kb.store_cache(self.pool, layer, k, v, out_loc)
+        return slots
+
+    def trim(self, rid, keep_from):
+        self._write(self.host.trim(rid, keep_from))
+
+    def attend(self, layer, rids, lens, window, step, scale=None, table_rows=True):
+        B = len(rids)
+        if self.ws is None or self.ws_batch < B:
+            self.ws = self.kb.alloc_workspace(self.pool, B, self.w.Hq, device=self.dev)
+            self.ws_batch = B
+        q = wl.q_rows(self.seed, step, layer, rids, self.w.Hq, self.w.D, dtype=self.dt, device=self.dev)
+        out = torch.empty_like(q)
+        scale = self.w.scale if scale is None else scale
+        self.kb.paged_decode_attention(
+            self.pool, layer, q, self.table,
+            self.kb.KVP_RAW_LOCATIONS if self.mode == "raw" else self.kb.KVP_BLOCK_TABLE,
+            self._i32(lens), window, scale, out, self.ws,
+            table_rows=self._i32(rids) if table_rows else None)
+        return out
+
+    def gather(self, rids, lens, window, max_tokens):
+        out = torch.empty((len(rids), max_tokens), dtype=torch.int32, device=self.dev)
+        self.kb.gather_indices(self.pool, self.table,
+                               self.kb.KVP_RAW_LOCATIONS if self.mode == "raw" else self.kb.KVP_BLOCK_TABLE,
+                               self._i32(lens), window, out, table_rows=self._i32(rids))
+        return out
+
+    def error(self):
+        return self.kb.kvp_sync_error(self.pool)
+
+
+class OracleSession:
+    def __init__(self, w, max_requests, mode="block", layers=None, seed=0, track=None, raw_cols=None):
+        self.w, self.mode, self.seed = w, mode, seed
+        self.P = w.P
+        self.layers = layers or w.layers
+        self.pt = PageTable(w.num_pages, w.P, free_order=w.free_order)
+        self.raw = None
+        if mode == "raw":
+            self.raw = RawLocationTable(w.num_pages, w.P, max_requests, raw_cols or w.num_pages * w.P,
+                                        free_page_order=w.free_order)
+        self.stores = [OA.SlotStore() for _ in range(self.layers)]
+        self.track = track  # rids whose rows are stored (None: all)
+        self.dt = TORCH_DT[w.dtype]
+
+    def new(self, rid):
+        self.pt.new(rid)
+
+    def fork(self, src, dst):
+        self.pt.fork(src, dst)
+
+    def release(self, rid):
+        self.pt.release(rid)
+
+    def append(self, rids, positions):
+        before = {r: self.pt.length[r] for r in set(rids)}
+        res = [self.pt.append(r) for r in rids]
+        if self.raw is not None:
+            # one allocation call for the whole batch, requests in first-seen order
+            order, seen = [], set()
+            for r in rids:
+                if r not in seen:
+                    seen.add(r)
+                    order.append(r)
+            self.raw.allocate_paged([(r, before[r], self.pt.length[r]) for r in order])
+        for r in res:
+            if r["cow"] is not None:
+                for st in self.stores:
+                    st.copy_page(r["cow"][0], r["cow"][1], self.P)
+        keep = [i for i, r in enumerate(rids) if self.track is None or r in self.track]
+        if keep:
+            kr = [rids[i] for i in keep]
+            kp = [positions[i] for i in keep]
+            slots = [res[i]["slot"] for i in keep]
+            for layer, st in enumerate(self.stores):
+                k, v = wl.kv_rows(self.seed, layer, kr, kp, self.w.Hkv, self.w.D, dtype=self.dt)
+                st.store_cache(slots, k.float().numpy(), v.float().numpy())
+        return [r["slot"] for r in res]
+
+    def trim(self, rid, keep_from):
+        return self.pt.trim(rid, keep_from)
+
+    def slots(self, rid, lo, L):
+        if self.mode == "raw":
+            return OA.gather_raw(self.raw.page_table[rid], lo, L)
+        return OA.gather_block(self.pt.block_row(rid), self.P, lo, L)
+
+    def attend(self, layer, rid, L, window, step, scale=None):
+        q = wl.q_rows(self.seed, step, layer, [rid], self.w.Hq, self.w.D, dtype=self.dt)[0].float().numpy()
+        lo = OA.window_lo(L, window)
+        scale = self.w.scale if scale is None else scale
+        return OA.attend_request(self.stores[layer], q, self.slots(rid, lo, L), scale)
+
+    def table_row(self, rid):
+        """The device-visible prefix of this request's table row."""
+        if self.mode == "raw":
+            n = len(self.pt.block_row(rid)) * self.P
+            return [int(x) for x in self.raw.page_table[rid, :n]]
+        return self.pt.block_row(rid)
+
+
+def tol_for(dtype):
+    return 2e-2 if dtype == "bf16" else 1e-5
+
+
+def max_abs(a, b):
+    return float(np.max(np.abs(np.asarray(a, dtype=np.float64) - np.asarray(b, dtype=np.float64))))
+
+
+def scale_of(D):
+    return 1.0 / math.sqrt(D)
