@@ -1,0 +1,763 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged decode-attention hot path (one GB300, or N replicas).
+
+One step = one decode step of the whole hot path for every request of the
+workload: host bookkeeping (append, copy-on-write, window trim), the device
+table write, copy-on-write page copies, store_cache of the new K/V rows and
+paged decode attention (plan + attention + split-K combine), for every
+layer. Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle on the same workload
+
+``value`` is the achieved HBM GB/s of the step's algorithmic bytes (K/V rows
+attended, q, out, table entries, store_cache rows, table writes and page
+copies) with every input already in HBM; ``e2e`` is the same metric through
+the public driver (paged_decode_attention_store_gb300.engine) with the
+step's q/k/v in pinned host memory, host bookkeeping in the loop and the
+output read back each step.
+"""
+
+from __future__ import annotations
+
+import os
+
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")  # the CPU oracle runs on one core
+
+import argparse
+import datetime
+import json
+import math
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from paged_decode_attention_store_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "paged decode-attention achieved HBM GB/s (% of GB300 peak); decode tokens/s"
+UNIT = "GB/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+WORKLOADS = ("gqa_decode", "sliding_window", "prefix_sharing", "large_batch_p16", "large_batch_p1")
+DEFAULT_WORKLOAD = "gqa_decode"
+
+
+# ---------------------------------------------------------------------------
+# Workloads as host-operation scripts, replayed by the product and the oracle.
+# ---------------------------------------------------------------------------
+class Scenario:
+    def __init__(self, name, seed):
+        self.name = name
+        self.seed = seed
+        if name == "gqa_decode":
+            w = wl.gqa_decode(seed)
+        elif name == "sliding_window":
+            w = wl.sliding_window(seed)
+        elif name == "prefix_sharing":
+            w = wl.prefix_sharing(seed)
+        elif name.startswith("large_batch_p"):
+            w = wl.large_batch(seed, P=int(name[len("large_batch_p"):]))
+        else:
+            raise ValueError(f"unknown workload {name}")
+        self.w = w
+        self.ops = []           # prefill script
+        self.accumulate = True  # appends touch distinct slots until the first decode step
+        if name == "prefix_sharing":
+            x = w.extra
+            n_req = x["n_prompts"] * x["forks"]
+            self.rids = list(range(n_req))
+            self.max_requests = n_req + x["n_prompts"]
+            for i in range(x["n_prompts"]):
+                self.ops.append(("new", n_req + i))
+                self.ops.append(("append", n_req + i, x["prompt_len"], 0))
+            for f in range(n_req):
+                self.ops.append(("fork", n_req + f // x["forks"], f))
+            self.ops.append(("batch", list(range(n_req))))  # first suffix token: copy-on-write
+            for i in range(x["n_prompts"]):
+                self.ops.append(("release", n_req + i))
+            for f in range(n_req):
+                if x["suffix"][f] > 1:
+                    self.ops.append(("append", f, x["suffix"][f] - 1, 0))
+            self.lengths = [x["prompt_len"] + s for s in x["suffix"]]
+            self.accumulate = False
+        else:
+            B = len(w.lengths)
+            self.rids = list(range(B))
+            self.max_requests = B
+            self.lengths = list(w.lengths)
+            for b, L in enumerate(w.lengths):
+                self.ops.append(("new", b))
+                if w.window > 0:
+                    # the real append + trim path, in chunks of 256 rows; only
+                    # rows a later window can reach get data
+                    t = 0
+                    while t < L:
+                        n = min(256, L - t)
+                        self.ops.append(("append", b, n, max(0, L - w.window)))
+                        t += n
+                        self.ops.append(("trim", b, max(0, t + 1 - w.window)))
+                    self.accumulate = False
+                else:
+                    self.ops.append(("append", b, L, 0))
+        self.raw = w.table_mode == "raw"
+        self.max_seq_len = w.extra.get("max_seq_len") if self.raw else max(self.lengths) + 512
+        self.window = w.window
+
+
+def attention_bytes(sc, lens):
+    """Algorithmic bytes of one attention launch: attended K/V rows, q, out,
+    table entries and context lengths."""
+    w = sc.w
+    row_kv = 2 * w.Hkv * w.D * (2 if w.dtype == "bf16" else 4)
+    elem = 2 if w.dtype == "bf16" else 4
+    kv = tab = 0
+    for L in lens:
+        lo = max(0, L - w.window) if w.window > 0 else 0
+        kv += (L - lo) * row_kv
+        tab += 4 * ((L - lo) if sc.raw else (-(-L // w.P) - lo // w.P))
+    qo = 2 * len(lens) * w.Hq * w.D * elem
+    return kv + qo + tab + 4 * len(lens)
+
+
+def step_bytes(sc, lens, n_writes, n_cows, n_trim_writes):
+    w = sc.w
+    elem = 2 if w.dtype == "bf16" else 4
+    row = w.Hkv * w.D * elem
+    B = len(lens)
+    store = 4 * B * row + 4 * B  # read k and v, write them, read out_loc
+    expand = w.P if sc.raw else 1
+    tw = (n_writes + n_trim_writes) * (12 + 4 * expand)
+    copies = n_cows * w.layers * 2 * 2 * w.P * row
+    return w.layers * (attention_bytes(sc, lens) + store) + tw + copies
+
+
+# ---------------------------------------------------------------------------
+# GPU arm.
+# ---------------------------------------------------------------------------
+def _i32(xs, dev):
+    return torch.tensor(list(xs), dtype=torch.int32, device=dev)
+
+
+def build_product(sc, dev):
+    from paged_decode_attention_store_gb300.engine import PagedKVCache
+
+    w = sc.w
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    cache = PagedKVCache(w.num_pages, w.P, w.Hkv, w.D, w.layers, w.dtype, max_requests=sc.max_requests,
+                         table_mode=w.table_mode, max_seq_len=sc.max_seq_len, free_stack=w.free_order, device=dev)
+    lengths = {}
+    pend = []  # (rids, positions, slots) waiting to be stored
+
+    def flush():
+        if not pend:
+            return
+        rids = torch.cat([p[0] for p in pend])
+        pos = torch.cat([p[1] for p in pend])
+        slots = torch.cat([p[2] for p in pend])
+        step = 1 << 18
+        for layer in range(w.layers):
+            for s in range(0, rids.numel(), step):
+                k, v = wl.kv_rows(sc.seed, layer, rids[s:s + step], pos[s:s + step], w.Hkv, w.D, dtype=tdt,
+                                  device=dev)
+                cache.store(layer, k, v, slots[s:s + step].contiguous())
+        pend.clear()
+
+    def add_store(rid_list, pos_list, slots):
+        pend.append((torch.as_tensor(rid_list, dtype=torch.int64, device=dev),
+                     torch.as_tensor(pos_list, dtype=torch.int64, device=dev), slots))
+
+    for op in sc.ops:
+        kind = op[0]
+        if kind == "new":
+            cache.new(op[1])
+            lengths[op[1]] = 0
+        elif kind == "append":
+            _, rid, n, store_from = op
+            L0 = lengths[rid]
+            slots = cache.append([rid] * n)
+            lengths[rid] = L0 + n
+            first = max(store_from, L0)
+            if first < L0 + n:
+                add_store([rid] * (L0 + n - first), list(range(first, L0 + n)), slots[first - L0:])
+        elif kind == "batch":
+            rids = op[1]
+            flush()
+            slots = cache.append(rids)
+            add_store(rids, [lengths[r] for r in rids], slots)
+            for r in rids:
+                lengths[r] += 1
+        elif kind == "trim":
+            cache.trim(op[1], op[2])
+        elif kind == "fork":
+            flush()
+            cache.fork(op[1], op[2])
+            lengths[op[2]] = lengths[op[1]]
+        elif kind == "release":
+            cache.release(op[1])
+            del lengths[op[1]]
+        if not sc.accumulate:
+            flush()
+    flush()
+    torch.cuda.synchronize(dev)
+    cache.check()
+    return cache, [lengths[r] for r in sc.rids]
+
+
+class StepData:
+    """Host decisions and device inputs of one decode step, prepared up front."""
+
+
+def prepare_steps(sc, cache, lens, first_step, n_steps, dev, host_inputs=False):
+    w = sc.w
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    steps = []
+    lens = list(lens)
+    for s in range(first_step, first_step + n_steps):
+        st = StepData()
+        slots, writes, cows = cache.host.append(sc.rids)
+        st.n_writes, st.n_cows = len(writes), len(cows)
+        st.pre = None if not writes else tuple(_i32(x, dev) for x in zip(*writes))
+        st.cows = None if not cows else tuple(_i32(x, dev) for x in zip(*cows))
+        st.out_loc = _i32(slots, dev)
+        positions = list(lens)
+        lens = [L + 1 for L in lens]
+        st.lens_list = list(lens)
+        st.lens = _i32(lens, dev)
+        post = []
+        if sc.window > 0:
+            for r, L in zip(sc.rids, lens):
+                post += cache.host.trim(r, max(0, L + 1 - sc.window))
+        st.n_post = len(post)
+        st.post = None if not post else tuple(_i32(x, dev) for x in zip(*post))
+        st.q, st.k, st.v = [], [], []
+        for layer in range(w.layers):
+            q = wl.q_rows(sc.seed, s, layer, sc.rids, w.Hq, w.D, dtype=tdt, device=dev)
+            k, v = wl.kv_rows(sc.seed, layer, sc.rids, positions, w.Hkv, w.D, dtype=tdt, device=dev)
+            if host_inputs:
+                q, k, v = (x.cpu().pin_memory() for x in (q, k, v))
+            st.q.append(q)
+            st.k.append(k)
+            st.v.append(v)
+        st.bytes = step_bytes(sc, lens, st.n_writes, st.n_cows, st.n_post)
+        st.attn_bytes = attention_bytes(sc, lens)
+        steps.append(st)
+    return steps, lens
+
+
+def run_step(sc, cache, st, outs, events=None):
+    """Issue one prepared step; returns the number of kernels launched."""
+    from paged_decode_attention_store_gb300 import binding as kb
+
+    w = sc.w
+    P = w.P
+    n = 0
+    if st.pre is not None:
+        kb.page_table_write(cache.table, *st.pre, expand=P if sc.raw else 1, error_word=cache.pool.error_word)
+        n += 1
+    if st.cows is not None:
+        kb.copy_pages(cache.pool, *st.cows)
+        n += 1
+    per_attn = 3 if (w.dtype == "bf16" and w.D == 128) else 1
+    for layer in range(w.layers):
+        cache.store(layer, st.k[layer], st.v[layer], st.out_loc)
+        if events is not None:
+            kb.kvp_pool_set_timing_events(cache.pool, *events.pop())
+        cache.attend(layer, st.q[layer], st.lens, sc.window, w.scale, outs[layer])
+        n += 1 + per_attn
+    if st.post is not None:
+        kb.page_table_write(cache.table, *st.post, expand=P if sc.raw else 1, error_word=cache.pool.error_word)
+        n += 1
+    return n
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while it runs."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev_index):
+        self.proc = None
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            uuid = str(torch.cuda.get_device_properties(dev_index).uuid)
+            sel = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            sel = str(dev_index)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", sel, f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        self.proc.wait(timeout=10)
+        self.file.seek(0)
+        rows = []
+        for line in self.file.read().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != 7:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[3:]))
+            except ValueError:
+                continue
+        self.file.close()
+        os.unlink(self.file.name)
+        inside = [r for r in rows if t0 - 0.25 <= r[0] <= t1 + 0.25] or rows
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside) if inside else None,
+                "sm_max_mhz": max(r[2] for r in inside) if inside else None,
+                "reasons": reasons, "samples": len(inside)}
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def ncu_traffic(workload):
+    """DRAM bytes per launch of the attention kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    import hashlib
+
+    src = os.path.join(ROOT, "paged_decode_attention_store_gb300", "csrc", "attention_tc.cu")
+    path = os.path.join(ROOT, "profiles", f"tc_decode_kernel_{workload}.txt")
+    try:
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        vals = {}
+        for line in open(path):
+            if ":" in line:
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+        if vals.get("kernel_source_sha256_16") != digest:
+            return None
+        return float(vals["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+def run_gpu(args, rank, world, local_rank):
+    from paged_decode_attention_store_gb300 import binding as kb
+    from paged_decode_attention_store_gb300.engine import PagedKVCache  # noqa: F401  (fail loudly if missing)
+
+    kb.lib()
+    dev = torch.device(f"cuda:{local_rank}")
+    torch.cuda.set_device(dev)
+    sc = Scenario(args.workload, args.seed + rank)
+    w = sc.w
+    cache, lens = build_product(sc, dev)
+    K, W = args.steps, args.warmup
+    steps, lens_after = prepare_steps(sc, cache, lens, 1, W + K, dev)
+    tdt = cache.tdt
+    outs = [torch.empty((len(sc.rids), w.Hq, w.D), dtype=tdt, device=dev) for _ in range(w.layers)]
+
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    # soak: repeat the current state's attention ~1 s so clocks settle and get sampled
+    t_soak = time.time()
+    while time.time() - t_soak < args.soak:
+        for layer in range(w.layers):
+            cache.attend(layer, steps[0].q[layer], _i32(lens, dev), sc.window, w.scale, outs[layer])
+        torch.cuda.synchronize(dev)
+    for i in range(W):
+        run_step(sc, cache, steps[i], outs)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+
+    n_attn = K * w.layers
+    ev_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_attn)]
+    for a, b in ev_pairs:  # torch creates the CUDA event at its first record
+        a.record()
+        b.record()
+    torch.cuda.synchronize(dev)
+    pending = list(reversed(ev_pairs))
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches = 0
+    t0 = time.time()
+    start.record()
+    for i in range(W, W + K):
+        launches += run_step(sc, cache, steps[i], outs, events=pending)
+    end.record()
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    elapsed_ms = start.elapsed_time(end)
+    if world > 1:
+        torch.distributed.barrier()
+    cache.check()
+    attn_ms = [a.elapsed_time(b) for a, b in ev_pairs]
+    total_bytes = sum(st.bytes for st in steps[W:W + K])
+    attn_bytes_mean = statistics.mean(st.attn_bytes for st in steps[W:W + K])
+
+    # end to end through the driver, host buffers
+    e2e = run_e2e(args, sc, cache, lens_after, W + K + 1, dev)
+    clocks = sampler.stop(t0, t1) if sampler else None
+
+    # max over ranks of the timed region; sum of bytes and tokens
+    stats = torch.tensor([elapsed_ms, float(total_bytes), float(K * len(sc.rids)), e2e["ms"], e2e["bytes"]],
+                         dtype=torch.float64, device=dev)
+    if world > 1:
+        mx = stats.clone()
+        torch.distributed.all_reduce(mx, op=torch.distributed.ReduceOp.MAX)
+        sm = stats.clone()
+        torch.distributed.all_reduce(sm, op=torch.distributed.ReduceOp.SUM)
+        elapsed_ms, total_bytes, tokens, e2e_ms, e2e_bytes = mx[0].item(), sm[1].item(), sm[2].item(), \
+            mx[3].item(), sm[4].item()
+    else:
+        tokens, e2e_ms, e2e_bytes = float(K * len(sc.rids)), e2e["ms"], e2e["bytes"]
+    if rank != 0:
+        return None
+
+    peak, peak_kind = measured_peak()
+    value = total_bytes / (elapsed_ms * 1e-3) / 1e9
+    achieved = attn_bytes_mean / (statistics.mean(attn_ms) * 1e-3) / 1e9
+    traffic = ncu_traffic(sc.name)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": round(elapsed_ms / K, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.dtype,
+        "data": "synthetic (seeded counter-based generator; lengths from the workload's distribution)",
+        "config": {
+            "workload": sc.name,
+            "batch": len(sc.rids),
+            "q_heads": w.Hq,
+            "kv_heads": w.Hkv,
+            "head_dim": w.D,
+            "page_size": w.P,
+            "layers": w.layers,
+            "window": w.window,
+            "table": "raw token locations" if sc.raw else "block table",
+            "mean_attended_tokens": round(statistics.mean(
+                (L - (max(0, L - w.window) if w.window > 0 else 0)) for L in steps[W].lens_list), 1),
+            "kv_bytes_per_step": int(sum(
+                (L - (max(0, L - w.window) if w.window > 0 else 0)) for L in steps[W].lens_list)
+                * 2 * w.Hkv * w.D * 2 * w.layers),
+            "l2": "no flush: inputs larger than L2 (K/V read per step >> 129 MB)",
+            "seed": args.seed,
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "tokens_per_s": round(tokens / (elapsed_ms * 1e-3), 1),
+        "pct_of_peak": round(100.0 * value / peak, 2),
+        "pct_of_nominal_8tbs": round(100.0 * value / NOMINAL_HBM_GBS, 2),
+        "gpu_launches": launches,
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "tc_decode_kernel",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "peak_kind": f"{peak_kind} hbm_gbs (copy, burst)",
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
+            "traffic": traffic,
+            "algorithmic_bytes_per_launch": int(attn_bytes_mean),
+            "mean_launch_us": round(1e3 * statistics.mean(attn_ms), 2),
+            "launches_timed": len(attn_ms),
+        },
+        "e2e": {
+            "value": round(e2e_bytes / (e2e_ms * 1e-3) / 1e9, 2),
+            "unit": UNIT,
+            "tokens_per_s": round(tokens / (e2e_ms * 1e-3), 1),
+            "ms_per_step": round(e2e_ms / K, 4),
+            "h2d_bytes_per_step": e2e["h2d"],
+            "d2h_bytes_per_step": e2e["d2h"],
+        },
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(sc, args.cpu_seconds)
+    return line
+
+
+def run_e2e(args, sc, cache, lens, first_step, dev):
+    """K steps through PagedKVCache with host-resident q/k/v and outputs."""
+    w = sc.w
+    K = args.steps
+    host_steps = _host_inputs(sc, first_step, K, lens)
+    out_dev = [torch.empty((len(sc.rids), w.Hq, w.D), dtype=cache.tdt, device=dev) for _ in range(w.layers)]
+    out_host = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in out_dev]
+    lens = list(lens)
+    total_bytes = h2d = d2h = 0
+    torch.cuda.synchronize(dev)
+    cache.h2d_bytes = 0
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for s in range(K):
+        q_h, k_h, v_h = host_steps[s]
+        qd = [x.to(dev, non_blocking=True) for x in q_h]
+        kd = [x.to(dev, non_blocking=True) for x in k_h]
+        vd = [x.to(dev, non_blocking=True) for x in v_h]
+        h2d += sum(x.numel() * x.element_size() for x in q_h + k_h + v_h)
+        out_loc = cache.append(sc.rids)
+        lens = [L + 1 for L in lens]
+        lens_d = cache._to_device(lens)
+        for layer in range(w.layers):
+            cache.store(layer, kd[layer], vd[layer], out_loc)
+            cache.attend(layer, qd[layer], lens_d, sc.window, w.scale, out_dev[layer])
+            out_host[layer].copy_(out_dev[layer], non_blocking=True)
+            d2h += out_dev[layer].numel() * out_dev[layer].element_size()
+        n_post = 0
+        if sc.window > 0:
+            for r, L in zip(sc.rids, lens):
+                n_post += cache.trim(r, max(0, L + 1 - sc.window))
+        torch.cuda.current_stream(dev).synchronize()  # this step's output is on the host
+        total_bytes += step_bytes(sc, lens, cache.last_writes, cache.last_copies, n_post)
+    end.record()
+    torch.cuda.synchronize(dev)
+    cache.check()
+    h2d += cache.h2d_bytes
+    return {"ms": start.elapsed_time(end), "bytes": total_bytes, "h2d": h2d // K, "d2h": d2h // K}
+
+
+def _host_inputs(sc, first_step, K, lens):
+    """Pinned host copies of each step's q, k, v (generated on the device)."""
+    w = sc.w
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    dev = torch.device("cuda", torch.cuda.current_device())
+    out = []
+    for i, s in enumerate(range(first_step, first_step + K)):
+        positions = [L + i for L in lens]
+        qs, ks, vs = [], [], []
+        for layer in range(w.layers):
+            q = wl.q_rows(sc.seed, s, layer, sc.rids, w.Hq, w.D, dtype=tdt, device=dev)
+            k, v = wl.kv_rows(sc.seed, layer, sc.rids, positions, w.Hkv, w.D, dtype=tdt, device=dev)
+            qs.append(q.cpu().pin_memory())
+            ks.append(k.cpu().pin_memory())
+            vs.append(v.cpu().pin_memory())
+        out.append((qs, ks, vs))
+    return out
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (cpu_baseline leg and --impl reference).
+# ---------------------------------------------------------------------------
+class OracleSample:
+    """The oracle replaying the scenario's script, storing rows of ``track`` only."""
+
+    def __init__(self, sc, track):
+        import oracle.attention as OA
+        from oracle.pagetable import PageTable
+        from oracle.raw_locations import RawLocationTable
+
+        self.OA = OA
+        self.sc, w = sc, sc.w
+        self.track = set(track)
+        self.pt = PageTable(w.num_pages, w.P, free_order=w.free_order)
+        self.raw = None
+        if sc.raw:
+            self.raw = RawLocationTable(w.num_pages, w.P, sc.max_requests, sc.max_seq_len,
+                                        free_page_order=w.free_order)
+        self.stores = [OA.SlotStore() for _ in range(w.layers)]
+        self.tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+        for op in sc.ops:
+            self._op(op)
+
+    def _store(self, rid, positions, slots):
+        if rid not in self.track or not positions:
+            return
+        w = self.sc.w
+        for layer, st in enumerate(self.stores):
+            k, v = wl.kv_rows(self.sc.seed, layer, rid, positions, w.Hkv, w.D, dtype=self.tdt)
+            st.store_cache(slots, k.float().numpy(), v.float().numpy())
+
+    def _append(self, rids):
+        before = {}
+        for r in rids:
+            before.setdefault(r, self.pt.length[r])
+        res = [self.pt.append(r) for r in rids]
+        if self.raw is not None:
+            seen = []
+            for r in rids:
+                if r not in seen:
+                    seen.append(r)
+            self.raw.allocate_paged([(r, before[r], self.pt.length[r]) for r in seen])
+        for x in res:
+            if x["cow"] is not None:
+                for st in self.stores:
+                    st.copy_page(x["cow"][0], x["cow"][1], self.sc.w.P)
+        return [x["slot"] for x in res]
+
+    def _op(self, op):
+        kind = op[0]
+        if kind == "new":
+            self.pt.new(op[1])
+        elif kind == "append":
+            _, rid, n, store_from = op
+            L0 = self.pt.length[rid]
+            slots = self._append([rid] * n)
+            first = max(store_from, L0)
+            self._store(rid, list(range(first, L0 + n)), slots[first - L0:])
+        elif kind == "batch":
+            pos = [self.pt.length[r] for r in op[1]]
+            slots = self._append(op[1])
+            for r, p, s in zip(op[1], pos, slots):
+                self._store(r, [p], [s])
+        elif kind == "trim":
+            self.pt.trim(op[1], op[2])
+        elif kind == "fork":
+            self.pt.fork(op[1], op[2])
+        elif kind == "release":
+            self.pt.release(op[1])
+
+    def step(self, step_index, attend_rids):
+        """One decode step: bookkeeping for every request, store + attention for ``attend_rids``."""
+        sc, w, OA = self.sc, self.sc.w, self.OA
+        pos = [self.pt.length[r] for r in sc.rids]
+        slots = self._append(sc.rids)
+        by_rid = dict(zip(sc.rids, zip(pos, slots)))
+        outs = {}
+        for r in attend_rids:
+            p, s = by_rid[r]
+            self._store(r, [p], [s])
+        for r in attend_rids:
+            L = self.pt.length[r]
+            lo = OA.window_lo(L, sc.window)
+            for layer in range(w.layers):
+                q = wl.q_rows(sc.seed, step_index, layer, [r], w.Hq, w.D, dtype=self.tdt)[0].float().numpy()
+                if self.raw is not None:
+                    sl = OA.gather_raw(self.raw.page_table[r], lo, L)
+                else:
+                    sl = OA.gather_block(self.pt.block_row(r), w.P, lo, L)
+                outs[(r, layer)] = OA.attend_request(self.stores[layer], q, sl, w.scale)
+        if sc.window > 0:
+            for r in sc.rids:
+                self.pt.trim(r, max(0, self.pt.length[r] + 1 - sc.window))
+        return outs
+
+
+def _sample_rids(sc, n):
+    # spread the sample over the batch (first, last and evenly between)
+    B = len(sc.rids)
+    idx = sorted({int(round(i * (B - 1) / max(1, n - 1))) for i in range(n)})
+    return [sc.rids[i] for i in idx]
+
+
+def cpu_baseline(sc, seconds):
+    """The oracle, as it stands, on one host core: decode steps of a sample of
+    requests of the same workload, timed for about ``seconds``."""
+    n = 4 if sc.w.layers == 1 else 2
+    sample = _sample_rids(sc, n)
+    orc = OracleSample(sc, sample)
+    done_bytes, t_total, steps = 0, 0.0, 0
+    while t_total < seconds or steps == 0:
+        steps += 1
+        t = time.perf_counter()
+        orc.step(10_000 + steps, sample)
+        t_total += time.perf_counter() - t
+        lens = [orc.pt.length[r] for r in sample]
+        done_bytes += sc.w.layers * attention_bytes(sc, lens)
+    return {
+        "value": round(done_bytes / t_total / 1e9, 6),
+        "unit": UNIT,
+        "cores": 1,
+        "kind": "oracle",
+        "sample": f"{steps} decode steps of {len(sample)} of {len(sc.rids)} requests (all {sc.w.layers} layers); "
+                  f"bookkeeping for every request, store + float64 attention for the sample",
+        "seconds": round(t_total, 2),
+    }
+
+
+def run_reference(args):
+    """--impl reference: the CPU oracle on the same workload, metric and unit."""
+    sc = Scenario(args.workload, args.seed)
+    n = 2 if sc.w.layers == 1 else 1
+    sample = _sample_rids(sc, n)
+    orc = OracleSample(sc, sample)
+    for i in range(args.warmup):
+        orc.step(1 + i, sample)
+    t = time.perf_counter()
+    done = 0
+    for i in range(args.steps):
+        orc.step(1 + args.warmup + i, sample)
+        done += sc.w.layers * attention_bytes(sc, [orc.pt.length[r] for r in sample])
+    el = time.perf_counter() - t
+    value = done / el / 1e9
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 6),
+        "unit": UNIT,
+        "n_gpus": 0,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(1e3 * el / args.steps, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (same seeded workload as the GPU arm)",
+        "config": {"workload": sc.name, "batch": len(sc.rids), "sampled_requests": len(sample),
+                   "layers": sc.w.layers, "seed": args.seed},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{len(sample)} of {len(sc.rids)} requests per step, all layers"},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", choices=WORKLOADS, default=DEFAULT_WORKLOAD)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--soak", type=float, default=1.0, help="seconds of untimed attention before warm-up")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device(f"cuda:{local_rank}"))
+    line = run_gpu(args, rank, world, local_rank)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -184,6 +184,13 @@ int gather_indices(const kvp_pool* pool, const int32_t* table,
  * into *err (0 = none) and clear it. */
 int kvp_sync_error(const kvp_pool* pool, void* stream, int* err);
 
+/* kvp_pool_set_timing_events: measurement hook. When both events are
+ * non-NULL (cudaEvent_t, caller-owned), the next paged_decode_attention call
+ * on this pool records ``before`` on its stream just before its main
+ * attention kernel and ``after`` just after it, then forgets them; NULL
+ * clears the hook. No effect on results. */
+int kvp_pool_set_timing_events(kvp_pool* pool, void* before, void* after);
+
 /* ========================================================================
  * Host bookkeeping (pure host C++; no CUDA). Chapter 15, section "The
  * model", restated: LIFO free list, reference counts, block tables indexed

@@ -48,6 +48,7 @@ SIGNATURES = {
     "paged_decode_attention": [_vp, _i, _vp, _i, _i, _vp, _i, _i, _i, _vp, _vp, _i, _f, _vp, _vp, _sz, _vp],
     "gather_indices": [_vp, _vp, _i, _i, _i, _vp, _vp, _i, _i, _vp, _i, _vp],
     "kvp_sync_error": [_vp, _vp, _ip],
+    "kvp_pool_set_timing_events": [_vp, _vp, _vp],
     "kvp_host_create": [_i, _i, _i, _vp, ctypes.POINTER(_vp)],
     "kvp_host_destroy": [_vp],
     "kvp_host_new": [_vp, _i],
@@ -223,6 +224,13 @@ def gather_indices(pool, table, table_mode, context_lens, window, slots_out, tab
     _check(lib().gather_indices(pool.handle, _ptr(table), table.shape[0], table.shape[1], table_mode,
                                 _ptr(table_rows), _ptr(context_lens), B, int(window or 0), _ptr(slots_out),
                                 slots_out.shape[1], _stream(stream)), "gather_indices")
+
+
+def kvp_pool_set_timing_events(pool, before=None, after=None):
+    """Record ``before``/``after`` (torch.cuda.Event) around the next attention kernel."""
+    b = None if before is None else ctypes.c_void_p(before.cuda_event)
+    a = None if after is None else ctypes.c_void_p(after.cuda_event)
+    _check(lib().kvp_pool_set_timing_events(pool.handle, b, a), "kvp_pool_set_timing_events")
 
 
 def kvp_sync_error(pool, stream=None):

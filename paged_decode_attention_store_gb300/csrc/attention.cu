@@ -404,7 +404,14 @@ extern "C" int paged_decode_attention(const kvp_pool* pool, int layer, const voi
     ta.part_ml = reinterpret_cast<float*>(ws + L.part_ml);
     ta.part_o = reinterpret_cast<float*>(ws + L.part_o);
     ta.err = pool->err;
+    kvp_pool* mp = const_cast<kvp_pool*>(pool);
+    const bool timed = mp->ev_before != nullptr;
+    if (timed && cudaEventRecord(static_cast<cudaEvent_t>(mp->ev_before), st) != cudaSuccess) return KVP_ERR_CUDA;
     if (launch_tc(ta, pool->num_sms, st) != cudaSuccess) return KVP_ERR_CUDA;
+    if (timed) {
+      if (cudaEventRecord(static_cast<cudaEvent_t>(mp->ev_after), st) != cudaSuccess) return KVP_ERR_CUDA;
+      mp->ev_before = mp->ev_after = nullptr;
+    }
 
     CombineArgs ca;
     ca.req = reinterpret_cast<const ReqInfo*>(ws + L.req);
@@ -440,10 +447,17 @@ extern "C" int paged_decode_attention(const kvp_pool* pool, int layer, const voi
   ga.err = pool->err;
   const long long warps = (long long)batch * num_q_heads;
   const unsigned blocks = (unsigned)((warps + kGenWarps - 1) / kGenWarps);
+  kvp_pool* mp = const_cast<kvp_pool*>(pool);
+  const bool timed = mp->ev_before != nullptr;
+  if (timed && cudaEventRecord(static_cast<cudaEvent_t>(mp->ev_before), st) != cudaSuccess) return KVP_ERR_CUDA;
   if (pool->dtype == KVP_F32)
     generic_decode_kernel<float><<<blocks, 32 * kGenWarps, 0, st>>>(ga);
   else
     generic_decode_kernel<__nv_bfloat16><<<blocks, 32 * kGenWarps, 0, st>>>(ga);
+  if (timed) {
+    if (cudaEventRecord(static_cast<cudaEvent_t>(mp->ev_after), st) != cudaSuccess) return KVP_ERR_CUDA;
+    mp->ev_before = mp->ev_after = nullptr;
+  }
   return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
 }
 

@@ -36,6 +36,8 @@ extern "C" int kv_pool_create(int num_pages, int page_size, int kv_heads, int he
   p->err = error_word;
   p->num_sms = sms;
   p->device = dev;
+  p->ev_before = nullptr;
+  p->ev_after = nullptr;
   *out = p;
   return KVP_OK;
 }
@@ -56,5 +58,12 @@ extern "C" int kvp_sync_error(const kvp_pool* pool, void* stream, int* err) {
     if (cudaStreamSynchronize(st) != cudaSuccess) return KVP_ERR_CUDA;
   }
   *err = h;
+  return KVP_OK;
+}
+
+extern "C" int kvp_pool_set_timing_events(kvp_pool* pool, void* before, void* after) {
+  if (!pool || (before == nullptr) != (after == nullptr)) return KVP_ERR_INVALID_ARG;
+  pool->ev_before = before;
+  pool->ev_after = after;
   return KVP_OK;
 }

@@ -23,6 +23,8 @@ struct kvp_pool {
   int32_t* err;
   int num_sms;
   int device;
+  void* ev_before;  // optional timing events around the next attention kernel
+  void* ev_after;
 };
 
 namespace kvp {
