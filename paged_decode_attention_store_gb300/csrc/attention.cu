@@ -1,176 +1,10 @@
-// Decode attention: work plan, split-K combine, the general CUDA-core kernel,
-// the index dump, and the C ABI that picks between the kernels.
-//
-// Split-K plan (the flash-decoding idea, sized for a persistent grid): the
-// attended positions of all requests are laid end to end in one token stream
-// and the stream is cut into one equal range per CTA, so every CTA streams
-// the same number of K/V bytes whatever the length mix. A request that falls
-// inside one range is finished by that CTA; a request cut by range
-// boundaries leaves one fp32 partial per piece, merged by the combine kernel
-// with the usual rescaling: M = max m_i, out = sum 2^(m_i-M) o_i / sum
-// 2^(m_i-M) l_i (pieces with no token have m_i = -inf and weight 0).
+// Decode attention: the general CUDA-core kernel, the index dump, and the C
+// ABI that picks between it and the tensor-core kernel (attention_tc.cu).
 #include "attention.cuh"
 
 namespace kvp {
 
 namespace {
-
-constexpr int kPlanThreads = 1024;
-constexpr int kMinTokensPerCta = 64;
-
-// Exclusive scan of one value per thread over a 1024-thread block.
-__device__ long long block_exclusive_scan(long long x, long long* total) {
-  __shared__ long long warp_sums[32];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  long long incl = x;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    long long y = __shfl_up_sync(0xffffffffu, incl, d);
-    if (lane >= d) incl += y;
-  }
-  if (lane == 31) warp_sums[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    const int nw = blockDim.x >> 5;
-    long long v = lane < nw ? warp_sums[lane] : 0;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      long long y = __shfl_up_sync(0xffffffffu, v, d);
-      if (lane >= d) v += y;
-    }
-    if (lane < nw) warp_sums[lane] = v;  // inclusive over warps
-  }
-  __syncthreads();
-  const long long before = (warp > 0 ? warp_sums[warp - 1] : 0) + incl - x;
-  *total = warp_sums[(blockDim.x >> 5) - 1];
-  __syncthreads();
-  return before;
-}
-
-__device__ __forceinline__ long long ceil_div_ll(long long a, long long b) { return (a + b - 1) / b; }
-
-__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs p) {
-  int* cta_first = reinterpret_cast<int*>(p.ws + p.L.cta_first);
-  ReqInfo* req = reinterpret_cast<ReqInfo*>(p.ws + p.L.req);
-  int* nv = reinterpret_cast<int*>(p.ws + p.L.nv);
-  long long* sv = reinterpret_cast<long long*>(p.ws + p.L.sv);
-  WorkItem* items = reinterpret_cast<WorkItem*>(p.ws + p.L.items);
-
-  const int V = p.B * p.n_groups;
-  const int per = (V + kPlanThreads - 1) / kPlanThreads;
-  const int v0 = min(V, (int)threadIdx.x * per), v1 = min(V, v0 + per);
-  const long long cap = table_capacity(p.T);
-
-  // Phase 1: attended positions per virtual request, stream offsets.
-  long long local = 0;
-  for (int v = v0; v < v1; ++v) {
-    const int b = v / p.n_groups;
-    const int L = p.context_lens[b];
-    const int row = p.table_rows ? p.table_rows[b] : b;
-    const bool valid = L >= 1 && L <= cap && row >= 0 && row < p.T.rows_total;
-    if (!valid && (v % p.n_groups) == 0) set_error(p.err, KVP_ERR_BAD_INDEX);
-    const int n = valid ? L - window_lo(L, p.window) : 0;
-    nv[v] = n;
-    local += n;
-  }
-  long long T;
-  long long base = block_exclusive_scan(local, &T);
-  for (int v = v0; v < v1; ++v) {
-    sv[v] = base;
-    base += nv[v];
-  }
-  const long long Ne = T > 0 ? min((long long)p.num_ctas, ceil_div_ll(T, kMinTokensPerCta)) : 0;
-
-  // Phase 2: items per virtual request (1 + CTA boundaries strictly inside it).
-  local = 0;
-  for (int v = v0; v < v1; ++v) {
-    const long long n = nv[v], S = sv[v];
-    if (n == 0) continue;
-    const long long k_lo = ceil_div_ll((S + 1) * Ne, T);
-    const long long k_hi = ceil_div_ll((S + n) * Ne, T) - 1;
-    local += 1 + max(0LL, k_hi - k_lo + 1);
-  }
-  long long n_items;
-  long long first = block_exclusive_scan(local, &n_items);
-  for (int v = v0; v < v1; ++v) {
-    const long long n = nv[v], S = sv[v];
-    const int b = v / p.n_groups, grp = v % p.n_groups;
-    if (n == 0) {
-      req[v] = ReqInfo{(int)first, 0};
-      continue;
-    }
-    const int L = p.context_lens[b];
-    const int lo = window_lo(L, p.window);
-    const int row = p.table_rows ? p.table_rows[b] : b;
-    const long long k_lo = ceil_div_ll((S + 1) * Ne, T);
-    const long long k_hi = ceil_div_ll((S + n) * Ne, T) - 1;
-    const long long kz = ceil_div_ll(S * Ne, T);
-    const int cnt = 1 + (int)max(0LL, k_hi - k_lo + 1);
-    req[v] = ReqInfo{(int)first, cnt};
-    for (long long k = kz; k < k_lo; ++k) cta_first[k] = (int)first;  // ranges that start at S
-    long long seg_start = S;
-    for (int j = 0; j < cnt; ++j) {
-      const long long k = k_lo + j;  // boundary ending segment j
-      const long long seg_end = (j == cnt - 1) ? S + n : (k * T) / Ne;
-      WorkItem w;
-      w.v = v;
-      w.b = b;
-      w.row = row;
-      w.group = grp;
-      w.t_begin = lo + (int)(seg_start - S);
-      w.t_end = lo + (int)(seg_end - S);
-      w.part = cnt > 1 ? (int)(first + j) : -1;
-      w.pad = 0;
-      items[first + j] = w;
-      if (j > 0) cta_first[k_lo + j - 1] = (int)(first + j);
-      seg_start = seg_end;
-    }
-    first += cnt;
-  }
-  for (long long k = Ne + threadIdx.x; k <= p.num_ctas; k += blockDim.x) cta_first[k] = (int)n_items;
-}
-
-// One warp per (virtual request, query head of its group).
-__global__ void combine_kernel(const CombineArgs a) {
-  const long long wid = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (wid >= (long long)a.V * a.QH) return;
-  const int v = (int)(wid / a.QH), qhl = (int)(wid % a.QH);
-  const ReqInfo r = a.req[v];
-  if (r.count == 1) return;  // finished by the attention kernel
-  const int b = v / a.n_groups, grp = v % a.n_groups;
-  const size_t orow = ((size_t)b * a.Hq + (size_t)grp * a.QH + qhl) * a.D;
-  float M = -INFINITY;
-  for (int i = 0; i < r.count; ++i) M = fmaxf(M, a.part_ml[((size_t)(r.first + i) * a.QH + qhl) * 2]);
-  for (int d0 = lane * 4; d0 < a.D; d0 += 128) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float Ls = 0.f;
-    for (int i = 0; i < r.count; ++i) {
-      const size_t pi = (size_t)(r.first + i) * a.QH + qhl;
-      const float mi = a.part_ml[pi * 2], li = a.part_ml[pi * 2 + 1];
-      const float wgt = (mi == -INFINITY) ? 0.f : exp2f(mi - M);
-      Ls += wgt * li;
-      const float4 o = *reinterpret_cast<const float4*>(a.part_o + pi * a.D + d0);
-      acc.x += wgt * o.x;
-      acc.y += wgt * o.y;
-      acc.z += wgt * o.z;
-      acc.w += wgt * o.w;
-    }
-    const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-    if (a.dtype == KVP_BF16) {
-      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + orow + d0;
-      __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-      __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-      uint2 packed;
-      packed.x = *reinterpret_cast<uint32_t*>(&lo2);
-      packed.y = *reinterpret_cast<uint32_t*>(&hi2);
-      *reinterpret_cast<uint2*>(out) = packed;
-    } else {
-      float* out = static_cast<float*>(a.out) + orow + d0;
-      *reinterpret_cast<float4*>(out) = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-    }
-  }
-}
 
 // ---------------------------------------------------------------------------
 // General kernel (any dtype, head_dim <= 256, any group size): one warp per
@@ -301,7 +135,7 @@ __global__ void gather_indices_kernel(TableRef T, const int32_t* context_lens, c
   }
 }
 
-bool tc_eligible(const kvp_pool* pool, int Hq, int* HG_out) {
+bool tc_eligible(const kvp_pool* pool, int Hq, int B, int* HG_out) {
   if (pool->dtype != KVP_BF16 || pool->head_dim != 128) return false;
   const int Hkv = pool->kv_heads;
   if (Hq % Hkv) return false;
@@ -310,6 +144,7 @@ bool tc_eligible(const kvp_pool* pool, int Hq, int* HG_out) {
   for (int HG = 8; HG >= 1; --HG) {
     if (Hkv % HG) continue;
     if (tc_smem_bytes(HG, G) == 0) continue;
+    if (B > tc_max_batch(HG)) return false;
     *HG_out = HG;
     return true;
   }
@@ -338,13 +173,12 @@ extern "C" int paged_decode_attention_workspace_size(const kvp_pool* pool, int b
                                                      size_t* bytes) {
   if (!pool || !bytes || batch <= 0 || num_q_heads <= 0) return KVP_ERR_INVALID_ARG;
   int HG = 0;
-  if (!tc_eligible(pool, num_q_heads, &HG)) {
+  if (!tc_eligible(pool, num_q_heads, batch, &HG)) {
     *bytes = 256;  // the general kernel needs no scratch
     return KVP_OK;
   }
-  const int n_groups = pool->kv_heads / HG;
   const int QH = HG * (num_q_heads / pool->kv_heads);
-  *bytes = ws_layout(batch * n_groups, pool->num_sms, QH, 128).total;
+  *bytes = ws_layout(pool->num_sms, QH, 128).total;
   return KVP_OK;
 }
 
@@ -365,28 +199,15 @@ extern "C" int paged_decode_attention(const kvp_pool* pool, int layer, const voi
   const float scale_log2 = scale * 1.4426950408889634f;
 
   int HG = 0;
-  if (tc_eligible(pool, num_q_heads, &HG)) {
+  kvp_pool* mp = const_cast<kvp_pool*>(pool);
+  if (tc_eligible(pool, num_q_heads, batch, &HG)) {
     if (reinterpret_cast<uintptr_t>(q) & 15) return KVP_ERR_INVALID_ARG;
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255)) return KVP_ERR_INVALID_ARG;
     const int G = num_q_heads / pool->kv_heads;
-    const int n_groups = pool->kv_heads / HG;
     const int QH = HG * G;
-    const WsLayout L = ws_layout(batch * n_groups, pool->num_sms, QH, 128);
+    const WsLayout L = ws_layout(pool->num_sms, QH, 128);
     if (workspace_bytes < L.total) return KVP_ERR_INVALID_ARG;
     char* ws = static_cast<char*>(workspace);
-
-    PlanArgs pa;
-    pa.T = T;
-    pa.context_lens = context_lens;
-    pa.table_rows = table_rows;
-    pa.B = batch;
-    pa.n_groups = n_groups;
-    pa.window = window;
-    pa.num_ctas = pool->num_sms;
-    pa.ws = ws;
-    pa.L = L;
-    pa.err = pool->err;
-    plan_kernel<<<1, kPlanThreads, 0, st>>>(pa);
 
     TcArgs ta;
     ta.T = T;
@@ -395,38 +216,34 @@ extern "C" int paged_decode_attention(const kvp_pool* pool, int layer, const voi
     ta.row_bytes = pool->row_bytes;
     ta.q = static_cast<const __nv_bfloat16*>(q);
     ta.out = static_cast<__nv_bfloat16*>(out);
+    ta.context_lens = context_lens;
+    ta.table_rows = table_rows;
+    ta.B = batch;
     ta.Hq = num_q_heads;
     ta.G = G;
     ta.HG = HG;
+    ta.n_groups = pool->kv_heads / HG;
+    ta.window = window;
+    ta.num_ctas = pool->num_sms;
     ta.scale_log2 = scale_log2;
-    ta.cta_first = reinterpret_cast<const int*>(ws + L.cta_first);
-    ta.items = reinterpret_cast<const WorkItem*>(ws + L.items);
+    ta.merge = reinterpret_cast<int4*>(ws + L.merge);
     ta.part_ml = reinterpret_cast<float*>(ws + L.part_ml);
     ta.part_o = reinterpret_cast<float*>(ws + L.part_o);
     ta.err = pool->err;
-    kvp_pool* mp = const_cast<kvp_pool*>(pool);
-    const bool timed = mp->ev_before != nullptr;
-    if (timed && cudaEventRecord(static_cast<cudaEvent_t>(mp->ev_before), st) != cudaSuccess) return KVP_ERR_CUDA;
-    if (launch_tc(ta, pool->num_sms, st) != cudaSuccess) return KVP_ERR_CUDA;
-    if (timed) {
-      if (cudaEventRecord(static_cast<cudaEvent_t>(mp->ev_after), st) != cudaSuccess) return KVP_ERR_CUDA;
-      mp->ev_before = mp->ev_after = nullptr;
-    }
 
     CombineArgs ca;
-    ca.req = reinterpret_cast<const ReqInfo*>(ws + L.req);
+    ca.merge = ta.merge;
     ca.part_ml = ta.part_ml;
     ca.part_o = ta.part_o;
     ca.out = out;
     ca.dtype = pool->dtype;
-    ca.V = batch * n_groups;
-    ca.n_groups = n_groups;
+    ca.n_groups = ta.n_groups;
     ca.QH = QH;
     ca.Hq = num_q_heads;
     ca.D = 128;
-    const long long warps = (long long)ca.V * QH;
-    combine_kernel<<<(unsigned)((warps * 32 + 255) / 256), 256, 0, st>>>(ca);
-    return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
+    const cudaError_t e = launch_tc(ta, ca, st, mp->ev_before, mp->ev_after);
+    mp->ev_before = mp->ev_after = nullptr;
+    return e == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
   }
 
   if (pool->head_dim > kGenMaxD) return KVP_ERR_INVALID_ARG;
@@ -447,7 +264,6 @@ extern "C" int paged_decode_attention(const kvp_pool* pool, int layer, const voi
   ga.err = pool->err;
   const long long warps = (long long)batch * num_q_heads;
   const unsigned blocks = (unsigned)((warps + kGenWarps - 1) / kGenWarps);
-  kvp_pool* mp = const_cast<kvp_pool*>(pool);
   const bool timed = mp->ev_before != nullptr;
   if (timed && cudaEventRecord(static_cast<cudaEvent_t>(mp->ev_before), st) != cudaSuccess) return KVP_ERR_CUDA;
   if (pool->dtype == KVP_F32)

@@ -5,98 +5,112 @@
 
 namespace kvp {
 
-// A virtual request is one (request b, KV-head group g) pair: v = b * n_groups + g.
-// Its attended positions [lo, L) form one segment of a token stream that
-// concatenates all virtual requests; the stream is cut into one equal range
-// per CTA, and a work item is the intersection of a range with a request.
-struct __align__(16) WorkItem {
-  int v;        // virtual request
-  int b;        // request
-  int row;      // table row of the request
-  int group;    // KV-head group
-  int t_begin;  // first position of this item
-  int t_end;    // one past its last position
-  int part;     // partial slot (the item index) when the request is split, else -1
-  int pad;
-};
-
-struct ReqInfo {
-  int first;  // first item of the virtual request
-  int count;  // its number of items: 0 invalid (zero output), 1 direct, >1 combined
-};
+// Work split. A virtual request is one (request b, KV-head group g) pair,
+// v = b * n_groups + g. The attended positions [lo, L) of all virtual
+// requests are laid end to end in one token stream of T positions; CTA k of
+// Ne takes the range [k*T/Ne, (k+1)*T/Ne), so every CTA streams the same
+// number of K/V bytes whatever the length mix. A request cut by a range
+// boundary leaves one fp32 partial per piece in a fixed slot: the first piece
+// of CTA k (it starts at the range start) uses slot 2k, its last piece slot
+// 2k+1. The CTA that holds a split request's final piece records the request
+// in merge[k] = {v, k_first, slot_first, k}; the combine kernel merges the
+// pieces: slot_first, then 2j for k_first < j <= k.
 
 // Workspace layout (offsets in bytes from the 256-byte aligned base).
 struct WsLayout {
-  size_t cta_first;  // int[num_ctas + 1]
-  size_t req;        // ReqInfo[V]
-  size_t nv;         // int[V]    attended positions per virtual request
-  size_t sv;         // long long[V] stream offset per virtual request
-  size_t items;      // WorkItem[cap]
-  size_t part_ml;    // float[cap * QH * 2]  (running max in log2 units, sum)
-  size_t part_o;     // float[cap * QH * D]  (unnormalised output)
+  size_t merge;    // int4[num_ctas]
+  size_t part_ml;  // float[2 * num_ctas * QH * 2]  (running max in log2 units, sum)
+  size_t part_o;   // float[2 * num_ctas * QH * D]  (unnormalised output)
   size_t total;
-  int cap;           // maximum number of items
 };
 
 __host__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-__host__ inline WsLayout ws_layout(int V, int num_ctas, int QH, int D) {
+__host__ inline WsLayout ws_layout(int num_ctas, int QH, int D) {
   WsLayout w;
-  w.cap = V + num_ctas + 1;
   size_t o = 0;
-  w.cta_first = o; o = align256(o + sizeof(int) * (num_ctas + 1));
-  w.req = o;       o = align256(o + sizeof(ReqInfo) * V);
-  w.nv = o;        o = align256(o + sizeof(int) * V);
-  w.sv = o;        o = align256(o + sizeof(long long) * V);
-  w.items = o;     o = align256(o + sizeof(WorkItem) * w.cap);
-  w.part_ml = o;   o = align256(o + sizeof(float) * 2 * (size_t)w.cap * QH);
-  w.part_o = o;    o = align256(o + sizeof(float) * (size_t)w.cap * QH * D);
+  w.merge = o;
+  o = align256(o + sizeof(int4) * num_ctas);
+  w.part_ml = o;
+  o = align256(o + sizeof(float) * 2 * 2 * (size_t)num_ctas * QH);
+  w.part_o = o;
+  o = align256(o + sizeof(float) * 2 * (size_t)num_ctas * QH * D);
   w.total = o;
   return w;
 }
 
-struct PlanArgs {
-  TableRef T;
-  const int32_t* context_lens;
-  const int32_t* table_rows;
-  int B;
-  int n_groups;
-  int window;
-  int num_ctas;
-  char* ws;
-  WsLayout L;
-  int32_t* err;
-};
-
 struct TcArgs {
   TableRef T;
-  const char* kv_layer;     // K of this layer
-  size_t kv_bytes;          // K -> V distance
-  size_t row_bytes;         // one token, all KV heads
-  const __nv_bfloat16* q;   // [B, Hq, D]
-  __nv_bfloat16* out;       // [B, Hq, D]
-  int Hq, G, HG;            // q heads, group size, KV heads per CTA
+  const char* kv_layer;    // K of this layer
+  size_t kv_bytes;         // K -> V distance
+  size_t row_bytes;        // one token, all KV heads
+  const __nv_bfloat16* q;  // [B, Hq, D]
+  __nv_bfloat16* out;      // [B, Hq, D]
+  const int32_t* context_lens;
+  const int32_t* table_rows;
+  int B, Hq, G, HG, n_groups, window, num_ctas;
   float scale_log2;
-  const int* cta_first;
-  const WorkItem* items;
+  int4* merge;
   float* part_ml;
   float* part_o;
   int32_t* err;
 };
 
 struct CombineArgs {
-  const ReqInfo* req;
+  const int4* merge;
   const float* part_ml;
   const float* part_o;
   void* out;
   int dtype;
-  int V, n_groups, QH, Hq, D;
+  int n_groups, QH, Hq, D;
 };
+
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialization attribute may start while its predecessor in the
+// stream is still running; griddep_wait() blocks until that predecessor has
+// completed and its memory is visible. Every kernel here waits before its
+// first global access, so the overlap only hides launch latency.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Exclusive scan of one value per thread over the whole block (at most 32
+// warps); *total receives the sum. Contains __syncthreads.
+__device__ __forceinline__ long long block_exclusive_scan(long long x, long long* total) {
+  __shared__ long long warp_sums[32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+  long long incl = x;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const long long y = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += y;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    long long v = lane < nw ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, v, d);
+      if (lane >= d) v += y;
+    }
+    if (lane < nw) warp_sums[lane] = v;  // inclusive over warps
+  }
+  __syncthreads();
+  const long long before = (warp > 0 ? warp_sums[warp - 1] : 0) + incl - x;
+  *total = warp_sums[nw - 1];
+  __syncthreads();
+  return before;
+}
 
 // Shared-memory bytes of the tensor-core kernel for HG KV heads per CTA and
 // G query heads per KV head (0 if it does not fit).
 size_t tc_smem_bytes(int HG, int G);
-// Launch the bf16, head_dim-128 kernel (NT = 1 for G <= 8, 2 for G <= 16).
-cudaError_t launch_tc(const TcArgs& a, int num_ctas, cudaStream_t stream);
+// Largest batch the in-kernel work split can take for HG.
+int tc_max_batch(int HG);
+// Launch the bf16, head_dim-128 kernel (one CTA per SM) and the combine
+// kernel after it, both as programmatic dependents.
+cudaError_t launch_tc(const TcArgs& a, const CombineArgs& c, cudaStream_t stream, void* ev_before, void* ev_after);
 
 }  // namespace kvp

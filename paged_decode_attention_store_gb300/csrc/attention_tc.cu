@@ -11,11 +11,14 @@
 // How (GB300 design):
 // * The path is HBM-bound (G flop per byte of K/V), so the kernel is built to
 //   keep bytes in flight: one CTA per SM, persistent over an equal share of
-//   the batch's attended tokens (see the plan kernel), one PRODUCER warp that
-//   issues one cp.async.bulk per token row (all KV heads of the group,
-//   HG*256 contiguous bytes, K and V) into a 3-stage ring of 16-token stages
-//   completed by mbarrier transaction counts, and HG CONSUMER warps, one per
-//   KV head.
+//   the batch's attended tokens, two PRODUCER warps that issue one
+//   cp.async.bulk per token row (all KV heads of the group, HG*256 contiguous
+//   bytes, K and V) into a 3-stage ring of 16-token stages completed by
+//   mbarrier transaction counts, and HG CONSUMER warps, one per KV head.
+//   The producers take alternate stages: the copy engine drains one
+//   producer's 32 row copies while the other does its bookkeeping, so it
+//   never waits for work (one producer alone left it idle part of every
+//   stage, which capped the stream below the DRAM rate).
 // * Rows land at a pitch of HG*256+16 bytes, so the 8 rows an ldmatrix reads
 //   fall in 8 different 16-byte bank groups.
 // * Each consumer warp runs the GQA group of its KV head on the legacy
@@ -31,9 +34,14 @@
 // * Online softmax in log2 units with warp-shuffle reductions over the
 //   token rows; P is rounded to bf16 for the MMA and the row sum is taken of
 //   the rounded values so numerator and denominator agree.
-// * An item that covers a whole request writes the final bf16 output; a
-//   request split across CTAs writes fp32 partials (max, sum, unnormalised
-//   output) for the combine kernel (split-K, flash-decoding style).
+// * Work split without a separate planning kernel: every CTA reads the
+//   batch's context lengths, scans them in shared memory and takes an equal
+//   share of the attended tokens (see attention.cuh); the producer then walks
+//   the requests of its share. A request that ends inside the share writes
+//   the final bf16 output; a request cut by a share boundary writes fp32
+//   partials (max, sum, unnormalised output) that the combine kernel merges
+//   (split-K, flash-decoding style). Both kernels are programmatic dependent
+//   launches, so their launch latency hides behind the preceding kernel.
 // * Every wait is bounded (2 s); on timeout the CTA records KVP_ERR_TIMEOUT,
 //   raises its abort flag, waits (bounded) for its own copies and returns.
 #include "attention.cuh"
@@ -44,20 +52,45 @@ namespace {
 
 constexpr int kTok = 16;      // tokens per stage (the MMA M dimension)
 constexpr int kStages = 3;    // ring depth
+constexpr int kProducers = 2; // producer warps, alternate stages
+constexpr int kAhead = 2;     // own stages whose table entries are fetched ahead of issue
+constexpr int kQueue = 4;     // entry-queue slots per producer (> kAhead)
 constexpr int kD = 128;       // head_dim
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr int kMinTokensPerCta = 64;
+constexpr int kStaticSmemBound = 512;                      // PlanState + the scan's warp sums
+constexpr int kMaxDynamicSmem = 232448 - kStaticSmemBound;  // per-block opt-in limit minus static
 
+// Stage header, written by the producer, read by the consumers.
 struct __align__(16) StageHdr {
-  int item;    // work item index, -1 = end of work
+  int live;    // 1: a stage of a piece, 0: no more work
   int t0;      // first position of the stage
   int vmask;   // bit j: token t0+j has K/V rows in the stage
-  int flags;   // 1 first stage of the item, 2 last stage, (qbuf << 2)
+  int flags;   // 1 first stage of the piece, 2 last stage, (qbuf << 2)
+  int b;       // request
+  int group;   // KV-head group
+  int part;    // partial slot of a split piece, -1 when the piece is the whole request
+  int pad;
+};
+
+// What the producer's lookahead cursor records for a stage it has queued.
+struct __align__(16) StageMeta {
+  int live;    // 0: no more work; t0 then holds the number of stages of the CTA
+  int t0;
+  int t_end;   // end of the piece
+  int flags;   // 1 first stage of the piece, 2 last stage
+  int b;
+  int group;
+  int part;
+  int piece;   // index of the piece within the CTA (selects the Q buffer)
 };
 
 struct SmemMap {
   int pitch, stage_bytes, qbytes;
   unsigned char* stages;
   unsigned char* qbuf;
+  StageMeta* meta;     // [kProducers][kQueue]
+  int* entries;        // [kProducers][kQueue][kTok] table entries of queued stages
   StageHdr* hdr;
   uint64_t* full;
   uint64_t* empty;
@@ -72,17 +105,14 @@ __device__ __forceinline__ SmemMap map_smem(unsigned char* smem, int HG, int G) 
   s.qbytes = HG * G * kD * 2;
   s.stages = smem;
   s.qbuf = smem + kStages * s.stage_bytes;
-  s.hdr = reinterpret_cast<StageHdr*>(s.qbuf + 2 * s.qbytes);
+  s.meta = reinterpret_cast<StageMeta*>(s.qbuf + 2 * s.qbytes);
+  s.entries = reinterpret_cast<int*>(s.meta + kProducers * kQueue);
+  s.hdr = reinterpret_cast<StageHdr*>(s.entries + kProducers * kQueue * kTok);
   s.full = reinterpret_cast<uint64_t*>(s.hdr + kStages);
   s.empty = s.full + kStages;
   s.qempty = s.empty + kStages;
   s.abort_flag = reinterpret_cast<volatile int*>(s.qempty + 2);
   return s;
-}
-
-__device__ __forceinline__ int load_entry(const TableRef& T, int row, int t) {
-  const int32_t* r = T.table + (size_t)row * T.cols;
-  return __ldg(r + (T.raw ? t : t / T.page_size));
 }
 
 __device__ __forceinline__ int entry_to_slot(const TableRef& T, int e, int t, int32_t* err) {
@@ -100,103 +130,314 @@ __device__ __forceinline__ int entry_to_slot(const TableRef& T, int e, int t, in
   return e * T.page_size + t % T.page_size;
 }
 
+// Attended positions of a request (0 when its length or table row is invalid).
+__device__ __forceinline__ int attended(const TcArgs& a, int L, int row, long long cap, int* lo) {
+  const bool valid = L >= 1 && L <= cap && row >= 0 && row < a.T.rows_total;
+  *lo = valid ? window_lo(L, a.window) : 0;
+  return valid ? L - *lo : 0;
+}
+
+// ---------------------------------------------------------------------------
+// Work split of this CTA (see attention.cuh), computed by the whole CTA with
+// the stage buffers as scratch: n_b in shared ints, their exclusive prefix
+// sums in shared 64-bit ints.
+// ---------------------------------------------------------------------------
+struct PlanState {
+  long long R0, R1;  // this CTA's share of the token stream
+  long long Sv0;     // stream start of the first virtual request in the share
+  int active;        // the share is not empty
+  int b0, g0;        // first request and group of the share
+  int L0, row0;      // its context length and table row
+  int merge_v, merge_ka, merge_sa;  // split request whose final piece is here
+};
+
+// Scratch of the plan, in the stage buffers: per request n, L, row (ints)
+// and the exclusive prefix of n (64-bit).
+constexpr int kPlanScratchPerRequest = 20;
+
+__device__ void plan_cta(const TcArgs& a, const SmemMap& s, PlanState* ps) {
+  long long* sS = reinterpret_cast<long long*>(s.stages);
+  int* sN = reinterpret_cast<int*>(sS + a.B);
+  int* sL = sN + a.B;
+  int* sR = sL + a.B;
+  const long long cap = table_capacity(a.T);
+  for (int b = threadIdx.x; b < a.B; b += blockDim.x) {
+    const int L = __ldg(a.context_lens + b);
+    const int row = a.table_rows ? __ldg(a.table_rows + b) : b;
+    int lo;
+    const int n = attended(a, L, row, cap, &lo);
+    sN[b] = n;
+    sL[b] = L;
+    sR[b] = row;
+    if (n == 0 && blockIdx.x == 0) set_error(a.err, KVP_ERR_BAD_INDEX);
+  }
+  __syncthreads();
+  const int per = (a.B + blockDim.x - 1) / blockDim.x;
+  const int b0 = min(a.B, (int)threadIdx.x * per), b1 = min(a.B, b0 + per);
+  long long local = 0;
+  for (int b = b0; b < b1; ++b) local += sN[b];
+  long long total;
+  long long base = block_exclusive_scan(local, &total);
+  for (int b = b0; b < b1; ++b) {
+    sS[b] = base;
+    base += sN[b];
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const long long T = total * a.n_groups;
+    const long long Ne = T > 0 ? min((long long)a.num_ctas, (T + kMinTokensPerCta - 1) / kMinTokensPerCta) : 0;
+    const long long k = blockIdx.x;
+    ps->active = k < Ne;
+    ps->merge_v = -1;
+    ps->merge_ka = ps->merge_sa = 0;
+    if (k < Ne) {
+      const long long R0 = k * T / Ne, R1 = (k + 1) * T / Ne;
+      int lo = 0, hi = a.B - 1;  // first request whose stream range ends after R0
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if ((long long)a.n_groups * (sS[mid] + sN[mid]) > R0)
+          hi = mid;
+        else
+          lo = mid + 1;
+      }
+      const int b = lo;
+      const long long nb = sN[b];
+      const long long base_b = (long long)a.n_groups * sS[b];
+      const int g = (int)((R0 - base_b) / nb);
+      const long long Sv = base_b + g * nb;
+      ps->R0 = R0;
+      ps->R1 = R1;
+      ps->Sv0 = Sv;
+      ps->b0 = b;
+      ps->g0 = g;
+      ps->L0 = sL[b];
+      ps->row0 = sR[b];
+      if ((Sv < R0 || Sv + nb > R1) && Sv + nb <= R1) {  // split, and its final piece is here
+        const long long ka = ((Sv + 1) * Ne + T - 1) / T - 1;  // CTA holding the request's first piece
+        ps->merge_v = b * a.n_groups + g;
+        ps->merge_ka = (int)ka;
+        ps->merge_sa = (int)((ka * T / Ne == Sv) ? 2 * ka : 2 * ka + 1);
+      }
+    }
+  }
+  __syncthreads();
+}
+
+// The producer's walk over the pieces of its share.
+struct Cursor {
+  long long R0, R1, x, Sv, cap;
+  int k, B;
+  int b, g, row, lo, n;              // current virtual request
+  int t_begin, t_end, part, t0;      // current piece, next stage start
+  int piece;                         // index of the current piece
+  bool done;
+  int nb, nL, nrow;                  // next request, prefetched
+};
+
+__device__ __forceinline__ void cur_set_piece(Cursor& c) {
+  const long long e = min(c.R1, c.Sv + c.n);
+  c.t_begin = c.lo + (int)(c.x - c.Sv);
+  c.t_end = c.lo + (int)(e - c.Sv);
+  const bool split = c.Sv < c.R0 || c.Sv + c.n > c.R1;
+  c.part = split ? (c.x == c.R0 ? 2 * c.k : 2 * c.k + 1) : -1;
+  c.t0 = c.t_begin;
+}
+
+__device__ __forceinline__ void cur_prefetch(const TcArgs& a, Cursor& c) {
+  c.nb = c.b + 1;
+  if (c.nb < c.B) {
+    c.nL = __ldg(a.context_lens + c.nb);
+    c.nrow = a.table_rows ? __ldg(a.table_rows + c.nb) : c.nb;
+  }
+}
+
+__device__ void cur_init(const TcArgs& a, const PlanState& ps, Cursor& c) {
+  c.k = blockIdx.x;
+  c.B = a.B;
+  c.cap = table_capacity(a.T);
+  c.done = !ps.active;
+  if (c.done) return;
+  c.R0 = ps.R0;
+  c.R1 = ps.R1;
+  c.x = ps.R0;
+  c.Sv = ps.Sv0;
+  c.b = ps.b0;
+  c.g = ps.g0;
+  c.row = ps.row0;
+  c.n = attended(a, ps.L0, c.row, c.cap, &c.lo);
+  c.piece = 0;
+  cur_prefetch(a, c);
+  cur_set_piece(c);
+}
+
+
+__device__ void cur_next_piece(const TcArgs& a, Cursor& c) {
+  c.x = min(c.R1, c.Sv + c.n);
+  if (c.x >= c.R1) {
+    c.done = true;
+    return;
+  }
+  if (c.g + 1 < a.n_groups) {
+    ++c.g;
+    c.Sv += c.n;
+    cur_set_piece(c);
+    return;
+  }
+  for (;;) {
+    if (c.nb >= c.B) {  // cannot happen while x < R1; stop rather than read past the batch
+      c.done = true;
+      return;
+    }
+    c.b = c.nb;
+    c.row = c.nrow;
+    const int L = c.nL;
+    cur_prefetch(a, c);
+    c.n = attended(a, L, c.row, c.cap, &c.lo);
+    if (c.n > 0) break;
+  }
+  c.g = 0;
+  c.Sv = c.x;
+  cur_set_piece(c);
+}
+
+// Move the cursor past one stage.
+__device__ __forceinline__ void cur_advance(const TcArgs& a, Cursor& c) {
+  c.t0 += kTok;
+  if (c.t0 >= c.t_end) {
+    cur_next_piece(a, c);
+    ++c.piece;
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Producer warp.
 // ---------------------------------------------------------------------------
-__device__ void tc_producer(const TcArgs& a, const SmemMap& s, int lane) {
+__device__ void tc_producer(const TcArgs& a, const SmemMap& s, const PlanState& ps, int pid, int lane) {
   const int HG = a.HG;
   const uint32_t row_copy = (uint32_t)HG * 256u;
   const int j = lane & 15;          // token within the stage
   const bool is_v = lane >= 16;     // lanes 16..31 copy V rows
-  const int first = a.cta_first[blockIdx.x];
-  const int end = a.cta_first[blockIdx.x + 1];
+  StageMeta* meta = s.meta + pid * kQueue;
+  int* entries = s.entries + pid * kQueue * kTok;
 
-  long long issued = 0;  // stages issued
-  int started = 0;       // items started
-  bool ok = true;
-
-  int idx = first;
-  WorkItem w{};
-  if (idx < end) w = a.items[idx];
-  WorkItem wn = (idx + 1 < end) ? a.items[idx + 1] : w;
-  int t0 = w.t_begin;
-  int entry = (idx < end && t0 + j < w.t_end) ? load_entry(a.T, w.row, t0 + j) : -1;
-
-  while (idx < end) {
-    // Look one stage ahead: which stage comes next, and its table entry.
-    int idx2 = idx, t02 = t0 + kTok;
-    WorkItem w2 = w;
-    if (t02 >= w.t_end) {
-      idx2 = idx + 1;
-      w2 = wn;
-      t02 = wn.t_begin;
-      if (idx2 < end) wn = (idx2 + 1 < end) ? a.items[idx2 + 1] : wn;
+  // Lookahead cursor over all of the CTA's stages; for this producer's own
+  // stages (global index = pid mod 2) it records the metadata and starts the
+  // asynchronous fetch of the table entries kAhead own stages before issue,
+  // so that issuing never waits on a global load.
+  Cursor c;
+  cur_init(a, ps, c);
+  long long next_gs = 0;  // global index of the stage the cursor describes
+  long long queued = 0;   // own stages queued
+  auto queue_next = [&]() {
+    while (!c.done && (next_gs & 1) != pid) {
+      cur_advance(a, c);
+      ++next_gs;
     }
-    const int entry2 = (idx2 < end && t02 + j < w2.t_end) ? load_entry(a.T, w2.row, t02 + j) : -1;
+    const int qs = (int)(queued % kQueue);
+    if (!c.done) {
+      if (lane == 0) {
+        StageMeta m;
+        m.live = 1;
+        m.t0 = c.t0;
+        m.t_end = c.t_end;
+        m.flags = (c.t0 == c.t_begin ? 1 : 0) | (c.t0 + kTok >= c.t_end ? 2 : 0);
+        m.b = c.b;
+        m.group = c.g;
+        m.part = c.part;
+        m.piece = c.piece;
+        meta[qs] = m;
+      }
+      if (lane < kTok && c.t0 + lane < c.t_end) {
+        const int t = c.t0 + lane;
+        cp_async4(&entries[qs * kTok + lane],
+                  a.T.table + (size_t)c.row * a.T.cols + (a.T.raw ? t : t / a.T.page_size));
+      }
+      cur_advance(a, c);
+      ++next_gs;
+    } else if (lane == 0) {
+      meta[qs].live = 0;
+      meta[qs].t0 = (int)next_gs;  // stages of the CTA
+    }
+    cp_async_commit();
+    ++queued;
+  };
+  for (int k = 0; k < kAhead; ++k) queue_next();
 
-    const bool first_stage = (t0 == w.t_begin);
-    const bool last_stage = (t0 + kTok >= w.t_end);
-    const int qi = started & 1;
-    if (first_stage && started >= 2) {
-      ok = __all_sync(0xffffffffu,
-                      mbar_wait_bounded(&s.qempty[qi], ((started - 2) >> 1) & 1, s.abort_flag, a.err, kWaitLimitNs));
+  long long gs = pid;     // global index of the stage to issue
+  long long n_stages = -1;
+  bool ok = true;
+  for (long long k = 0;; ++k, gs += kProducers) {
+    queue_next();
+    cp_async_wait<kAhead>();  // the entries of own stage k have landed
+    __syncwarp();
+    const int qs = (int)(k % kQueue);
+    const StageMeta m = meta[qs];
+    if (!m.live) {
+      n_stages = m.t0;
+      break;
+    }
+    const bool first_stage = m.flags & 1;
+    const bool last_stage = m.flags & 2;
+    const int qi = m.piece & 1;
+    if (first_stage && m.piece >= 2) {
+      ok = __all_sync(0xffffffffu, mbar_wait_bounded(&s.qempty[qi], ((m.piece - 2) >> 1) & 1, s.abort_flag, a.err,
+                                                     kWaitLimitNs));
       if (!ok) break;
     }
-    const int st = (int)(issued % kStages);
-    if (issued >= kStages) {
-      ok = __all_sync(0xffffffffu, mbar_wait_bounded(&s.empty[st], (uint32_t)((issued / kStages - 1) & 1),
+    const int st = (int)(gs % kStages);
+    if (gs >= kStages) {
+      ok = __all_sync(0xffffffffu, mbar_wait_bounded(&s.empty[st], (uint32_t)((gs / kStages - 1) & 1),
                                                      s.abort_flag, a.err, kWaitLimitNs));
       if (!ok) break;
     }
-    const bool has_row = (t0 + j < w.t_end);
-    const int slot = has_row ? entry_to_slot(a.T, entry, t0 + j, a.err) : -1;
+    const int t = m.t0 + j;
+    const int slot = t < m.t_end ? entry_to_slot(a.T, entries[qs * kTok + j], t, a.err) : -1;
     const unsigned copies = __ballot_sync(0xffffffffu, slot >= 0);
     if (lane == 0) {
       StageHdr h;
-      h.item = idx;
-      h.t0 = t0;
+      h.live = 1;
+      h.t0 = m.t0;
       h.vmask = (int)(copies & copies >> 16 & 0xffffu);
       h.flags = (first_stage ? 1 : 0) | (last_stage ? 2 : 0) | (qi << 2);
+      h.b = m.b;
+      h.group = m.group;
+      h.part = m.part;
+      h.pad = 0;
       s.hdr[st] = h;
       const uint32_t tx = (uint32_t)__popc(copies) * row_copy + (first_stage ? (uint32_t)s.qbytes : 0u);
       mbar_arrive_expect_tx(&s.full[st], tx);
     }
     __syncwarp();
     if (slot >= 0) {
-      const char* src = a.kv_layer + (is_v ? a.kv_bytes : 0) + (size_t)slot * a.row_bytes + (size_t)w.group * row_copy;
+      const char* src = a.kv_layer + (is_v ? a.kv_bytes : 0) + (size_t)slot * a.row_bytes + (size_t)m.group * row_copy;
       unsigned char* dst = s.stages + (size_t)st * s.stage_bytes + (is_v ? kTok * s.pitch : 0) + j * s.pitch;
       bulk_g2s(dst, src, row_copy, &s.full[st]);
     }
     if (first_stage && lane == 0) {
-      const __nv_bfloat16* qsrc = a.q + ((size_t)w.b * a.Hq + (size_t)w.group * HG * a.G) * kD;
+      const __nv_bfloat16* qsrc = a.q + ((size_t)m.b * a.Hq + (size_t)m.group * HG * a.G) * kD;
       bulk_g2s(s.qbuf + qi * s.qbytes, qsrc, (uint32_t)s.qbytes, &s.full[st]);
     }
-    ++issued;
-    if (last_stage) ++started;
-    idx = idx2;
-    w = w2;
-    t0 = t02;
-    entry = entry2;
   }
+  cp_async_wait<0>();
 
-  if (ok) {
-    const int st = (int)(issued % kStages);
-    if (issued >= kStages)
-      ok = __all_sync(0xffffffffu, mbar_wait_bounded(&s.empty[st], (uint32_t)((issued / kStages - 1) & 1),
+  // The producer that owns the first stage without work tells the consumers.
+  if (ok && n_stages >= 0 && (n_stages % kProducers) == pid) {
+    const int st = (int)(n_stages % kStages);
+    if (n_stages >= kStages)
+      ok = __all_sync(0xffffffffu, mbar_wait_bounded(&s.empty[st], (uint32_t)((n_stages / kStages - 1) & 1),
                                                      s.abort_flag, a.err, kWaitLimitNs));
     if (ok && lane == 0) {
-      s.hdr[st].item = -1;
+      s.hdr[st].live = 0;
       mbar_arrive(&s.full[st]);
     }
   }
   if (!ok) {
     // Abort: let the copies this warp issued land before the CTA exits.
     *s.abort_flag = 1;
-    const long long from = issued > kStages ? issued - kStages : 0;
-    for (long long k = from; k < issued; ++k) {
-      const int st = (int)(k % kStages);
+    for (long long g2 = gs - kProducers; g2 >= 0 && g2 >= gs - kProducers * kStages; g2 -= kProducers) {
+      const int st = (int)(g2 % kStages);
       const uint64_t t_start = global_timer_ns();
-      while (!mbar_try_wait(&s.full[st], (uint32_t)((k / kStages) & 1))) {
+      while (!mbar_try_wait(&s.full[st], (uint32_t)((g2 / kStages) & 1))) {
         if (global_timer_ns() - t_start > 100000000ull) break;
       }
     }
@@ -233,16 +474,14 @@ __device__ void tc_consumer(const TcArgs& a, const SmemMap& s, int h, int lane) 
                                                    a.err, kWaitLimitNs)))
       return;
     const volatile StageHdr* vh = &s.hdr[st];
-    StageHdr hd;
-    hd.item = vh->item;
-    hd.t0 = vh->t0;
-    hd.vmask = vh->vmask;
-    hd.flags = vh->flags;
-    if (hd.item < 0) return;
+    const int live = vh->live;
+    if (!live) return;
+    const int vm = vh->vmask;
+    const int flags = vh->flags;
     const uint32_t sbase = stages_u32 + (uint32_t)st * (uint32_t)s.stage_bytes;
 
-    if (hd.flags & 1) {  // first stage of an item: Q^T fragments, reset state
-      const int qi = (hd.flags >> 2) & 1;
+    if (flags & 1) {  // first stage of a piece: Q^T fragments, reset state
+      const int qi = (flags >> 2) & 1;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         const int head = nt * 8 + (lane & 7);
@@ -273,7 +512,6 @@ __device__ void tc_consumer(const TcArgs& a, const SmemMap& s, int h, int lane) 
       }
     }
 
-    const int vm = hd.vmask;
     if (vm != 0xffff) {  // rows without data: zero this head's V so that 0 * garbage cannot be NaN
       for (int r = lane >> 4; r < kTok; r += 2) {
         if (!((vm >> r) & 1)) {
@@ -348,11 +586,12 @@ __device__ void tc_consumer(const TcArgs& a, const SmemMap& s, int h, int lane) 
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(o[i][nt], af, pb[nt][0], pb[nt][1]);
     }
+    // Read the rest of the header before the stage can be refilled.
+    const int hb = vh->b, hgroup = vh->group, hpart = vh->part;
     __syncwarp();
     if (lane == 0) mbar_arrive(&s.empty[st]);
 
-    if (hd.flags & 2) {  // last stage of the item: write the result
-      const WorkItem w = a.items[hd.item];
+    if (flags & 2) {  // last stage of the piece: write the result
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
@@ -363,16 +602,16 @@ __device__ void tc_consumer(const TcArgs& a, const SmemMap& s, int h, int lane) 
           const int hh = nt * 8 + 2 * c + e;
           if (hh >= G) continue;
           const int qh = h * G + hh;  // query head within the group
-          if (w.part < 0) {
+          if (hpart < 0) {
             const float inv = ls > 0.f ? 1.f / ls : 0.f;
-            __nv_bfloat16* dst = a.out + ((size_t)w.b * a.Hq + (size_t)w.group * HG * G + qh) * kD;
+            __nv_bfloat16* dst = a.out + ((size_t)hb * a.Hq + (size_t)hgroup * HG * G + qh) * kD;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               dst[16 * i + g] = __float2bfloat16_rn(o[i][nt][e] * inv);
               dst[16 * i + g + 8] = __float2bfloat16_rn(o[i][nt][2 + e] * inv);
             }
           } else {
-            const size_t base = (size_t)w.part * HG * G + qh;
+            const size_t base = (size_t)hpart * HG * G + qh;
             float* po = a.part_o + base * kD;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
@@ -391,8 +630,9 @@ __device__ void tc_consumer(const TcArgs& a, const SmemMap& s, int h, int lane) 
 }
 
 template <int NT>
-__global__ void __launch_bounds__(32 * 9, 1) tc_decode_kernel(const TcArgs a) {
+__global__ void __launch_bounds__(32 * (8 + kProducers), 1) tc_decode_kernel(const TcArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ PlanState ps;
   const SmemMap s = map_smem(smem, a.HG, a.G);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -405,45 +645,125 @@ __global__ void __launch_bounds__(32 * 9, 1) tc_decode_kernel(const TcArgs a) {
     *s.abort_flag = 0;
     fence_mbar_init();
   }
-  __syncthreads();
-  if (warp == a.HG)
-    tc_producer(a, s, lane);
+  griddep_wait();  // the previous kernel's writes (new K/V rows, tables) are visible from here on
+  griddep_launch_dependents();
+  plan_cta(a, s, &ps);
+  if (threadIdx.x == 0) a.merge[blockIdx.x] = make_int4(ps.merge_v, ps.merge_ka, ps.merge_sa, (int)blockIdx.x);
+  {  // requests whose length or table row is invalid get a zero output
+    const int* sN = reinterpret_cast<const int*>(reinterpret_cast<const long long*>(s.stages) + a.B);
+    for (int b = blockIdx.x; b < a.B; b += a.num_ctas) {
+      if (sN[b] != 0) continue;
+      __nv_bfloat16* o = a.out + (size_t)b * a.Hq * kD;
+      for (int i = threadIdx.x; i < a.Hq * kD; i += blockDim.x) o[i] = __float2bfloat16_rn(0.f);
+    }
+  }
+  __syncthreads();  // the scratch in the stage buffers is free from here on
+  if (warp >= a.HG)
+    tc_producer(a, s, ps, warp - a.HG, lane);
   else
     tc_consumer<NT>(a, s, warp, lane);
+}
+
+// Merge the pieces of the split request recorded by CTA blockIdx.x: one warp
+// per query head, M = max m_i, out = sum 2^(m_i-M) o_i / sum 2^(m_i-M) l_i.
+__global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
+  griddep_wait();
+  const int4 mg = a.merge[blockIdx.x];
+  if (mg.x < 0) return;
+  const int v = mg.x, ka = mg.y, sa = mg.z, kb = mg.w;
+  const int b = v / a.n_groups, grp = v % a.n_groups;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  const int pieces = 1 + kb - ka;
+  for (int qhl = blockIdx.y * nw + warp; qhl < a.QH; qhl += nw * gridDim.y) {
+    float M = -INFINITY;
+    for (int i = 0; i < pieces; ++i) {
+      const int slot = i == 0 ? sa : 2 * (ka + i);
+      M = fmaxf(M, __ldcg(a.part_ml + ((size_t)slot * a.QH + qhl) * 2));
+    }
+    const size_t orow = ((size_t)b * a.Hq + (size_t)grp * a.QH + qhl) * a.D;
+    for (int d0 = lane * 4; d0 < a.D; d0 += 128) {
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      float Ls = 0.f;
+      for (int i = 0; i < pieces; ++i) {
+        const size_t pi = (size_t)(i == 0 ? sa : 2 * (ka + i)) * a.QH + qhl;
+        const float mi = __ldcg(a.part_ml + pi * 2), li = __ldcg(a.part_ml + pi * 2 + 1);
+        const float wgt = (mi == -INFINITY) ? 0.f : exp2f(mi - M);
+        Ls += wgt * li;
+        const float4 o = __ldcg(reinterpret_cast<const float4*>(a.part_o + pi * a.D + d0));
+        acc.x += wgt * o.x;
+        acc.y += wgt * o.y;
+        acc.z += wgt * o.z;
+        acc.w += wgt * o.w;
+      }
+      const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + orow + d0;
+      out[0] = __float2bfloat16_rn(acc.x * inv);
+      out[1] = __float2bfloat16_rn(acc.y * inv);
+      out[2] = __float2bfloat16_rn(acc.z * inv);
+      out[3] = __float2bfloat16_rn(acc.w * inv);
+    }
+  }
 }
 
 }  // namespace
 
 size_t tc_smem_bytes(int HG, int G) {
   const size_t pitch = (size_t)HG * 256 + 16;
-  const size_t bytes = kStages * 2 * kTok * pitch + 2 * (size_t)HG * G * kD * 2 + kStages * sizeof(StageHdr) +
+  const size_t bytes = kStages * 2 * kTok * pitch + 2 * (size_t)HG * G * kD * 2 +
+                       kProducers * kQueue * (sizeof(StageMeta) + kTok * sizeof(int)) + kStages * sizeof(StageHdr) +
                        (2 * kStages + 2) * sizeof(uint64_t) + 16;
-  return bytes <= 232448 ? bytes : 0;
+  // the dynamic allocation plus the kernel's static shared memory (under
+  // kStaticSmemBound) must fit one block
+  return bytes <= kMaxDynamicSmem ? bytes : 0;
 }
 
-cudaError_t launch_tc(const TcArgs& a, int num_ctas, cudaStream_t stream) {
+int tc_max_batch(int HG) {
+  const size_t scratch = kStages * 2 * kTok * ((size_t)HG * 256 + 16);
+  return (int)(scratch / kPlanScratchPerRequest);
+}
+
+cudaError_t launch_tc(const TcArgs& a, const CombineArgs& cb, cudaStream_t stream, void* ev_before, void* ev_after) {
   const size_t smem = tc_smem_bytes(a.HG, a.G);
-  if (smem == 0 || a.G > 16 || a.HG > 8) return cudaErrorInvalidValue;
-  const dim3 block(32 * (a.HG + 1));
+  if (smem == 0 || a.G > 16 || a.HG > 8 || a.B > tc_max_batch(a.HG)) return cudaErrorInvalidValue;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.num_ctas);
+  cfg.blockDim = dim3(32 * (a.HG + kProducers));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   cudaError_t e;
+  if (ev_before && (e = cudaEventRecord(static_cast<cudaEvent_t>(ev_before), stream)) != cudaSuccess) return e;
   if (a.G <= 8) {
     static bool attr1 = false;
     if (!attr1) {
-      e = cudaFuncSetAttribute(tc_decode_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+      e = cudaFuncSetAttribute(tc_decode_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynamicSmem);
       if (e != cudaSuccess) return e;
       attr1 = true;
     }
-    tc_decode_kernel<1><<<num_ctas, block, smem, stream>>>(a);
+    e = cudaLaunchKernelEx(&cfg, tc_decode_kernel<1>, a);
   } else {
     static bool attr2 = false;
     if (!attr2) {
-      e = cudaFuncSetAttribute(tc_decode_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+      e = cudaFuncSetAttribute(tc_decode_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynamicSmem);
       if (e != cudaSuccess) return e;
       attr2 = true;
     }
-    tc_decode_kernel<2><<<num_ctas, block, smem, stream>>>(a);
+    e = cudaLaunchKernelEx(&cfg, tc_decode_kernel<2>, a);
   }
-  return cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (ev_after && (e = cudaEventRecord(static_cast<cudaEvent_t>(ev_after), stream)) != cudaSuccess) return e;
+  cudaLaunchConfig_t cc = {};
+  cc.gridDim = dim3(a.num_ctas, (cb.QH + 7) / 8);
+  cc.blockDim = dim3(256);
+  cc.dynamicSmemBytes = 0;
+  cc.stream = stream;
+  cc.attrs = attr;
+  cc.numAttrs = 1;
+  return cudaLaunchKernelEx(&cc, combine_kernel, cb);
 }
 
 }  // namespace kvp

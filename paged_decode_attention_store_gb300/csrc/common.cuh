@@ -166,6 +166,16 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
+// 4-byte asynchronous copy global -> shared (sm_80 cp.async), grouped per commit.
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // Order this thread's generic-proxy shared-memory writes before later
 // async-proxy (bulk copy) writes to the same addresses.
 __device__ __forceinline__ void fence_proxy_async_smem() {
