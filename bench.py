@@ -267,7 +267,7 @@ def run_step(sc, cache, st, outs, events=None):
     if st.cows is not None:
         kb.copy_pages(cache.pool, *st.cows)
         n += 1
-    per_attn = 3 if (w.dtype == "bf16" and w.D == 128) else 1
+    per_attn = 2 if (w.dtype == "bf16" and w.D == 128) else 1  # attention + combine, or the general kernel
     for layer in range(w.layers):
         cache.store(layer, st.k[layer], st.v[layer], st.out_loc)
         if events is not None:
