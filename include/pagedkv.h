@@ -167,6 +167,36 @@ int paged_decode_attention(const kvp_pool* pool, int layer, const void* q,
                            size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * paged_decode_attention_noalloc: paged_decode_attention for callers that
+ * cannot allocate device memory at the point where they run attention (code
+ * inside another framework's memory pool or under a budget that forbids new
+ * reservations, callers that may not enter an allocator from their thread,
+ * plug-in hosts that only receive their input and output buffers). There is
+ * no counterpart in the source pages: it is an interface convenience.
+ * Same arguments and results as paged_decode_attention minus the workspace:
+ * the split-K scratch is a fixed 12 MiB array in the library's own device
+ * memory, held by every GPU that loads it until the process exits.
+ *  - The pool's device must be current. The first call on a device looks up
+ *    the array's device address (cudaGetSymbolAddress) and keeps it; make
+ *    that first call before any stream capture.
+ *  - No allocation of any kind (no cudaMalloc/cudaFree, no library
+ *    allocator) happens in any call.
+ *  - A shape whose scratch would exceed 12 MiB is rejected with
+ *    KVP_ERR_INVALID_ARG and nothing is launched.
+ *  - Every call on a device shares the one array: calls that overlap on the
+ *    GPU (different streams, or different pools on the same device) race and
+ *    must be serialised by the caller. The array keeps the last call's
+ *    contents; nothing in it needs to start at zero.
+ * ---------------------------------------------------------------------- */
+int paged_decode_attention_noalloc(const kvp_pool* pool, int layer,
+                                   const void* q, int batch, int num_q_heads,
+                                   const int32_t* table, int table_rows_total,
+                                   int table_cols, int table_mode,
+                                   const int32_t* table_rows,
+                                   const int32_t* context_lens, int window,
+                                   float scale, void* out, void* stream);
+
+/* ------------------------------------------------------------------------
  * gather_indices: the slots paged_decode_attention would read, for
  * bit-exact checks of the index arithmetic ("PagedAttention block
  * allocator", section "Sequence block table"; chapter 15 Figure 15.1).

@@ -46,6 +46,7 @@ SIGNATURES = {
     "copy_pages": [_vp, _vp, _vp, _i, _vp],
     "paged_decode_attention_workspace_size": [_vp, _i, _i, _szp],
     "paged_decode_attention": [_vp, _i, _vp, _i, _i, _vp, _i, _i, _i, _vp, _vp, _i, _f, _vp, _vp, _sz, _vp],
+    "paged_decode_attention_noalloc": [_vp, _i, _vp, _i, _i, _vp, _i, _i, _i, _vp, _vp, _i, _f, _vp, _vp],
     "gather_indices": [_vp, _vp, _i, _i, _i, _vp, _vp, _i, _i, _vp, _i, _vp],
     "kvp_sync_error": [_vp, _vp, _ip],
     "kvp_pool_set_timing_events": [_vp, _vp, _vp],
@@ -214,6 +215,27 @@ def paged_decode_attention(pool, layer, q, table, table_mode, context_lens, wind
                                         table.shape[1], table_mode, _ptr(table_rows), _ptr(context_lens),
                                         int(window or 0), float(scale), _ptr(out), ws_ptr, ws_bytes,
                                         _stream(stream)), "paged_decode_attention")
+
+
+def paged_decode_attention_noalloc(pool, layer, q, table, table_mode, context_lens, window, scale, out,
+                                   table_rows=None, stream=None):
+    """paged_decode_attention without a workspace argument, for callers that
+    cannot allocate: the library uses a fixed scratch array of its own (see
+    include/pagedkv.h). Overlapping calls on one device must be serialised."""
+    dt = _TORCH_DTYPE[pool.dtype]
+    _dev(q, dt, "q")
+    _dev(out, dt, "out")
+    _dev(table, torch.int32, "table")
+    _dev(context_lens, torch.int32, "context_lens")
+    if table_rows is not None:
+        _dev(table_rows, torch.int32, "table_rows")
+    B, Hq = q.shape[0], q.shape[1]
+    if out.shape != q.shape or context_lens.numel() != B:
+        raise ValueError("q/out must be [B, Hq, D] and context_lens [B]")
+    _check(lib().paged_decode_attention_noalloc(pool.handle, layer, _ptr(q), B, Hq, _ptr(table), table.shape[0],
+                                                table.shape[1], table_mode, _ptr(table_rows), _ptr(context_lens),
+                                                int(window or 0), float(scale), _ptr(out), _stream(stream)),
+           "paged_decode_attention_noalloc")
 
 
 def gather_indices(pool, table, table_mode, context_lens, window, slots_out, table_rows=None, stream=None):
