@@ -565,7 +565,7 @@ def _host_inputs(sc, first_step, K, lens):
 class OracleSample:
     """The oracle replaying the scenario's script, storing rows of ``track`` only."""
 
-    def __init__(self, sc, track):
+    def __init__(self, sc, track, layers=None):
         import oracle.attention as OA
         from oracle.pagetable import PageTable
         from oracle.raw_locations import RawLocationTable
@@ -579,6 +579,7 @@ class OracleSample:
             self.raw = RawLocationTable(w.num_pages, w.P, sc.max_requests, sc.max_seq_len,
                                         free_page_order=w.free_order)
         self.stores = [OA.SlotStore() for _ in range(w.layers)]
+        self.layers = list(range(w.layers)) if layers is None else list(layers)
         self.tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
         for op in sc.ops:
             self._op(op)
@@ -587,9 +588,9 @@ class OracleSample:
         if rid not in self.track or not positions:
             return
         w = self.sc.w
-        for layer, st in enumerate(self.stores):
+        for layer in self.layers:
             k, v = wl.kv_rows(self.sc.seed, layer, rid, positions, w.Hkv, w.D, dtype=self.tdt)
-            st.store_cache(slots, k.float().numpy(), v.float().numpy())
+            self.stores[layer].store_cache(slots, k.float().numpy(), v.float().numpy())
 
     def _append(self, rids):
         before = {}
@@ -604,9 +605,16 @@ class OracleSample:
             self.raw.allocate_paged([(r, before[r], self.pt.length[r]) for r in seen])
         for x in res:
             if x["cow"] is not None:
-                for st in self.stores:
-                    st.copy_page(x["cow"][0], x["cow"][1], self.sc.w.P)
+                for layer in self.layers:
+                    self.stores[layer].copy_page(x["cow"][0], x["cow"][1], self.sc.w.P)
         return [x["slot"] for x in res]
+
+    def table_row(self, rid):
+        """The device-visible prefix of a request's table row."""
+        if self.raw is not None:
+            n = len(self.pt.block_row(rid)) * self.sc.w.P
+            return [int(x) for x in self.raw.page_table[rid, :n]]
+        return self.pt.block_row(rid)
 
     def _op(self, op):
         kind = op[0]
@@ -630,8 +638,10 @@ class OracleSample:
         elif kind == "release":
             self.pt.release(op[1])
 
-    def step(self, step_index, attend_rids):
-        """One decode step: bookkeeping for every request, store + attention for ``attend_rids``."""
+    def step(self, step_index, attend_rids, with_slots=False):
+        """One decode step: bookkeeping for every request, store + attention for ``attend_rids``.
+
+        Returns {(rid, layer): output}, and also the step's slots when ``with_slots``."""
         sc, w, OA = self.sc, self.sc.w, self.OA
         pos = [self.pt.length[r] for r in sc.rids]
         slots = self._append(sc.rids)
@@ -643,7 +653,7 @@ class OracleSample:
         for r in attend_rids:
             L = self.pt.length[r]
             lo = OA.window_lo(L, sc.window)
-            for layer in range(w.layers):
+            for layer in self.layers:
                 q = wl.q_rows(sc.seed, step_index, layer, [r], w.Hq, w.D, dtype=self.tdt)[0].float().numpy()
                 if self.raw is not None:
                     sl = OA.gather_raw(self.raw.page_table[r], lo, L)
@@ -653,7 +663,7 @@ class OracleSample:
         if sc.window > 0:
             for r in sc.rids:
                 self.pt.trim(r, max(0, self.pt.length[r] + 1 - sc.window))
-        return outs
+        return (outs, slots) if with_slots else outs
 
 
 def _sample_rids(sc, n):

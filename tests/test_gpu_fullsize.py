@@ -1,0 +1,64 @@
+"""Parity at the workloads' full sizes, in the launch configuration bench.py
+times (same scenario scripts, same per-step device calls).
+
+Bit-exact for every request: the slots each decode step writes and the
+device table rows. Attention: every layer checked (32-layer workloads:
+three layers) for a sample of requests spread over the batch, each output
+computed one by one by the oracle, max |gpu - oracle| <= 2e-2 (bf16).
+"""
+
+import gc
+
+import numpy as np
+import pytest
+import torch
+
+import bench
+from gpu_harness import max_abs
+from libbuild import ensure_built
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module")
+def kb():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    return ensure_built()
+
+
+@pytest.mark.parametrize("workload", bench.WORKLOADS)
+def test_full_size_parity(kb, workload):
+    sc = bench.Scenario(workload, 0)
+    n_sample = 3
+    sample = bench._sample_rids(sc, n_sample)
+    track = set(sample)
+    if workload == "prefix_sharing":  # the shared prompts are stored under the prompt requests
+        x = sc.w.extra
+        track |= {len(sc.rids) + f // x["forks"] for f in sample}
+    layers = list(range(sc.w.layers)) if sc.w.layers == 1 else [0, sc.w.layers // 2, sc.w.layers - 1]
+    orc = bench.OracleSample(sc, track, layers=layers)
+    cache, lens = bench.build_product(sc, dev=DEV)
+    steps, _ = bench.prepare_steps(sc, cache, lens, 1, 2, DEV)
+    outs = [torch.empty((len(sc.rids), sc.w.Hq, sc.w.D), dtype=cache.tdt, device=DEV) for _ in range(sc.w.layers)]
+    for i, st in enumerate(steps):
+        bench.run_step(sc, cache, st, outs)
+        torch.cuda.synchronize(DEV)
+        ref, slots = orc.step(i + 1, sample, with_slots=True)
+        assert st.out_loc.cpu().tolist() == slots, "decode-step slots differ"
+        got = {layer: outs[layer].float().cpu().numpy() for layer in layers}
+        for r in sample:
+            b = sc.rids.index(r)
+            for layer in layers:
+                d = max_abs(got[layer][b], ref[(r, layer)])
+                assert d <= 2e-2, f"{workload} step {i + 1} request {r} layer {layer}: max |diff| {d}"
+    tab = cache.table.cpu().numpy()
+    for r in sc.rids:
+        row = orc.table_row(r)
+        assert tab[r, :len(row)].tolist() == row, f"table row {r}"
+    cache.check()
+    del cache, steps, outs
+    gc.collect()
+    torch.cuda.empty_cache()
