@@ -359,6 +359,18 @@ def ncu_traffic(workload):
         return None
 
 
+def reduce_over_ranks(elapsed_ms, total_bytes, tokens, e2e_ms, e2e_bytes, world, device):
+    """Whole-job totals: the slowest rank's times, every rank's bytes and tokens."""
+    if world <= 1:
+        return elapsed_ms, total_bytes, tokens, e2e_ms, e2e_bytes
+    stats = torch.tensor([elapsed_ms, total_bytes, tokens, e2e_ms, e2e_bytes], dtype=torch.float64, device=device)
+    mx = stats.clone()
+    torch.distributed.all_reduce(mx, op=torch.distributed.ReduceOp.MAX)
+    sm = stats.clone()
+    torch.distributed.all_reduce(sm, op=torch.distributed.ReduceOp.SUM)
+    return mx[0].item(), sm[1].item(), sm[2].item(), mx[3].item(), sm[4].item()
+
+
 def run_gpu(args, rank, world, local_rank):
     from paged_decode_attention_store_gb300 import binding as kb
     from paged_decode_attention_store_gb300.engine import PagedKVCache  # noqa: F401  (fail loudly if missing)
@@ -416,18 +428,8 @@ def run_gpu(args, rank, world, local_rank):
     e2e = run_e2e(args, sc, cache, lens_after, W + K + 1, dev)
     clocks = sampler.stop(t0, t1) if sampler else None
 
-    # max over ranks of the timed region; sum of bytes and tokens
-    stats = torch.tensor([elapsed_ms, float(total_bytes), float(K * len(sc.rids)), e2e["ms"], e2e["bytes"]],
-                         dtype=torch.float64, device=dev)
-    if world > 1:
-        mx = stats.clone()
-        torch.distributed.all_reduce(mx, op=torch.distributed.ReduceOp.MAX)
-        sm = stats.clone()
-        torch.distributed.all_reduce(sm, op=torch.distributed.ReduceOp.SUM)
-        elapsed_ms, total_bytes, tokens, e2e_ms, e2e_bytes = mx[0].item(), sm[1].item(), sm[2].item(), \
-            mx[3].item(), sm[4].item()
-    else:
-        tokens, e2e_ms, e2e_bytes = float(K * len(sc.rids)), e2e["ms"], e2e["bytes"]
+    elapsed_ms, total_bytes, tokens, e2e_ms, e2e_bytes = reduce_over_ranks(
+        elapsed_ms, float(total_bytes), float(K * len(sc.rids)), e2e["ms"], float(e2e["bytes"]), world, dev)
     if rank != 0:
         return None
 
