@@ -382,7 +382,11 @@ def run_gpu(args, rank, world, local_rank):
     w = sc.w
     cache, lens = build_product(sc, dev)
     K, W = args.steps, args.warmup
-    steps, lens_after = prepare_steps(sc, cache, lens, 1, W + K, dev)
+    # W warm-up steps, K timed steps for `value` (nothing between the kernels
+    # but the step's own launches), then K more steps with events around each
+    # attention kernel for the roofline (an event between two kernels stops
+    # the second from launching early, so it is kept out of the first pass).
+    steps, lens_after = prepare_steps(sc, cache, lens, 1, W + 2 * K, dev)
     tdt = cache.tdt
     outs = [torch.empty((len(sc.rids), w.Hq, w.D), dtype=tdt, device=dev) for _ in range(w.layers)]
 
@@ -400,6 +404,19 @@ def run_gpu(args, rank, world, local_rank):
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
 
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches = 0
+    t0 = time.time()
+    start.record()
+    for i in range(W, W + K):
+        launches += run_step(sc, cache, steps[i], outs)
+    end.record()
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    elapsed_ms = start.elapsed_time(end)
+    if world > 1:
+        torch.distributed.barrier()
+
     n_attn = K * w.layers
     ev_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_attn)]
     for a, b in ev_pairs:  # torch creates the CUDA event at its first record
@@ -407,25 +424,16 @@ def run_gpu(args, rank, world, local_rank):
         b.record()
     torch.cuda.synchronize(dev)
     pending = list(reversed(ev_pairs))
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    launches = 0
-    t0 = time.time()
-    start.record()
-    for i in range(W, W + K):
-        launches += run_step(sc, cache, steps[i], outs, events=pending)
-    end.record()
+    for i in range(W + K, W + 2 * K):
+        run_step(sc, cache, steps[i], outs, events=pending)
     torch.cuda.synchronize(dev)
-    t1 = time.time()
-    elapsed_ms = start.elapsed_time(end)
-    if world > 1:
-        torch.distributed.barrier()
     cache.check()
     attn_ms = [a.elapsed_time(b) for a, b in ev_pairs]
     total_bytes = sum(st.bytes for st in steps[W:W + K])
-    attn_bytes_mean = statistics.mean(st.attn_bytes for st in steps[W:W + K])
+    attn_bytes_mean = statistics.mean(st.attn_bytes for st in steps[W + K:W + 2 * K])
 
     # end to end through the driver, host buffers
-    e2e = run_e2e(args, sc, cache, lens_after, W + K + 1, dev)
+    e2e = run_e2e(args, sc, cache, lens_after, W + 2 * K + 1, dev)
     clocks = sampler.stop(t0, t1) if sampler else None
 
     elapsed_ms, total_bytes, tokens, e2e_ms, e2e_bytes = reduce_over_ranks(
