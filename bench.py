@@ -225,6 +225,7 @@ def prepare_steps(sc, cache, lens, first_step, n_steps, dev, host_inputs=False):
     for s in range(first_step, first_step + n_steps):
         st = StepData()
         slots, writes, cows = cache.host.append(sc.rids)
+        np.add.at(cache.lengths, np.asarray(sc.rids, np.int64), 1)
         st.n_writes, st.n_cows = len(writes), len(cows)
         st.pre = None if not writes else tuple(_i32(x, dev) for x in zip(*writes))
         st.cows = None if not cows else tuple(_i32(x, dev) for x in zip(*cows))
@@ -236,7 +237,9 @@ def prepare_steps(sc, cache, lens, first_step, n_steps, dev, host_inputs=False):
         post = []
         if sc.window > 0:
             for r, L in zip(sc.rids, lens):
-                post += cache.host.trim(r, max(0, L + 1 - sc.window))
+                wr = cache.host.trim(r, max(0, L + 1 - sc.window))
+                cache.dropped[r] += len(wr)
+                post += wr
         st.n_post = len(post)
         st.post = None if not post else tuple(_i32(x, dev) for x in zip(*post))
         st.q, st.k, st.v = [], [], []
@@ -502,6 +505,7 @@ def run_gpu(args, rank, world, local_rank):
             "ms_per_step": round(e2e_ms / K, 4),
             "h2d_bytes_per_step": e2e["h2d"],
             "d2h_bytes_per_step": e2e["d2h"],
+            "host_link": e2e["link"],
         },
         "clocks": clocks,
     }
@@ -511,43 +515,48 @@ def run_gpu(args, rank, world, local_rank):
 
 
 def run_e2e(args, sc, cache, lens, first_step, dev):
-    """K steps through PagedKVCache with host-resident q/k/v and outputs."""
+    """K steps through PagedKVCache.decode_step with pinned host q/k/v and
+    outputs: host bookkeeping, all copies and the output read-back (the call
+    returns once the step's output is on the host) are inside the timing."""
     w = sc.w
     K = args.steps
     host_steps = _host_inputs(sc, first_step, K, lens)
-    out_dev = [torch.empty((len(sc.rids), w.Hq, w.D), dtype=cache.tdt, device=dev) for _ in range(w.layers)]
-    out_host = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in out_dev]
-    lens = list(lens)
-    total_bytes = h2d = d2h = 0
+    out_host = [torch.empty((len(sc.rids), w.Hq, w.D), dtype=cache.tdt, pin_memory=True) for _ in range(w.layers)]
+    rids = np.asarray(sc.rids, np.int32)
+    total_bytes = 0
     torch.cuda.synchronize(dev)
     cache.h2d_bytes = 0
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record()
     for s in range(K):
         q_h, k_h, v_h = host_steps[s]
-        qd = [x.to(dev, non_blocking=True) for x in q_h]
-        kd = [x.to(dev, non_blocking=True) for x in k_h]
-        vd = [x.to(dev, non_blocking=True) for x in v_h]
-        h2d += sum(x.numel() * x.element_size() for x in q_h + k_h + v_h)
-        out_loc = cache.append(sc.rids)
-        lens = [L + 1 for L in lens]
-        lens_d = cache._to_device(lens)
-        for layer in range(w.layers):
-            cache.store(layer, kd[layer], vd[layer], out_loc)
-            cache.attend(layer, qd[layer], lens_d, sc.window, w.scale, out_dev[layer])
-            out_host[layer].copy_(out_dev[layer], non_blocking=True)
-            d2h += out_dev[layer].numel() * out_dev[layer].element_size()
-        n_post = 0
-        if sc.window > 0:
-            for r, L in zip(sc.rids, lens):
-                n_post += cache.trim(r, max(0, L + 1 - sc.window))
-        torch.cuda.current_stream(dev).synchronize()  # this step's output is on the host
-        total_bytes += step_bytes(sc, lens, cache.last_writes, cache.last_copies, n_post)
+        cache.decode_step(rids, q_h, k_h, v_h, out_host, sc.window, w.scale)
+        total_bytes += step_bytes(sc, [int(x) for x in cache.lengths[rids]], cache.last_writes, cache.last_copies,
+                                  cache.last_trims)
     end.record()
     torch.cuda.synchronize(dev)
     cache.check()
-    h2d += cache.h2d_bytes
-    return {"ms": start.elapsed_time(end), "bytes": total_bytes, "h2d": h2d // K, "d2h": d2h // K}
+    d2h = sum(o.numel() * o.element_size() for o in out_host)
+    return {"ms": start.elapsed_time(end), "bytes": total_bytes, "h2d": cache.h2d_bytes // K, "d2h": d2h,
+            "link": link_rates(dev)}
+
+
+def link_rates(dev, nbytes=128 << 20):
+    """Host<->device copy rates of this machine (pinned memory), GB/s."""
+    h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    out = {}
+    for name, dst, src in (("h2d_gbs", d, h), ("d2h_gbs", h, d)):
+        dst.copy_(src, non_blocking=True)
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(3):
+            dst.copy_(src, non_blocking=True)
+        b.record()
+        torch.cuda.synchronize(dev)
+        out[name] = round(3 * nbytes / (a.elapsed_time(b) * 1e-3) / 1e9, 1)
+    return out
 
 
 def _host_inputs(sc, first_step, K, lens):

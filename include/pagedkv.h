@@ -268,6 +268,45 @@ int kvp_host_append(kvp_host* h, const int32_t* rids, int n, int32_t* slots,
 int kvp_host_trim(kvp_host* h, int rid, int keep_from, int32_t* tw_rows,
                   int32_t* tw_cols, int32_t* tw_vals, int tw_cap, int* n_tw);
 
+/* ------------------------------------------------------------------------
+ * kvp_decode_step: one decode step of the whole path in one call, in the
+ * order of chapter 15's host loop ("The model") with the attention after a
+ * separate store:
+ *   1. host bookkeeping: one token for each request rids[0..n) (request id
+ *      = table row; each id at most once); all-or-nothing on exhaustion;
+ *   2. one host->device copy of the step's metadata, packed in host_meta
+ *      (caller-owned PINNED host memory) and copied to dev_meta (device):
+ *      [slots n | table writes 3*w | copy pairs 2*c | lengths n | rows n |
+ *       trim writes 3*t];
+ *   3. page_table_write, copy_pages, then for each layer l: wait for
+ *      layer_ready[l] (a cudaEvent_t, or NULL), store_cache(k[l], v[l]),
+ *      paged_decode_attention(q[l] -> out[l]), record layer_done[l] (or
+ *      NULL); q/k/v/out are per-layer DEVICE pointers;
+ *   4. the window's trim writes (released pages are read by this step).
+ * meta_cap bounds host_meta/dev_meta in int32 entries (8n plus three per
+ * page the window releases suffices); it and every argument are checked
+ * before anything changes. host_meta is read asynchronously: reuse it only
+ * after the stream has passed this call. ``info`` receives the counts.
+ * Errors: as the calls it makes; KVP_ERR_OUT_OF_PAGES leaves the host
+ * bookkeeping unchanged and launches nothing.
+ * ---------------------------------------------------------------------- */
+typedef struct kvp_step_info {
+  int n_table_writes;  /* new pages and copy-on-write replacements */
+  int n_copies;        /* copy-on-write page pairs */
+  int n_trim_writes;   /* pages released by the window */
+  int meta_ints;       /* int32 entries copied to the device */
+} kvp_step_info;
+
+int kvp_decode_step(kvp_host* h, const kvp_pool* pool, int32_t* table,
+                    int table_rows_total, int table_cols, int table_mode,
+                    const int32_t* rids, int n, int window, int num_q_heads,
+                    float scale, const void* const* q, const void* const* k,
+                    const void* const* v, void* const* out,
+                    void* const* layer_ready, void* const* layer_done,
+                    int32_t* host_meta, int32_t* dev_meta, int meta_cap,
+                    void* workspace, size_t workspace_bytes, void* stream,
+                    kvp_step_info* info);
+
 /* Queries. kvp_host_block_row writes dropped+live entries (-1 for released
  * pages) to out (capacity cap) and the count to *n. */
 int kvp_host_used(const kvp_host* h, int* used);

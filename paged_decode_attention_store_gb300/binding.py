@@ -62,7 +62,14 @@ SIGNATURES = {
     "kvp_host_block_row": [_vp, _i, _vp, _i, _ip],
     "kvp_host_refcounts": [_vp, _vp, _i],
     "kvp_host_free_list": [_vp, _vp, _i, _ip],
+    "kvp_decode_step": [_vp, _vp, _vp, _i, _i, _i, _vp, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i,
+                        _vp, _sz, _vp, _vp],
 }
+
+
+class StepInfo(ctypes.Structure):
+    _fields_ = [("n_table_writes", ctypes.c_int), ("n_copies", ctypes.c_int), ("n_trim_writes", ctypes.c_int),
+                ("meta_ints", ctypes.c_int)]
 
 _lib = None
 
@@ -313,6 +320,27 @@ class HostPageTable:
         writes = list(zip(tr[:ntw.value], tc[:ntw.value], tv[:ntw.value]))
         cows = list(zip(cs[:ncow.value], cd[:ncow.value]))
         return list(slots[:n]), writes, cows
+
+    def append_into(self, rids, slots, tw, cow):
+        """Fast form of :meth:`append` over numpy buffers.
+
+        ``rids`` int32[n]; outputs go to ``slots`` int32[n], ``tw`` int32[3, n]
+        (rows, cols, vals) and ``cow`` int32[2, n] (src, dst). Returns the
+        numbers of table writes and copy-on-write pairs."""
+        n = int(rids.shape[0])
+        ntw, ncow = ctypes.c_int(), ctypes.c_int()
+        p = lambda a: a.ctypes.data_as(ctypes.c_void_p)  # noqa: E731
+        _check(lib().kvp_host_append(self.handle, p(rids), n, p(slots), p(tw[0]), p(tw[1]), p(tw[2]), n,
+                                     ctypes.byref(ntw), p(cow[0]), p(cow[1]), ctypes.byref(ncow)), "kvp_host_append")
+        return ntw.value, ncow.value
+
+    def trim_into(self, rid, keep_from, tw, cap):
+        """Fast form of :meth:`trim`: writes go to ``tw`` int32[3, cap]; returns their number."""
+        n = ctypes.c_int()
+        p = lambda a: a.ctypes.data_as(ctypes.c_void_p)  # noqa: E731
+        _check(lib().kvp_host_trim(self.handle, rid, int(keep_from), p(tw[0]), p(tw[1]), p(tw[2]), cap,
+                                   ctypes.byref(n)), "kvp_host_trim")
+        return n.value
 
     def trim(self, rid, keep_from):
         cap = max(1, self.length(rid)[0] // self.page_size + 1)

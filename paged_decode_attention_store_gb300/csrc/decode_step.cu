@@ -1,0 +1,123 @@
+// kvp_decode_step: one decode step of the whole path in one native call.
+//
+// The order of chapter 15's host loop ("A Paged KV Cache and Sliding-Window
+// Attention", section "The model"), with the attention after a separate
+// store: host bookkeeping appends one token per request (a fresh page on a
+// page boundary, a copy of a shared tail page), the step's slots, table
+// writes, copy pairs, lengths and rows go to the device in one copy (the
+// mini-sglang code series, part 4: host-built lists, one scatter), then the
+// table writes, page copies, store_cache and attention of every layer, and
+// last the window's trim writes (the pages a step attends are released only
+// after it).
+#include <cstring>
+#include <vector>
+
+#include "common.cuh"
+
+namespace {
+
+int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+}  // namespace
+
+extern "C" int kvp_decode_step(kvp_host* h, const kvp_pool* pool, int32_t* table, int table_rows_total,
+                               int table_cols, int table_mode, const int32_t* rids, int n, int window,
+                               int num_q_heads, float scale, const void* const* q, const void* const* k,
+                               const void* const* v, void* const* out, void* const* layer_ready,
+                               void* const* layer_done, int32_t* host_meta, int32_t* dev_meta, int meta_cap,
+                               void* workspace, size_t workspace_bytes, void* stream, kvp_step_info* info) {
+  if (!h || !pool || !table || !rids || n <= 0 || !q || !k || !v || !out || !host_meta || !dev_meta || !info)
+    return KVP_ERR_INVALID_ARG;
+  if (table_mode != KVP_BLOCK_TABLE && table_mode != KVP_RAW_LOCATIONS) return KVP_ERR_INVALID_ARG;
+  const int P = pool->page_size;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  // Lengths and dropped pages before the step, and the trim writes the step
+  // will need, so that every capacity is checked before anything changes.
+  std::vector<int> len0(n), drop0(n);
+  for (int i = 0; i < n; ++i) {
+    if (kvp_host_length(h, rids[i], &len0[i], &drop0[i]) != KVP_OK) return KVP_ERR_INVALID_ARG;
+    for (int j = 0; j < i; ++j)
+      if (rids[j] == rids[i]) return KVP_ERR_INVALID_ARG;  // one token per request per step
+  }
+  int trims = 0;
+  if (window > 0) {
+    for (int i = 0; i < n; ++i) {
+      const int L = len0[i] + 1, keep = L + 1 - window;
+      const int pages = ceil_div(L, P);
+      const int to = keep > 0 ? (keep / P < pages ? keep / P : pages) : 0;  // pages wholly below keep
+      if (to > drop0[i]) trims += to - drop0[i];
+    }
+  }
+  const long long need = 3LL * n + 3LL * n + 2LL * n + 3LL * trims;  // slots, tw, cow, lens, rows, trim
+  if (need > meta_cap) return KVP_ERR_INVALID_ARG;
+
+  int32_t* slots = host_meta;
+  std::vector<int32_t> tw(3 * n), cow(2 * n);
+  int ntw = 0, ncow = 0;
+  int rc = kvp_host_append(h, rids, n, slots, tw.data(), tw.data() + n, tw.data() + 2 * n, n, &ntw, cow.data(),
+                           cow.data() + n, &ncow);
+  if (rc != KVP_OK) return rc;  // nothing changed (out of pages is all-or-nothing)
+  int32_t* p = host_meta + n;
+  const int o_tw = n;
+  std::memcpy(p, tw.data(), sizeof(int32_t) * ntw);
+  std::memcpy(p + ntw, tw.data() + n, sizeof(int32_t) * ntw);
+  std::memcpy(p + 2 * ntw, tw.data() + 2 * n, sizeof(int32_t) * ntw);
+  p += 3 * ntw;
+  const int o_cow = o_tw + 3 * ntw;
+  std::memcpy(p, cow.data(), sizeof(int32_t) * ncow);
+  std::memcpy(p + ncow, cow.data() + n, sizeof(int32_t) * ncow);
+  p += 2 * ncow;
+  const int o_len = o_cow + 2 * ncow;
+  for (int i = 0; i < n; ++i) p[i] = len0[i] + 1;
+  p += n;
+  const int o_rows = o_len + n;
+  std::memcpy(p, rids, sizeof(int32_t) * n);
+  p += n;
+  const int o_trim = o_rows + n;
+  int ntrim = 0;
+  if (trims > 0) {
+    std::vector<int32_t> tr(3 * trims);
+    for (int i = 0; i < n; ++i) {
+      const int keep = len0[i] + 2 - window;
+      int got = 0;
+      rc = kvp_host_trim(h, rids[i], keep, tr.data() + ntrim, tr.data() + trims + ntrim, tr.data() + 2 * trims + ntrim,
+                         trims - ntrim, &got);
+      if (rc != KVP_OK) return rc;
+      ntrim += got;
+    }
+    std::memcpy(p, tr.data(), sizeof(int32_t) * ntrim);
+    std::memcpy(p + ntrim, tr.data() + trims, sizeof(int32_t) * ntrim);
+    std::memcpy(p + 2 * ntrim, tr.data() + 2 * trims, sizeof(int32_t) * ntrim);
+  }
+  const int total = o_trim + 3 * ntrim;
+  info->n_table_writes = ntw;
+  info->n_copies = ncow;
+  info->n_trim_writes = ntrim;
+  info->meta_ints = total;
+
+  if (cudaMemcpyAsync(dev_meta, host_meta, sizeof(int32_t) * total, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return KVP_ERR_CUDA;
+  const int expand = table_mode == KVP_RAW_LOCATIONS ? P : 1;
+  if (ntw && (rc = page_table_write(table, table_rows_total, table_cols, dev_meta + o_tw, dev_meta + o_tw + ntw,
+                                    dev_meta + o_tw + 2 * ntw, ntw, expand, pool->err, stream)) != KVP_OK)
+    return rc;
+  if (ncow && (rc = copy_pages(pool, dev_meta + o_cow, dev_meta + o_cow + ncow, ncow, stream)) != KVP_OK) return rc;
+  for (int l = 0; l < pool->num_layers; ++l) {
+    if (layer_ready && layer_ready[l] &&
+        cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(layer_ready[l]), 0) != cudaSuccess)
+      return KVP_ERR_CUDA;
+    if ((rc = store_cache(pool, l, k[l], v[l], dev_meta, n, stream)) != KVP_OK) return rc;
+    if ((rc = paged_decode_attention(pool, l, q[l], n, num_q_heads, table, table_rows_total, table_cols, table_mode,
+                                     dev_meta + o_rows, dev_meta + o_len, window, scale, out[l], workspace,
+                                     workspace_bytes, stream)) != KVP_OK)
+      return rc;
+    if (layer_done && layer_done[l] && cudaEventRecord(static_cast<cudaEvent_t>(layer_done[l]), st) != cudaSuccess)
+      return KVP_ERR_CUDA;
+  }
+  if (ntrim && (rc = page_table_write(table, table_rows_total, table_cols, dev_meta + o_trim,
+                                      dev_meta + o_trim + ntrim, dev_meta + o_trim + 2 * ntrim, ntrim, expand,
+                                      pool->err, stream)) != KVP_OK)
+    return rc;
+  return KVP_OK;
+}

@@ -19,6 +19,9 @@ staging buffers); everything else stays on the device.
 
 from __future__ import annotations
 
+import ctypes
+
+import numpy as np
 import torch
 
 from . import binding as kb
@@ -56,6 +59,9 @@ class PagedKVCache:
             self.table = torch.full((max_requests, cols), -1, dtype=torch.int32, device=self.dev)
         self.table_mode = kb.KVP_RAW_LOCATIONS if self.raw else kb.KVP_BLOCK_TABLE
         self._ws = {}
+        self._steps = {}
+        self.lengths = np.zeros(max_requests, np.int64)  # rows stored, per request (mirrors the host table)
+        self.dropped = np.zeros(max_requests, np.int64)  # pages released by the window, per request
         self.copies = 0
         self.h2d_bytes = 0  # bytes this driver has copied host -> device
 
@@ -79,17 +85,21 @@ class PagedKVCache:
     # -- request lifecycle ---------------------------------------------------
     def new(self, rid):
         self.host.new(rid)
+        self.lengths[rid] = self.dropped[rid] = 0
 
     def fork(self, src, dst):
         self._write_table(self.host.fork(src, dst))
+        self.lengths[dst], self.dropped[dst] = self.lengths[src], self.dropped[src]
 
     def release(self, rid):
         self.host.release(rid)
+        self.lengths[rid] = self.dropped[rid] = 0
 
     def trim(self, rid, keep_from):
         """Release front pages below keep_from; returns the number of table writes."""
         writes = self.host.trim(rid, keep_from)
         self._write_table(writes)
+        self.dropped[rid] += len(writes)
         return len(writes)
 
     def append(self, rids):
@@ -98,6 +108,7 @@ class PagedKVCache:
         Also leaves the counts of this call's table writes and copies in
         ``last_writes`` / ``last_copies``."""
         slots, writes, cows = self.host.append(rids)
+        np.add.at(self.lengths, np.asarray(rids, np.int64), 1)
         self.last_writes, self.last_copies = len(writes), len(cows)
         n, nw, nc = len(slots), len(writes), len(cows)
         flat = list(slots)
@@ -136,3 +147,119 @@ class PagedKVCache:
         e = kb.kvp_sync_error(self.pool)
         if e != 0:
             raise kb.KvpError(e, "device")
+
+
+    # -- one decode step, host buffers in and out ----------------------------
+    def decode_step(self, rids, q, k, v, out, window, scale):
+        """One decode step for the requests ``rids`` (one token each; request
+        id = table row), through the native kvp_decode_step.
+
+        ``q`` [layers][B, Hq, D], ``k``/``v`` [layers][B, Hkv, D] and ``out``
+        [layers][B, Hq, D] are lists of tensors, all on the host (pinned) or
+        all on the device. With several layers, host inputs are copied per
+        layer on a side stream and each layer's store + attention waits only
+        for its own inputs, and each output is copied back on another side
+        stream as soon as its layer is done; a single layer copies on the
+        step's own stream. Returns when ``out`` holds the results.
+        """
+        L = kb.lib()
+        n = len(rids)
+        Hq = q[0].shape[1]
+        st = self._step_state(n, Hq)
+        rids = np.ascontiguousarray(rids, dtype=np.int32)
+        stream = torch.cuda.current_stream(self.dev)
+        slot = st["ring"][st["next"]]
+        st["next"] ^= 1
+        slot["event"].synchronize()  # its previous copy has finished reading it
+        host_io = not q[0].is_cuda
+        vp = ctypes.c_void_p
+        arr = lambda ts: (vp * self.layers)(*[t.data_ptr() for t in ts])  # noqa: E731
+        ready = done = None
+        if host_io:
+            qd, kd, vd = st["in"]
+            od = st["out"]
+            qp, kp, vpp, op = st["in_p"][0], st["in_p"][1], st["in_p"][2], st["out_p"]
+            side = self.layers > 1  # overlap the per-layer copies with the other layers' kernels
+            cs = st["h2d"] if side else stream
+            if side:
+                st["h2d"].wait_stream(stream)  # the previous step's kernels are done with the buffers
+            with torch.cuda.stream(cs):
+                for layer in range(self.layers):
+                    qd[layer].copy_(q[layer], non_blocking=True)
+                    kd[layer].copy_(k[layer], non_blocking=True)
+                    vd[layer].copy_(v[layer], non_blocking=True)
+                    if side:
+                        st["ready"][layer].record(cs)
+            self.h2d_bytes += sum(t[i].numel() * t[i].element_size() for t in (q, k, v) for i in range(self.layers))
+            if side:
+                ready, done = st["ready_p"], st["done_p"]
+        else:
+            side = False
+            qp, kp, vpp, op = arr(q), arr(k), arr(v), arr(out)
+        info = kb.StepInfo()
+        ws = self.workspace(n, Hq)
+        kb._check(L.kvp_decode_step(self.host.handle, self.pool.handle, vp(self.table.data_ptr()), self.table.shape[0],
+                                    self.table.shape[1], self.table_mode, rids.ctypes.data_as(vp), n,
+                                    int(window or 0), Hq, float(scale), qp, kp, vpp, op, ready,
+                                    done, vp(slot["host"].data_ptr()), vp(st["dev"].data_ptr()), st["cap"],
+                                    vp(ws.data_ptr()), ws.numel(), vp(stream.cuda_stream), ctypes.byref(info)),
+                  "kvp_decode_step")
+        slot["event"].record(stream)
+        self.h2d_bytes += 4 * info.meta_ints
+        self.last_writes, self.last_copies, self.last_trims = info.n_table_writes, info.n_copies, info.n_trim_writes
+        self.copies += info.n_copies
+        np.add.at(self.lengths, rids, 1)
+        if window and window > 0 and info.n_trim_writes:
+            # mirror the released pages: the native call releases every page that
+            # lies wholly below keep_from = L + 1 - window
+            Lr = self.lengths[rids]
+            keep = Lr + 1 - window
+            to = np.minimum(np.maximum(keep, 0) // self.P, -(-Lr // self.P))
+            self.dropped[rids] = np.maximum(self.dropped[rids], to)
+        if host_io:
+            if side:
+                with torch.cuda.stream(st["d2h"]):
+                    for layer in range(self.layers):
+                        st["d2h"].wait_event(st["done"][layer])
+                        out[layer].copy_(od[layer], non_blocking=True)
+                st["d2h"].synchronize()
+            else:
+                for layer in range(self.layers):
+                    out[layer].copy_(od[layer], non_blocking=True)
+        stream.synchronize()  # the step's outputs are in `out`
+        return 4 * info.meta_ints
+
+    def _step_state(self, n, Hq):
+        key = (n, Hq)
+        st = self._steps.get(key)
+        if st is not None:
+            return st
+        cap = 8 * n + 3 * (4 * n + 64)
+        ring = []
+        for _ in range(2):
+            host = torch.zeros(cap, dtype=torch.int32, pin_memory=True)
+            ev = torch.cuda.Event()
+            ev.record(torch.cuda.current_stream(self.dev))
+            ring.append({"host": host, "event": ev})
+        ready = [torch.cuda.Event() for _ in range(self.layers)]
+        done = [torch.cuda.Event() for _ in range(self.layers)]
+        for e in ready + done:  # torch creates the CUDA event at its first record
+            e.record(torch.cuda.current_stream(self.dev))
+        vp = ctypes.c_void_p
+        st = {
+            "cap": cap, "ring": ring, "next": 0,
+            "dev": torch.empty(cap, dtype=torch.int32, device=self.dev),
+            "in": [[torch.empty((n, Hq, self.D), dtype=self.tdt, device=self.dev) for _ in range(self.layers)],
+                   [torch.empty((n, self.Hkv, self.D), dtype=self.tdt, device=self.dev) for _ in range(self.layers)],
+                   [torch.empty((n, self.Hkv, self.D), dtype=self.tdt, device=self.dev) for _ in range(self.layers)]],
+            "out": [torch.empty((n, Hq, self.D), dtype=self.tdt, device=self.dev) for _ in range(self.layers)],
+            "h2d": torch.cuda.Stream(self.dev), "d2h": torch.cuda.Stream(self.dev),
+            "ready": ready, "done": done,
+            "ready_p": (vp * self.layers)(*[e.cuda_event for e in ready]),
+            "done_p": (vp * self.layers)(*[e.cuda_event for e in done]),
+        }
+        st["in_p"] = [(vp * self.layers)(*[t.data_ptr() for t in ts]) for ts in st["in"]]
+        st["out_p"] = (vp * self.layers)(*[t.data_ptr() for t in st["out"]])
+        torch.cuda.synchronize(self.dev)
+        self._steps[key] = st
+        return st

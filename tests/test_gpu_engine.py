@@ -1,0 +1,85 @@
+"""PagedKVCache.decode_step (the per-step driver) against the oracle.
+
+Host-resident and device-resident inputs and outputs, a sliding window whose
+trims release pages during the steps, and a fork whose first append copies
+the shared tail page. Slots, tables and page counts bit-exact; outputs within
+2e-2 (bf16)."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_harness import OracleSession, max_abs
+from libbuild import ensure_built
+from paged_decode_attention_store_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module")
+def kb():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    return ensure_built()
+
+
+@pytest.mark.parametrize("window,host_io", [(0, True), (40, True), (40, False)])
+def test_decode_step_matches_the_oracle(kb, window, host_io):
+    from paged_decode_attention_store_gb300.engine import PagedKVCache
+
+    Hq, Hkv, D, P, seed = 32, 8, 128, 16, 71
+    lengths = [300, 17, 64, 5]
+    B, steps = len(lengths), 24
+    num_pages = sum(-(-(L + steps) // P) for L in lengths) + 16
+    order = wl.free_stack_for_order(wl.permutation(seed, num_pages))
+    w = wl.Workload("engine", "bf16", Hq, Hkv, D, P, 1, num_pages, order, lengths, window=window,
+                    scale=1.0 / math.sqrt(D))
+    cache = PagedKVCache(num_pages, P, Hkv, D, 1, "bf16", max_requests=B + 1, max_seq_len=512, free_stack=order,
+                         device=DEV)
+    orc = OracleSession(w, B + 1, seed=seed)
+    # prefill requests 0..2 through the driver; request 3 is forked from 1 and then grows
+    for b in range(3):
+        cache.new(b)
+        orc.new(b)
+        slots = cache.append([b] * lengths[b])
+        k, v = wl.kv_rows(seed, 0, b, list(range(lengths[b])), Hkv, D, device=DEV)
+        cache.store(0, k, v, slots)
+        orc.append([b] * lengths[b], list(range(lengths[b])))
+        if window:
+            cache.trim(b, max(0, lengths[b] + 1 - window))
+            orc.trim(b, max(0, lengths[b] + 1 - window))
+    cache.fork(1, 3)
+    orc.fork(1, 3)
+    rids = np.arange(B, dtype=np.int32)
+    lens = [300, 17, 64, 17]
+    for step in range(1, steps + 1):
+        q = wl.q_rows(seed, step, 0, list(range(B)), Hq, D, device=DEV)
+        k, v = wl.kv_rows(seed, 0, list(range(B)), lens, Hkv, D, device=DEV)
+        if host_io:
+            qi, ki, vi = (x.cpu().pin_memory() for x in (q, k, v))
+            out = torch.empty((B, Hq, D), dtype=torch.bfloat16, pin_memory=True)
+        else:
+            qi, ki, vi = q, k, v
+            out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=DEV)
+        cache.decode_step(rids, [qi], [ki], [vi], [out], window, w.scale)
+        assert orc.append(list(range(B)), lens) is not None
+        lens = [L + 1 for L in lens]
+        got = out.float().cpu().numpy()
+        for b in range(B):
+            ref = orc.attend(0, b, lens[b], window, step=step)
+            assert max_abs(got[b], ref) <= 2e-2, f"step {step} request {b}"
+        if window:
+            for b in range(B):
+                orc.trim(b, max(0, lens[b] + 1 - window))
+        assert cache.host.used() == orc.pt.used()
+        assert cache.lengths[:B].tolist() == lens
+    assert cache.copies == 1  # request 3's first append copied the shared tail page
+    tab = cache.table.cpu().numpy()
+    for b in range(B):
+        row = orc.table_row(b)
+        assert tab[b, :len(row)].tolist() == row
+    cache.check()
