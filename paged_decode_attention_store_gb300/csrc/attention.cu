@@ -1,5 +1,7 @@
 // Decode attention: the general CUDA-core kernel, the index dump, and the C
 // ABI that picks between it and the tensor-core kernel (attention_tc.cu).
+#include <cstring>
+
 #include "attention.cuh"
 
 namespace kvp {
@@ -143,7 +145,7 @@ bool tc_eligible(const kvp_pool* pool, int Hq, int B, int* HG_out) {
   if (G > 16) return false;
   for (int HG = 8; HG >= 1; --HG) {
     if (Hkv % HG) continue;
-    if (tc_smem_bytes(HG, G) == 0) continue;
+    if (tc_num_qbuf(HG, G) == 0) continue;
     if (B > tc_max_batch(HG)) return false;
     *HG_out = HG;
     return true;
@@ -210,6 +212,16 @@ extern "C" int paged_decode_attention(const kvp_pool* pool, int layer, const voi
     char* ws = static_cast<char*>(workspace);
 
     TcArgs ta;
+    // The map is encoded once per pool and head group. Whether a stage can
+    // use it (16 contiguous, 16-aligned slots) is decided per stage in the
+    // kernel; without a map every row is loaded with its own copy.
+    if (mp->tmap_hg != HG && mp->tmap_hg != -HG) mp->tmap_hg = tc_encode_tmap(pool, HG, &mp->tmap) ? HG : -HG;
+    ta.use_tmap = mp->tmap_hg == HG;
+    if (ta.use_tmap) ta.tmap = mp->tmap;
+    else memset(&ta.tmap, 0, sizeof(ta.tmap));
+    ta.kvl_k = layer;
+    ta.kvl_v = pool->num_layers + layer;
+    ta.nq = tc_num_qbuf(HG, G);
     ta.T = T;
     ta.kv_layer = kv_layer;
     ta.kv_bytes = pool->kv_bytes;

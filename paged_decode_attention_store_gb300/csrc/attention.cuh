@@ -1,6 +1,8 @@
 // Internal declarations of the decode-attention kernels of libpagedkv.
 #pragma once
 
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace kvp {
@@ -40,6 +42,14 @@ __host__ inline WsLayout ws_layout(int num_ctas, int QH, int D) {
 }
 
 struct TcArgs {
+  // Tensor map over the whole KV buffer viewed as (d, slot, kv head, K/V x
+  // layer) with strides (2 B, row bytes, 256 B, layer bytes): the slot and
+  // head axes are deliberately not in stride order, so that a box of 16
+  // slots x HG heads lands in shared memory head-major (rows head*16+slot).
+  CUtensorMap tmap;
+  int use_tmap;            // load full, contiguous 16-slot groups with tensor copies
+  int kvl_k, kvl_v;        // the map's last coordinate for this layer's K and V
+  int nq;                  // Q buffers in shared memory (1 or 2)
   TableRef T;
   const char* kv_layer;    // K of this layer
   size_t kv_bytes;         // K -> V distance
@@ -105,8 +115,13 @@ __device__ __forceinline__ long long block_exclusive_scan(long long x, long long
 }
 
 // Shared-memory bytes of the tensor-core kernel for HG KV heads per CTA and
-// G query heads per KV head (0 if it does not fit).
-size_t tc_smem_bytes(int HG, int G);
+// G query heads per KV head with nq Q buffers (0 if it does not fit), and the
+// number of Q buffers it will use (2 when they fit, else 1; 0 if neither).
+size_t tc_smem_bytes(int HG, int G, int nq);
+int tc_num_qbuf(int HG, int G);
+// Encode the tensor map of a bf16 pool for HG heads per box; false if the
+// driver refuses it.
+bool tc_encode_tmap(const kvp_pool* pool, int HG, CUtensorMap* out);
 // Largest batch the in-kernel work split can take for HG.
 int tc_max_batch(int HG);
 // Launch the bf16, head_dim-128 kernel (one CTA per SM) and the combine

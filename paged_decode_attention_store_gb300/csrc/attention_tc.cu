@@ -19,8 +19,16 @@
 //   producer's 32 row copies while the other does its bookkeeping, so it
 //   never waits for work (one producer alone left it idle part of every
 //   stage, which capped the stream below the DRAM rate).
-// * Rows land at a pitch of HG*256+16 bytes, so the 8 rows an ldmatrix reads
-//   fall in 8 different 16-byte bank groups.
+// * Stages are 16-position groups aligned to multiples of 16. A full group
+//   whose 16 slots are contiguous and 16-aligned (always true for a block
+//   table whose page size is a multiple of 16; checked per stage for a raw
+//   location table) is loaded with four TMA tensor copies (K and V, two
+//   64-element halves of head_dim, 16 slots x HG heads each) through a map
+//   whose slot and head axes are swapped, so the rows land head-major with
+//   the 128-byte swizzle and ldmatrix stays conflict-free. Other stages
+//   (partial groups, scattered slots) take one bulk copy per token row at a
+//   pitch of HG*256+16 bytes, which spreads an ldmatrix's 8 rows over 8 bank
+//   groups as well.
 // * Each consumer warp runs the GQA group of its KV head on the legacy
 //   tensor-core path (mma.sync m16n8k16, bf16 in, fp32 accumulate) with the
 //   16 TOKENS of a stage on the M dimension and the G <= 8 query heads on N:
@@ -44,6 +52,8 @@
 //   launches, so their launch latency hides behind the preceding kernel.
 // * Every wait is bounded (2 s); on timeout the CTA records KVP_ERR_TIMEOUT,
 //   raises its abort flag, waits (bounded) for its own copies and returns.
+#include <cudaTypedefs.h>
+
 #include "attention.cuh"
 
 namespace kvp {
@@ -59,6 +69,7 @@ constexpr int kD = 128;       // head_dim
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr int kMinTokensPerCta = 64;
 constexpr int kStaticSmemBound = 512;                      // PlanState + the scan's warp sums
+constexpr int kAlignSlack = 1024;                          // the stage buffers start on 1024 bytes
 constexpr int kMaxDynamicSmem = 232448 - kStaticSmemBound;  // per-block opt-in limit minus static
 
 // Stage header, written by the producer, read by the consumers.
@@ -66,7 +77,7 @@ struct __align__(16) StageHdr {
   int live;    // 1: a stage of a piece, 0: no more work
   int t0;      // first position of the stage
   int vmask;   // bit j: token t0+j has K/V rows in the stage
-  int flags;   // 1 first stage of the piece, 2 last stage, (qbuf << 2)
+  int flags;   // 1 first stage of the piece, 2 last stage, (qbuf << 2), 8 tensor-copy layout
   int b;       // request
   int group;   // KV-head group
   int part;    // partial slot of a split piece, -1 when the piece is the whole request
@@ -86,7 +97,7 @@ struct __align__(16) StageMeta {
 };
 
 struct SmemMap {
-  int pitch, stage_bytes, qbytes;
+  int pitch, stage_bytes, qbytes, nq;
   unsigned char* stages;
   unsigned char* qbuf;
   StageMeta* meta;     // [kProducers][kQueue]
@@ -98,14 +109,19 @@ struct SmemMap {
   volatile int* abort_flag;
 };
 
-__device__ __forceinline__ SmemMap map_smem(unsigned char* smem, int HG, int G) {
+__host__ __device__ __forceinline__ int stage_stride(int HG) {
+  return (2 * kTok * (HG * 256 + 16) + 1023) & ~1023;
+}
+
+__device__ __forceinline__ SmemMap map_smem(unsigned char* smem, int HG, int G, int nq) {
   SmemMap s;
   s.pitch = HG * 256 + 16;
-  s.stage_bytes = 2 * kTok * s.pitch;
+  s.stage_bytes = stage_stride(HG);
   s.qbytes = HG * G * kD * 2;
-  s.stages = smem;
-  s.qbuf = smem + kStages * s.stage_bytes;
-  s.meta = reinterpret_cast<StageMeta*>(s.qbuf + 2 * s.qbytes);
+  s.nq = nq;
+  s.stages = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem) + 1023) & ~uintptr_t(1023));
+  s.qbuf = s.stages + kStages * s.stage_bytes;
+  s.meta = reinterpret_cast<StageMeta*>(s.qbuf + nq * s.qbytes);
   s.entries = reinterpret_cast<int*>(s.meta + kProducers * kQueue);
   s.hdr = reinterpret_cast<StageHdr*>(s.entries + kProducers * kQueue * kTok);
   s.full = reinterpret_cast<uint64_t*>(s.hdr + kStages);
@@ -300,9 +316,12 @@ __device__ void cur_next_piece(const TcArgs& a, Cursor& c) {
   cur_set_piece(c);
 }
 
+// End of the stage that starts at t0: the next multiple of 16, or the piece end.
+__device__ __forceinline__ int stage_end(int t0, int t_end) { return min((t0 & ~(kTok - 1)) + kTok, t_end); }
+
 // Move the cursor past one stage.
 __device__ __forceinline__ void cur_advance(const TcArgs& a, Cursor& c) {
-  c.t0 += kTok;
+  c.t0 = (c.t0 & ~(kTok - 1)) + kTok;
   if (c.t0 >= c.t_end) {
     cur_next_piece(a, c);
     ++c.piece;
@@ -340,14 +359,14 @@ __device__ void tc_producer(const TcArgs& a, const SmemMap& s, const PlanState& 
         m.live = 1;
         m.t0 = c.t0;
         m.t_end = c.t_end;
-        m.flags = (c.t0 == c.t_begin ? 1 : 0) | (c.t0 + kTok >= c.t_end ? 2 : 0);
+        m.flags = (c.t0 == c.t_begin ? 1 : 0) | ((c.t0 & ~(kTok - 1)) + kTok >= c.t_end ? 2 : 0);
         m.b = c.b;
         m.group = c.g;
         m.part = c.part;
         m.piece = c.piece;
         meta[qs] = m;
       }
-      if (lane < kTok && c.t0 + lane < c.t_end) {
+      if (lane < kTok && c.t0 + lane < stage_end(c.t0, c.t_end)) {
         const int t = c.t0 + lane;
         cp_async4(&entries[qs * kTok + lane],
                   a.T.table + (size_t)c.row * a.T.cols + (a.T.raw ? t : t / a.T.page_size));
@@ -378,10 +397,10 @@ __device__ void tc_producer(const TcArgs& a, const SmemMap& s, const PlanState& 
     }
     const bool first_stage = m.flags & 1;
     const bool last_stage = m.flags & 2;
-    const int qi = m.piece & 1;
-    if (first_stage && m.piece >= 2) {
-      ok = __all_sync(0xffffffffu, mbar_wait_bounded(&s.qempty[qi], ((m.piece - 2) >> 1) & 1, s.abort_flag, a.err,
-                                                     kWaitLimitNs));
+    const int qi = m.piece % s.nq;
+    if (first_stage && m.piece >= s.nq) {
+      ok = __all_sync(0xffffffffu, mbar_wait_bounded(&s.qempty[qi], ((m.piece - s.nq) / s.nq) & 1, s.abort_flag,
+                                                     a.err, kWaitLimitNs));
       if (!ok) break;
     }
     const int st = (int)(gs % kStages);
@@ -391,27 +410,57 @@ __device__ void tc_producer(const TcArgs& a, const SmemMap& s, const PlanState& 
       if (!ok) break;
     }
     const int t = m.t0 + j;
-    const int slot = t < m.t_end ? entry_to_slot(a.T, entries[qs * kTok + j], t, a.err) : -1;
-    const unsigned copies = __ballot_sync(0xffffffffu, slot >= 0);
-    if (lane == 0) {
-      StageHdr h;
-      h.live = 1;
-      h.t0 = m.t0;
-      h.vmask = (int)(copies & copies >> 16 & 0xffffu);
-      h.flags = (first_stage ? 1 : 0) | (last_stage ? 2 : 0) | (qi << 2);
-      h.b = m.b;
-      h.group = m.group;
-      h.part = m.part;
-      h.pad = 0;
-      s.hdr[st] = h;
-      const uint32_t tx = (uint32_t)__popc(copies) * row_copy + (first_stage ? (uint32_t)s.qbytes : 0u);
-      mbar_arrive_expect_tx(&s.full[st], tx);
-    }
-    __syncwarp();
-    if (slot >= 0) {
-      const char* src = a.kv_layer + (is_v ? a.kv_bytes : 0) + (size_t)slot * a.row_bytes + (size_t)m.group * row_copy;
-      unsigned char* dst = s.stages + (size_t)st * s.stage_bytes + (is_v ? kTok * s.pitch : 0) + j * s.pitch;
-      bulk_g2s(dst, src, row_copy, &s.full[st]);
+    const int send = stage_end(m.t0, m.t_end);
+    const int slot = t < send ? entry_to_slot(a.T, entries[qs * kTok + j], t, a.err) : -1;
+    // A full, 16-aligned group of contiguous, 16-aligned slots goes by tensor copies.
+    const int slot0 = __shfl_sync(0xffffffffu, slot, 0);
+    const bool page = a.use_tmap && (m.t0 & (kTok - 1)) == 0 && send - m.t0 == kTok && slot0 >= 0 &&
+                      (slot0 & (kTok - 1)) == 0 && __all_sync(0xffffffffu, slot == slot0 + j);
+    unsigned char* sbuf = s.stages + (size_t)st * s.stage_bytes;
+    if (page) {
+      if (lane == 0) {
+        StageHdr h;
+        h.live = 1;
+        h.t0 = m.t0;
+        h.vmask = 0xffff;
+        h.flags = (first_stage ? 1 : 0) | (last_stage ? 2 : 0) | (qi << 2) | 8;
+        h.b = m.b;
+        h.group = m.group;
+        h.part = m.part;
+        h.pad = 0;
+        s.hdr[st] = h;
+        const uint32_t box = (uint32_t)HG * kTok * 128u;  // 16 slots x HG heads x 64 elements
+        mbar_arrive_expect_tx(&s.full[st], 4 * box + (first_stage ? (uint32_t)s.qbytes : 0u));
+        const int hd0 = m.group * HG;
+        tma_load_4d(sbuf, &a.tmap, 0, slot0, hd0, a.kvl_k, &s.full[st]);
+        tma_load_4d(sbuf + box, &a.tmap, 64, slot0, hd0, a.kvl_k, &s.full[st]);
+        tma_load_4d(sbuf + 2 * box, &a.tmap, 0, slot0, hd0, a.kvl_v, &s.full[st]);
+        tma_load_4d(sbuf + 3 * box, &a.tmap, 64, slot0, hd0, a.kvl_v, &s.full[st]);
+      }
+      __syncwarp();
+    } else {
+      const unsigned copies = __ballot_sync(0xffffffffu, slot >= 0);
+      if (lane == 0) {
+        StageHdr h;
+        h.live = 1;
+        h.t0 = m.t0;
+        h.vmask = (int)(copies & copies >> 16 & 0xffffu);
+        h.flags = (first_stage ? 1 : 0) | (last_stage ? 2 : 0) | (qi << 2);
+        h.b = m.b;
+        h.group = m.group;
+        h.part = m.part;
+        h.pad = 0;
+        s.hdr[st] = h;
+        const uint32_t tx = (uint32_t)__popc(copies) * row_copy + (first_stage ? (uint32_t)s.qbytes : 0u);
+        mbar_arrive_expect_tx(&s.full[st], tx);
+      }
+      __syncwarp();
+      if (slot >= 0) {
+        const char* src =
+            a.kv_layer + (is_v ? a.kv_bytes : 0) + (size_t)slot * a.row_bytes + (size_t)m.group * row_copy;
+        unsigned char* dst = sbuf + (is_v ? kTok * s.pitch : 0) + j * s.pitch;
+        bulk_g2s(dst, src, row_copy, &s.full[st]);
+      }
     }
     if (first_stage && lane == 0) {
       const __nv_bfloat16* qsrc = a.q + ((size_t)m.b * a.Hq + (size_t)m.group * HG * a.G) * kD;
@@ -455,9 +504,15 @@ __device__ void tc_consumer(const TcArgs& a, const SmemMap& s, int h, int lane) 
   const uint32_t qbuf_u32 = smem_u32(s.qbuf);
   // ldmatrix row addresses of this lane (see the fragment layouts of
   // mma.m16n8k16: K as A[token][d], V^T as A[d][token] via .trans).
-  const uint32_t k_off = (uint32_t)(((lane & 7) + ((lane >> 3) & 1) * 8) * s.pitch + h * 256 + (lane >> 4) * 16);
-  const uint32_t v_off =
-      (uint32_t)(kTok * s.pitch + ((lane & 7) + (lane >> 4) * 8) * s.pitch + h * 256 + ((lane >> 3) & 1) * 16);
+  const int ktok = (lane & 7) + ((lane >> 3) & 1) * 8, vtok = (lane & 7) + (lane >> 4) * 8;
+  const uint32_t k_off = (uint32_t)(ktok * s.pitch + h * 256 + (lane >> 4) * 16);
+  const uint32_t v_off = (uint32_t)(kTok * s.pitch + vtok * s.pitch + h * 256 + ((lane >> 3) & 1) * 16);
+  // Tensor-copy layout: four boxes [K d0-63 | K d64-127 | V d0-63 | V d64-127],
+  // each rows (head*16 + slot) of 128 bytes, 16-byte chunk c stored at
+  // c ^ (row % 8); row % 8 is lane % 8 for both fragment row maps.
+  const uint32_t box = (uint32_t)HG * kTok * 128u;
+  const uint32_t kp_row = (uint32_t)(h * kTok + ktok) * 128u, vp_row = (uint32_t)(h * kTok + vtok) * 128u;
+  const uint32_t sw = (uint32_t)(lane & 7);
 
   uint32_t qf[8][NT][2];
   float o[8][NT][4];
@@ -530,10 +585,12 @@ __device__ void tc_consumer(const TcArgs& a, const SmemMap& s, int h, int lane) 
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) sa[nt][e] = sb[nt][e] = 0.f;
+    const bool pg = flags & 8;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       uint32_t af[4];
-      ldmatrix_x4(af, sbase + k_off + k * 32);
+      const uint32_t chunk = (uint32_t)(((k & 3) << 1) | (lane >> 4));
+      ldmatrix_x4(af, pg ? sbase + (uint32_t)(k >> 2) * box + kp_row + ((chunk ^ sw) << 4) : sbase + k_off + k * 32);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         if (k & 1)
@@ -582,7 +639,9 @@ __device__ void tc_consumer(const TcArgs& a, const SmemMap& s, int h, int lane) 
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       uint32_t af[4];
-      ldmatrix_x4_trans(af, sbase + v_off + i * 32);
+      const uint32_t chunk = (uint32_t)(((i & 3) << 1) | ((lane >> 3) & 1));
+      ldmatrix_x4_trans(af, pg ? sbase + (uint32_t)(2 + (i >> 2)) * box + vp_row + ((chunk ^ sw) << 4)
+                               : sbase + v_off + i * 32);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(o[i][nt], af, pb[nt][0], pb[nt][1]);
     }
@@ -630,18 +689,17 @@ __device__ void tc_consumer(const TcArgs& a, const SmemMap& s, int h, int lane) 
 }
 
 template <int NT>
-__global__ void __launch_bounds__(32 * (8 + kProducers), 1) tc_decode_kernel(const TcArgs a) {
+__global__ void __launch_bounds__(32 * (8 + kProducers), 1) tc_decode_kernel(const __grid_constant__ TcArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ PlanState ps;
-  const SmemMap s = map_smem(smem, a.HG, a.G);
+  const SmemMap s = map_smem(smem, a.HG, a.G, a.nq);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&s.full[i], 1);
       mbar_init(&s.empty[i], a.HG);
     }
-    mbar_init(&s.qempty[0], a.HG);
-    mbar_init(&s.qempty[1], a.HG);
+    for (int i = 0; i < a.nq; ++i) mbar_init(&s.qempty[i], a.HG);
     *s.abort_flag = 0;
     fence_mbar_init();
   }
@@ -707,9 +765,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
 
 }  // namespace
 
-size_t tc_smem_bytes(int HG, int G) {
-  const size_t pitch = (size_t)HG * 256 + 16;
-  const size_t bytes = kStages * 2 * kTok * pitch + 2 * (size_t)HG * G * kD * 2 +
+size_t tc_smem_bytes(int HG, int G, int nq) {
+  const size_t bytes = kAlignSlack + (size_t)kStages * stage_stride(HG) + (size_t)nq * HG * G * kD * 2 +
                        kProducers * kQueue * (sizeof(StageMeta) + kTok * sizeof(int)) + kStages * sizeof(StageHdr) +
                        (2 * kStages + 2) * sizeof(uint64_t) + 16;
   // the dynamic allocation plus the kernel's static shared memory (under
@@ -717,13 +774,41 @@ size_t tc_smem_bytes(int HG, int G) {
   return bytes <= kMaxDynamicSmem ? bytes : 0;
 }
 
+int tc_num_qbuf(int HG, int G) {
+  if (tc_smem_bytes(HG, G, 2)) return 2;
+  return tc_smem_bytes(HG, G, 1) ? 1 : 0;
+}
+
+bool tc_encode_tmap(const kvp_pool* pool, int HG, CUtensorMap* out) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  static bool looked_up = false;
+  if (!looked_up) {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    looked_up = true;
+  }
+  if (!encode || pool->dtype != KVP_BF16 || pool->head_dim != kD) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)pool->num_slots, (cuuint64_t)pool->kv_heads,
+                        (cuuint64_t)(2 * pool->num_layers)};
+  cuuint64_t strides[3] = {(cuuint64_t)pool->row_bytes, (cuuint64_t)kD * 2, (cuuint64_t)pool->layer_bytes};
+  cuuint32_t box[4] = {64, (cuuint32_t)kTok, (cuuint32_t)HG, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return encode(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, pool->buf, dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int tc_max_batch(int HG) {
-  const size_t scratch = kStages * 2 * kTok * ((size_t)HG * 256 + 16);
+  const size_t scratch = (size_t)kStages * stage_stride(HG);
   return (int)(scratch / kPlanScratchPerRequest);
 }
 
 cudaError_t launch_tc(const TcArgs& a, const CombineArgs& cb, cudaStream_t stream, void* ev_before, void* ev_after) {
-  const size_t smem = tc_smem_bytes(a.HG, a.G);
+  const size_t smem = tc_smem_bytes(a.HG, a.G, a.nq);
   if (smem == 0 || a.G > 16 || a.HG > 8 || a.B > tc_max_batch(a.HG)) return cudaErrorInvalidValue;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

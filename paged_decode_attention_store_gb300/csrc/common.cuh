@@ -1,6 +1,7 @@
 // Shared device helpers of libpagedkv (CUDA path only).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -25,6 +26,8 @@ struct kvp_pool {
   int device;
   void* ev_before;  // optional timing events around the next attention kernel
   void* ev_after;
+  CUtensorMap tmap;  // tensor map of the whole buffer for the tensor-core kernel,
+  int tmap_hg;       // heads per box it was encoded for (0: none yet, -HG: refused for HG)
 };
 
 namespace kvp {
@@ -164,6 +167,17 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
+}
+
+// TMA tensor load of one box of a 4-D tensor map into this CTA's shared
+// memory, completing its bytes on ``bar``. The map lives in kernel-parameter
+// (grid constant) memory; c0 is the innermost coordinate.
+__device__ __forceinline__ void tma_load_4d(void* dst, const void* tmap, int c0, int c1, int c2, int c3, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+      "[%6];" ::"r"(smem_u32(dst)),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+      : "memory");
 }
 
 // 4-byte asynchronous copy global -> shared (sm_80 cp.async), grouped per commit.

@@ -238,6 +238,43 @@ def test_bf16_block_decode_parity(kb, case):
     assert prod.error() == 0
 
 
+@pytest.mark.parametrize("P,mode", [(16, "block"), (4, "block"), (32, "block"), (1, "raw"), (8, "raw")])
+def test_bf16_mixed_contiguous_and_scattered_groups(kb, P, mode):
+    """Pages handed out mostly in address order, with a few swapped, so that
+    some 16-token groups are 16 contiguous, 16-aligned slots, some are
+    contiguous but misaligned and some are scattered; two layers, so that both
+    layers' K and V are addressed. Every kind of group must give the same
+    result as the oracle."""
+    lengths = [700, 45, 1290, 16, 333]
+    B, layers, steps = len(lengths), 2, 2
+    num_pages = sum(-(-(L + steps) // P) for L in lengths) + 8
+    order = list(range(num_pages))
+    rng = random.Random(P)
+    for _ in range(max(2, num_pages // 40)):
+        i, j = rng.randrange(num_pages), rng.randrange(num_pages)
+        order[i], order[j] = order[j], order[i]
+    w = wl.Workload("test", "bf16", 32, 8, 128, P, layers, num_pages, wl.free_stack_for_order(order),
+                    list(lengths), scale=1.0 / math.sqrt(128))
+    cols = (max(lengths) + steps + 64) if mode == "raw" else max(-(-(L + steps) // P) for L in lengths) + 2
+    prod = ProductSession(kb, w, DEV, max_requests=B, cols=cols, mode=mode, seed=11)
+    orc = OracleSession(w, B, mode=mode, seed=11, raw_cols=prod.table.shape[1] if mode == "raw" else None)
+    for b, L in enumerate(lengths):
+        prod.new(b)
+        orc.new(b)
+        assert prod.append([b] * L, list(range(L))) == orc.append([b] * L, list(range(L)))
+    lens = list(lengths)
+    for step in range(1, steps + 1):
+        rids = list(range(B))
+        assert prod.append(rids, lens) == orc.append(rids, lens)
+        lens = [L + 1 for L in lens]
+        for layer in range(layers):
+            out = prod.attend(layer, rids, lens, 0, step=step).float().cpu().numpy()
+            for b in range(B):
+                d = max_abs(out[b], orc.attend(layer, b, lens[b], 0, step=step))
+                assert d <= 2e-2, f"layer {layer} step {step} request {b}: {d}"
+    assert prod.error() == 0
+
+
 @pytest.mark.parametrize("P", [16, 1])
 def test_bf16_raw_location_parity_with_dummy_row(kb, P):
     """mini-sglang layout: (2, layers, pages + 1 dummy, P, 8, 128), raw token
