@@ -167,6 +167,43 @@ int paged_decode_attention(const kvp_pool* pool, int layer, const void* q,
                            size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * store_cache_and_attention: one layer of a decode step in one launch:
+ *     page_table_write(table, tw_rows, tw_cols, tw_vals, n_tw, expand);
+ *     store_cache(pool, layer, k, v, out_loc, batch);
+ *     paged_decode_attention(pool, layer, q, ...);
+ * with expand = page_size for a raw-location table, else 1; the results
+ * (table, cache rows, out) are those of the three calls in that order (the
+ * mini-sglang code series, part 4: host-built lists, one scatter, then the
+ * attention). Not a separate operation of the source pages: it saves two
+ * launches and their ramps per step.
+ * In one launch the attention cannot wait for the writes, so the call
+ * relies on what a decode step guarantees:
+ *   - out_loc[b] is the slot of request b's newest position
+ *     (context_lens[b] - 1): that position is read from k[b], v[b];
+ *   - the table writes touch no entry of an attended position other than
+ *     the newest ones (new pages for this step's tokens). Releases of a
+ *     sliding window and copy-on-write pages are written before (copy) or
+ *     after (release) the call, not through it.
+ *   k, v      device [batch, kv_heads, head_dim], pool dtype, 16-byte aligned.
+ *   out_loc   device int32 [batch].
+ *   tw_*      device int32 [n_tw] (n_tw may be 0; then they may be NULL).
+ * Other arguments, the workspace and the errors as for
+ * paged_decode_attention and the two writes. Pools without the fused kernel
+ * (fp32, head_dim other than 128) run the three operations in sequence.
+ * ---------------------------------------------------------------------- */
+int store_cache_and_attention(const kvp_pool* pool, int layer, const void* q,
+                              const void* k, const void* v,
+                              const int32_t* out_loc, int batch,
+                              int num_q_heads, int32_t* table,
+                              int table_rows_total, int table_cols,
+                              int table_mode, const int32_t* table_rows,
+                              const int32_t* context_lens,
+                              const int32_t* tw_rows, const int32_t* tw_cols,
+                              const int32_t* tw_vals, int n_tw, int window,
+                              float scale, void* out, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * paged_decode_attention_noalloc: paged_decode_attention for callers that
  * cannot allocate device memory at the point where they run attention (code
  * inside another framework's memory pool or under a budget that forbids new

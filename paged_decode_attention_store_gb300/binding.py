@@ -47,6 +47,8 @@ SIGNATURES = {
     "paged_decode_attention_workspace_size": [_vp, _i, _i, _szp],
     "paged_decode_attention": [_vp, _i, _vp, _i, _i, _vp, _i, _i, _i, _vp, _vp, _i, _f, _vp, _vp, _sz, _vp],
     "paged_decode_attention_noalloc": [_vp, _i, _vp, _i, _i, _vp, _i, _i, _i, _vp, _vp, _i, _f, _vp, _vp],
+    "store_cache_and_attention": [_vp, _i, _vp, _vp, _vp, _vp, _i, _i, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _i,
+                                  _i, _f, _vp, _vp, _sz, _vp],
     "gather_indices": [_vp, _vp, _i, _i, _i, _vp, _vp, _i, _i, _vp, _i, _vp],
     "kvp_sync_error": [_vp, _vp, _ip],
     "kvp_pool_set_timing_events": [_vp, _vp, _vp],
@@ -222,6 +224,38 @@ def paged_decode_attention(pool, layer, q, table, table_mode, context_lens, wind
                                         table.shape[1], table_mode, _ptr(table_rows), _ptr(context_lens),
                                         int(window or 0), float(scale), _ptr(out), ws_ptr, ws_bytes,
                                         _stream(stream)), "paged_decode_attention")
+
+
+def store_cache_and_attention(pool, layer, q, k, v, out_loc, table, table_mode, context_lens, window, scale, out,
+                              workspace, table_rows=None, table_writes=None, stream=None):
+    """store_cache + paged_decode_attention of one layer in one launch, with
+    the step's new-page table writes (rows, cols, vals device int32 tensors)
+    applied in the same launch. out_loc[b] must be the slot of request b's
+    newest position; see include/pagedkv.h for what the table writes may be."""
+    dt = _TORCH_DTYPE[pool.dtype]
+    for name, x in (("q", q), ("k", k), ("v", v), ("out", out)):
+        _dev(x, dt, name)
+    _dev(out_loc, torch.int32, "out_loc")
+    _dev(table, torch.int32, "table")
+    _dev(context_lens, torch.int32, "context_lens")
+    if table_rows is not None:
+        _dev(table_rows, torch.int32, "table_rows")
+    B, Hq = q.shape[0], q.shape[1]
+    if out.shape != q.shape or context_lens.numel() != B or out_loc.numel() != B or k.shape[0] != B:
+        raise ValueError("q/out [B, Hq, D], k/v [B, Hkv, D], out_loc and context_lens [B]")
+    if table_writes is None:
+        tw = (None, None, None, 0)
+    else:
+        r, c, vals = table_writes
+        for name, x in (("rows", r), ("cols", c), ("vals", vals)):
+            _dev(x, torch.int32, name)
+        tw = (_ptr(r), _ptr(c), _ptr(vals), r.numel())
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (_ptr(workspace), workspace.numel() * workspace.element_size())
+    _check(lib().store_cache_and_attention(pool.handle, layer, _ptr(q), _ptr(k), _ptr(v), _ptr(out_loc), B, Hq,
+                                           _ptr(table), table.shape[0], table.shape[1], table_mode,
+                                           _ptr(table_rows), _ptr(context_lens), *tw, int(window or 0),
+                                           float(scale), _ptr(out), ws_ptr, ws_bytes, _stream(stream)),
+           "store_cache_and_attention")
 
 
 def paged_decode_attention_noalloc(pool, layer, q, table, table_mode, context_lens, window, scale, out,

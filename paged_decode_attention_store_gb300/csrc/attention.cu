@@ -184,11 +184,24 @@ extern "C" int paged_decode_attention_workspace_size(const kvp_pool* pool, int b
   return KVP_OK;
 }
 
-extern "C" int paged_decode_attention(const kvp_pool* pool, int layer, const void* q, int batch, int num_q_heads,
-                                      const int32_t* table, int table_rows_total, int table_cols, int table_mode,
-                                      const int32_t* table_rows, const int32_t* context_lens, int window,
-                                      float scale, void* out, void* workspace, size_t workspace_bytes,
-                                      void* stream) {
+namespace {
+
+// The extra inputs of a fused step (store_cache_and_attention).
+struct FuseIn {
+  const void* k;
+  const void* v;
+  const int32_t* out_loc;
+  int32_t* table;
+  const int32_t* tw_rows;
+  const int32_t* tw_cols;
+  const int32_t* tw_vals;
+  int n_tw;
+};
+
+int attention_impl(const kvp_pool* pool, int layer, const void* q, int batch, int num_q_heads, const int32_t* table,
+                   int table_rows_total, int table_cols, int table_mode, const int32_t* table_rows,
+                   const int32_t* context_lens, int window, float scale, void* out, void* workspace,
+                   size_t workspace_bytes, void* stream, const FuseIn* fz) {
   if (!pool || !q || !table || !context_lens || !out) return KVP_ERR_INVALID_ARG;
   if (layer < 0 || layer >= pool->num_layers || batch <= 0 || num_q_heads <= 0) return KVP_ERR_INVALID_ARG;
   if (num_q_heads % pool->kv_heads) return KVP_ERR_INVALID_ARG;
@@ -202,6 +215,16 @@ extern "C" int paged_decode_attention(const kvp_pool* pool, int layer, const voi
 
   int HG = 0;
   kvp_pool* mp = const_cast<kvp_pool*>(pool);
+  const int expand = table_mode == KVP_RAW_LOCATIONS ? pool->page_size : 1;
+  if (fz && !tc_eligible(pool, num_q_heads, batch, &HG)) {
+    // no fused kernel for this pool: the same three operations in sequence
+    int rc;
+    if (fz->n_tw && (rc = page_table_write(fz->table, table_rows_total, table_cols, fz->tw_rows, fz->tw_cols,
+                                           fz->tw_vals, fz->n_tw, expand, pool->err, stream)) != KVP_OK)
+      return rc;
+    if ((rc = store_cache(pool, layer, fz->k, fz->v, fz->out_loc, batch, stream)) != KVP_OK) return rc;
+    fz = nullptr;
+  }
   if (tc_eligible(pool, num_q_heads, batch, &HG)) {
     if (reinterpret_cast<uintptr_t>(q) & 15) return KVP_ERR_INVALID_ARG;
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255)) return KVP_ERR_INVALID_ARG;
@@ -242,6 +265,16 @@ extern "C" int paged_decode_attention(const kvp_pool* pool, int layer, const voi
     ta.part_ml = reinterpret_cast<float*>(ws + L.part_ml);
     ta.part_o = reinterpret_cast<float*>(ws + L.part_o);
     ta.err = pool->err;
+    ta.fused = fz != nullptr;
+    ta.knew = static_cast<const uint4*>(fz ? fz->k : nullptr);
+    ta.vnew = static_cast<const uint4*>(fz ? fz->v : nullptr);
+    ta.out_loc = fz ? fz->out_loc : nullptr;
+    ta.tw_table = fz ? fz->table : nullptr;
+    ta.tw_rows = fz ? fz->tw_rows : nullptr;
+    ta.tw_cols = fz ? fz->tw_cols : nullptr;
+    ta.tw_vals = fz ? fz->tw_vals : nullptr;
+    ta.n_tw = fz ? fz->n_tw : 0;
+    ta.tw_expand = expand;
 
     CombineArgs ca;
     ca.merge = ta.merge;
@@ -287,6 +320,32 @@ extern "C" int paged_decode_attention(const kvp_pool* pool, int layer, const voi
     mp->ev_before = mp->ev_after = nullptr;
   }
   return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" int paged_decode_attention(const kvp_pool* pool, int layer, const void* q, int batch, int num_q_heads,
+                                      const int32_t* table, int table_rows_total, int table_cols, int table_mode,
+                                      const int32_t* table_rows, const int32_t* context_lens, int window,
+                                      float scale, void* out, void* workspace, size_t workspace_bytes,
+                                      void* stream) {
+  return attention_impl(pool, layer, q, batch, num_q_heads, table, table_rows_total, table_cols, table_mode,
+                        table_rows, context_lens, window, scale, out, workspace, workspace_bytes, stream, nullptr);
+}
+
+extern "C" int store_cache_and_attention(const kvp_pool* pool, int layer, const void* q, const void* k,
+                                         const void* v, const int32_t* out_loc, int batch, int num_q_heads,
+                                         int32_t* table, int table_rows_total, int table_cols, int table_mode,
+                                         const int32_t* table_rows, const int32_t* context_lens,
+                                         const int32_t* tw_rows, const int32_t* tw_cols, const int32_t* tw_vals,
+                                         int n_tw, int window, float scale, void* out, void* workspace,
+                                         size_t workspace_bytes, void* stream) {
+  if (!k || !v || !out_loc || n_tw < 0 || (n_tw > 0 && (!tw_rows || !tw_cols || !tw_vals)))
+    return KVP_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15) return KVP_ERR_INVALID_ARG;
+  const FuseIn fz = {k, v, out_loc, table, tw_rows, tw_cols, tw_vals, n_tw};
+  return attention_impl(pool, layer, q, batch, num_q_heads, table, table_rows_total, table_cols, table_mode,
+                        table_rows, context_lens, window, scale, out, workspace, workspace_bytes, stream, &fz);
 }
 
 extern "C" int gather_indices(const kvp_pool* pool, const int32_t* table, int table_rows_total, int table_cols,

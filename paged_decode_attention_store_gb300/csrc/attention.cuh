@@ -64,6 +64,18 @@ struct TcArgs {
   float* part_ml;
   float* part_o;
   int32_t* err;
+  // Fused step (store_cache_and_attention): this launch also applies the
+  // step's table writes and stores the new K/V rows; each request's newest
+  // position is read from the new rows rather than from the cache.
+  int fused;
+  const uint4* knew;       // [B, kv_heads, D] new K rows
+  const uint4* vnew;       // [B, kv_heads, D] new V rows
+  const int32_t* out_loc;  // [B] slots of the new rows
+  int32_t* tw_table;       // the table, writable
+  const int32_t* tw_rows;
+  const int32_t* tw_cols;
+  const int32_t* tw_vals;
+  int n_tw, tw_expand;
 };
 
 struct CombineArgs {

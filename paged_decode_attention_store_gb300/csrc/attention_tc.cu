@@ -77,7 +77,8 @@ struct __align__(16) StageHdr {
   int live;    // 1: a stage of a piece, 0: no more work
   int t0;      // first position of the stage
   int vmask;   // bit j: token t0+j has K/V rows in the stage
-  int flags;   // 1 first stage of the piece, 2 last stage, (qbuf << 2), 8 tensor-copy layout
+  int flags;   // 1 first stage of the piece, 2 last stage, (qbuf << 2), 8 tensor-copy layout,
+               // 16 odd piece (selects the qempty barrier)
   int b;       // request
   int group;   // KV-head group
   int part;    // partial slot of a split piece, -1 when the piece is the whole request
@@ -89,7 +90,7 @@ struct __align__(16) StageMeta {
   int live;    // 0: no more work; t0 then holds the number of stages of the CTA
   int t0;
   int t_end;   // end of the piece
-  int flags;   // 1 first stage of the piece, 2 last stage
+  int flags;   // 1 first stage of the piece, 2 last stage, 16 the stage holds a fused step's newest position
   int b;
   int group;
   int part;
@@ -354,22 +355,28 @@ __device__ void tc_producer(const TcArgs& a, const SmemMap& s, const PlanState& 
     }
     const int qs = (int)(queued % kQueue);
     if (!c.done) {
+      const int se = stage_end(c.t0, c.t_end);
+      // In a fused step the request's newest position (the piece ends at
+      // the request's end) is read from the new rows, at the slot out_loc
+      // gives: its table entry may be written by this very launch.
+      const int t_new = (a.fused && c.t_end == c.lo + c.n && se == c.t_end) ? c.t_end - 1 : -1;
       if (lane == 0) {
         StageMeta m;
         m.live = 1;
         m.t0 = c.t0;
         m.t_end = c.t_end;
-        m.flags = (c.t0 == c.t_begin ? 1 : 0) | ((c.t0 & ~(kTok - 1)) + kTok >= c.t_end ? 2 : 0);
+        m.flags = (c.t0 == c.t_begin ? 1 : 0) | (se == c.t_end ? 2 : 0) | (t_new >= 0 ? 16 : 0);
         m.b = c.b;
         m.group = c.g;
         m.part = c.part;
         m.piece = c.piece;
         meta[qs] = m;
       }
-      if (lane < kTok && c.t0 + lane < stage_end(c.t0, c.t_end)) {
+      if (lane < kTok && c.t0 + lane < se) {
         const int t = c.t0 + lane;
-        cp_async4(&entries[qs * kTok + lane],
-                  a.T.table + (size_t)c.row * a.T.cols + (a.T.raw ? t : t / a.T.page_size));
+        cp_async4(&entries[qs * kTok + lane], t == t_new ? a.out_loc + c.b
+                                                         : a.T.table + (size_t)c.row * a.T.cols +
+                                                               (a.T.raw ? t : t / a.T.page_size));
       }
       cur_advance(a, c);
       ++next_gs;
@@ -398,24 +405,43 @@ __device__ void tc_producer(const TcArgs& a, const SmemMap& s, const PlanState& 
     const bool first_stage = m.flags & 1;
     const bool last_stage = m.flags & 2;
     const int qi = m.piece % s.nq;
-    if (first_stage && m.piece >= s.nq) {
-      ok = __all_sync(0xffffffffu, mbar_wait_bounded(&s.qempty[qi], ((m.piece - s.nq) / s.nq) & 1, s.abort_flag,
-                                                     a.err, kWaitLimitNs));
-      if (!ok) break;
-    }
     const int st = (int)(gs % kStages);
     if (gs >= kStages) {
       ok = __all_sync(0xffffffffu, mbar_wait_bounded(&s.empty[st], (uint32_t)((gs / kStages - 1) & 1),
                                                      s.abort_flag, a.err, kWaitLimitNs));
       if (!ok) break;
     }
+    // Q buffer reuse: piece p overwrites the buffer of piece p - nq, so it
+    // waits until the consumers have loaded that piece's Q. Consumers
+    // arrive on qempty[piece & 1]; piece p - nq is phase (p - nq) / 2 of
+    // barrier (p - nq) & 1. The parity test is exact because every stage
+    // up to gs - kStages is consumed (the wait above), so the barrier's
+    // previous piece (p - nq - 2, whose first stage is at most gs - 3) has
+    // been loaded and the barrier is at most one phase behind.
+    if (first_stage && m.piece >= s.nq) {
+      const int pw = m.piece - s.nq;
+      ok = __all_sync(0xffffffffu, mbar_wait_bounded(&s.qempty[pw & 1], (uint32_t)((pw >> 1) & 1), s.abort_flag,
+                                                     a.err, kWaitLimitNs));
+      if (!ok) break;
+    }
     const int t = m.t0 + j;
     const int send = stage_end(m.t0, m.t_end);
-    const int slot = t < send ? entry_to_slot(a.T, entries[qs * kTok + j], t, a.err) : -1;
-    // A full, 16-aligned group of contiguous, 16-aligned slots goes by tensor copies.
+    const bool fresh = (m.flags & 16) && t == m.t_end - 1;  // the newest position of a fused step
+    int slot = -1;
+    if (fresh) {
+      slot = entries[qs * kTok + j];  // out_loc of the request
+      if ((unsigned)slot >= (unsigned)a.T.num_slots) {
+        set_error(a.err, KVP_ERR_BAD_INDEX);
+        slot = -1;
+      }
+    } else if (t < send) {
+      slot = entry_to_slot(a.T, entries[qs * kTok + j], t, a.err);
+    }
+    // A full, 16-aligned group of contiguous, 16-aligned slots goes by tensor
+    // copies (never the group of a fused step's newest position).
     const int slot0 = __shfl_sync(0xffffffffu, slot, 0);
-    const bool page = a.use_tmap && (m.t0 & (kTok - 1)) == 0 && send - m.t0 == kTok && slot0 >= 0 &&
-                      (slot0 & (kTok - 1)) == 0 && __all_sync(0xffffffffu, slot == slot0 + j);
+    const bool page = a.use_tmap && !(m.flags & 16) && (m.t0 & (kTok - 1)) == 0 && send - m.t0 == kTok &&
+                      slot0 >= 0 && (slot0 & (kTok - 1)) == 0 && __all_sync(0xffffffffu, slot == slot0 + j);
     unsigned char* sbuf = s.stages + (size_t)st * s.stage_bytes;
     if (page) {
       if (lane == 0) {
@@ -423,7 +449,7 @@ __device__ void tc_producer(const TcArgs& a, const SmemMap& s, const PlanState& 
         h.live = 1;
         h.t0 = m.t0;
         h.vmask = 0xffff;
-        h.flags = (first_stage ? 1 : 0) | (last_stage ? 2 : 0) | (qi << 2) | 8;
+        h.flags = (first_stage ? 1 : 0) | (last_stage ? 2 : 0) | (qi << 2) | 8 | ((m.piece & 1) << 4);
         h.b = m.b;
         h.group = m.group;
         h.part = m.part;
@@ -445,7 +471,7 @@ __device__ void tc_producer(const TcArgs& a, const SmemMap& s, const PlanState& 
         h.live = 1;
         h.t0 = m.t0;
         h.vmask = (int)(copies & copies >> 16 & 0xffffu);
-        h.flags = (first_stage ? 1 : 0) | (last_stage ? 2 : 0) | (qi << 2);
+        h.flags = (first_stage ? 1 : 0) | (last_stage ? 2 : 0) | (qi << 2) | ((m.piece & 1) << 4);
         h.b = m.b;
         h.group = m.group;
         h.part = m.part;
@@ -457,7 +483,9 @@ __device__ void tc_producer(const TcArgs& a, const SmemMap& s, const PlanState& 
       __syncwarp();
       if (slot >= 0) {
         const char* src =
-            a.kv_layer + (is_v ? a.kv_bytes : 0) + (size_t)slot * a.row_bytes + (size_t)m.group * row_copy;
+            fresh ? reinterpret_cast<const char*>(is_v ? a.vnew : a.knew) + (size_t)m.b * a.row_bytes +
+                        (size_t)m.group * row_copy
+                  : a.kv_layer + (is_v ? a.kv_bytes : 0) + (size_t)slot * a.row_bytes + (size_t)m.group * row_copy;
         unsigned char* dst = sbuf + (is_v ? kTok * s.pitch : 0) + j * s.pitch;
         bulk_g2s(dst, src, row_copy, &s.full[st]);
       }
@@ -514,6 +542,41 @@ __device__ void tc_consumer(const TcArgs& a, const SmemMap& s, int h, int lane) 
   const uint32_t kp_row = (uint32_t)(h * kTok + ktok) * 128u, vp_row = (uint32_t)(h * kTok + vtok) * 128u;
   const uint32_t sw = (uint32_t)(lane & 7);
 
+  if (a.fused) {
+    // The step's table writes and new K/V rows, spread over every consumer
+    // thread of the grid while the first stages are in flight. Nothing this
+    // launch reads depends on them (the newest positions come from the new
+    // rows; the table writes only add pages for those positions).
+    const long long tid = (long long)blockIdx.x * (HG * 32) + h * 32 + lane;
+    const long long nthreads = (long long)a.num_ctas * HG * 32;
+    const long long tw_total = (long long)a.n_tw * a.tw_expand;
+    for (long long u = tid; u < tw_total; u += nthreads) {
+      const int i = (int)(u / a.tw_expand), jj = (int)(u % a.tw_expand);
+      const int r = __ldg(a.tw_rows + i);
+      const long long col = (long long)__ldg(a.tw_cols + i) * a.tw_expand + jj;
+      const int v = __ldg(a.tw_vals + i);
+      if ((unsigned)r >= (unsigned)a.T.rows_total || col < 0 || col >= a.T.cols) {
+        set_error(a.err, KVP_ERR_BAD_INDEX);
+        continue;
+      }
+      a.tw_table[(size_t)r * a.T.cols + col] = v < 0 ? -1 : v * a.tw_expand + jj;
+    }
+    const int chunks = (int)(a.row_bytes / 16);
+    const long long st_total = (long long)a.B * 2 * chunks;
+    for (long long u = tid; u < st_total; u += nthreads) {
+      const int cch = (int)(u % chunks);
+      const long long ik = u / chunks;
+      const int kv = (int)(ik & 1), i = (int)(ik >> 1);
+      const int slot = __ldg(a.out_loc + i);
+      if ((unsigned)slot >= (unsigned)a.T.num_slots) {
+        if (kv == 0 && cch == 0) set_error(a.err, KVP_ERR_BAD_INDEX);
+        continue;
+      }
+      const uint4 val = __ldg((kv ? a.vnew : a.knew) + (size_t)i * chunks + cch);
+      reinterpret_cast<uint4*>(const_cast<char*>(a.kv_layer) + (kv ? a.kv_bytes : 0))[(size_t)slot * chunks + cch] = val;
+    }
+  }
+
   uint32_t qf[8][NT][2];
   float o[8][NT][4];
   float m[NT][2], l[NT][2];
@@ -557,7 +620,7 @@ __device__ void tc_consumer(const TcArgs& a, const SmemMap& s, int h, int lane) 
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s.qempty[qi]);
+      if (lane == 0) mbar_arrive(&s.qempty[(flags >> 4) & 1]);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         m[nt][0] = m[nt][1] = -INFINITY;
@@ -699,7 +762,7 @@ __global__ void __launch_bounds__(32 * (8 + kProducers), 1) tc_decode_kernel(con
       mbar_init(&s.full[i], 1);
       mbar_init(&s.empty[i], a.HG);
     }
-    for (int i = 0; i < a.nq; ++i) mbar_init(&s.qempty[i], a.HG);
+    for (int i = 0; i < 2; ++i) mbar_init(&s.qempty[i], a.HG);
     *s.abort_flag = 0;
     fence_mbar_init();
   }

@@ -204,6 +204,8 @@ BF16_CASES = [
     (32, 16, 16, [90, 1200], 0),                          # 16 KV heads: two head groups
     (32, 8, 16, [1000, 37, 2500], 100),                   # window without trim
     (32, 8, 1, [300, 1, 77], 0),                          # page size 1
+    # GQA 8 keeps one Q buffer: runs of one-stage pieces reuse it back to back
+    (64, 8, 8, [7, 8, 300, 1, 2, 3, 9, 1, 1, 17, 4, 33, 2, 5], 0),
 ]
 
 
