@@ -4,8 +4,10 @@
 One step = one decode step of the whole hot path for every request of the
 workload: host bookkeeping (append, copy-on-write, window trim), the device
 table write, copy-on-write page copies, store_cache of the new K/V rows and
-paged decode attention (plan + attention + split-K combine), for every
-layer. Prints one JSON line.
+paged decode attention (work split, attention, split-K combine), for every
+layer; the store, the table writes and the attention of a layer are one
+launch (store_cache_and_attention), followed by the combine. Prints one
+JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the CPU oracle on the same workload
@@ -129,16 +131,32 @@ def attention_bytes(sc, lens):
     return kv + qo + tab + 4 * len(lens)
 
 
+def store_bytes(sc, B):
+    """store_cache of one layer: read k and v, write them, read out_loc."""
+    w = sc.w
+    row = w.Hkv * w.D * (2 if w.dtype == "bf16" else 4)
+    return 4 * B * row + 4 * B
+
+
+def table_write_bytes(sc, n):
+    """n (row, col, value) writes: read 12 B, write one entry per page or P per page."""
+    return n * (12 + 4 * (sc.w.P if sc.raw else 1))
+
+
 def step_bytes(sc, lens, n_writes, n_cows, n_trim_writes):
     w = sc.w
-    elem = 2 if w.dtype == "bf16" else 4
-    row = w.Hkv * w.D * elem
-    B = len(lens)
-    store = 4 * B * row + 4 * B  # read k and v, write them, read out_loc
-    expand = w.P if sc.raw else 1
-    tw = (n_writes + n_trim_writes) * (12 + 4 * expand)
+    row = w.Hkv * w.D * (2 if w.dtype == "bf16" else 4)
     copies = n_cows * w.layers * 2 * 2 * w.P * row
-    return w.layers * (attention_bytes(sc, lens) + store) + tw + copies
+    return (w.layers * (attention_bytes(sc, lens) + store_bytes(sc, len(lens)))
+            + table_write_bytes(sc, n_writes + n_trim_writes) + copies)
+
+
+def fused_launch_bytes(sc, lens, n_writes, n_cows):
+    """Mean algorithmic bytes of one store_cache_and_attention launch of a
+    step: the layer's attention and store, and (first layer only, unless the
+    step copies pages) the step's table writes."""
+    tw = table_write_bytes(sc, n_writes) if n_cows == 0 else 0
+    return attention_bytes(sc, lens) + store_bytes(sc, len(lens)) + tw / sc.w.layers
 
 
 # ---------------------------------------------------------------------------
@@ -252,31 +270,39 @@ def prepare_steps(sc, cache, lens, first_step, n_steps, dev, host_inputs=False):
             st.k.append(k)
             st.v.append(v)
         st.bytes = step_bytes(sc, lens, st.n_writes, st.n_cows, st.n_post)
-        st.attn_bytes = attention_bytes(sc, lens)
+        st.attn_bytes = fused_launch_bytes(sc, lens, st.n_writes, st.n_cows)
         steps.append(st)
     return steps, lens
 
 
 def run_step(sc, cache, st, outs, events=None):
-    """Issue one prepared step; returns the number of kernels launched."""
+    """Issue one prepared step; returns the number of kernels launched.
+
+    Copy-on-write pages first (with the step's table writes when there are
+    copies: a copied tail page's entry is read by the attention), then one
+    store_cache_and_attention launch per layer, the first carrying the
+    step's new-page table writes; last the window's releases."""
     from paged_decode_attention_store_gb300 import binding as kb
 
     w = sc.w
     P = w.P
     n = 0
-    if st.pre is not None:
-        kb.page_table_write(cache.table, *st.pre, expand=P if sc.raw else 1, error_word=cache.pool.error_word)
-        n += 1
+    pre = st.pre
     if st.cows is not None:
         kb.copy_pages(cache.pool, *st.cows)
         n += 1
-    per_attn = 2 if (w.dtype == "bf16" and w.D == 128) else 1  # attention + combine, or the general kernel
+        if pre is not None:
+            kb.page_table_write(cache.table, *pre, expand=P if sc.raw else 1, error_word=cache.pool.error_word)
+            n += 1
+            pre = None
+    fused = w.dtype == "bf16" and w.D == 128  # one launch; else table write, store and the general kernel
     for layer in range(w.layers):
-        cache.store(layer, st.k[layer], st.v[layer], st.out_loc)
         if events is not None:
             kb.kvp_pool_set_timing_events(cache.pool, *events.pop())
-        cache.attend(layer, st.q[layer], st.lens, sc.window, w.scale, outs[layer])
-        n += 1 + per_attn
+        tw = pre if layer == 0 else None
+        cache.store_and_attend(layer, st.q[layer], st.k[layer], st.v[layer], st.out_loc, st.lens, sc.window,
+                               w.scale, outs[layer], table_writes=tw)
+        n += 2 if fused else 2 + (tw is not None)  # fused kernel + combine, or write, store, general kernel
     if st.post is not None:
         kb.page_table_write(cache.table, *st.post, expand=P if sc.raw else 1, error_word=cache.pool.error_word)
         n += 1

@@ -151,7 +151,8 @@ int copy_pages(const kvp_pool* pool, const int32_t* src, const int32_t* dst,
  *   workspace    device, >= paged_decode_attention_workspace_size() bytes,
  *                256-byte aligned; scratch for the work plan and split-K
  *                partials. Its contents need no initialisation and are
- *                clobbered.
+ *                clobbered; two calls that may run at the same time on the
+ *                GPU need separate workspaces.
  * Device-detected errors (L out of range, hole or out-of-range entry in the
  * attended range) set KVP_ERR_BAD_INDEX; an invalid request's output is
  * zero-filled.
@@ -315,10 +316,12 @@ int kvp_host_trim(kvp_host* h, int rid, int keep_from, int32_t* tw_rows,
  *      (caller-owned PINNED host memory) and copied to dev_meta (device):
  *      [slots n | table writes 3*w | copy pairs 2*c | lengths n | rows n |
  *       trim writes 3*t];
- *   3. page_table_write, copy_pages, then for each layer l: wait for
- *      layer_ready[l] (a cudaEvent_t, or NULL), store_cache(k[l], v[l]),
- *      paged_decode_attention(q[l] -> out[l]), record layer_done[l] (or
- *      NULL); q/k/v/out are per-layer DEVICE pointers;
+ *   3. copy_pages, then for each layer l: wait for layer_ready[l] (a
+ *      cudaEvent_t, or NULL), store_cache_and_attention(q[l], k[l], v[l]
+ *      -> out[l]; layer 0 also applies the step's table writes, or a
+ *      separate page_table_write precedes it when the step copies pages),
+ *      record layer_done[l] (or NULL); q/k/v/out are per-layer DEVICE
+ *      pointers;
  *   4. the window's trim writes (released pages are read by this step).
  * meta_cap bounds host_meta/dev_meta in int32 entries (8n plus three per
  * page the window releases suffices); it and every argument are checked

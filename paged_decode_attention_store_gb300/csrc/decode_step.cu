@@ -6,9 +6,12 @@
 // page boundary, a copy of a shared tail page), the step's slots, table
 // writes, copy pairs, lengths and rows go to the device in one copy (the
 // mini-sglang code series, part 4: host-built lists, one scatter), then the
-// table writes, page copies, store_cache and attention of every layer, and
-// last the window's trim writes (the pages a step attends are released only
-// after it).
+// page copies, the table writes, store_cache and attention of every layer,
+// and last the window's trim writes (the pages a step attends are released
+// only after it). Each layer is one store_cache_and_attention launch; the
+// first carries the step's new-page table writes. A step that copies pages
+// writes its table entries first, on their own: a copied tail page's entry
+// is one that the attention reads.
 #include <cstring>
 #include <vector>
 
@@ -99,18 +102,24 @@ extern "C" int kvp_decode_step(kvp_host* h, const kvp_pool* pool, int32_t* table
   if (cudaMemcpyAsync(dev_meta, host_meta, sizeof(int32_t) * total, cudaMemcpyHostToDevice, st) != cudaSuccess)
     return KVP_ERR_CUDA;
   const int expand = table_mode == KVP_RAW_LOCATIONS ? P : 1;
-  if (ntw && (rc = page_table_write(table, table_rows_total, table_cols, dev_meta + o_tw, dev_meta + o_tw + ntw,
-                                    dev_meta + o_tw + 2 * ntw, ntw, expand, pool->err, stream)) != KVP_OK)
-    return rc;
   if (ncow && (rc = copy_pages(pool, dev_meta + o_cow, dev_meta + o_cow + ncow, ncow, stream)) != KVP_OK) return rc;
+  int fused_tw = ntw;
+  if (ncow && ntw) {
+    if ((rc = page_table_write(table, table_rows_total, table_cols, dev_meta + o_tw, dev_meta + o_tw + ntw,
+                               dev_meta + o_tw + 2 * ntw, ntw, expand, pool->err, stream)) != KVP_OK)
+      return rc;
+    fused_tw = 0;
+  }
   for (int l = 0; l < pool->num_layers; ++l) {
     if (layer_ready && layer_ready[l] &&
         cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(layer_ready[l]), 0) != cudaSuccess)
       return KVP_ERR_CUDA;
-    if ((rc = store_cache(pool, l, k[l], v[l], dev_meta, n, stream)) != KVP_OK) return rc;
-    if ((rc = paged_decode_attention(pool, l, q[l], n, num_q_heads, table, table_rows_total, table_cols, table_mode,
-                                     dev_meta + o_rows, dev_meta + o_len, window, scale, out[l], workspace,
-                                     workspace_bytes, stream)) != KVP_OK)
+    const int ltw = l == 0 ? fused_tw : 0;
+    if ((rc = store_cache_and_attention(pool, l, q[l], k[l], v[l], dev_meta, n, num_q_heads, table, table_rows_total,
+                                        table_cols, table_mode, dev_meta + o_rows, dev_meta + o_len,
+                                        ltw ? dev_meta + o_tw : nullptr, ltw ? dev_meta + o_tw + ntw : nullptr,
+                                        ltw ? dev_meta + o_tw + 2 * ntw : nullptr, ltw, window, scale, out[l],
+                                        workspace, workspace_bytes, stream)) != KVP_OK)
       return rc;
     if (layer_done && layer_done[l] && cudaEventRecord(static_cast<cudaEvent_t>(layer_done[l]), st) != cudaSuccess)
       return KVP_ERR_CUDA;

@@ -142,6 +142,16 @@ class PagedKVCache:
         kb.paged_decode_attention(self.pool, layer, q, self.table, self.table_mode, context_lens, window, scale,
                                   out, ws, table_rows=table_rows)
 
+    def store_and_attend(self, layer, q, k, v, out_loc, context_lens, window, scale, out, table_writes=None,
+                         table_rows=None):
+        """store_cache + paged_decode_attention of one layer in one launch;
+        ``out_loc[b]`` must be the slot of request b's newest position, and
+        ``table_writes`` (rows, cols, vals device tensors) may only add the
+        pages of this step's new tokens."""
+        ws = self.workspace(q.shape[0], q.shape[1])
+        kb.store_cache_and_attention(self.pool, layer, q, k, v, out_loc, self.table, self.table_mode, context_lens,
+                                     window, scale, out, ws, table_rows=table_rows, table_writes=table_writes)
+
     def check(self):
         """Raise if a device-side error was recorded since the last check."""
         e = kb.kvp_sync_error(self.pool)
