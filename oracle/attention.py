@@ -18,6 +18,12 @@ attend the new token and at most ``W - 1`` earlier ones, i.e. positions
 runs, that is ``lo = max(0, L - W)`` up to ``L``; no window (``W`` absent or
 ``<= 0``) means ``lo = 0``.
 
+Attention sinks: chapter 15's exercise "Attention sinks" keeps the first
+``S`` rows as well and takes the last ``W - S`` for the rest, so the context
+is still ``W`` rows: positions ``0 … min(S, lo) - 1`` and ``lo … L - 1`` with
+``lo = max(0, L - (W - S))``. ``S = 0`` is the plain window; ``S`` must stay
+below ``W`` (the new token is always attended).
+
 Grouped-query heads: query head ``h`` reads KV head ``h // (Hq // Hkv)``
 (contiguous groups); the pages do not state a mapping, this is the plain one.
 
@@ -38,6 +44,23 @@ def window_lo(L: int, W) -> int:
     if W is None or W <= 0:
         return 0
     return max(0, L - W)
+
+
+def sink_window(L: int, W, S: int = 0):
+    """(sink_end, lo): a step with context ``L``, window ``W`` and ``S`` sink
+    rows attends ``0 <= t < sink_end`` and ``lo <= t < L``."""
+    if W is None or W <= 0:
+        return 0, 0
+    if S < 0 or S >= W:
+        raise ValueError("sink rows must satisfy 0 <= S < W")
+    lo = window_lo(L, W - S)
+    return min(S, lo), lo
+
+
+def attended_positions(L: int, W, S: int = 0) -> list:
+    """Every position a step with context ``L`` attends, in logical order."""
+    sink_end, lo = sink_window(L, W, S)
+    return list(range(0, sink_end)) + list(range(lo, L))
 
 
 def attention_one(q, K, V, scale: float):

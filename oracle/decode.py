@@ -12,6 +12,11 @@ the attention moved after a separate store):
    append) read through the table;
 4. trim the request to ``keep_from = L + 1 - W`` so that the page holding the
    first row the NEXT step needs is kept.
+
+With ``S`` attention sinks (chapter 15, exercise "Attention sinks") step 3
+attends ``0 .. min(S, lo) - 1`` and ``lo .. L - 1`` with ``lo = max(0, L -
+(W - S))``, and step 4 trims to ``keep_from = L + 1 - (W - S)`` keeping the
+sink pages.
 """
 
 from __future__ import annotations
@@ -21,15 +26,33 @@ import numpy as np
 from .attention import SlotStore, attend_request, gather_block, gather_raw, window_lo
 
 
+def _span(L: int, window, sinks: int):
+    """(sink_end, lo, keep_from) of a step with context ``L``."""
+    if window is None or window <= 0:
+        return 0, 0, 0
+    if sinks < 0 or sinks >= window:
+        raise ValueError("sink rows must satisfy 0 <= S < W")
+    lo = window_lo(L, window - sinks)
+    return min(sinks, lo), lo, max(0, L + 1 - (window - sinks))
+
+
 class BlockDecoder:
     """Decode loop in block-table mode (one layer)."""
 
-    def __init__(self, pt, window, scale: float):
+    def __init__(self, pt, window, scale: float, sinks: int = 0):
         self.pt = pt
         self.P = pt.page
         self.window = window
+        self.sinks = sinks
         self.scale = scale
         self.store = SlotStore()
+
+    def _trim(self, rid) -> None:
+        kf = _span(self.pt.length[rid], self.window, self.sinks)[2]
+        if self.sinks:
+            self.pt.trim(rid, kf, sink_rows=self.sinks)
+        else:
+            self.pt.trim(rid, kf)
 
     def prefill(self, rid, k, v) -> list:
         """Append ``len(k)`` rows to request ``rid`` (no attention); returns slots."""
@@ -41,7 +64,7 @@ class BlockDecoder:
             slots.append(r["slot"])
             self.store.store_cache([r["slot"]], k[i:i + 1], v[i:i + 1])
             if self.window is not None and self.window > 0:
-                self.pt.trim(rid, max(0, self.pt.length[rid] + 1 - self.window))
+                self._trim(rid)
         return slots
 
     def step(self, rids, q, k_new, v_new):
@@ -58,16 +81,23 @@ class BlockDecoder:
         outs = []
         for i, rid in enumerate(rids):
             L = self.pt.length[rid]
-            lo = window_lo(L, self.window)
-            s = gather_block(self.pt.block_row(rid), self.P, lo, L)
+            row = self.pt.block_row(rid)
+            if self.sinks:
+                sink_end, lo, _ = _span(L, self.window, self.sinks)
+                s = gather_block(row, self.P, 0, sink_end) + gather_block(row, self.P, lo, L)
+            else:
+                s = gather_block(row, self.P, window_lo(L, self.window), L)
             outs.append(attend_request(self.store, q[i], s, self.scale))
         if self.window is not None and self.window > 0:
             for rid in rids:
-                self.pt.trim(rid, max(0, self.pt.length[rid] + 1 - self.window))
+                self._trim(rid)
         return slots, cows, np.stack(outs)
 
 
-def attend_raw(store: SlotStore, raw_row, q, L: int, window, scale: float):
+def attend_raw(store: SlotStore, raw_row, q, L: int, window, scale: float, sinks: int = 0):
     """Decode attention of one request through a raw-location table row."""
+    if sinks:
+        sink_end, lo, _ = _span(L, window, sinks)
+        return attend_request(store, q, gather_raw(raw_row, 0, sink_end) + gather_raw(raw_row, lo, L), scale)
     lo = window_lo(L, window)
     return attend_request(store, q, gather_raw(raw_row, lo, L), scale)

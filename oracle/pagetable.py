@@ -19,6 +19,14 @@ section "The model"):
 * ``trim(keep_from)`` releases front pages whose rows all lie below
   ``keep_from``: page ``dropped`` goes while ``(dropped + 1) * page <=
   keep_from``;
+* with attention sinks (the chapter's exercise "Attention sinks": the first
+  ``S`` rows stay in every context), ``trim(keep_from, sink_rows=S)`` keeps
+  the first ``ceil(S / page)`` pages and releases the ones after them the
+  same way: page ``sp + dropped`` goes while ``(sp + dropped + 1) * page <=
+  keep_from``. Logical page ``i`` then lives at ``table[i]`` for ``i < sp``
+  and at ``table[i - dropped]`` from ``sp + dropped`` on (the chapter gives
+  no bookkeeping for sinks; this is the plain reading that releases exactly
+  the pages no later step reads);
 * ``fork`` copies table, length and dropped count and adds one reference to
   every page; ``release`` lets go of every page.
 
@@ -31,7 +39,8 @@ offset ``t % P``; outside ``[0, length)`` it is an error.
 
 The device-facing view used by the GPU path is :meth:`PageTable.block_row`:
 a row indexed by ABSOLUTE logical page, with ``-1`` for pages the window has
-released (the "hole at the front of the table" of chapter 15, Figure 15.1).
+released (the "hole at the front of the table" of chapter 15, Figure 15.1;
+behind the sink pages when there are sinks).
 """
 
 from __future__ import annotations
@@ -60,6 +69,7 @@ class PageTable:
         self.table: dict = {}
         self.length: dict = {}
         self.dropped: dict = {}
+        self.sinks: dict = {}  # sink pages kept in front of the released ones
 
     # -- pool ---------------------------------------------------------------
     def _alloc(self) -> int:
@@ -83,6 +93,7 @@ class PageTable:
         self.table[rid] = []
         self.length[rid] = 0
         self.dropped[rid] = 0
+        self.sinks[rid] = 0
 
     def append(self, rid, row=None) -> dict:
         """Store one row at the end of request ``rid``.
@@ -125,9 +136,12 @@ class PageTable:
         if pos < 0 or pos >= self.length[rid]:
             raise IndexError(f"position {pos} outside [0, {self.length[rid]})")
         logical = pos // self.page
-        if logical < self.dropped[rid]:
+        sp, d = self.sinks[rid], self.dropped[rid]
+        if logical < sp:
+            return self.table[rid][logical], pos % self.page
+        if logical < sp + d:
             raise IndexError(f"position {pos} lies in a released page")
-        return self.table[rid][logical - self.dropped[rid]], pos % self.page
+        return self.table[rid][logical - d], pos % self.page
 
     def slot(self, rid, pos: int) -> int:
         """Flat token location ``page * P + offset`` of logical position ``pos``."""
@@ -136,25 +150,28 @@ class PageTable:
 
     def rows(self, rid, lo: int, hi: int) -> list:
         """Rows ``lo <= i < hi`` read back through the block table."""
-        if lo < self.dropped[rid] * self.page:
-            raise IndexError("rows already released")
         out = []
         for i in range(lo, hi):
-            phys = self.table[rid][i // self.page - self.dropped[rid]]
-            out.append(self.pool[phys][i % self.page])
+            phys, off = self.translate(rid, i)
+            out.append(self.pool[phys][off])
         return out
 
-    def trim(self, rid, keep_from: int) -> list:
-        """Release the front pages that hold only rows below ``keep_from``.
+    def trim(self, rid, keep_from: int, sink_rows: int = 0) -> list:
+        """Release the front pages that hold only rows below ``keep_from``,
+        except the first ``ceil(sink_rows / page)`` pages.
 
         Returns the absolute logical indices of the released pages (they
         become ``-1`` holes in :meth:`block_row`).
         """
+        sp = -(-sink_rows // self.page)
+        if self.dropped[rid] > 0 and sp != self.sinks[rid]:
+            raise ValueError("the sink pages of a request cannot change once pages are released")
+        self.sinks[rid] = sp
         t = self.table[rid]
         released = []
-        while t and (self.dropped[rid] + 1) * self.page <= keep_from:
-            self._unref(t.pop(0))
-            released.append(self.dropped[rid])
+        while len(t) > sp and (sp + self.dropped[rid] + 1) * self.page <= keep_from:
+            self._unref(t.pop(sp))
+            released.append(sp + self.dropped[rid])
             self.dropped[rid] += 1
         return released
 
@@ -162,6 +179,7 @@ class PageTable:
         self.table[dst] = list(self.table[src])
         self.length[dst] = self.length[src]
         self.dropped[dst] = self.dropped[src]
+        self.sinks[dst] = self.sinks[src]
         for p in self.table[dst]:
             self.ref[p] += 1
 
@@ -170,6 +188,7 @@ class PageTable:
             self._unref(p)
         del self.length[rid]
         del self.dropped[rid]
+        del self.sinks[rid]
 
     # -- device-facing views --------------------------------------------------
     def block_row(self, rid) -> list:
@@ -178,7 +197,8 @@ class PageTable:
         Covers logical pages ``0 .. dropped + len(table) - 1``: everything a
         decode step of this request can address.
         """
-        return [-1] * self.dropped[rid] + list(self.table[rid])
+        t, sp = self.table[rid], self.sinks[rid]
+        return list(t[:sp]) + [-1] * self.dropped[rid] + list(t[sp:])
 
     def raw_row(self, rid) -> list:
         """The same row expanded to one entry per token position.

@@ -81,12 +81,12 @@ def check_invariances():
     return P
 
 
-def _decode_run(W, steps, P=4, seed=3, Hq=4, Hkv=2, D=16, pt_class=PageTable):
+def _decode_run(W, steps, P=4, seed=3, Hq=4, Hkv=2, D=16, pt_class=PageTable, sinks=0):
     """Oracle decode of one request; returns per-step (L, lo, q, out, pages in use)."""
     order = wl.free_stack_for_order(wl.permutation(seed, 64))
     pt = pt_class(64, P, free_order=order)
     pt.new(0)
-    dec = Dm.BlockDecoder(pt, W, 1.0 / math.sqrt(D))
+    dec = Dm.BlockDecoder(pt, W, 1.0 / math.sqrt(D), sinks=sinks)
     res = []
     for L in range(1, steps + 1):
         q = wl.q_rows(seed, L, 0, [0], Hq, D, dtype=torch.float32).numpy()
@@ -131,9 +131,57 @@ def check_decode_page_counts(pt_class=PageTable):
     return P
 
 
+SINK_CASES = ((6, 2, 4), (8, 2, 2), (5, 1, 1), (8, 4, 4), (9, 3, 2), (7, 2, 8))  # W, S, page
+
+
+def check_sink_semantics():
+    """Chapter 15, exercise "Attention sinks": the first S rows plus the last
+    W - S, so the context is still W rows. Each step must equal attention
+    over exactly those positions, with K/V regenerated from the generator
+    (not read back through the table)."""
+    P = []
+    Hkv, D = 2, 16
+    plain = _decode_run(6, 15)
+    zero = _decode_run(6, 15, sinks=0)
+    if any(np.max(np.abs(a[3] - b[3])) > 0 for a, b in zip(plain, zero)):
+        P.append("zero sinks differ from the plain window")
+    for W, S, page in SINK_CASES:
+        for L, _, q, out, _ in _decode_run(W, 21, P=page, sinks=S):
+            want = list(range(L)) if L <= W else list(range(S)) + list(range(L - (W - S), L))
+            if len(want) != min(L, W):
+                P.append("the sink context is not W rows")
+            k, v = wl.kv_rows(3, 0, 0, want, Hkv, D, dtype=torch.float32)
+            ref = _sdpa(q, k.numpy(), v.numpy(), 1.0 / math.sqrt(D))
+            if np.max(np.abs(out - ref)) > 1e-12:
+                P.append(f"W={W} S={S} page={page} step {L}: differs from the first {S} plus the last {W - S} rows")
+                break
+    # with sinks the result differs from the plain window once the window has slid
+    a, b = _decode_run(6, 12, sinks=2), _decode_run(6, 12)
+    if np.max(np.abs(a[-1][3] - b[-1][3])) < 1e-3:
+        P.append("sinks made no difference after the window slid")
+    return P
+
+
+def check_sink_page_counts(pt_class=PageTable):
+    """Pages in use equal a brute-force count: page j (of the ceil(L/P)
+    pages written) is kept iff it holds a row the next step can read, a sink
+    row (< S) or a row at or after keep_from = L + 1 - (W - S)."""
+    P = []
+    for W, S, page in SINK_CASES:
+        for L, _, _, _, used in _decode_run(W, 24, P=page, sinks=S, pt_class=pt_class):
+            kf = max(0, L + 1 - (W - S))
+            need = sum(1 for j in range(-(-L // page))
+                       if any(r < S or r >= kf for r in range(j * page, min(L, (j + 1) * page))))
+            if used != need:
+                P.append(f"W={W} S={S} page={page} after step {L}: {used} pages, brute force says {need}")
+                break
+    return P
+
+
 def all_attention_problems():
     return (check_closed_forms() + check_library_sdpa() + check_invariances()
-            + check_window_semantics() + check_decode_page_counts())
+            + check_window_semantics() + check_decode_page_counts() + check_sink_semantics()
+            + check_sink_page_counts())
 
 
 def test_closed_forms():
@@ -154,6 +202,38 @@ def test_window_semantics():
 
 def test_decode_loop_page_counts():
     assert check_decode_page_counts() == []
+
+
+def test_sink_semantics():
+    assert check_sink_semantics() == []
+
+
+def test_sink_page_counts():
+    assert check_sink_page_counts() == []
+
+
+def test_sink_positions_and_rows():
+    # context 10, window 6, 2 sinks: rows 0, 1 and 6..9
+    assert A.attended_positions(10, 6, 2) == [0, 1, 6, 7, 8, 9]
+    assert A.attended_positions(6, 6, 2) == list(range(6))
+    assert A.attended_positions(7, 6, 2) == [0, 1, 3, 4, 5, 6]
+    assert A.attended_positions(10, 6, 0) == list(range(4, 10))
+    assert A.attended_positions(10, None, 3) == list(range(10))
+    with pytest.raises(ValueError):
+        A.sink_window(10, 4, 4)
+    # the sink page stays in the table while the window slides past it
+    pt = PageTable(16, 4)
+    pt.new(0)
+    for _ in range(14):
+        pt.append(0)
+    assert pt.trim(0, 9, sink_rows=2) == [1]
+    assert pt.block_row(0)[:3] == [pt.table[0][0], -1, pt.table[0][1]]
+    assert pt.slot(0, 1) == pt.table[0][0] * 4 + 1
+    with pytest.raises(IndexError):
+        pt.slot(0, 5)
+    assert pt.trim(0, 12, sink_rows=2) == [2]
+    with pytest.raises(ValueError):
+        pt.trim(0, 12, sink_rows=5)
 
 
 def test_reading_a_hole_is_an_error():
@@ -204,7 +284,13 @@ MUTANTS = {
     "window keeps W+1 rows": [(Dm, "window_lo", lambda L, W: 0 if not W or W <= 0 else max(0, L - W - 1))],
     "window keeps W-1 rows": [(Dm, "window_lo", lambda L, W: 0 if not W or W <= 0 else max(0, L - W + 1))],
     "gather starts one row late": [(Dm, "gather_block", lambda row, P, lo, hi: A.gather_block(row, P, min(lo + 1, hi - 1), hi))],
+    "one sink row too many": [(Dm, "_span", lambda L, W, S: _orig_span(L, W, S + 1 if S else 0))],
+    "window part keeps W rows after the sinks": [(Dm, "_span", lambda L, W, S: (
+        min(S, A.window_lo(L, W)), A.window_lo(L, W), max(0, L + 1 - W)) if W and W > 0 else (0, 0, 0))],
+    "sink rows not attended": [(Dm, "_span", lambda L, W, S: (0,) + _orig_span(L, W, S)[1:])],
 }
+
+_orig_span = Dm._span
 
 
 @pytest.mark.parametrize("name", list(MUTANTS))
@@ -232,5 +318,23 @@ def test_decode_loop_mutants_are_caught():
         try:
             problems = check_decode_page_counts(cls)
         except IndexError as e:  # reading a released page is a catch too
+            problems = [repr(e)]
+        assert problems, f"{cls.__name__} survived"
+
+
+def test_sink_trim_mutants_are_caught():
+    # The sink pages released with the rest, and the sink pages never trimmed past.
+    class SinksReleased(PageTable):
+        def trim(self, rid, keep_from, sink_rows=0):
+            return super().trim(rid, keep_from)
+
+    class NoTrimWithSinks(PageTable):
+        def trim(self, rid, keep_from, sink_rows=0):
+            return super().trim(rid, keep_from, sink_rows) if not sink_rows else []
+
+    for cls in (SinksReleased, NoTrimWithSinks):
+        try:
+            problems = check_sink_page_counts(cls)
+        except IndexError as e:
             problems = [repr(e)]
         assert problems, f"{cls.__name__} survived"
