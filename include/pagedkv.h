@@ -135,9 +135,14 @@ int copy_pages(const kvp_pool* pool, const int32_t* src, const int32_t* dst,
  * requests, one query token each, reading K/V in place through the table.
  * For request b and query head h (GQA: KV head h / (num_q_heads/kv_heads)):
  *     L  = context_lens[b]            (includes the token stored this step)
- *     lo = window > 0 ? max(0, L - window) : 0
- *     s_t = scale * <q[b][h], K[slot(b,t)][h/G]>       for lo <= t < L
+ *     lo = window > 0 ? max(0, L - (window - sinks)) : 0
+ *     se = window > 0 ? min(sinks, lo) : 0
+ *     s_t = scale * <q[b][h], K[slot(b,t)][h/G]>  for 0 <= t < se, lo <= t < L
  *     out[b][h] = sum_t softmax(s)_t * V[slot(b,t)][h/G]
+ * sinks = 0 is the plain window; sinks > 0 keeps the first ``sinks`` rows
+ * in every windowed context (chapter 15, exercise "Attention sinks": the
+ * first S rows plus the last W - S). 0 <= sinks < window when window > 0
+ * (else KVP_ERR_INVALID_ARG); ignored without a window.
  * slot(b,t): block mode table[r][t/P]*P + t%P, raw mode table[r][t], with
  * r = table_rows ? table_rows[b] : b (the mini-sglang table_idx).
  * Sources: chapter 15, section "The model" (the window: the new token and at
@@ -164,8 +169,9 @@ int paged_decode_attention(const kvp_pool* pool, int layer, const void* q,
                            int table_rows_total, int table_cols,
                            int table_mode, const int32_t* table_rows,
                            const int32_t* context_lens, int window,
-                           float scale, void* out, void* workspace,
-                           size_t workspace_bytes, void* stream);
+                           int sinks, float scale, void* out,
+                           void* workspace, size_t workspace_bytes,
+                           void* stream);
 
 /* ------------------------------------------------------------------------
  * store_cache_and_attention: one layer of a decode step in one launch:
@@ -201,7 +207,7 @@ int store_cache_and_attention(const kvp_pool* pool, int layer, const void* q,
                               const int32_t* context_lens,
                               const int32_t* tw_rows, const int32_t* tw_cols,
                               const int32_t* tw_vals, int n_tw, int window,
-                              float scale, void* out, void* workspace,
+                              int sinks, float scale, void* out, void* workspace,
                               size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
@@ -238,15 +244,16 @@ int paged_decode_attention_noalloc(const kvp_pool* pool, int layer,
  * gather_indices: the slots paged_decode_attention would read, for
  * bit-exact checks of the index arithmetic ("PagedAttention block
  * allocator", section "Sequence block table"; chapter 15 Figure 15.1).
- * slots_out device int32 [batch, max_tokens]: row b holds slot(b, lo+i) for
- * i < L-lo and -1 after. L - lo > max_tokens, or an invalid entry, sets
- * KVP_ERR_BAD_INDEX (the entry is written as -1).
+ * slots_out device int32 [batch, max_tokens]: row b holds the slots of the
+ * attended positions in logical order (the se sink rows, then lo..L-1; see
+ * paged_decode_attention) and -1 after. More than max_tokens of them, or an
+ * invalid entry, sets KVP_ERR_BAD_INDEX (the entry is written as -1).
  * ---------------------------------------------------------------------- */
 int gather_indices(const kvp_pool* pool, const int32_t* table,
                    int table_rows_total, int table_cols, int table_mode,
                    const int32_t* table_rows, const int32_t* context_lens,
-                   int batch, int window, int32_t* slots_out, int max_tokens,
-                   void* stream);
+                   int batch, int window, int sinks, int32_t* slots_out,
+                   int max_tokens, void* stream);
 
 /* kvp_sync_error: wait for ``stream``, read the pool's device error word
  * into *err (0 = none) and clear it. */
@@ -306,6 +313,16 @@ int kvp_host_append(kvp_host* h, const int32_t* rids, int n, int32_t* slots,
 int kvp_host_trim(kvp_host* h, int rid, int keep_from, int32_t* tw_rows,
                   int32_t* tw_cols, int32_t* tw_vals, int tw_cap, int* n_tw);
 
+/* kvp_host_trim for a window with attention sinks (chapter 15, exercise
+ * "Attention sinks": the first S rows stay in every context). The first
+ * sp = ceil(sink_rows / P) pages are kept; after them page sp + dropped goes
+ * while (sp + dropped + 1) * P <= keep_from. sink_rows = 0 is kvp_host_trim.
+ * A request's sink count cannot change once it has released pages
+ * (KVP_ERR_INVALID_ARG, nothing changed). */
+int kvp_host_trim_sinks(kvp_host* h, int rid, int keep_from, int sink_rows,
+                        int32_t* tw_rows, int32_t* tw_cols, int32_t* tw_vals,
+                        int tw_cap, int* n_tw);
+
 /* ------------------------------------------------------------------------
  * kvp_decode_step: one decode step of the whole path in one call, in the
  * order of chapter 15's host loop ("The model") with the attention after a
@@ -322,7 +339,10 @@ int kvp_host_trim(kvp_host* h, int rid, int keep_from, int32_t* tw_rows,
  *      separate page_table_write precedes it when the step copies pages),
  *      record layer_done[l] (or NULL); q/k/v/out are per-layer DEVICE
  *      pointers;
- *   4. the window's trim writes (released pages are read by this step).
+ *   4. the window's trim writes (released pages are read by this step):
+ *      keep_from = L + 1 - (window - sinks), keeping the first
+ *      ceil(sinks / P) pages (kvp_host_trim_sinks); a request's sink count
+ *      must stay the same from step to step.
  * meta_cap bounds host_meta/dev_meta in int32 entries (8n plus three per
  * page the window releases suffices); it and every argument are checked
  * before anything changes. host_meta is read asynchronously: reuse it only
@@ -339,7 +359,8 @@ typedef struct kvp_step_info {
 
 int kvp_decode_step(kvp_host* h, const kvp_pool* pool, int32_t* table,
                     int table_rows_total, int table_cols, int table_mode,
-                    const int32_t* rids, int n, int window, int num_q_heads,
+                    const int32_t* rids, int n, int window, int sinks,
+                    int num_q_heads,
                     float scale, const void* const* q, const void* const* k,
                     const void* const* v, void* const* out,
                     void* const* layer_ready, void* const* layer_done,

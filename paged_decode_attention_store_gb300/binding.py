@@ -45,11 +45,11 @@ SIGNATURES = {
     "page_table_write": [_vp, _i, _i, _vp, _vp, _vp, _i, _i, _vp, _vp],
     "copy_pages": [_vp, _vp, _vp, _i, _vp],
     "paged_decode_attention_workspace_size": [_vp, _i, _i, _szp],
-    "paged_decode_attention": [_vp, _i, _vp, _i, _i, _vp, _i, _i, _i, _vp, _vp, _i, _f, _vp, _vp, _sz, _vp],
+    "paged_decode_attention": [_vp, _i, _vp, _i, _i, _vp, _i, _i, _i, _vp, _vp, _i, _i, _f, _vp, _vp, _sz, _vp],
     "paged_decode_attention_noalloc": [_vp, _i, _vp, _i, _i, _vp, _i, _i, _i, _vp, _vp, _i, _f, _vp, _vp],
     "store_cache_and_attention": [_vp, _i, _vp, _vp, _vp, _vp, _i, _i, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _i,
-                                  _i, _f, _vp, _vp, _sz, _vp],
-    "gather_indices": [_vp, _vp, _i, _i, _i, _vp, _vp, _i, _i, _vp, _i, _vp],
+                                  _i, _i, _f, _vp, _vp, _sz, _vp],
+    "gather_indices": [_vp, _vp, _i, _i, _i, _vp, _vp, _i, _i, _i, _vp, _i, _vp],
     "kvp_sync_error": [_vp, _vp, _ip],
     "kvp_pool_set_timing_events": [_vp, _vp, _vp],
     "kvp_host_create": [_i, _i, _i, _vp, ctypes.POINTER(_vp)],
@@ -59,13 +59,14 @@ SIGNATURES = {
     "kvp_host_release": [_vp, _i],
     "kvp_host_append": [_vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _ip, _vp, _vp, _ip],
     "kvp_host_trim": [_vp, _i, _i, _vp, _vp, _vp, _i, _ip],
+    "kvp_host_trim_sinks": [_vp, _i, _i, _i, _vp, _vp, _vp, _i, _ip],
     "kvp_host_used": [_vp, _ip],
     "kvp_host_length": [_vp, _i, _ip, _ip],
     "kvp_host_block_row": [_vp, _i, _vp, _i, _ip],
     "kvp_host_refcounts": [_vp, _vp, _i],
     "kvp_host_free_list": [_vp, _vp, _i, _ip],
-    "kvp_decode_step": [_vp, _vp, _vp, _i, _i, _i, _vp, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i,
-                        _vp, _sz, _vp, _vp],
+    "kvp_decode_step": [_vp, _vp, _vp, _i, _i, _i, _vp, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                        _i, _vp, _sz, _vp, _vp],
 }
 
 
@@ -208,7 +209,7 @@ def alloc_workspace(pool, batch, num_q_heads, device="cuda"):
 
 
 def paged_decode_attention(pool, layer, q, table, table_mode, context_lens, window, scale, out, workspace,
-                           table_rows=None, stream=None):
+                           table_rows=None, stream=None, sinks=0):
     dt = _TORCH_DTYPE[pool.dtype]
     _dev(q, dt, "q")
     _dev(out, dt, "out")
@@ -222,12 +223,12 @@ def paged_decode_attention(pool, layer, q, table, table_mode, context_lens, wind
     ws_ptr, ws_bytes = (None, 0) if workspace is None else (_ptr(workspace), workspace.numel() * workspace.element_size())
     _check(lib().paged_decode_attention(pool.handle, layer, _ptr(q), B, Hq, _ptr(table), table.shape[0],
                                         table.shape[1], table_mode, _ptr(table_rows), _ptr(context_lens),
-                                        int(window or 0), float(scale), _ptr(out), ws_ptr, ws_bytes,
+                                        int(window or 0), int(sinks), float(scale), _ptr(out), ws_ptr, ws_bytes,
                                         _stream(stream)), "paged_decode_attention")
 
 
 def store_cache_and_attention(pool, layer, q, k, v, out_loc, table, table_mode, context_lens, window, scale, out,
-                              workspace, table_rows=None, table_writes=None, stream=None):
+                              workspace, table_rows=None, table_writes=None, stream=None, sinks=0):
     """store_cache + paged_decode_attention of one layer in one launch, with
     the step's new-page table writes (rows, cols, vals device int32 tensors)
     applied in the same launch. out_loc[b] must be the slot of request b's
@@ -253,7 +254,7 @@ def store_cache_and_attention(pool, layer, q, k, v, out_loc, table, table_mode, 
     ws_ptr, ws_bytes = (None, 0) if workspace is None else (_ptr(workspace), workspace.numel() * workspace.element_size())
     _check(lib().store_cache_and_attention(pool.handle, layer, _ptr(q), _ptr(k), _ptr(v), _ptr(out_loc), B, Hq,
                                            _ptr(table), table.shape[0], table.shape[1], table_mode,
-                                           _ptr(table_rows), _ptr(context_lens), *tw, int(window or 0),
+                                           _ptr(table_rows), _ptr(context_lens), *tw, int(window or 0), int(sinks),
                                            float(scale), _ptr(out), ws_ptr, ws_bytes, _stream(stream)),
            "store_cache_and_attention")
 
@@ -279,13 +280,13 @@ def paged_decode_attention_noalloc(pool, layer, q, table, table_mode, context_le
            "paged_decode_attention_noalloc")
 
 
-def gather_indices(pool, table, table_mode, context_lens, window, slots_out, table_rows=None, stream=None):
+def gather_indices(pool, table, table_mode, context_lens, window, slots_out, table_rows=None, stream=None, sinks=0):
     _dev(table, torch.int32, "table")
     _dev(context_lens, torch.int32, "context_lens")
     _dev(slots_out, torch.int32, "slots_out")
     B = context_lens.numel()
     _check(lib().gather_indices(pool.handle, _ptr(table), table.shape[0], table.shape[1], table_mode,
-                                _ptr(table_rows), _ptr(context_lens), B, int(window or 0), _ptr(slots_out),
+                                _ptr(table_rows), _ptr(context_lens), B, int(window or 0), int(sinks), _ptr(slots_out),
                                 slots_out.shape[1], _stream(stream)), "gather_indices")
 
 
@@ -368,20 +369,26 @@ class HostPageTable:
                                      ctypes.byref(ntw), p(cow[0]), p(cow[1]), ctypes.byref(ncow)), "kvp_host_append")
         return ntw.value, ncow.value
 
-    def trim_into(self, rid, keep_from, tw, cap):
+    def trim_into(self, rid, keep_from, tw, cap, sinks=0):
         """Fast form of :meth:`trim`: writes go to ``tw`` int32[3, cap]; returns their number."""
         n = ctypes.c_int()
         p = lambda a: a.ctypes.data_as(ctypes.c_void_p)  # noqa: E731
-        _check(lib().kvp_host_trim(self.handle, rid, int(keep_from), p(tw[0]), p(tw[1]), p(tw[2]), cap,
-                                   ctypes.byref(n)), "kvp_host_trim")
+        _check(lib().kvp_host_trim_sinks(self.handle, rid, int(keep_from), int(sinks), p(tw[0]), p(tw[1]),
+                                         p(tw[2]), cap, ctypes.byref(n)), "kvp_host_trim_sinks")
         return n.value
 
-    def trim(self, rid, keep_from):
+    def trim(self, rid, keep_from, sinks=0):
+        """Release the pages no later step reads: below keep_from, except the
+        first ceil(sinks / P) pages. Returns the (rid, page, -1) table writes."""
         cap = max(1, self.length(rid)[0] // self.page_size + 1)
         tr, tc, tv = _i32(cap), _i32(cap), _i32(cap)
         n = ctypes.c_int()
-        _check(lib().kvp_host_trim(self.handle, rid, int(keep_from), tr, tc, tv, cap, ctypes.byref(n)),
-               "kvp_host_trim")
+        if sinks:
+            _check(lib().kvp_host_trim_sinks(self.handle, rid, int(keep_from), int(sinks), tr, tc, tv, cap,
+                                             ctypes.byref(n)), "kvp_host_trim_sinks")
+        else:
+            _check(lib().kvp_host_trim(self.handle, rid, int(keep_from), tr, tc, tv, cap, ctypes.byref(n)),
+                   "kvp_host_trim")
         return list(zip(tr[:n.value], tc[:n.value], tv[:n.value]))
 
     def used(self):

@@ -36,7 +36,7 @@ struct GenArgs {
   void* out;
   const int32_t* context_lens;
   const int32_t* table_rows;
-  int B, Hq, Hkv, D, window;
+  int B, Hq, Hkv, D, window, sinks;
   float scale_log2;
   int32_t* err;
 };
@@ -64,7 +64,8 @@ __global__ void __launch_bounds__(32 * kGenWarps) generic_decode_kernel(const Ge
   }
   for (int d = lane; d < D; d += 32) qs[warp][d] = to_f<T>(q[d]);
   __syncwarp();
-  const int lo = window_lo(L, a.window);
+  const Span sp = attend_span(L, a.window, a.sinks);
+  const int n = sp.se + L - sp.lo;  // attended rows: [0, se) and [lo, L)
   const size_t row_elems = (size_t)a.Hkv * D;
   const T* K = reinterpret_cast<const T*>(a.kv_layer);
   const T* Vp = reinterpret_cast<const T*>(a.kv_layer + a.kv_bytes);
@@ -73,12 +74,12 @@ __global__ void __launch_bounds__(32 * kGenWarps) generic_decode_kernel(const Ge
 #pragma unroll
   for (int i = 0; i < kPerLane; ++i) acc[i] = 0.f;
   float m = -INFINITY, l = 0.f;
-  for (int t0 = lo; t0 < L; t0 += 32) {
-    const int t = t0 + lane;
+  for (int o0 = 0; o0 < n; o0 += 32) {
+    const int o = o0 + lane;
     int slot = -1;
     float s = -INFINITY;
-    if (t < L) {
-      slot = resolve_slot(a.T, row, t, a.err);
+    if (o < n) {
+      slot = resolve_slot(a.T, row, span_pos(sp, o), a.err);
       if (slot >= 0) {
         const T* kr = K + (size_t)slot * row_elems + (size_t)kvh * D;
         float dot = 0.f;
@@ -100,7 +101,7 @@ __global__ void __launch_bounds__(32 * kGenWarps) generic_decode_kernel(const Ge
     m = mn;
 #pragma unroll
     for (int i = 0; i < kPerLane; ++i) acc[i] *= alpha;
-    const int nt = min(32, L - t0);
+    const int nt = min(32, n - o0);
     for (int jj = 0; jj < nt; ++jj) {
       const float pj = __shfl_sync(0xffffffffu, p, jj);
       const int sj = __shfl_sync(0xffffffffu, slot, jj);
@@ -122,17 +123,17 @@ __global__ void __launch_bounds__(32 * kGenWarps) generic_decode_kernel(const Ge
 }
 
 __global__ void gather_indices_kernel(TableRef T, const int32_t* context_lens, const int32_t* table_rows, int window,
-                                      int32_t* out, int max_tokens, int32_t* err) {
+                                      int sinks, int32_t* out, int max_tokens, int32_t* err) {
   const int b = blockIdx.x;
   const int L = context_lens[b];
   const int row = table_rows ? table_rows[b] : b;
   const bool valid = L >= 1 && L <= table_capacity(T) && row >= 0 && row < T.rows_total;
-  const int lo = valid ? window_lo(L, window) : 0;
-  const int n = valid ? L - lo : 0;
+  const Span sp = attend_span(valid ? L : 0, window, sinks);
+  const int n = valid ? sp.se + L - sp.lo : 0;
   if ((!valid || n > max_tokens) && threadIdx.x == 0) set_error(err, KVP_ERR_BAD_INDEX);
   for (int i = threadIdx.x; i < max_tokens; i += blockDim.x) {
     int s = -1;
-    if (i < n) s = resolve_slot(T, row, lo + i, err);
+    if (i < n) s = resolve_slot(T, row, span_pos(sp, i), err);
     out[(size_t)b * max_tokens + i] = s;
   }
 }
@@ -200,7 +201,7 @@ struct FuseIn {
 
 int attention_impl(const kvp_pool* pool, int layer, const void* q, int batch, int num_q_heads, const int32_t* table,
                    int table_rows_total, int table_cols, int table_mode, const int32_t* table_rows,
-                   const int32_t* context_lens, int window, float scale, void* out, void* workspace,
+                   const int32_t* context_lens, int window, int sinks, float scale, void* out, void* workspace,
                    size_t workspace_bytes, void* stream, const FuseIn* fz) {
   if (!pool || !q || !table || !context_lens || !out) return KVP_ERR_INVALID_ARG;
   if (layer < 0 || layer >= pool->num_layers || batch <= 0 || num_q_heads <= 0) return KVP_ERR_INVALID_ARG;
@@ -208,6 +209,8 @@ int attention_impl(const kvp_pool* pool, int layer, const void* q, int batch, in
   if (table_rows_total <= 0 || table_cols <= 0) return KVP_ERR_INVALID_ARG;
   if (table_mode != KVP_BLOCK_TABLE && table_mode != KVP_RAW_LOCATIONS) return KVP_ERR_INVALID_ARG;
   if (!(scale == scale)) return KVP_ERR_INVALID_ARG;
+  if (sinks < 0 || (window > 0 && sinks >= window)) return KVP_ERR_INVALID_ARG;
+  if (window <= 0) sinks = 0;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   const TableRef T = make_table(pool, table, table_rows_total, table_cols, table_mode);
   const char* kv_layer = pool->buf + (size_t)layer * pool->layer_bytes;
@@ -259,6 +262,7 @@ int attention_impl(const kvp_pool* pool, int layer, const void* q, int batch, in
     ta.HG = HG;
     ta.n_groups = pool->kv_heads / HG;
     ta.window = window;
+    ta.sinks = sinks;
     ta.num_ctas = pool->num_sms;
     ta.scale_log2 = scale_log2;
     ta.merge = reinterpret_cast<int4*>(ws + L.merge);
@@ -305,6 +309,7 @@ int attention_impl(const kvp_pool* pool, int layer, const void* q, int batch, in
   ga.Hkv = pool->kv_heads;
   ga.D = pool->head_dim;
   ga.window = window;
+  ga.sinks = sinks;
   ga.scale_log2 = scale_log2;
   ga.err = pool->err;
   const long long warps = (long long)batch * num_q_heads;
@@ -327,10 +332,11 @@ int attention_impl(const kvp_pool* pool, int layer, const void* q, int batch, in
 extern "C" int paged_decode_attention(const kvp_pool* pool, int layer, const void* q, int batch, int num_q_heads,
                                       const int32_t* table, int table_rows_total, int table_cols, int table_mode,
                                       const int32_t* table_rows, const int32_t* context_lens, int window,
-                                      float scale, void* out, void* workspace, size_t workspace_bytes,
+                                      int sinks, float scale, void* out, void* workspace, size_t workspace_bytes,
                                       void* stream) {
   return attention_impl(pool, layer, q, batch, num_q_heads, table, table_rows_total, table_cols, table_mode,
-                        table_rows, context_lens, window, scale, out, workspace, workspace_bytes, stream, nullptr);
+                        table_rows, context_lens, window, sinks, scale, out, workspace, workspace_bytes, stream,
+                        nullptr);
 }
 
 extern "C" int store_cache_and_attention(const kvp_pool* pool, int layer, const void* q, const void* k,
@@ -338,24 +344,27 @@ extern "C" int store_cache_and_attention(const kvp_pool* pool, int layer, const 
                                          int32_t* table, int table_rows_total, int table_cols, int table_mode,
                                          const int32_t* table_rows, const int32_t* context_lens,
                                          const int32_t* tw_rows, const int32_t* tw_cols, const int32_t* tw_vals,
-                                         int n_tw, int window, float scale, void* out, void* workspace,
+                                         int n_tw, int window, int sinks, float scale, void* out, void* workspace,
                                          size_t workspace_bytes, void* stream) {
   if (!k || !v || !out_loc || n_tw < 0 || (n_tw > 0 && (!tw_rows || !tw_cols || !tw_vals)))
     return KVP_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15) return KVP_ERR_INVALID_ARG;
   const FuseIn fz = {k, v, out_loc, table, tw_rows, tw_cols, tw_vals, n_tw};
   return attention_impl(pool, layer, q, batch, num_q_heads, table, table_rows_total, table_cols, table_mode,
-                        table_rows, context_lens, window, scale, out, workspace, workspace_bytes, stream, &fz);
+                        table_rows, context_lens, window, sinks, scale, out, workspace, workspace_bytes, stream,
+                        &fz);
 }
 
 extern "C" int gather_indices(const kvp_pool* pool, const int32_t* table, int table_rows_total, int table_cols,
                               int table_mode, const int32_t* table_rows, const int32_t* context_lens, int batch,
-                              int window, int32_t* slots_out, int max_tokens, void* stream) {
+                              int window, int sinks, int32_t* slots_out, int max_tokens, void* stream) {
   if (!pool || !table || !context_lens || !slots_out || batch <= 0 || max_tokens <= 0) return KVP_ERR_INVALID_ARG;
+  if (sinks < 0 || (window > 0 && sinks >= window)) return KVP_ERR_INVALID_ARG;
+  if (window <= 0) sinks = 0;
   if (table_rows_total <= 0 || table_cols <= 0) return KVP_ERR_INVALID_ARG;
   if (table_mode != KVP_BLOCK_TABLE && table_mode != KVP_RAW_LOCATIONS) return KVP_ERR_INVALID_ARG;
   const TableRef T = make_table(pool, table, table_rows_total, table_cols, table_mode);
   gather_indices_kernel<<<batch, 256, 0, static_cast<cudaStream_t>(stream)>>>(T, context_lens, table_rows, window,
-                                                                               slots_out, max_tokens, pool->err);
+                                                                               sinks, slots_out, max_tokens, pool->err);
   return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
 }

@@ -58,7 +58,7 @@ struct TcArgs {
   __nv_bfloat16* out;      // [B, Hq, D]
   const int32_t* context_lens;
   const int32_t* table_rows;
-  int B, Hq, G, HG, n_groups, window, num_ctas;
+  int B, Hq, G, HG, n_groups, window, sinks, num_ctas;
   float scale_log2;
   int4* merge;
   float* part_ml;

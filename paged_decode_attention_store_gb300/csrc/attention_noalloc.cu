@@ -57,5 +57,5 @@ extern "C" int paged_decode_attention_noalloc(const kvp_pool* pool, int layer, c
   // Nothing in the scratch has to start at zero: every call writes the merge
   // records and partials it reads.
   return paged_decode_attention(pool, layer, q, batch, num_q_heads, table, table_rows_total, table_cols, table_mode,
-                                table_rows, context_lens, window, scale, out, scratch, kNoAllocScratchBytes, stream);
+                                table_rows, context_lens, window, 0, scale, out, scratch, kNoAllocScratchBytes, stream);
 }

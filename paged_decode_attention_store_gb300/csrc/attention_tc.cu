@@ -147,11 +147,14 @@ __device__ __forceinline__ int entry_to_slot(const TableRef& T, int e, int t, in
   return e * T.page_size + t % T.page_size;
 }
 
-// Attended positions of a request (0 when its length or table row is invalid).
-__device__ __forceinline__ int attended(const TcArgs& a, int L, int row, long long cap, int* lo) {
+// Attended positions of a request (0 when its length or table row is
+// invalid): the se sink rows [0, se), then [lo, L) (see attend_span).
+__device__ __forceinline__ int attended(const TcArgs& a, int L, int row, long long cap, int* lo, int* se) {
   const bool valid = L >= 1 && L <= cap && row >= 0 && row < a.T.rows_total;
-  *lo = valid ? window_lo(L, a.window) : 0;
-  return valid ? L - *lo : 0;
+  const Span sp = attend_span(valid ? L : 0, a.window, a.sinks);
+  *lo = sp.lo;
+  *se = sp.se;
+  return valid ? sp.se + L - sp.lo : 0;
 }
 
 // ---------------------------------------------------------------------------
@@ -181,8 +184,8 @@ __device__ void plan_cta(const TcArgs& a, const SmemMap& s, PlanState* ps) {
   for (int b = threadIdx.x; b < a.B; b += blockDim.x) {
     const int L = __ldg(a.context_lens + b);
     const int row = a.table_rows ? __ldg(a.table_rows + b) : b;
-    int lo;
-    const int n = attended(a, L, row, cap, &lo);
+    int lo, se;
+    const int n = attended(a, L, row, cap, &lo, &se);
     sN[b] = n;
     sL[b] = L;
     sR[b] = row;
@@ -241,11 +244,16 @@ __device__ void plan_cta(const TcArgs& a, const SmemMap& s, PlanState* ps) {
 }
 
 // The producer's walk over the pieces of its share.
+// A piece covers the stream offsets [x - Sv, e - Sv) of its request, which
+// map to positions through the span: offsets below se are the sink rows
+// themselves, the rest start at lo. So a piece is one or two position
+// segments; the walk takes the stages of the first, then of the second.
 struct Cursor {
   long long R0, R1, x, Sv, cap;
   int k, B;
-  int b, g, row, lo, n;              // current virtual request
-  int t_begin, t_end, part, t0;      // current piece, next stage start
+  int b, g, row, lo, se, L, n;       // current virtual request
+  int t_begin, t_end, part, t0;      // current piece: first position, end of the current segment, next stage start
+  int nxt_begin, nxt_end;            // the piece's second segment, or nxt_begin = -1
   int piece;                         // index of the current piece
   bool done;
   int nb, nL, nrow;                  // next request, prefetched
@@ -253,8 +261,19 @@ struct Cursor {
 
 __device__ __forceinline__ void cur_set_piece(Cursor& c) {
   const long long e = min(c.R1, c.Sv + c.n);
-  c.t_begin = c.lo + (int)(c.x - c.Sv);
-  c.t_end = c.lo + (int)(e - c.Sv);
+  const int ob = (int)(c.x - c.Sv), oe = (int)(e - c.Sv);
+  c.nxt_begin = -1;
+  if (ob < c.se) {  // starts among the sink rows
+    c.t_begin = ob;
+    c.t_end = min(oe, c.se);
+    if (oe > c.se) {
+      c.nxt_begin = c.lo;
+      c.nxt_end = c.lo + (oe - c.se);
+    }
+  } else {
+    c.t_begin = c.lo + (ob - c.se);
+    c.t_end = c.lo + (oe - c.se);
+  }
   const bool split = c.Sv < c.R0 || c.Sv + c.n > c.R1;
   c.part = split ? (c.x == c.R0 ? 2 * c.k : 2 * c.k + 1) : -1;
   c.t0 = c.t_begin;
@@ -281,7 +300,8 @@ __device__ void cur_init(const TcArgs& a, const PlanState& ps, Cursor& c) {
   c.b = ps.b0;
   c.g = ps.g0;
   c.row = ps.row0;
-  c.n = attended(a, ps.L0, c.row, c.cap, &c.lo);
+  c.n = attended(a, ps.L0, c.row, c.cap, &c.lo, &c.se);
+  c.L = ps.L0;
   c.piece = 0;
   cur_prefetch(a, c);
   cur_set_piece(c);
@@ -309,7 +329,8 @@ __device__ void cur_next_piece(const TcArgs& a, Cursor& c) {
     c.row = c.nrow;
     const int L = c.nL;
     cur_prefetch(a, c);
-    c.n = attended(a, L, c.row, c.cap, &c.lo);
+    c.n = attended(a, L, c.row, c.cap, &c.lo, &c.se);
+    c.L = L;
     if (c.n > 0) break;
   }
   c.g = 0;
@@ -324,8 +345,14 @@ __device__ __forceinline__ int stage_end(int t0, int t_end) { return min((t0 & ~
 __device__ __forceinline__ void cur_advance(const TcArgs& a, Cursor& c) {
   c.t0 = (c.t0 & ~(kTok - 1)) + kTok;
   if (c.t0 >= c.t_end) {
-    cur_next_piece(a, c);
-    ++c.piece;
+    if (c.nxt_begin >= 0) {  // from the sink rows to the window
+      c.t0 = c.nxt_begin;
+      c.t_end = c.nxt_end;
+      c.nxt_begin = -1;
+    } else {
+      cur_next_piece(a, c);
+      ++c.piece;
+    }
   }
 }
 
@@ -356,16 +383,17 @@ __device__ void tc_producer(const TcArgs& a, const SmemMap& s, const PlanState& 
     const int qs = (int)(queued % kQueue);
     if (!c.done) {
       const int se = stage_end(c.t0, c.t_end);
+      const bool last = se == c.t_end && c.nxt_begin < 0;  // the piece's last stage
       // In a fused step the request's newest position (the piece ends at
       // the request's end) is read from the new rows, at the slot out_loc
       // gives: its table entry may be written by this very launch.
-      const int t_new = (a.fused && c.t_end == c.lo + c.n && se == c.t_end) ? c.t_end - 1 : -1;
+      const int t_new = (a.fused && last && c.t_end == c.L) ? c.t_end - 1 : -1;
       if (lane == 0) {
         StageMeta m;
         m.live = 1;
         m.t0 = c.t0;
         m.t_end = c.t_end;
-        m.flags = (c.t0 == c.t_begin ? 1 : 0) | (se == c.t_end ? 2 : 0) | (t_new >= 0 ? 16 : 0);
+        m.flags = (c.t0 == c.t_begin ? 1 : 0) | (last ? 2 : 0) | (t_new >= 0 ? 16 : 0);
         m.b = c.b;
         m.group = c.g;
         m.part = c.part;

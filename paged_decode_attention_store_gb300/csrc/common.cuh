@@ -81,6 +81,31 @@ __device__ __forceinline__ int window_lo(int L, int window) {
   return window > 0 ? max(0, L - window) : 0;
 }
 
+// The positions a step with context L attends: [0, se) and [lo, L).
+// Chapter 15 ("The model"): the window W is the new token and at most W-1
+// earlier ones; its exercise "Attention sinks" keeps the first S rows too
+// and takes the last W - S for the rest, so
+//   lo = max(0, L - (W - S)),  se = min(S, lo).
+// No window (W <= 0): everything. When the two ranges touch (lo <= S) the
+// span is the whole context and is returned as se = lo = 0.
+struct Span {
+  int se, lo;
+};
+
+__host__ __device__ __forceinline__ Span attend_span(int L, int window, int sinks) {
+  Span s = {0, 0};
+  if (window > 0) {
+    const int lo = L - (window - sinks);
+    s.lo = lo > 0 ? lo : 0;
+    s.se = sinks < s.lo ? sinks : s.lo;
+    if (s.se == s.lo) s.se = s.lo = 0;
+  }
+  return s;
+}
+
+// Position of the o-th attended row (0 <= o < se + L - lo).
+__host__ __device__ __forceinline__ int span_pos(const Span& s, int o) { return o < s.se ? o : s.lo + (o - s.se); }
+
 // ---------------------------------------------------------------------------
 // PTX wrappers (sm_90+ async proxy, sm_80+ tensor-core fragments).
 // ---------------------------------------------------------------------------

@@ -25,14 +25,17 @@ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 extern "C" int kvp_decode_step(kvp_host* h, const kvp_pool* pool, int32_t* table, int table_rows_total,
                                int table_cols, int table_mode, const int32_t* rids, int n, int window,
-                               int num_q_heads, float scale, const void* const* q, const void* const* k,
+                               int sinks, int num_q_heads, float scale, const void* const* q, const void* const* k,
                                const void* const* v, void* const* out, void* const* layer_ready,
                                void* const* layer_done, int32_t* host_meta, int32_t* dev_meta, int meta_cap,
                                void* workspace, size_t workspace_bytes, void* stream, kvp_step_info* info) {
   if (!h || !pool || !table || !rids || n <= 0 || !q || !k || !v || !out || !host_meta || !dev_meta || !info)
     return KVP_ERR_INVALID_ARG;
   if (table_mode != KVP_BLOCK_TABLE && table_mode != KVP_RAW_LOCATIONS) return KVP_ERR_INVALID_ARG;
+  if (sinks < 0 || (window > 0 && sinks >= window)) return KVP_ERR_INVALID_ARG;
+  if (window <= 0) sinks = 0;
   const int P = pool->page_size;
+  const int sp = ceil_div(sinks, P);  // sink pages, kept by the trim
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   // Lengths and dropped pages before the step, and the trim writes the step
@@ -46,10 +49,10 @@ extern "C" int kvp_decode_step(kvp_host* h, const kvp_pool* pool, int32_t* table
   int trims = 0;
   if (window > 0) {
     for (int i = 0; i < n; ++i) {
-      const int L = len0[i] + 1, keep = L + 1 - window;
+      const int L = len0[i] + 1, keep = L + 1 - (window - sinks);
       const int pages = ceil_div(L, P);
       const int to = keep > 0 ? (keep / P < pages ? keep / P : pages) : 0;  // pages wholly below keep
-      if (to > drop0[i]) trims += to - drop0[i];
+      if (to > sp + drop0[i]) trims += to - sp - drop0[i];
     }
   }
   const long long need = 3LL * n + 3LL * n + 2LL * n + 3LL * trims;  // slots, tw, cow, lens, rows, trim
@@ -82,10 +85,10 @@ extern "C" int kvp_decode_step(kvp_host* h, const kvp_pool* pool, int32_t* table
   if (trims > 0) {
     std::vector<int32_t> tr(3 * trims);
     for (int i = 0; i < n; ++i) {
-      const int keep = len0[i] + 2 - window;
+      const int keep = len0[i] + 2 - (window - sinks);
       int got = 0;
-      rc = kvp_host_trim(h, rids[i], keep, tr.data() + ntrim, tr.data() + trims + ntrim, tr.data() + 2 * trims + ntrim,
-                         trims - ntrim, &got);
+      rc = kvp_host_trim_sinks(h, rids[i], keep, sinks, tr.data() + ntrim, tr.data() + trims + ntrim,
+                               tr.data() + 2 * trims + ntrim, trims - ntrim, &got);
       if (rc != KVP_OK) return rc;
       ntrim += got;
     }
@@ -118,7 +121,7 @@ extern "C" int kvp_decode_step(kvp_host* h, const kvp_pool* pool, int32_t* table
     if ((rc = store_cache_and_attention(pool, l, q[l], k[l], v[l], dev_meta, n, num_q_heads, table, table_rows_total,
                                         table_cols, table_mode, dev_meta + o_rows, dev_meta + o_len,
                                         ltw ? dev_meta + o_tw : nullptr, ltw ? dev_meta + o_tw + ntw : nullptr,
-                                        ltw ? dev_meta + o_tw + 2 * ntw : nullptr, ltw, window, scale, out[l],
+                                        ltw ? dev_meta + o_tw + 2 * ntw : nullptr, ltw, window, sinks, scale, out[l],
                                         workspace, workspace_bytes, stream)) != KVP_OK)
       return rc;
     if (layer_done && layer_done[l] && cudaEventRecord(static_cast<cudaEvent_t>(layer_done[l]), st) != cudaSuccess)

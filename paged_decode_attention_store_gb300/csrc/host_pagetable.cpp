@@ -6,7 +6,10 @@
 // request, a fresh page when the length reaches a page boundary, a whole-page
 // copy before writing into a shared tail page (lazy copy-on-write), fork by
 // sharing every page, release of front pages that the window no longer
-// reaches, release of a finished request.
+// reaches, release of a finished request. With attention sinks (the
+// chapter's exercise "Attention sinks": the first S rows stay in every
+// context) the first ceil(S / P) pages are kept and the pages after them are
+// released the same way.
 //
 // Layout here is built for the device: each request keeps its pages in a
 // vector indexed by ABSOLUTE logical page, with -1 for pages the window has
@@ -26,7 +29,8 @@ namespace {
 struct Request {
   bool live = false;
   int length = 0;            // rows stored
-  int dropped = 0;           // front pages released by trim
+  int dropped = 0;           // pages released by trim (after the sink pages)
+  int sink_pages = 0;        // front pages kept for attention sinks
   std::vector<int32_t> pages;  // absolute logical page -> physical page (-1 = hole)
 };
 
@@ -131,6 +135,7 @@ int kvp_host_new(kvp_host* h, int rid) {
   r.live = true;
   r.length = 0;
   r.dropped = 0;
+  r.sink_pages = 0;
   r.pages.clear();
   return KVP_OK;
 }
@@ -161,7 +166,7 @@ int kvp_host_release(kvp_host* h, int rid) {
     if (p >= 0) unref_page(h, p);
   r.live = false;
   r.pages.clear();
-  r.length = r.dropped = 0;
+  r.length = r.dropped = r.sink_pages = 0;
   return KVP_OK;
 }
 
@@ -226,17 +231,22 @@ int kvp_host_append(kvp_host* h, const int32_t* rids, int n, int32_t* slots,
   return KVP_OK;
 }
 
-int kvp_host_trim(kvp_host* h, int rid, int keep_from, int32_t* tw_rows,
-                  int32_t* tw_cols, int32_t* tw_vals, int tw_cap, int* n_tw) {
-  if (!valid_rid(h, rid) || !h->req[rid].live || !n_tw) return KVP_ERR_INVALID_ARG;
+int kvp_host_trim_sinks(kvp_host* h, int rid, int keep_from, int sink_rows, int32_t* tw_rows,
+                        int32_t* tw_cols, int32_t* tw_vals, int tw_cap, int* n_tw) {
+  if (!valid_rid(h, rid) || !h->req[rid].live || !n_tw || sink_rows < 0) return KVP_ERR_INVALID_ARG;
   Request& r = h->req[rid];
   const int P = h->page_size;
+  const int sp = static_cast<int>((static_cast<long long>(sink_rows) + P - 1) / P);
+  if (r.dropped > 0 && sp != r.sink_pages) return KVP_ERR_INVALID_ARG;  // sinks fixed once pages went
   // Count first so that a short output buffer changes nothing.
   int count = 0;
-  for (int d = r.dropped; d < static_cast<int>(r.pages.size()) && (d + 1) * P <= keep_from; ++d) ++count;
+  for (int d = sp + r.dropped; d < static_cast<int>(r.pages.size()) && static_cast<long long>(d + 1) * P <= keep_from;
+       ++d)
+    ++count;
   if (count > 0 && (!tw_rows || !tw_cols || !tw_vals || count > tw_cap)) return KVP_ERR_INVALID_ARG;
+  r.sink_pages = sp;
   for (int k = 0; k < count; ++k) {
-    const int d = r.dropped;
+    const int d = sp + r.dropped;
     unref_page(h, r.pages[d]);
     r.pages[d] = -1;
     tw_rows[k] = rid;
@@ -246,6 +256,11 @@ int kvp_host_trim(kvp_host* h, int rid, int keep_from, int32_t* tw_rows,
   }
   *n_tw = count;
   return KVP_OK;
+}
+
+int kvp_host_trim(kvp_host* h, int rid, int keep_from, int32_t* tw_rows,
+                  int32_t* tw_cols, int32_t* tw_vals, int tw_cap, int* n_tw) {
+  return kvp_host_trim_sinks(h, rid, keep_from, 0, tw_rows, tw_cols, tw_vals, tw_cap, n_tw);
 }
 
 int kvp_host_used(const kvp_host* h, int* used) {

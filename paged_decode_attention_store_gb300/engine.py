@@ -95,9 +95,10 @@ class PagedKVCache:
         self.host.release(rid)
         self.lengths[rid] = self.dropped[rid] = 0
 
-    def trim(self, rid, keep_from):
-        """Release front pages below keep_from; returns the number of table writes."""
-        writes = self.host.trim(rid, keep_from)
+    def trim(self, rid, keep_from, sinks=0):
+        """Release the pages below keep_from (except the first ceil(sinks / P));
+        returns the number of table writes."""
+        writes = self.host.trim(rid, keep_from, sinks=sinks)
         self._write_table(writes)
         self.dropped[rid] += len(writes)
         return len(writes)
@@ -137,20 +138,21 @@ class PagedKVCache:
             self._ws[key] = kb.alloc_workspace(self.pool, batch, num_q_heads, device=self.dev)
         return self._ws[key]
 
-    def attend(self, layer, q, context_lens, window, scale, out, table_rows=None):
+    def attend(self, layer, q, context_lens, window, scale, out, table_rows=None, sinks=0):
         ws = self.workspace(q.shape[0], q.shape[1])
         kb.paged_decode_attention(self.pool, layer, q, self.table, self.table_mode, context_lens, window, scale,
-                                  out, ws, table_rows=table_rows)
+                                  out, ws, table_rows=table_rows, sinks=sinks)
 
     def store_and_attend(self, layer, q, k, v, out_loc, context_lens, window, scale, out, table_writes=None,
-                         table_rows=None):
+                         table_rows=None, sinks=0):
         """store_cache + paged_decode_attention of one layer in one launch;
         ``out_loc[b]`` must be the slot of request b's newest position, and
         ``table_writes`` (rows, cols, vals device tensors) may only add the
         pages of this step's new tokens."""
         ws = self.workspace(q.shape[0], q.shape[1])
         kb.store_cache_and_attention(self.pool, layer, q, k, v, out_loc, self.table, self.table_mode, context_lens,
-                                     window, scale, out, ws, table_rows=table_rows, table_writes=table_writes)
+                                     window, scale, out, ws, table_rows=table_rows, table_writes=table_writes,
+                                     sinks=sinks)
 
     def check(self):
         """Raise if a device-side error was recorded since the last check."""
@@ -160,7 +162,7 @@ class PagedKVCache:
 
 
     # -- one decode step, host buffers in and out ----------------------------
-    def decode_step(self, rids, q, k, v, out, window, scale):
+    def decode_step(self, rids, q, k, v, out, window, scale, sinks=0):
         """One decode step for the requests ``rids`` (one token each; request
         id = table row), through the native kvp_decode_step.
 
@@ -210,7 +212,7 @@ class PagedKVCache:
         ws = self.workspace(n, Hq)
         kb._check(L.kvp_decode_step(self.host.handle, self.pool.handle, vp(self.table.data_ptr()), self.table.shape[0],
                                     self.table.shape[1], self.table_mode, rids.ctypes.data_as(vp), n,
-                                    int(window or 0), Hq, float(scale), qp, kp, vpp, op, ready,
+                                    int(window or 0), int(sinks), Hq, float(scale), qp, kp, vpp, op, ready,
                                     done, vp(slot["host"].data_ptr()), vp(st["dev"].data_ptr()), st["cap"],
                                     vp(ws.data_ptr()), ws.numel(), vp(stream.cuda_stream), ctypes.byref(info)),
                   "kvp_decode_step")
@@ -221,11 +223,13 @@ class PagedKVCache:
         np.add.at(self.lengths, rids, 1)
         if window and window > 0 and info.n_trim_writes:
             # mirror the released pages: the native call releases every page that
-            # lies wholly below keep_from = L + 1 - window
+            # lies wholly below keep_from = L + 1 - (window - sinks), after the
+            # first ceil(sinks / P)
             Lr = self.lengths[rids]
-            keep = Lr + 1 - window
+            keep = Lr + 1 - (window - sinks)
+            sp = -(-sinks // self.P)
             to = np.minimum(np.maximum(keep, 0) // self.P, -(-Lr // self.P))
-            self.dropped[rids] = np.maximum(self.dropped[rids], to)
+            self.dropped[rids] = np.maximum(self.dropped[rids], to - sp)
         if host_io:
             if side:
                 with torch.cuda.stream(st["d2h"]):

@@ -77,10 +77,10 @@ class ProductSession:
             self.kb.store_cache(self.pool, layer, k, v, out_loc)
         return slots
 
-    def trim(self, rid, keep_from):
-        self._write(self.host.trim(rid, keep_from))
+    def trim(self, rid, keep_from, sinks=0):
+        self._write(self.host.trim(rid, keep_from, sinks=sinks))
 
-    def attend(self, layer, rids, lens, window, step, scale=None, table_rows=True):
+    def attend(self, layer, rids, lens, window, step, scale=None, table_rows=True, sinks=0):
         B = len(rids)
         if self.ws is None or self.ws_batch < B:
             self.ws = self.kb.alloc_workspace(self.pool, B, self.w.Hq, device=self.dev)
@@ -92,14 +92,14 @@ class ProductSession:
             self.pool, layer, q, self.table,
             self.kb.KVP_RAW_LOCATIONS if self.mode == "raw" else self.kb.KVP_BLOCK_TABLE,
             self._i32(lens), window, scale, out, self.ws,
-            table_rows=self._i32(rids) if table_rows else None)
+            table_rows=self._i32(rids) if table_rows else None, sinks=sinks)
         return out
 
-    def gather(self, rids, lens, window, max_tokens):
+    def gather(self, rids, lens, window, max_tokens, sinks=0):
         out = torch.empty((len(rids), max_tokens), dtype=torch.int32, device=self.dev)
         self.kb.gather_indices(self.pool, self.table,
                                self.kb.KVP_RAW_LOCATIONS if self.mode == "raw" else self.kb.KVP_BLOCK_TABLE,
-                               self._i32(lens), window, out, table_rows=self._i32(rids))
+                               self._i32(lens), window, out, table_rows=self._i32(rids), sinks=sinks)
         return out
 
     def error(self):
@@ -107,13 +107,20 @@ class ProductSession:
 
 
 class OracleSession:
-    def __init__(self, w, max_requests, mode="block", layers=None, seed=0, track=None, raw_cols=None):
+    """``raw_from_pages``: in raw mode, take a request's raw row as its block
+    row expanded to tokens (``PageTable.raw_row``) instead of running the
+    mini-sglang allocator, which has no window trim: needed once trims hand
+    pages back to the free list."""
+
+    def __init__(self, w, max_requests, mode="block", layers=None, seed=0, track=None, raw_cols=None,
+                 raw_from_pages=False):
         self.w, self.mode, self.seed = w, mode, seed
         self.P = w.P
         self.layers = layers or w.layers
         self.pt = PageTable(w.num_pages, w.P, free_order=w.free_order)
         self.raw = None
-        if mode == "raw":
+        self.raw_from_pages = raw_from_pages
+        if mode == "raw" and not raw_from_pages:
             self.raw = RawLocationTable(w.num_pages, w.P, max_requests, raw_cols or w.num_pages * w.P,
                                         free_page_order=w.free_order)
         self.stores = [OA.SlotStore() for _ in range(self.layers)]
@@ -154,22 +161,35 @@ class OracleSession:
                 st.store_cache(slots, k.float().numpy(), v.float().numpy())
         return [r["slot"] for r in res]
 
-    def trim(self, rid, keep_from):
+    def trim(self, rid, keep_from, sinks=0):
+        if sinks:
+            return self.pt.trim(rid, keep_from, sink_rows=sinks)
         return self.pt.trim(rid, keep_from)
 
     def slots(self, rid, lo, L):
+        if self.mode == "raw" and self.raw_from_pages:
+            return OA.gather_raw(self.pt.raw_row(rid), lo, L)
         if self.mode == "raw":
             return OA.gather_raw(self.raw.page_table[rid], lo, L)
         return OA.gather_block(self.pt.block_row(rid), self.P, lo, L)
 
-    def attend(self, layer, rid, L, window, step, scale=None):
+    def span_slots(self, rid, L, window, sinks):
+        """Slots of every position the step attends (sink rows first)."""
+        sink_end, lo = OA.sink_window(L, window, sinks)
+        return self.slots(rid, 0, sink_end) + self.slots(rid, lo, L)
+
+    def attend(self, layer, rid, L, window, step, scale=None, sinks=0):
         q = wl.q_rows(self.seed, step, layer, [rid], self.w.Hq, self.w.D, dtype=self.dt)[0].float().numpy()
-        lo = OA.window_lo(L, window)
         scale = self.w.scale if scale is None else scale
+        if sinks:
+            return OA.attend_request(self.stores[layer], q, self.span_slots(rid, L, window, sinks), scale)
+        lo = OA.window_lo(L, window)
         return OA.attend_request(self.stores[layer], q, self.slots(rid, lo, L), scale)
 
     def table_row(self, rid):
         """The device-visible prefix of this request's table row."""
+        if self.mode == "raw" and self.raw_from_pages:
+            return self.pt.raw_row(rid)
         if self.mode == "raw":
             n = len(self.pt.block_row(rid)) * self.P
             return [int(x) for x in self.raw.page_table[rid, :n]]

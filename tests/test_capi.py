@@ -38,9 +38,9 @@ def test_argument_checks_fail_before_launch():
     assert lib.copy_pages(null, null, null, 1, null) == kb.KVP_ERR_INVALID_ARG
     assert lib.page_table_write(null, 1, 1, null, null, null, 1, 1, null, null) == kb.KVP_ERR_INVALID_ARG
     assert lib.page_table_write(ctypes.c_void_p(16), 1, 1, null, null, null, 1, 0, null, null) == kb.KVP_ERR_INVALID_ARG
-    assert lib.paged_decode_attention(null, 0, null, 1, 1, null, 1, 1, 0, null, null, 0, 1.0, null, null, 0,
+    assert lib.paged_decode_attention(null, 0, null, 1, 1, null, 1, 1, 0, null, null, 0, 0, 1.0, null, null, 0,
                                       null) == kb.KVP_ERR_INVALID_ARG
-    assert lib.gather_indices(null, null, 1, 1, 0, null, null, 1, 0, null, 1, null) == kb.KVP_ERR_INVALID_ARG
+    assert lib.gather_indices(null, null, 1, 1, 0, null, null, 1, 0, 0, null, 1, null) == kb.KVP_ERR_INVALID_ARG
     out = ctypes.c_void_p()
     # misaligned buffer and bad dtype are rejected before any CUDA call
     assert lib.kv_pool_create(4, 4, 1, 16, 1, 1, ctypes.c_void_p(8), ctypes.c_void_p(64),

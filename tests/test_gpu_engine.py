@@ -27,8 +27,9 @@ def kb():
     return ensure_built()
 
 
-@pytest.mark.parametrize("window,host_io", [(0, True), (40, True), (40, False)])
-def test_decode_step_matches_the_oracle(kb, window, host_io):
+@pytest.mark.parametrize("window,host_io,sinks", [(0, True, 0), (40, True, 0), (40, False, 0), (40, True, 2),
+                                                  (40, False, 20)])
+def test_decode_step_matches_the_oracle(kb, window, host_io, sinks):
     from paged_decode_attention_store_gb300.engine import PagedKVCache
 
     Hq, Hkv, D, P, seed = 32, 8, 128, 16, 71
@@ -50,8 +51,8 @@ def test_decode_step_matches_the_oracle(kb, window, host_io):
         cache.store(0, k, v, slots)
         orc.append([b] * lengths[b], list(range(lengths[b])))
         if window:
-            cache.trim(b, max(0, lengths[b] + 1 - window))
-            orc.trim(b, max(0, lengths[b] + 1 - window))
+            cache.trim(b, max(0, lengths[b] + 1 - (window - sinks)), sinks=sinks)
+            orc.trim(b, max(0, lengths[b] + 1 - (window - sinks)), sinks=sinks)
     cache.fork(1, 3)
     orc.fork(1, 3)
     rids = np.arange(B, dtype=np.int32)
@@ -65,16 +66,16 @@ def test_decode_step_matches_the_oracle(kb, window, host_io):
         else:
             qi, ki, vi = q, k, v
             out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=DEV)
-        cache.decode_step(rids, [qi], [ki], [vi], [out], window, w.scale)
+        cache.decode_step(rids, [qi], [ki], [vi], [out], window, w.scale, sinks=sinks)
         assert orc.append(list(range(B)), lens) is not None
         lens = [L + 1 for L in lens]
         got = out.float().cpu().numpy()
         for b in range(B):
-            ref = orc.attend(0, b, lens[b], window, step=step)
+            ref = orc.attend(0, b, lens[b], window, step=step, sinks=sinks)
             assert max_abs(got[b], ref) <= 2e-2, f"step {step} request {b}"
         if window:
             for b in range(B):
-                orc.trim(b, max(0, lens[b] + 1 - window))
+                orc.trim(b, max(0, lens[b] + 1 - (window - sinks)), sinks=sinks)
         assert cache.host.used() == orc.pt.used()
         assert cache.lengths[:B].tolist() == lens
     assert cache.copies == 1  # request 3's first append copied the shared tail page

@@ -24,11 +24,14 @@ def _state_equal(host, opt, live):
         assert host.length(rid) == (opt.length[rid], opt.dropped[rid])
 
 
-@pytest.mark.parametrize("seed", range(12))
+@pytest.mark.parametrize("seed", range(18))
 def test_shadow_ops_match_the_oracle(seed):
+    """Seeds 12-17 give each request a fixed number of attention-sink rows
+    that its trims keep (chapter 15, exercise "Attention sinks")."""
     kb = ensure_built()
     R = random.Random(seed)
-    n_pages, P = (24, 4) if seed < 6 else (64, R.choice([1, 3, 16]))
+    n_pages, P = (24, 4) if seed < 6 or seed >= 12 else (64, R.choice([1, 3, 16]))
+    sinks = {}
     order = list(range(n_pages))
     R.shuffle(order)
     host = kb.HostPageTable(n_pages, P, 16, order)
@@ -42,6 +45,7 @@ def test_shadow_ops_match_the_oracle(seed):
             host.new(rid)
             opt.new(rid)
             live.append(rid)
+            sinks[rid] = R.choice([0, 1, 2, 4, 5, 9]) if seed >= 12 else 0
         elif op in ("append", "batch") and live:
             rids = [R.choice(live) for _ in range(1 if op == "append" else R.randrange(1, 6))]
             snapshot = (opt.free[:], opt.ref[:], {r: (opt.table[r][:], opt.length[r]) for r in live})
@@ -65,13 +69,14 @@ def test_shadow_ops_match_the_oracle(seed):
             src, dst = R.choice(live), free_rids[0]
             writes = host.fork(src, dst)
             opt.fork(src, dst)
+            sinks[dst] = sinks[src]
             assert writes == [(dst, i, p) for i, p in enumerate(opt.block_row(dst))]
             live.append(dst)
         elif op == "trim" and live:
             rid = R.choice(live)
             k = R.randrange(0, opt.length[rid] + 1)
-            writes = host.trim(rid, k)
-            released = opt.trim(rid, k)
+            writes = host.trim(rid, k, sinks=sinks[rid])
+            released = opt.trim(rid, k, sink_rows=sinks[rid]) if sinks[rid] else opt.trim(rid, k)
             assert writes == [(rid, d, -1) for d in released]
         elif op == "release" and live:
             rid = R.choice(live)
