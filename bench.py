@@ -50,7 +50,8 @@ METRIC = "paged decode-attention achieved HBM GB/s (% of GB300 peak); decode tok
 UNIT = "GB/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-WORKLOADS = ("gqa_decode", "sliding_window", "prefix_sharing", "large_batch_p16", "large_batch_p1")
+WORKLOADS = ("gqa_decode", "sliding_window", "sliding_window_sinks", "prefix_sharing", "large_batch_p16",
+             "large_batch_p1")
 DEFAULT_WORKLOAD = "gqa_decode"
 
 
@@ -65,6 +66,8 @@ class Scenario:
             w = wl.gqa_decode(seed)
         elif name == "sliding_window":
             w = wl.sliding_window(seed)
+        elif name == "sliding_window_sinks":
+            w = wl.sliding_window_sinks(seed)
         elif name == "prefix_sharing":
             w = wl.prefix_sharing(seed)
         elif name.startswith("large_batch_p"):
@@ -81,7 +84,7 @@ class Scenario:
             self.max_requests = n_req + x["n_prompts"]
             for i in range(x["n_prompts"]):
                 self.ops.append(("new", n_req + i))
-                self.ops.append(("append", n_req + i, x["prompt_len"], 0))
+                self.ops.append(("append", n_req + i, x["prompt_len"], 0, 0))
             for f in range(n_req):
                 self.ops.append(("fork", n_req + f // x["forks"], f))
             self.ops.append(("batch", list(range(n_req))))  # first suffix token: copy-on-write
@@ -89,7 +92,7 @@ class Scenario:
                 self.ops.append(("release", n_req + i))
             for f in range(n_req):
                 if x["suffix"][f] > 1:
-                    self.ops.append(("append", f, x["suffix"][f] - 1, 0))
+                    self.ops.append(("append", f, x["suffix"][f] - 1, 0, 0))
             self.lengths = [x["prompt_len"] + s for s in x["suffix"]]
             self.accumulate = False
         else:
@@ -101,19 +104,36 @@ class Scenario:
                 self.ops.append(("new", b))
                 if w.window > 0:
                     # the real append + trim path, in chunks of 256 rows; only
-                    # rows a later window can reach get data
+                    # rows a later window can reach get data (the sink rows
+                    # and the last W - S)
                     t = 0
                     while t < L:
                         n = min(256, L - t)
-                        self.ops.append(("append", b, n, max(0, L - w.window)))
+                        self.ops.append(("append", b, n, max(0, L - (w.window - w.sinks)), w.sinks))
                         t += n
-                        self.ops.append(("trim", b, max(0, t + 1 - w.window)))
+                        self.ops.append(("trim", b, max(0, t + 1 - (w.window - w.sinks)), w.sinks))
                     self.accumulate = False
                 else:
-                    self.ops.append(("append", b, L, 0))
+                    self.ops.append(("append", b, L, 0, 0))
         self.raw = w.table_mode == "raw"
         self.max_seq_len = w.extra.get("max_seq_len") if self.raw else max(self.lengths) + 512
         self.window = w.window
+        self.sinks = w.sinks
+
+
+def attended_span(sc, L):
+    """(se, lo): a step with context L reads rows [0, se) and [lo, L)."""
+    W, S = sc.w.window, sc.w.sinks
+    if W <= 0:
+        return 0, 0
+    lo = max(0, L - (W - S))
+    se = min(S, lo)
+    return (0, 0) if se == lo else (se, lo)
+
+
+def attended_count(sc, L):
+    se, lo = attended_span(sc, L)
+    return se + L - lo
 
 
 def attention_bytes(sc, lens):
@@ -124,9 +144,10 @@ def attention_bytes(sc, lens):
     elem = 2 if w.dtype == "bf16" else 4
     kv = tab = 0
     for L in lens:
-        lo = max(0, L - w.window) if w.window > 0 else 0
-        kv += (L - lo) * row_kv
-        tab += 4 * ((L - lo) if sc.raw else (-(-L // w.P) - lo // w.P))
+        se, lo = attended_span(sc, L)
+        n = se + L - lo
+        kv += n * row_kv
+        tab += 4 * (n if sc.raw else (-(-se // w.P) + -(-L // w.P) - lo // w.P))
     qo = 2 * len(lens) * w.Hq * w.D * elem
     return kv + qo + tab + 4 * len(lens)
 
@@ -200,13 +221,16 @@ def build_product(sc, dev):
             cache.new(op[1])
             lengths[op[1]] = 0
         elif kind == "append":
-            _, rid, n, store_from = op
+            _, rid, n, store_from, store_below = op
             L0 = lengths[rid]
             slots = cache.append([rid] * n)
             lengths[rid] = L0 + n
             first = max(store_from, L0)
             if first < L0 + n:
                 add_store([rid] * (L0 + n - first), list(range(first, L0 + n)), slots[first - L0:])
+            sink_end = min(store_below, first, L0 + n)  # sink rows below the stored tail
+            if L0 < sink_end:
+                add_store([rid] * (sink_end - L0), list(range(L0, sink_end)), slots[:sink_end - L0])
         elif kind == "batch":
             rids = op[1]
             flush()
@@ -215,7 +239,7 @@ def build_product(sc, dev):
             for r in rids:
                 lengths[r] += 1
         elif kind == "trim":
-            cache.trim(op[1], op[2])
+            cache.trim(op[1], op[2], sinks=op[3])
         elif kind == "fork":
             flush()
             cache.fork(op[1], op[2])
@@ -255,7 +279,7 @@ def prepare_steps(sc, cache, lens, first_step, n_steps, dev, host_inputs=False):
         post = []
         if sc.window > 0:
             for r, L in zip(sc.rids, lens):
-                wr = cache.host.trim(r, max(0, L + 1 - sc.window))
+                wr = cache.host.trim(r, max(0, L + 1 - (sc.window - sc.sinks)), sinks=sc.sinks)
                 cache.dropped[r] += len(wr)
                 post += wr
         st.n_post = len(post)
@@ -301,7 +325,7 @@ def run_step(sc, cache, st, outs, events=None):
             kb.kvp_pool_set_timing_events(cache.pool, *events.pop())
         tw = pre if layer == 0 else None
         cache.store_and_attend(layer, st.q[layer], st.k[layer], st.v[layer], st.out_loc, st.lens, sc.window,
-                               w.scale, outs[layer], table_writes=tw)
+                               w.scale, outs[layer], table_writes=tw, sinks=sc.sinks)
         n += 2 if fused else 2 + (tw is not None)  # fused kernel + combine, or write, store, general kernel
     if st.post is not None:
         kb.page_table_write(cache.table, *st.post, expand=P if sc.raw else 1, error_word=cache.pool.error_word)
@@ -420,11 +444,14 @@ def run_gpu(args, rank, world, local_rank):
     outs = [torch.empty((len(sc.rids), w.Hq, w.D), dtype=tdt, device=dev) for _ in range(w.layers)]
 
     sampler = ClockSampler(local_rank) if rank == 0 else None
-    # soak: repeat the current state's attention ~1 s so clocks settle and get sampled
+    # soak: repeat the current state's attention ~1 s so clocks settle and get
+    # sampled. The history was trimmed for the first decode step (context
+    # L + 1), so at context L the window is one row shorter.
     t_soak = time.time()
+    soak_window = sc.window - 1 if sc.window > 0 else 0
     while time.time() - t_soak < args.soak:
         for layer in range(w.layers):
-            cache.attend(layer, steps[0].q[layer], _i32(lens, dev), sc.window, w.scale, outs[layer])
+            cache.attend(layer, steps[0].q[layer], _i32(lens, dev), soak_window, w.scale, outs[layer], sinks=sc.sinks)
         torch.cuda.synchronize(dev)
     for i in range(W):
         run_step(sc, cache, steps[i], outs)
@@ -496,12 +523,12 @@ def run_gpu(args, rank, world, local_rank):
             "page_size": w.P,
             "layers": w.layers,
             "window": w.window,
+            "sinks": w.sinks,
             "table": "raw token locations" if sc.raw else "block table",
             "mean_attended_tokens": round(statistics.mean(
-                (L - (max(0, L - w.window) if w.window > 0 else 0)) for L in steps[W].lens_list), 1),
-            "kv_bytes_per_step": int(sum(
-                (L - (max(0, L - w.window) if w.window > 0 else 0)) for L in steps[W].lens_list)
-                * 2 * w.Hkv * w.D * 2 * w.layers),
+                attended_count(sc, L) for L in steps[W].lens_list), 1),
+            "kv_bytes_per_step": int(sum(attended_count(sc, L) for L in steps[W].lens_list)
+                                     * 2 * w.Hkv * w.D * 2 * w.layers),
             "l2": "no flush: inputs larger than L2 (K/V read per step >> 129 MB)",
             "seed": args.seed,
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
@@ -556,7 +583,7 @@ def run_e2e(args, sc, cache, lens, first_step, dev):
     start.record()
     for s in range(K):
         q_h, k_h, v_h = host_steps[s]
-        cache.decode_step(rids, q_h, k_h, v_h, out_host, sc.window, w.scale)
+        cache.decode_step(rids, q_h, k_h, v_h, out_host, sc.window, w.scale, sinks=sc.sinks)
         total_bytes += step_bytes(sc, [int(x) for x in cache.lengths[rids]], cache.last_writes, cache.last_copies,
                                   cache.last_trims)
     end.record()
@@ -666,18 +693,24 @@ class OracleSample:
         if kind == "new":
             self.pt.new(op[1])
         elif kind == "append":
-            _, rid, n, store_from = op
+            _, rid, n, store_from, store_below = op
             L0 = self.pt.length[rid]
             slots = self._append([rid] * n)
             first = max(store_from, L0)
             self._store(rid, list(range(first, L0 + n)), slots[first - L0:])
+            sink_end = min(store_below, first, L0 + n)
+            if L0 < sink_end:
+                self._store(rid, list(range(L0, sink_end)), slots[:sink_end - L0])
         elif kind == "batch":
             pos = [self.pt.length[r] for r in op[1]]
             slots = self._append(op[1])
             for r, p, s in zip(op[1], pos, slots):
                 self._store(r, [p], [s])
         elif kind == "trim":
-            self.pt.trim(op[1], op[2])
+            if op[3]:
+                self.pt.trim(op[1], op[2], sink_rows=op[3])
+            else:
+                self.pt.trim(op[1], op[2])
         elif kind == "fork":
             self.pt.fork(op[1], op[2])
         elif kind == "release":
@@ -697,17 +730,23 @@ class OracleSample:
             self._store(r, [p], [s])
         for r in attend_rids:
             L = self.pt.length[r]
-            lo = OA.window_lo(L, sc.window)
+            pos = OA.attended_positions(L, sc.window, sc.sinks)
             for layer in self.layers:
                 q = wl.q_rows(sc.seed, step_index, layer, [r], w.Hq, w.D, dtype=self.tdt)[0].float().numpy()
                 if self.raw is not None:
-                    sl = OA.gather_raw(self.raw.page_table[r], lo, L)
+                    row = self.raw.page_table[r]
+                    sl = [s for p in pos for s in OA.gather_raw(row, p, p + 1)]
                 else:
-                    sl = OA.gather_block(self.pt.block_row(r), w.P, lo, L)
+                    row = self.pt.block_row(r)
+                    sl = [s for p in pos for s in OA.gather_block(row, w.P, p, p + 1)]
                 outs[(r, layer)] = OA.attend_request(self.stores[layer], q, sl, w.scale)
         if sc.window > 0:
             for r in sc.rids:
-                self.pt.trim(r, max(0, self.pt.length[r] + 1 - sc.window))
+                kf = max(0, self.pt.length[r] + 1 - (sc.window - sc.sinks))
+                if sc.sinks:
+                    self.pt.trim(r, kf, sink_rows=sc.sinks)
+                else:
+                    self.pt.trim(r, kf)
         return (outs, slots) if with_slots else outs
 
 

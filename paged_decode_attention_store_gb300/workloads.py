@@ -142,6 +142,7 @@ class Workload:
     free_order: list           # free-list stack, top = end
     lengths: list              # context length of each request before the first decode step
     window: int = 0            # <= 0: none
+    sinks: int = 0             # attention-sink rows kept in every windowed context
     scale: float = 0.0
     table_mode: str = "block"  # "block" or "raw"
     extra: dict = field(default_factory=dict)
@@ -184,6 +185,20 @@ def sliding_window(seed: int = 0) -> Workload:
     return Workload("sliding_window", "bf16", 32, 8, 128, P, 1, n_pages,
                     free_stack_for_order(order), lengths, window=W,
                     scale=1.0 / math.sqrt(128))
+
+
+def sliding_window_sinks(seed: int = 0, sinks: int = 2) -> Workload:
+    """sliding_window with attention sinks (chapter 15, exercise "Attention
+    sinks": the first 2 rows plus the last W - 2): the same lengths and pool,
+    the first page of each request kept past the window."""
+    w = sliding_window(seed)
+    P, B = w.P, len(w.lengths)
+    live = -(-sinks // P) + -(-(w.window - sinks - 1) // P) + 1
+    n_pages = int(math.ceil(B * live * 1.1))
+    order = np.random.RandomState(seed * 7919 + 5).permutation(n_pages)
+    return Workload("sliding_window_sinks", "bf16", w.Hq, w.Hkv, w.D, P, 1, n_pages,
+                    free_stack_for_order(order), list(w.lengths), window=w.window, sinks=sinks,
+                    scale=w.scale)
 
 
 def prefix_sharing(seed: int = 0) -> Workload:
