@@ -63,6 +63,16 @@ def attended_positions(L: int, W, S: int = 0) -> list:
     return list(range(0, sink_end)) + list(range(lo, L))
 
 
+def verify_positions(L: int, M: int, W, S: int = 0) -> list:
+    """Multi-token verify: the M newest tokens of a request with context L
+    (positions L - M .. L - 1) are queries at once. Query j attends what a
+    single-token step with context L - M + j + 1 attends (causal: nothing
+    after its own position). Returns one position list per query."""
+    if M < 1 or M > L:
+        raise ValueError("need 1 <= M <= L")
+    return [attended_positions(L - M + j + 1, W, S) for j in range(M)]
+
+
 def attention_one(q, K, V, scale: float):
     """One query row against ``n >= 1`` key/value rows, float64.
 

@@ -28,7 +28,15 @@ section "The model"):
   no bookkeeping for sinks; this is the plain reading that releases exactly
   the pages no later step reads);
 * ``fork`` copies table, length and dropped count and adds one reference to
-  every page; ``release`` lets go of every page.
+  every page; ``release`` lets go of every page;
+* ``rewind(n)`` ("Week 3 Day 3: Paged KV Cache", tiny-llm: drop the newest
+  ``n`` logical tokens, free the whole pages no longer needed and shorten
+  the valid length of the last page that remains) lets go of the pages past
+  ``ceil((length - n) / page)``. The page is silent on the order in which
+  freed pages return; they are pushed tail first, so that the stack hands
+  them back in logical order and re-appending the same tokens rebuilds the
+  same table. Rows that a later step may read must stay: the new length may
+  not reach below the released front (the window's or the sinks' holes).
 
 Exhaustion raises :class:`OutOfPages` before any state changes, so a failed
 append leaves the request untouched (chapter 15, section "Tests", item 2).
@@ -174,6 +182,26 @@ class PageTable:
             released.append(sp + self.dropped[rid])
             self.dropped[rid] += 1
         return released
+
+    def rewind(self, rid, n: int) -> list:
+        """Drop the newest ``n`` tokens; returns the absolute logical indices
+        of the pages let go (tail first)."""
+        L = self.length[rid]
+        if n < 0 or n > L:
+            raise ValueError(f"cannot rewind {n} of {L} tokens")
+        keep_len = L - n
+        sp, d = self.sinks[rid], self.dropped[rid]
+        if d > 0 and keep_len < (sp + d) * self.page:
+            raise ValueError("rewind would reach into released pages")
+        keep_pages = -(-keep_len // self.page)  # absolute logical pages that keep rows
+        t = self.table[rid]
+        gone = []
+        while t and d + len(t) > keep_pages and (d == 0 or len(t) > sp):
+            logical = d + len(t) - 1
+            self._unref(t.pop())
+            gone.append(logical)
+        self.length[rid] = keep_len
+        return gone
 
     def fork(self, src, dst) -> None:
         self.table[dst] = list(self.table[src])
