@@ -174,6 +174,36 @@ int paged_decode_attention(const kvp_pool* pool, int layer, const void* q,
                            void* stream);
 
 /* ------------------------------------------------------------------------
+ * paged_verify_attention: multi-token verify for speculative decoding. The
+ * M = num_q_tokens newest tokens of each request (already stored; L =
+ * context_lens[b] counts them) are queries at once: query j sits at
+ * position p = L - M + j and attends what a one-token step with context
+ * p + 1 attends (causal; the same window and sinks), i.e.
+ *     out[b][j][h] = paged_decode_attention with context p + 1.
+ * "Week 3 Day 3: Paged KV Cache" (tiny-llm) names speculative decoding as
+ * the user of rewind(n) (kvp_host_rewind); the verify formula is the
+ * decode step's, applied per query position. The K/V rows are read once
+ * for all M queries.
+ *   q    device [batch, M, num_q_heads, head_dim], pool dtype, 16-byte aligned.
+ *   out  device [batch, M, num_q_heads, head_dim], pool dtype.
+ *   context_lens  M <= L <= table capacity (else KVP_ERR_BAD_INDEX, zeros).
+ *   1 <= M <= 32. Workspace from paged_verify_attention_workspace_size;
+ * everything else as paged_decode_attention.
+ * ---------------------------------------------------------------------- */
+int paged_verify_attention_workspace_size(const kvp_pool* pool, int batch,
+                                          int num_q_tokens, int num_q_heads,
+                                          size_t* bytes);
+int paged_verify_attention(const kvp_pool* pool, int layer, const void* q,
+                           int batch, int num_q_tokens, int num_q_heads,
+                           const int32_t* table, int table_rows_total,
+                           int table_cols, int table_mode,
+                           const int32_t* table_rows,
+                           const int32_t* context_lens, int window,
+                           int sinks, float scale, void* out,
+                           void* workspace, size_t workspace_bytes,
+                           void* stream);
+
+/* ------------------------------------------------------------------------
  * store_cache_and_attention: one layer of a decode step in one launch:
  *     page_table_write(table, tw_rows, tw_cols, tw_vals, n_tw, expand);
  *     store_cache(pool, layer, k, v, out_loc, batch);
@@ -322,6 +352,17 @@ int kvp_host_trim(kvp_host* h, int rid, int keep_from, int32_t* tw_rows,
 int kvp_host_trim_sinks(kvp_host* h, int rid, int keep_from, int sink_rows,
                         int32_t* tw_rows, int32_t* tw_cols, int32_t* tw_vals,
                         int tw_cap, int* n_tw);
+
+/* Drop the newest n tokens of request rid ("Week 3 Day 3: Paged KV Cache",
+ * tiny-llm: rewind(n) frees the whole pages no longer needed and shortens
+ * the valid length of the last page; speculative decoding uses it when
+ * drafted tokens are rejected). Pages past ceil((length - n) / P) are let go
+ * tail first, so that the free stack hands them back in logical order, and
+ * emitted as (rid, logical page, -1) table writes (capacity tw_cap, count in
+ * *n_tw). The new length may not reach below the pages a window or its sinks
+ * released (KVP_ERR_INVALID_ARG, nothing changed); n > length likewise. */
+int kvp_host_rewind(kvp_host* h, int rid, int n, int32_t* tw_rows,
+                    int32_t* tw_cols, int32_t* tw_vals, int tw_cap, int* n_tw);
 
 /* ------------------------------------------------------------------------
  * kvp_decode_step: one decode step of the whole path in one call, in the

@@ -46,6 +46,8 @@ SIGNATURES = {
     "copy_pages": [_vp, _vp, _vp, _i, _vp],
     "paged_decode_attention_workspace_size": [_vp, _i, _i, _szp],
     "paged_decode_attention": [_vp, _i, _vp, _i, _i, _vp, _i, _i, _i, _vp, _vp, _i, _i, _f, _vp, _vp, _sz, _vp],
+    "paged_verify_attention_workspace_size": [_vp, _i, _i, _i, _szp],
+    "paged_verify_attention": [_vp, _i, _vp, _i, _i, _i, _vp, _i, _i, _i, _vp, _vp, _i, _i, _f, _vp, _vp, _sz, _vp],
     "paged_decode_attention_noalloc": [_vp, _i, _vp, _i, _i, _vp, _i, _i, _i, _vp, _vp, _i, _f, _vp, _vp],
     "store_cache_and_attention": [_vp, _i, _vp, _vp, _vp, _vp, _i, _i, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _i,
                                   _i, _i, _f, _vp, _vp, _sz, _vp],
@@ -60,6 +62,7 @@ SIGNATURES = {
     "kvp_host_append": [_vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _ip, _vp, _vp, _ip],
     "kvp_host_trim": [_vp, _i, _i, _vp, _vp, _vp, _i, _ip],
     "kvp_host_trim_sinks": [_vp, _i, _i, _i, _vp, _vp, _vp, _i, _ip],
+    "kvp_host_rewind": [_vp, _i, _i, _vp, _vp, _vp, _i, _ip],
     "kvp_host_used": [_vp, _ip],
     "kvp_host_length": [_vp, _i, _ip, _ip],
     "kvp_host_block_row": [_vp, _i, _vp, _i, _ip],
@@ -227,6 +230,40 @@ def paged_decode_attention(pool, layer, q, table, table_mode, context_lens, wind
                                         _stream(stream)), "paged_decode_attention")
 
 
+def paged_verify_attention_workspace_size(pool, batch, num_q_tokens, num_q_heads):
+    n = ctypes.c_size_t()
+    _check(lib().paged_verify_attention_workspace_size(pool.handle, batch, num_q_tokens, num_q_heads,
+                                                       ctypes.byref(n)), "paged_verify_attention_workspace_size")
+    return n.value
+
+
+def alloc_verify_workspace(pool, batch, num_q_tokens, num_q_heads, device="cuda"):
+    nbytes = paged_verify_attention_workspace_size(pool, batch, num_q_tokens, num_q_heads)
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def paged_verify_attention(pool, layer, q, table, table_mode, context_lens, window, scale, out, workspace,
+                           table_rows=None, stream=None, sinks=0):
+    """Multi-token verify: q/out [B, M, Hq, D]; query j of request b sits at
+    position context_lens[b] - M + j and attends causally (see
+    include/pagedkv.h)."""
+    dt = _TORCH_DTYPE[pool.dtype]
+    _dev(q, dt, "q")
+    _dev(out, dt, "out")
+    _dev(table, torch.int32, "table")
+    _dev(context_lens, torch.int32, "context_lens")
+    if table_rows is not None:
+        _dev(table_rows, torch.int32, "table_rows")
+    if q.dim() != 4 or out.shape != q.shape or context_lens.numel() != q.shape[0]:
+        raise ValueError("q/out must be [B, M, Hq, D] and context_lens [B]")
+    B, M, Hq = q.shape[0], q.shape[1], q.shape[2]
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (_ptr(workspace), workspace.numel() * workspace.element_size())
+    _check(lib().paged_verify_attention(pool.handle, layer, _ptr(q), B, M, Hq, _ptr(table), table.shape[0],
+                                        table.shape[1], table_mode, _ptr(table_rows), _ptr(context_lens),
+                                        int(window or 0), int(sinks), float(scale), _ptr(out), ws_ptr, ws_bytes,
+                                        _stream(stream)), "paged_verify_attention")
+
+
 def store_cache_and_attention(pool, layer, q, k, v, out_loc, table, table_mode, context_lens, window, scale, out,
                               workspace, table_rows=None, table_writes=None, stream=None, sinks=0):
     """store_cache + paged_decode_attention of one layer in one launch, with
@@ -390,6 +427,15 @@ class HostPageTable:
             _check(lib().kvp_host_trim(self.handle, rid, int(keep_from), tr, tc, tv, cap, ctypes.byref(n)),
                    "kvp_host_trim")
         return list(zip(tr[:n.value], tc[:n.value], tv[:n.value]))
+
+    def rewind(self, rid, n):
+        """Drop the newest n tokens; returns the (rid, page, -1) table writes
+        of the pages let go (tail first)."""
+        cap = max(1, self.length(rid)[0] // self.page_size + 1)
+        tr, tc, tv = _i32(cap), _i32(cap), _i32(cap)
+        k = ctypes.c_int()
+        _check(lib().kvp_host_rewind(self.handle, rid, int(n), tr, tc, tv, cap, ctypes.byref(k)), "kvp_host_rewind")
+        return list(zip(tr[:k.value], tc[:k.value], tv[:k.value]))
 
     def used(self):
         u = ctypes.c_int()

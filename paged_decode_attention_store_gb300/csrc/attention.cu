@@ -37,6 +37,7 @@ struct GenArgs {
   const int32_t* context_lens;
   const int32_t* table_rows;
   int B, Hq, Hkv, D, window, sinks;
+  int M;  // query tokens per request (query j at position L - M + j)
   float scale_log2;
   int32_t* err;
 };
@@ -49,19 +50,21 @@ __global__ void __launch_bounds__(32 * kGenWarps) generic_decode_kernel(const Ge
   __shared__ float qs[kGenWarps][kGenMaxD];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long wid = (long long)blockIdx.x * kGenWarps + warp;
-  if (wid >= (long long)a.B * a.Hq) return;
-  const int b = (int)(wid / a.Hq), h = (int)(wid % a.Hq);
+  if (wid >= (long long)a.B * a.M * a.Hq) return;
+  const int bj = (int)(wid / a.Hq), h = (int)(wid % a.Hq);  // (request, query token), query head
+  const int b = bj / a.M, j = bj % a.M;
   const int G = a.Hq / a.Hkv, kvh = h / G;
   const int D = a.D;
-  T* out = static_cast<T*>(a.out) + ((size_t)b * a.Hq + h) * D;
-  const T* q = static_cast<const T*>(a.q) + ((size_t)b * a.Hq + h) * D;
-  const int L = a.context_lens[b];
+  T* out = static_cast<T*>(a.out) + ((size_t)bj * a.Hq + h) * D;
+  const T* q = static_cast<const T*>(a.q) + ((size_t)bj * a.Hq + h) * D;
+  const int Lr = a.context_lens[b];
   const int row = a.table_rows ? a.table_rows[b] : b;
-  if (L < 1 || L > table_capacity(a.T) || row < 0 || row >= a.T.rows_total) {
-    if (h == 0 && lane == 0) set_error(a.err, KVP_ERR_BAD_INDEX);
+  if (Lr < a.M || Lr < 1 || Lr > table_capacity(a.T) || row < 0 || row >= a.T.rows_total) {
+    if (h == 0 && j == 0 && lane == 0) set_error(a.err, KVP_ERR_BAD_INDEX);
     for (int d = lane; d < D; d += 32) out[d] = from_f<T>(0.f);
     return;
   }
+  const int L = Lr - a.M + j + 1;  // the query token's own context (causal)
   for (int d = lane; d < D; d += 32) qs[warp][d] = to_f<T>(q[d]);
   __syncwarp();
   const Span sp = attend_span(L, a.window, a.sinks);
@@ -138,20 +141,38 @@ __global__ void gather_indices_kernel(TableRef T, const int32_t* context_lens, c
   }
 }
 
-bool tc_eligible(const kvp_pool* pool, int Hq, int B, int* HG_out) {
+// The tensor-core kernel's shape for Hq query heads and M query tokens per
+// request: the M * G (token, head) columns of a KV head go to T consumer
+// warps of NT 8-column tiles, HG KV heads per CTA, HG * T <= 8 warps.
+struct TcShape {
+  int HG, NT, T;
+};
+
+bool tc_eligible(const kvp_pool* pool, int Hq, int B, int M, TcShape* out) {
   if (pool->dtype != KVP_BF16 || pool->head_dim != 128) return false;
   const int Hkv = pool->kv_heads;
-  if (Hq % Hkv) return false;
-  const int G = Hq / Hkv;
-  if (G > 16) return false;
-  for (int HG = 8; HG >= 1; --HG) {
+  if (Hq % Hkv || M < 1 || M > 32) return false;
+  const int C = (Hq / Hkv) * M;
+  const int NT = C <= 8 ? 1 : 2;
+  const int T = (C + 8 * NT - 1) / (8 * NT);
+  if (T > 8) return false;
+  for (int HG = 8 / T; HG >= 1; --HG) {
     if (Hkv % HG) continue;
-    if (tc_num_qbuf(HG, G) == 0) continue;
+    if (tc_num_qbuf(HG, C) == 0) continue;
     if (B > tc_max_batch(HG)) return false;
-    *HG_out = HG;
+    out->HG = HG;
+    out->NT = NT;
+    out->T = T;
     return true;
   }
   return false;
+}
+
+size_t workspace_bytes_for(const kvp_pool* pool, int batch, int M, int num_q_heads) {
+  TcShape sh;
+  if (!tc_eligible(pool, num_q_heads, batch, M, &sh)) return 256;  // the general kernel needs no scratch
+  const int QH = sh.HG * (num_q_heads / pool->kv_heads);
+  return ws_layout(pool->num_sms, M * QH, 128).total;
 }
 
 TableRef make_table(const kvp_pool* pool, const int32_t* table, int rows_total, int cols, int mode) {
@@ -175,13 +196,14 @@ using namespace kvp;
 extern "C" int paged_decode_attention_workspace_size(const kvp_pool* pool, int batch, int num_q_heads,
                                                      size_t* bytes) {
   if (!pool || !bytes || batch <= 0 || num_q_heads <= 0) return KVP_ERR_INVALID_ARG;
-  int HG = 0;
-  if (!tc_eligible(pool, num_q_heads, batch, &HG)) {
-    *bytes = 256;  // the general kernel needs no scratch
-    return KVP_OK;
-  }
-  const int QH = HG * (num_q_heads / pool->kv_heads);
-  *bytes = ws_layout(pool->num_sms, QH, 128).total;
+  *bytes = workspace_bytes_for(pool, batch, 1, num_q_heads);
+  return KVP_OK;
+}
+
+extern "C" int paged_verify_attention_workspace_size(const kvp_pool* pool, int batch, int num_q_tokens,
+                                                     int num_q_heads, size_t* bytes) {
+  if (!pool || !bytes || batch <= 0 || num_q_heads <= 0 || num_q_tokens < 1) return KVP_ERR_INVALID_ARG;
+  *bytes = workspace_bytes_for(pool, batch, num_q_tokens, num_q_heads);
   return KVP_OK;
 }
 
@@ -199,11 +221,12 @@ struct FuseIn {
   int n_tw;
 };
 
-int attention_impl(const kvp_pool* pool, int layer, const void* q, int batch, int num_q_heads, const int32_t* table,
-                   int table_rows_total, int table_cols, int table_mode, const int32_t* table_rows,
-                   const int32_t* context_lens, int window, int sinks, float scale, void* out, void* workspace,
-                   size_t workspace_bytes, void* stream, const FuseIn* fz) {
+int attention_impl(const kvp_pool* pool, int layer, const void* q, int batch, int M, int num_q_heads,
+                   const int32_t* table, int table_rows_total, int table_cols, int table_mode,
+                   const int32_t* table_rows, const int32_t* context_lens, int window, int sinks, float scale,
+                   void* out, void* workspace, size_t workspace_bytes, void* stream, const FuseIn* fz) {
   if (!pool || !q || !table || !context_lens || !out) return KVP_ERR_INVALID_ARG;
+  if (M < 1 || M > 32 || (fz && M != 1)) return KVP_ERR_INVALID_ARG;
   if (layer < 0 || layer >= pool->num_layers || batch <= 0 || num_q_heads <= 0) return KVP_ERR_INVALID_ARG;
   if (num_q_heads % pool->kv_heads) return KVP_ERR_INVALID_ARG;
   if (table_rows_total <= 0 || table_cols <= 0) return KVP_ERR_INVALID_ARG;
@@ -216,10 +239,10 @@ int attention_impl(const kvp_pool* pool, int layer, const void* q, int batch, in
   const char* kv_layer = pool->buf + (size_t)layer * pool->layer_bytes;
   const float scale_log2 = scale * 1.4426950408889634f;
 
-  int HG = 0;
+  TcShape sh;
   kvp_pool* mp = const_cast<kvp_pool*>(pool);
   const int expand = table_mode == KVP_RAW_LOCATIONS ? pool->page_size : 1;
-  if (fz && !tc_eligible(pool, num_q_heads, batch, &HG)) {
+  if (fz && !tc_eligible(pool, num_q_heads, batch, M, &sh)) {
     // no fused kernel for this pool: the same three operations in sequence
     int rc;
     if (fz->n_tw && (rc = page_table_write(fz->table, table_rows_total, table_cols, fz->tw_rows, fz->tw_cols,
@@ -228,12 +251,13 @@ int attention_impl(const kvp_pool* pool, int layer, const void* q, int batch, in
     if ((rc = store_cache(pool, layer, fz->k, fz->v, fz->out_loc, batch, stream)) != KVP_OK) return rc;
     fz = nullptr;
   }
-  if (tc_eligible(pool, num_q_heads, batch, &HG)) {
+  if (tc_eligible(pool, num_q_heads, batch, M, &sh)) {
     if (reinterpret_cast<uintptr_t>(q) & 15) return KVP_ERR_INVALID_ARG;
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255)) return KVP_ERR_INVALID_ARG;
+    const int HG = sh.HG;
     const int G = num_q_heads / pool->kv_heads;
     const int QH = HG * G;
-    const WsLayout L = ws_layout(pool->num_sms, QH, 128);
+    const WsLayout L = ws_layout(pool->num_sms, M * QH, 128);
     if (workspace_bytes < L.total) return KVP_ERR_INVALID_ARG;
     char* ws = static_cast<char*>(workspace);
 
@@ -247,7 +271,7 @@ int attention_impl(const kvp_pool* pool, int layer, const void* q, int batch, in
     else memset(&ta.tmap, 0, sizeof(ta.tmap));
     ta.kvl_k = layer;
     ta.kvl_v = pool->num_layers + layer;
-    ta.nq = tc_num_qbuf(HG, G);
+    ta.nq = tc_num_qbuf(HG, G * M);
     ta.T = T;
     ta.kv_layer = kv_layer;
     ta.kv_bytes = pool->kv_bytes;
@@ -263,6 +287,10 @@ int attention_impl(const kvp_pool* pool, int layer, const void* q, int batch, in
     ta.n_groups = pool->kv_heads / HG;
     ta.window = window;
     ta.sinks = sinks;
+    ta.M = M;
+    ta.NT = sh.NT;
+    ta.tiles = sh.T;
+    ta.CW = HG * sh.T;
     ta.num_ctas = pool->num_sms;
     ta.scale_log2 = scale_log2;
     ta.merge = reinterpret_cast<int4*>(ws + L.merge);
@@ -290,6 +318,7 @@ int attention_impl(const kvp_pool* pool, int layer, const void* q, int batch, in
     ca.QH = QH;
     ca.Hq = num_q_heads;
     ca.D = 128;
+    ca.M = M;
     const cudaError_t e = launch_tc(ta, ca, st, mp->ev_before, mp->ev_after);
     mp->ev_before = mp->ev_after = nullptr;
     return e == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
@@ -310,9 +339,10 @@ int attention_impl(const kvp_pool* pool, int layer, const void* q, int batch, in
   ga.D = pool->head_dim;
   ga.window = window;
   ga.sinks = sinks;
+  ga.M = M;
   ga.scale_log2 = scale_log2;
   ga.err = pool->err;
-  const long long warps = (long long)batch * num_q_heads;
+  const long long warps = (long long)batch * M * num_q_heads;
   const unsigned blocks = (unsigned)((warps + kGenWarps - 1) / kGenWarps);
   const bool timed = mp->ev_before != nullptr;
   if (timed && cudaEventRecord(static_cast<cudaEvent_t>(mp->ev_before), st) != cudaSuccess) return KVP_ERR_CUDA;
@@ -334,9 +364,19 @@ extern "C" int paged_decode_attention(const kvp_pool* pool, int layer, const voi
                                       const int32_t* table_rows, const int32_t* context_lens, int window,
                                       int sinks, float scale, void* out, void* workspace, size_t workspace_bytes,
                                       void* stream) {
-  return attention_impl(pool, layer, q, batch, num_q_heads, table, table_rows_total, table_cols, table_mode,
+  return attention_impl(pool, layer, q, batch, 1, num_q_heads, table, table_rows_total, table_cols, table_mode,
                         table_rows, context_lens, window, sinks, scale, out, workspace, workspace_bytes, stream,
                         nullptr);
+}
+
+extern "C" int paged_verify_attention(const kvp_pool* pool, int layer, const void* q, int batch, int num_q_tokens,
+                                      int num_q_heads, const int32_t* table, int table_rows_total, int table_cols,
+                                      int table_mode, const int32_t* table_rows, const int32_t* context_lens,
+                                      int window, int sinks, float scale, void* out, void* workspace,
+                                      size_t workspace_bytes, void* stream) {
+  return attention_impl(pool, layer, q, batch, num_q_tokens, num_q_heads, table, table_rows_total, table_cols,
+                        table_mode, table_rows, context_lens, window, sinks, scale, out, workspace, workspace_bytes,
+                        stream, nullptr);
 }
 
 extern "C" int store_cache_and_attention(const kvp_pool* pool, int layer, const void* q, const void* k,
@@ -350,7 +390,7 @@ extern "C" int store_cache_and_attention(const kvp_pool* pool, int layer, const 
     return KVP_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15) return KVP_ERR_INVALID_ARG;
   const FuseIn fz = {k, v, out_loc, table, tw_rows, tw_cols, tw_vals, n_tw};
-  return attention_impl(pool, layer, q, batch, num_q_heads, table, table_rows_total, table_cols, table_mode,
+  return attention_impl(pool, layer, q, batch, 1, num_q_heads, table, table_rows_total, table_cols, table_mode,
                         table_rows, context_lens, window, sinks, scale, out, workspace, workspace_bytes, stream,
                         &fz);
 }

@@ -54,11 +54,16 @@ struct TcArgs {
   const char* kv_layer;    // K of this layer
   size_t kv_bytes;         // K -> V distance
   size_t row_bytes;        // one token, all KV heads
-  const __nv_bfloat16* q;  // [B, Hq, D]
-  __nv_bfloat16* out;      // [B, Hq, D]
+  const __nv_bfloat16* q;  // [B, M, Hq, D]
+  __nv_bfloat16* out;      // [B, M, Hq, D]
   const int32_t* context_lens;
   const int32_t* table_rows;
   int B, Hq, G, HG, n_groups, window, sinks, num_ctas;
+  // Query tokens per request (1: decode; M > 1: the M newest tokens verified
+  // at once, query j at position L - M + j, causal). The M * G (token, head)
+  // columns of a KV head are split over ``tiles`` consumer warps of NT
+  // 8-column MMA tiles each; CW = HG * tiles consumer warps in all.
+  int M, NT, tiles, CW;
   float scale_log2;
   int4* merge;
   float* part_ml;
@@ -85,6 +90,7 @@ struct CombineArgs {
   void* out;
   int dtype;
   int n_groups, QH, Hq, D;
+  int M;  // query tokens per request: the partials hold M * QH columns, token-major
 };
 
 // Programmatic dependent launch: a kernel launched with the programmatic
@@ -127,10 +133,11 @@ __device__ __forceinline__ long long block_exclusive_scan(long long x, long long
 }
 
 // Shared-memory bytes of the tensor-core kernel for HG KV heads per CTA and
-// G query heads per KV head with nq Q buffers (0 if it does not fit), and the
-// number of Q buffers it will use (2 when they fit, else 1; 0 if neither).
-size_t tc_smem_bytes(int HG, int G, int nq);
-int tc_num_qbuf(int HG, int G);
+// C query columns per KV head (G heads x M tokens) with nq Q buffers (0 if it
+// does not fit), and the number of Q buffers it will use (2 when they fit,
+// else 1; 0 if neither).
+size_t tc_smem_bytes(int HG, int C, int nq);
+int tc_num_qbuf(int HG, int C);
 // Encode the tensor map of a bf16 pool for HG heads per box; false if the
 // driver refuses it.
 bool tc_encode_tmap(const kvp_pool* pool, int HG, CUtensorMap* out);

@@ -82,7 +82,7 @@ struct __align__(16) StageHdr {
   int b;       // request
   int group;   // KV-head group
   int part;    // partial slot of a split piece, -1 when the piece is the whole request
-  int pad;
+  int L;       // context length of the request (positions of multi-token queries)
 };
 
 // What the producer's lookahead cursor records for a stage it has queued.
@@ -95,6 +95,8 @@ struct __align__(16) StageMeta {
   int group;
   int part;
   int piece;   // index of the piece within the CTA (selects the Q buffer)
+  int L;       // context length of the request
+  int pad0, pad1, pad2;
 };
 
 struct SmemMap {
@@ -114,11 +116,11 @@ __host__ __device__ __forceinline__ int stage_stride(int HG) {
   return (2 * kTok * (HG * 256 + 16) + 1023) & ~1023;
 }
 
-__device__ __forceinline__ SmemMap map_smem(unsigned char* smem, int HG, int G, int nq) {
+__device__ __forceinline__ SmemMap map_smem(unsigned char* smem, int HG, int C, int nq) {
   SmemMap s;
   s.pitch = HG * 256 + 16;
   s.stage_bytes = stage_stride(HG);
-  s.qbytes = HG * G * kD * 2;
+  s.qbytes = HG * C * kD * 2;  // C = G * M query columns per KV head
   s.nq = nq;
   s.stages = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem) + 1023) & ~uintptr_t(1023));
   s.qbuf = s.stages + kStages * s.stage_bytes;
@@ -149,9 +151,11 @@ __device__ __forceinline__ int entry_to_slot(const TableRef& T, int e, int t, in
 
 // Attended positions of a request (0 when its length or table row is
 // invalid): the se sink rows [0, se), then [lo, L) (see attend_span).
+// With M query tokens the span is the union of theirs: query 0 (context
+// L - M + 1) reaches furthest back, so the window is widened by M - 1.
 __device__ __forceinline__ int attended(const TcArgs& a, int L, int row, long long cap, int* lo, int* se) {
-  const bool valid = L >= 1 && L <= cap && row >= 0 && row < a.T.rows_total;
-  const Span sp = attend_span(valid ? L : 0, a.window, a.sinks);
+  const bool valid = L >= a.M && L >= 1 && L <= cap && row >= 0 && row < a.T.rows_total;
+  const Span sp = attend_span(valid ? L : 0, a.window > 0 ? a.window + a.M - 1 : a.window, a.sinks);
   *lo = sp.lo;
   *se = sp.se;
   return valid ? sp.se + L - sp.lo : 0;
@@ -398,6 +402,7 @@ __device__ void tc_producer(const TcArgs& a, const SmemMap& s, const PlanState& 
         m.group = c.g;
         m.part = c.part;
         m.piece = c.piece;
+        m.L = c.L;
         meta[qs] = m;
       }
       if (lane < kTok && c.t0 + lane < se) {
@@ -481,7 +486,7 @@ __device__ void tc_producer(const TcArgs& a, const SmemMap& s, const PlanState& 
         h.b = m.b;
         h.group = m.group;
         h.part = m.part;
-        h.pad = 0;
+        h.L = m.L;
         s.hdr[st] = h;
         const uint32_t box = (uint32_t)HG * kTok * 128u;  // 16 slots x HG heads x 64 elements
         mbar_arrive_expect_tx(&s.full[st], 4 * box + (first_stage ? (uint32_t)s.qbytes : 0u));
@@ -503,7 +508,7 @@ __device__ void tc_producer(const TcArgs& a, const SmemMap& s, const PlanState& 
         h.b = m.b;
         h.group = m.group;
         h.part = m.part;
-        h.pad = 0;
+        h.L = m.L;
         s.hdr[st] = h;
         const uint32_t tx = (uint32_t)__popc(copies) * row_copy + (first_stage ? (uint32_t)s.qbytes : 0u);
         mbar_arrive_expect_tx(&s.full[st], tx);
@@ -518,9 +523,10 @@ __device__ void tc_producer(const TcArgs& a, const SmemMap& s, const PlanState& 
         bulk_g2s(dst, src, row_copy, &s.full[st]);
       }
     }
-    if (first_stage && lane == 0) {
-      const __nv_bfloat16* qsrc = a.q + ((size_t)m.b * a.Hq + (size_t)m.group * HG * a.G) * kD;
-      bulk_g2s(s.qbuf + qi * s.qbytes, qsrc, (uint32_t)s.qbytes, &s.full[st]);
+    if (first_stage && lane < a.M) {  // the group's heads of each query token
+      const uint32_t tok_bytes = (uint32_t)HG * a.G * kD * 2;
+      const __nv_bfloat16* qsrc = a.q + (((size_t)m.b * a.M + lane) * a.Hq + (size_t)m.group * HG * a.G) * kD;
+      bulk_g2s(s.qbuf + qi * s.qbytes + lane * tok_bytes, qsrc, tok_bytes, &s.full[st]);
     }
   }
   cp_async_wait<0>();
@@ -553,8 +559,11 @@ __device__ void tc_producer(const TcArgs& a, const SmemMap& s, const PlanState& 
 // Consumer warps: one KV head each.
 // ---------------------------------------------------------------------------
 template <int NT>
-__device__ void tc_consumer(const TcArgs& a, const SmemMap& s, int h, int lane) {
-  const int G = a.G, HG = a.HG;
+__device__ void tc_consumer(const TcArgs& a, const SmemMap& s, int w, int lane) {
+  const int G = a.G, HG = a.HG, M = a.M;
+  const int h = w / a.tiles;                   // KV head within the group
+  const int col0 = (w % a.tiles) * 8 * NT;     // first (token, head) column of this warp
+  const int C = M * G;                     // columns of the KV head
   const int g = lane >> 2, c = lane & 3;
   const uint32_t stages_u32 = smem_u32(s.stages);
   const uint32_t qbuf_u32 = smem_u32(s.qbuf);
@@ -575,8 +584,8 @@ __device__ void tc_consumer(const TcArgs& a, const SmemMap& s, int h, int lane) 
     // thread of the grid while the first stages are in flight. Nothing this
     // launch reads depends on them (the newest positions come from the new
     // rows; the table writes only add pages for those positions).
-    const long long tid = (long long)blockIdx.x * (HG * 32) + h * 32 + lane;
-    const long long nthreads = (long long)a.num_ctas * HG * 32;
+    const long long tid = (long long)blockIdx.x * (a.CW * 32) + w * 32 + lane;
+    const long long nthreads = (long long)a.num_ctas * a.CW * 32;
     const long long tw_total = (long long)a.n_tw * a.tw_expand;
     for (long long u = tid; u < tw_total; u += nthreads) {
       const int i = (int)(u / a.tw_expand), jj = (int)(u % a.tw_expand);
@@ -608,10 +617,14 @@ __device__ void tc_consumer(const TcArgs& a, const SmemMap& s, int h, int lane) 
   uint32_t qf[8][NT][2];
   float o[8][NT][4];
   float m[NT][2], l[NT][2];
+  // Multi-token queries: position p, and the window [lo, p] plus sinks
+  // [0, se), of the query token of each of this lane's columns.
+  int qp[NT][2], qlo[NT][2], qse[NT][2];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     m[nt][0] = m[nt][1] = -INFINITY;
     l[nt][0] = l[nt][1] = 0.f;
+    qp[nt][0] = qp[nt][1] = qlo[nt][0] = qlo[nt][1] = qse[nt][0] = qse[nt][1] = 0;
   }
 
   for (long long it = 0;; ++it) {
@@ -630,9 +643,11 @@ __device__ void tc_consumer(const TcArgs& a, const SmemMap& s, int h, int lane) 
       const int qi = (flags >> 2) & 1;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        const int head = nt * 8 + (lane & 7);
-        const uint32_t row = qbuf_u32 + (uint32_t)qi * (uint32_t)s.qbytes +
-                             (uint32_t)((head < G ? h * G + head : 0) * kD * 2) + (uint32_t)(lane >> 3) * 16u;
+        // column (token j, head hh) of the KV head; Q is [M][HG * G][D] in shared memory
+        const int col = col0 + nt * 8 + (lane & 7);
+        const int qrow = col < C ? (col / G) * HG * G + h * G + col % G : 0;
+        const uint32_t row = qbuf_u32 + (uint32_t)qi * (uint32_t)s.qbytes + (uint32_t)(qrow * kD * 2) +
+                             (uint32_t)(lane >> 3) * 16u;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           uint32_t r[4];
@@ -642,9 +657,21 @@ __device__ void tc_consumer(const TcArgs& a, const SmemMap& s, int h, int lane) 
           qf[2 * kk + 1][nt][0] = r[2];
           qf[2 * kk + 1][nt][1] = r[3];
         }
-        if (nt * 8 + g >= G) {
+        if (col0 + nt * 8 + g >= C) {
 #pragma unroll
           for (int k = 0; k < 8; ++k) qf[k][nt][0] = qf[k][nt][1] = 0u;
+        }
+        if (M > 1) {
+          const int Lh = vh->L;
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int cj = min(col0 + nt * 8 + 2 * c + e, C - 1) / G;
+            const int p = Lh - M + cj;
+            const Span sq = attend_span(p + 1, a.window, a.sinks);
+            qp[nt][e] = p;
+            qlo[nt][e] = sq.lo;
+            qse[nt][e] = sq.se;
+          }
         }
       }
       __syncwarp();
@@ -693,13 +720,21 @@ __device__ void tc_consumer(const TcArgs& a, const SmemMap& s, int h, int lane) 
 
     // Online softmax over the stage's 16 tokens (rows g and g+8 of S^T).
     const bool va = (vm >> g) & 1, vb = (vm >> (g + 8)) & 1;
+    const int ta = vh->t0 + g, tb = ta + 8;  // positions of rows g and g+8
     uint32_t pb[NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const float x0 = va ? (sa[nt][0] + sb[nt][0]) * a.scale_log2 : -INFINITY;
-      const float x1 = va ? (sa[nt][1] + sb[nt][1]) * a.scale_log2 : -INFINITY;
-      const float x2 = vb ? (sa[nt][2] + sb[nt][2]) * a.scale_log2 : -INFINITY;
-      const float x3 = vb ? (sa[nt][3] + sb[nt][3]) * a.scale_log2 : -INFINITY;
+      bool va0 = va, va1 = va, vb0 = vb, vb1 = vb;
+      if (M > 1) {  // causal window of each column's query token
+        va0 = va0 && ta <= qp[nt][0] && (ta >= qlo[nt][0] || ta < qse[nt][0]);
+        va1 = va1 && ta <= qp[nt][1] && (ta >= qlo[nt][1] || ta < qse[nt][1]);
+        vb0 = vb0 && tb <= qp[nt][0] && (tb >= qlo[nt][0] || tb < qse[nt][0]);
+        vb1 = vb1 && tb <= qp[nt][1] && (tb >= qlo[nt][1] || tb < qse[nt][1]);
+      }
+      const float x0 = va0 ? (sa[nt][0] + sb[nt][0]) * a.scale_log2 : -INFINITY;
+      const float x1 = va1 ? (sa[nt][1] + sb[nt][1]) * a.scale_log2 : -INFINITY;
+      const float x2 = vb0 ? (sa[nt][2] + sb[nt][2]) * a.scale_log2 : -INFINITY;
+      const float x3 = vb1 ? (sa[nt][3] + sb[nt][3]) * a.scale_log2 : -INFINITY;
       float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
       for (int sh = 4; sh < 32; sh <<= 1) {
@@ -749,19 +784,20 @@ __device__ void tc_consumer(const TcArgs& a, const SmemMap& s, int h, int lane) 
           float ls = l[nt][e];
 #pragma unroll
           for (int sh = 4; sh < 32; sh <<= 1) ls += __shfl_xor_sync(0xffffffffu, ls, sh);
-          const int hh = nt * 8 + 2 * c + e;
-          if (hh >= G) continue;
-          const int qh = h * G + hh;  // query head within the group
+          const int col = col0 + nt * 8 + 2 * c + e;
+          if (col >= C) continue;
+          const int cj = col / G;              // query token
+          const int qh = h * G + col % G;      // query head within the group
           if (hpart < 0) {
             const float inv = ls > 0.f ? 1.f / ls : 0.f;
-            __nv_bfloat16* dst = a.out + ((size_t)hb * a.Hq + (size_t)hgroup * HG * G + qh) * kD;
+            __nv_bfloat16* dst = a.out + (((size_t)hb * M + cj) * a.Hq + (size_t)hgroup * HG * G + qh) * kD;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               dst[16 * i + g] = __float2bfloat16_rn(o[i][nt][e] * inv);
               dst[16 * i + g + 8] = __float2bfloat16_rn(o[i][nt][2 + e] * inv);
             }
           } else {
-            const size_t base = (size_t)hpart * HG * G + qh;
+            const size_t base = ((size_t)hpart * M + cj) * HG * G + qh;
             float* po = a.part_o + base * kD;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
@@ -783,14 +819,14 @@ template <int NT>
 __global__ void __launch_bounds__(32 * (8 + kProducers), 1) tc_decode_kernel(const __grid_constant__ TcArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ PlanState ps;
-  const SmemMap s = map_smem(smem, a.HG, a.G, a.nq);
+  const SmemMap s = map_smem(smem, a.HG, a.G * a.M, a.nq);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&s.full[i], 1);
-      mbar_init(&s.empty[i], a.HG);
+      mbar_init(&s.empty[i], a.CW);
     }
-    for (int i = 0; i < 2; ++i) mbar_init(&s.qempty[i], a.HG);
+    for (int i = 0; i < 2; ++i) mbar_init(&s.qempty[i], a.CW);
     *s.abort_flag = 0;
     fence_mbar_init();
   }
@@ -802,13 +838,13 @@ __global__ void __launch_bounds__(32 * (8 + kProducers), 1) tc_decode_kernel(con
     const int* sN = reinterpret_cast<const int*>(reinterpret_cast<const long long*>(s.stages) + a.B);
     for (int b = blockIdx.x; b < a.B; b += a.num_ctas) {
       if (sN[b] != 0) continue;
-      __nv_bfloat16* o = a.out + (size_t)b * a.Hq * kD;
-      for (int i = threadIdx.x; i < a.Hq * kD; i += blockDim.x) o[i] = __float2bfloat16_rn(0.f);
+      __nv_bfloat16* o = a.out + (size_t)b * a.M * a.Hq * kD;
+      for (int i = threadIdx.x; i < a.M * a.Hq * kD; i += blockDim.x) o[i] = __float2bfloat16_rn(0.f);
     }
   }
   __syncthreads();  // the scratch in the stage buffers is free from here on
-  if (warp >= a.HG)
-    tc_producer(a, s, ps, warp - a.HG, lane);
+  if (warp >= a.CW)
+    tc_producer(a, s, ps, warp - a.CW, lane);
   else
     tc_consumer<NT>(a, s, warp, lane);
 }
@@ -823,18 +859,20 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
   const int b = v / a.n_groups, grp = v % a.n_groups;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
   const int pieces = 1 + kb - ka;
-  for (int qhl = blockIdx.y * nw + warp; qhl < a.QH; qhl += nw * gridDim.y) {
+  const int MQ = a.M * a.QH;  // columns: query token j, head hl at j * QH + hl
+  for (int qhl = blockIdx.y * nw + warp; qhl < MQ; qhl += nw * gridDim.y) {
     float M = -INFINITY;
     for (int i = 0; i < pieces; ++i) {
       const int slot = i == 0 ? sa : 2 * (ka + i);
-      M = fmaxf(M, __ldcg(a.part_ml + ((size_t)slot * a.QH + qhl) * 2));
+      M = fmaxf(M, __ldcg(a.part_ml + ((size_t)slot * MQ + qhl) * 2));
     }
-    const size_t orow = ((size_t)b * a.Hq + (size_t)grp * a.QH + qhl) * a.D;
+    const int cj = qhl / a.QH, hl = qhl % a.QH;
+    const size_t orow = (((size_t)b * a.M + cj) * a.Hq + (size_t)grp * a.QH + hl) * a.D;
     for (int d0 = lane * 4; d0 < a.D; d0 += 128) {
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
       float Ls = 0.f;
       for (int i = 0; i < pieces; ++i) {
-        const size_t pi = (size_t)(i == 0 ? sa : 2 * (ka + i)) * a.QH + qhl;
+        const size_t pi = (size_t)(i == 0 ? sa : 2 * (ka + i)) * MQ + qhl;
         const float mi = __ldcg(a.part_ml + pi * 2), li = __ldcg(a.part_ml + pi * 2 + 1);
         const float wgt = (mi == -INFINITY) ? 0.f : exp2f(mi - M);
         Ls += wgt * li;
@@ -856,8 +894,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
 
 }  // namespace
 
-size_t tc_smem_bytes(int HG, int G, int nq) {
-  const size_t bytes = kAlignSlack + (size_t)kStages * stage_stride(HG) + (size_t)nq * HG * G * kD * 2 +
+size_t tc_smem_bytes(int HG, int C, int nq) {
+  const size_t bytes = kAlignSlack + (size_t)kStages * stage_stride(HG) + (size_t)nq * HG * C * kD * 2 +
                        kProducers * kQueue * (sizeof(StageMeta) + kTok * sizeof(int)) + kStages * sizeof(StageHdr) +
                        (2 * kStages + 2) * sizeof(uint64_t) + 16;
   // the dynamic allocation plus the kernel's static shared memory (under
@@ -865,9 +903,9 @@ size_t tc_smem_bytes(int HG, int G, int nq) {
   return bytes <= kMaxDynamicSmem ? bytes : 0;
 }
 
-int tc_num_qbuf(int HG, int G) {
-  if (tc_smem_bytes(HG, G, 2)) return 2;
-  return tc_smem_bytes(HG, G, 1) ? 1 : 0;
+int tc_num_qbuf(int HG, int C) {
+  if (tc_smem_bytes(HG, C, 2)) return 2;
+  return tc_smem_bytes(HG, C, 1) ? 1 : 0;
 }
 
 bool tc_encode_tmap(const kvp_pool* pool, int HG, CUtensorMap* out) {
@@ -899,21 +937,23 @@ int tc_max_batch(int HG) {
 }
 
 cudaError_t launch_tc(const TcArgs& a, const CombineArgs& cb, cudaStream_t stream, void* ev_before, void* ev_after) {
-  const size_t smem = tc_smem_bytes(a.HG, a.G, a.nq);
-  if (smem == 0 || a.G > 16 || a.HG > 8 || a.B > tc_max_batch(a.HG)) return cudaErrorInvalidValue;
+  const size_t smem = tc_smem_bytes(a.HG, a.G * a.M, a.nq);
+  if (smem == 0 || a.NT < 1 || a.NT > 2 || a.CW != a.HG * a.tiles || a.CW > 8 || a.tiles * 8 * a.NT < a.G * a.M ||
+      a.M > 32 || a.B > tc_max_batch(a.HG))
+    return cudaErrorInvalidValue;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.num_ctas);
-  cfg.blockDim = dim3(32 * (a.HG + kProducers));
+  cfg.blockDim = dim3(32 * (a.CW + kProducers));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cudaError_t e;
   if (ev_before && (e = cudaEventRecord(static_cast<cudaEvent_t>(ev_before), stream)) != cudaSuccess) return e;
-  if (a.G <= 8) {
+  if (a.NT == 1) {
     static bool attr1 = false;
     if (!attr1) {
       e = cudaFuncSetAttribute(tc_decode_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynamicSmem);
@@ -933,7 +973,7 @@ cudaError_t launch_tc(const TcArgs& a, const CombineArgs& cb, cudaStream_t strea
   if (e != cudaSuccess) return e;
   if (ev_after && (e = cudaEventRecord(static_cast<cudaEvent_t>(ev_after), stream)) != cudaSuccess) return e;
   cudaLaunchConfig_t cc = {};
-  cc.gridDim = dim3(a.num_ctas, (cb.QH + 7) / 8);
+  cc.gridDim = dim3(a.num_ctas, (cb.M * cb.QH + 7) / 8);
   cc.blockDim = dim3(256);
   cc.dynamicSmemBytes = 0;
   cc.stream = stream;

@@ -263,6 +263,33 @@ int kvp_host_trim(kvp_host* h, int rid, int keep_from, int32_t* tw_rows,
   return kvp_host_trim_sinks(h, rid, keep_from, 0, tw_rows, tw_cols, tw_vals, tw_cap, n_tw);
 }
 
+int kvp_host_rewind(kvp_host* h, int rid, int n, int32_t* tw_rows, int32_t* tw_cols, int32_t* tw_vals,
+                    int tw_cap, int* n_tw) {
+  if (!valid_rid(h, rid) || !h->req[rid].live || !n_tw) return KVP_ERR_INVALID_ARG;
+  Request& r = h->req[rid];
+  const int P = h->page_size;
+  if (n < 0 || n > r.length) return KVP_ERR_INVALID_ARG;
+  const int keep_len = r.length - n;
+  // Rows a later step may read must stay: no rewind into released pages.
+  if (r.dropped > 0 && static_cast<long long>(keep_len) < static_cast<long long>(r.sink_pages + r.dropped) * P)
+    return KVP_ERR_INVALID_ARG;
+  const int keep_pages = static_cast<int>((static_cast<long long>(keep_len) + P - 1) / P);
+  const int count = static_cast<int>(r.pages.size()) - keep_pages;
+  if (count > 0 && (!tw_rows || !tw_cols || !tw_vals || count > tw_cap)) return KVP_ERR_INVALID_ARG;
+  // Tail first, so that the stack hands the pages back in logical order.
+  for (int k = 0; k < count; ++k) {
+    const int d = static_cast<int>(r.pages.size()) - 1;
+    unref_page(h, r.pages[d]);
+    r.pages.pop_back();
+    tw_rows[k] = rid;
+    tw_cols[k] = d;
+    tw_vals[k] = -1;
+  }
+  r.length = keep_len;
+  *n_tw = count > 0 ? count : 0;
+  return KVP_OK;
+}
+
 int kvp_host_used(const kvp_host* h, int* used) {
   if (!h || !used) return KVP_ERR_INVALID_ARG;
   *used = h->num_pages - static_cast<int>(h->free_stack.size());

@@ -38,7 +38,7 @@ def test_shadow_ops_match_the_oracle(seed):
     opt = PageTable(n_pages, P, free_order=order)
     live = []
     for step in range(400):
-        op = R.choice(["append"] * 6 + ["new", "fork", "trim", "release", "batch"])
+        op = R.choice(["append"] * 6 + ["new", "fork", "trim", "release", "batch", "rewind"])
         free_rids = [r for r in range(16) if r not in live]
         if op == "new" and len(live) < 6:
             rid = free_rids[0]
@@ -78,6 +78,17 @@ def test_shadow_ops_match_the_oracle(seed):
             writes = host.trim(rid, k, sinks=sinks[rid])
             released = opt.trim(rid, k, sink_rows=sinks[rid]) if sinks[rid] else opt.trim(rid, k)
             assert writes == [(rid, d, -1) for d in released]
+        elif op == "rewind" and live:
+            rid = R.choice(live)
+            L, d = opt.length[rid], opt.dropped[rid]
+            floor = (opt.sinks[rid] + d) * P if d else 0
+            n = R.randrange(0, L - floor + 1)
+            writes = host.rewind(rid, n)
+            gone = opt.rewind(rid, n)
+            assert writes == [(rid, g, -1) for g in gone]
+            if d:  # one row past the released front is refused and changes nothing
+                with pytest.raises(kb.KvpError):
+                    host.rewind(rid, opt.length[rid] - floor + 1)
         elif op == "release" and live:
             rid = R.choice(live)
             host.release(rid)
