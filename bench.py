@@ -51,7 +51,7 @@ UNIT = "GB/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 WORKLOADS = ("gqa_decode", "sliding_window", "sliding_window_sinks", "prefix_sharing", "large_batch_p16",
-             "large_batch_p1")
+             "large_batch_p1", "gqa_verify4")
 DEFAULT_WORKLOAD = "gqa_decode"
 
 
@@ -68,6 +68,8 @@ class Scenario:
             w = wl.sliding_window(seed)
         elif name == "sliding_window_sinks":
             w = wl.sliding_window_sinks(seed)
+        elif name.startswith("gqa_verify"):
+            w = wl.gqa_verify(seed, M=int(name[len("gqa_verify"):]))
         elif name == "prefix_sharing":
             w = wl.prefix_sharing(seed)
         elif name.startswith("large_batch_p"):
@@ -119,16 +121,24 @@ class Scenario:
         self.max_seq_len = w.extra.get("max_seq_len") if self.raw else max(self.lengths) + 512
         self.window = w.window
         self.sinks = w.sinks
+        self.verify = w.extra.get("verify", 0)  # drafted tokens verified per request and step (0: decode)
 
 
 def attended_span(sc, L):
-    """(se, lo): a step with context L reads rows [0, se) and [lo, L)."""
+    """(se, lo): a step with context L reads rows [0, se) and [lo, L) (for a
+    verify step, the union of its M queries' spans)."""
     W, S = sc.w.window, sc.w.sinks
     if W <= 0:
         return 0, 0
-    lo = max(0, L - (W - S))
+    lo = max(0, L - (W + max(sc.verify, 1) - 1 - S))
     se = min(S, lo)
     return (0, 0) if se == lo else (se, lo)
+
+
+def out_shape(sc):
+    """Attention output of one layer: [B, Hq, D], or [B, M, Hq, D] for verify steps."""
+    B, w = len(sc.rids), sc.w
+    return (B, sc.verify, w.Hq, w.D) if sc.verify else (B, w.Hq, w.D)
 
 
 def attended_count(sc, L):
@@ -148,7 +158,7 @@ def attention_bytes(sc, lens):
         n = se + L - lo
         kv += n * row_kv
         tab += 4 * (n if sc.raw else (-(-se // w.P) + -(-L // w.P) - lo // w.P))
-    qo = 2 * len(lens) * w.Hq * w.D * elem
+    qo = 2 * len(lens) * max(sc.verify, 1) * w.Hq * w.D * elem
     return kv + qo + tab + 4 * len(lens)
 
 
@@ -168,7 +178,7 @@ def step_bytes(sc, lens, n_writes, n_cows, n_trim_writes):
     w = sc.w
     row = w.Hkv * w.D * (2 if w.dtype == "bf16" else 4)
     copies = n_cows * w.layers * 2 * 2 * w.P * row
-    return (w.layers * (attention_bytes(sc, lens) + store_bytes(sc, len(lens)))
+    return (w.layers * (attention_bytes(sc, lens) + store_bytes(sc, len(lens) * max(sc.verify, 1)))
             + table_write_bytes(sc, n_writes + n_trim_writes) + copies)
 
 
@@ -265,6 +275,10 @@ def prepare_steps(sc, cache, lens, first_step, n_steps, dev, host_inputs=False):
     steps = []
     lens = list(lens)
     for s in range(first_step, first_step + n_steps):
+        if sc.verify:
+            st, lens = _prepare_verify_step(sc, cache, lens, s, dev, host_inputs)
+            steps.append(st)
+            continue
         st = StepData()
         slots, writes, cows = cache.host.append(sc.rids)
         np.add.at(cache.lengths, np.asarray(sc.rids, np.int64), 1)
@@ -299,6 +313,46 @@ def prepare_steps(sc, cache, lens, first_step, n_steps, dev, host_inputs=False):
     return steps, lens
 
 
+def _prepare_verify_step(sc, cache, lens, s, dev, host_inputs):
+    """A speculative step: M drafted tokens per request appended and stored,
+    verified at once, a seeded number accepted, the rest rewound."""
+    w, M = sc.w, sc.verify
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    st = StepData()
+    rr = [r for r in sc.rids for _ in range(M)]
+    slots, writes, cows = cache.host.append(rr)
+    np.add.at(cache.lengths, np.asarray(rr, np.int64), 1)
+    st.n_writes, st.n_cows = len(writes), len(cows)
+    st.pre = None if not writes else tuple(_i32(x, dev) for x in zip(*writes))
+    st.cows = None if not cows else tuple(_i32(x, dev) for x in zip(*cows))
+    st.out_loc = _i32(slots, dev)
+    positions = [L + j for L in lens for j in range(M)]
+    ctx = [L + M for L in lens]
+    st.lens_list = list(ctx)
+    st.lens = _i32(ctx, dev)
+    acc = wl.accepted_drafts(sc.seed, s, len(sc.rids), M)
+    post = []
+    for r, a in zip(sc.rids, acc):
+        post += cache.host.rewind(r, M - a)
+        cache.lengths[r] -= M - a
+    st.n_post = len(post)
+    st.post = None if not post else tuple(_i32(x, dev) for x in zip(*post))
+    st.q, st.k, st.v = [], [], []
+    for layer in range(w.layers):
+        q = torch.stack([wl.q_rows(sc.seed, s * M + j, layer, sc.rids, w.Hq, w.D, dtype=tdt, device=dev)
+                         for j in range(M)], dim=1).contiguous()
+        k, v = wl.kv_rows(sc.seed, layer, rr, positions, w.Hkv, w.D, dtype=tdt, device=dev)
+        if host_inputs:
+            q, k, v = (x.cpu().pin_memory() for x in (q, k, v))
+        st.q.append(q)
+        st.k.append(k)
+        st.v.append(v)
+    st.bytes = step_bytes(sc, ctx, st.n_writes, st.n_cows, st.n_post)
+    st.attn_bytes = attention_bytes(sc, ctx)
+    st.accepted = sum(acc)
+    return st, [L + a for L, a in zip(lens, acc)]
+
+
 def run_step(sc, cache, st, outs, events=None):
     """Issue one prepared step; returns the number of kernels launched.
 
@@ -311,6 +365,23 @@ def run_step(sc, cache, st, outs, events=None):
     w = sc.w
     P = w.P
     n = 0
+    if sc.verify:  # table writes, store of the M drafts, verify (+ combine), rewind writes
+        if st.pre is not None:
+            kb.page_table_write(cache.table, *st.pre, expand=P if sc.raw else 1, error_word=cache.pool.error_word)
+            n += 1
+        if st.cows is not None:
+            kb.copy_pages(cache.pool, *st.cows)
+            n += 1
+        for layer in range(w.layers):
+            cache.store(layer, st.k[layer], st.v[layer], st.out_loc)
+            if events is not None:
+                kb.kvp_pool_set_timing_events(cache.pool, *events.pop())
+            cache.verify(layer, st.q[layer], st.lens, sc.window, w.scale, outs[layer], sinks=sc.sinks)
+            n += 3
+        if st.post is not None:
+            kb.page_table_write(cache.table, *st.post, expand=P if sc.raw else 1, error_word=cache.pool.error_word)
+            n += 1
+        return n
     pre = st.pre
     if st.cows is not None:
         kb.copy_pages(cache.pool, *st.cows)
@@ -441,7 +512,8 @@ def run_gpu(args, rank, world, local_rank):
     # the second from launching early, so it is kept out of the first pass).
     steps, lens_after = prepare_steps(sc, cache, lens, 1, W + 2 * K, dev)
     tdt = cache.tdt
-    outs = [torch.empty((len(sc.rids), w.Hq, w.D), dtype=tdt, device=dev) for _ in range(w.layers)]
+    outs = [torch.empty(out_shape(sc), dtype=tdt, device=dev) for _ in range(w.layers)]
+    soak_out = torch.empty((len(sc.rids), w.Hq, w.D), dtype=tdt, device=dev)
 
     sampler = ClockSampler(local_rank) if rank == 0 else None
     # soak: repeat the current state's attention ~1 s so clocks settle and get
@@ -451,7 +523,8 @@ def run_gpu(args, rank, world, local_rank):
     soak_window = sc.window - 1 if sc.window > 0 else 0
     while time.time() - t_soak < args.soak:
         for layer in range(w.layers):
-            cache.attend(layer, steps[0].q[layer], _i32(lens, dev), soak_window, w.scale, outs[layer], sinks=sc.sinks)
+            q0 = steps[0].q[layer][:, 0].contiguous() if sc.verify else steps[0].q[layer]
+            cache.attend(layer, q0, _i32(lens, dev), soak_window, w.scale, soak_out, sinks=sc.sinks)
         torch.cuda.synchronize(dev)
     for i in range(W):
         run_step(sc, cache, steps[i], outs)
@@ -486,6 +559,8 @@ def run_gpu(args, rank, world, local_rank):
     cache.check()
     attn_ms = [a.elapsed_time(b) for a, b in ev_pairs]
     total_bytes = sum(st.bytes for st in steps[W:W + K])
+    # tokens a step adds: one per request, or the accepted drafts of a verify step
+    timed_tokens = sum(st.accepted for st in steps[W:W + K]) if sc.verify else K * len(sc.rids)
     attn_bytes_mean = statistics.mean(st.attn_bytes for st in steps[W + K:W + 2 * K])
 
     # end to end through the driver, host buffers
@@ -493,7 +568,7 @@ def run_gpu(args, rank, world, local_rank):
     clocks = sampler.stop(t0, t1) if sampler else None
 
     elapsed_ms, total_bytes, tokens, e2e_ms, e2e_bytes = reduce_over_ranks(
-        elapsed_ms, float(total_bytes), float(K * len(sc.rids)), e2e["ms"], float(e2e["bytes"]), world, dev)
+        elapsed_ms, float(total_bytes), float(timed_tokens), e2e["ms"], float(e2e["bytes"]), world, dev)
     if rank != 0:
         return None
 
@@ -524,6 +599,7 @@ def run_gpu(args, rank, world, local_rank):
             "layers": w.layers,
             "window": w.window,
             "sinks": w.sinks,
+            "verify_tokens": sc.verify,
             "table": "raw token locations" if sc.raw else "block table",
             "mean_attended_tokens": round(statistics.mean(
                 attended_count(sc, L) for L in steps[W].lens_list), 1),
@@ -574,7 +650,7 @@ def run_e2e(args, sc, cache, lens, first_step, dev):
     w = sc.w
     K = args.steps
     host_steps = _host_inputs(sc, first_step, K, lens)
-    out_host = [torch.empty((len(sc.rids), w.Hq, w.D), dtype=cache.tdt, pin_memory=True) for _ in range(w.layers)]
+    out_host = [torch.empty(out_shape(sc), dtype=cache.tdt, pin_memory=True) for _ in range(w.layers)]
     rids = np.asarray(sc.rids, np.int32)
     total_bytes = 0
     torch.cuda.synchronize(dev)
@@ -583,6 +659,16 @@ def run_e2e(args, sc, cache, lens, first_step, dev):
     start.record()
     for s in range(K):
         q_h, k_h, v_h = host_steps[s]
+        if sc.verify:  # draft M, verify, accept the seeded count, rewind the rest
+            M = sc.verify
+            cache.verify_step(rids, q_h, k_h, v_h, out_host, sc.window, w.scale, sinks=sc.sinks)
+            ctx = [int(x) for x in cache.lengths[rids]]
+            n_writes, n_cows = cache.last_writes, cache.last_copies
+            n_back = 0
+            for r, a in zip(sc.rids, wl.accepted_drafts(sc.seed, first_step + s, len(sc.rids), M)):
+                n_back += cache.rewind(r, M - a)
+            total_bytes += step_bytes(sc, ctx, n_writes, n_cows, n_back)
+            continue
         cache.decode_step(rids, q_h, k_h, v_h, out_host, sc.window, w.scale, sinks=sc.sinks)
         total_bytes += step_bytes(sc, [int(x) for x in cache.lengths[rids]], cache.last_writes, cache.last_copies,
                                   cache.last_trims)
@@ -618,6 +704,23 @@ def _host_inputs(sc, first_step, K, lens):
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     dev = torch.device("cuda", torch.cuda.current_device())
     out = []
+    if sc.verify:
+        M = sc.verify
+        lens = list(lens)
+        rr = [r for r in sc.rids for _ in range(M)]
+        for s in range(first_step, first_step + K):
+            positions = [L + j for L in lens for j in range(M)]
+            qs, ks, vs = [], [], []
+            for layer in range(w.layers):
+                q = torch.stack([wl.q_rows(sc.seed, s * M + j, layer, sc.rids, w.Hq, w.D, dtype=tdt, device=dev)
+                                 for j in range(M)], dim=1)
+                k, v = wl.kv_rows(sc.seed, layer, rr, positions, w.Hkv, w.D, dtype=tdt, device=dev)
+                qs.append(q.cpu().pin_memory())
+                ks.append(k.cpu().pin_memory())
+                vs.append(v.cpu().pin_memory())
+            out.append((qs, ks, vs))
+            lens = [L + a for L, a in zip(lens, wl.accepted_drafts(sc.seed, s, len(sc.rids), M))]
+        return out
     for i, s in enumerate(range(first_step, first_step + K)):
         positions = [L + i for L in lens]
         qs, ks, vs = [], [], []
@@ -716,10 +819,38 @@ class OracleSample:
         elif kind == "release":
             self.pt.release(op[1])
 
+    def _verify_step(self, step_index, attend_rids, with_slots):
+        """A speculative step: M drafts appended per request, the ones of
+        ``attend_rids`` stored and verified, the seeded acceptance applied by
+        rewinding the rest."""
+        sc, w, OA, M = self.sc, self.sc.w, self.OA, self.sc.verify
+        pos0 = {r: self.pt.length[r] for r in sc.rids}
+        rr = [r for r in sc.rids for _ in range(M)]
+        slots = self._append(rr)
+        outs = {}
+        for r in attend_rids:
+            i = sc.rids.index(r)
+            self._store(r, [pos0[r] + j for j in range(M)], slots[i * M:(i + 1) * M])
+        for r in attend_rids:
+            L = self.pt.length[r]
+            row = self.pt.block_row(r)
+            for layer in self.layers:
+                per_q = []
+                for j, pos in enumerate(OA.verify_positions(L, M, sc.window, sc.sinks)):
+                    q = wl.q_rows(sc.seed, step_index * M + j, layer, [r], w.Hq, w.D, dtype=self.tdt)[0]
+                    sl = [s for p in pos for s in OA.gather_block(row, w.P, p, p + 1)]
+                    per_q.append(OA.attend_request(self.stores[layer], q.float().numpy(), sl, w.scale))
+                outs[(r, layer)] = np.stack(per_q)
+        for r, a in zip(sc.rids, wl.accepted_drafts(sc.seed, step_index, len(sc.rids), M)):
+            self.pt.rewind(r, M - a)
+        return (outs, slots) if with_slots else outs
+
     def step(self, step_index, attend_rids, with_slots=False):
         """One decode step: bookkeeping for every request, store + attention for ``attend_rids``.
 
         Returns {(rid, layer): output}, and also the step's slots when ``with_slots``."""
+        if self.sc.verify:
+            return self._verify_step(step_index, attend_rids, with_slots)
         sc, w, OA = self.sc, self.sc.w, self.OA
         pos = [self.pt.length[r] for r in sc.rids]
         slots = self._append(sc.rids)

@@ -145,24 +145,32 @@ __global__ void gather_indices_kernel(TableRef T, const int32_t* context_lens, c
 // request: the M * G (token, head) columns of a KV head go to T consumer
 // warps of NT 8-column tiles, HG KV heads per CTA, HG * T <= 8 warps.
 struct TcShape {
-  int HG, NT, T;
+  int HG, NT, T, S;
 };
 
 bool tc_eligible(const kvp_pool* pool, int Hq, int B, int M, TcShape* out) {
   if (pool->dtype != KVP_BF16 || pool->head_dim != 128) return false;
   const int Hkv = pool->kv_heads;
   if (Hq % Hkv || M < 1 || M > 32) return false;
+  // One 8-column tile per warp keeps a consumer warp's stage work (and its
+  // registers) at the decode kernel's; two tiles only when eight warps of
+  // one tile cannot hold the columns.
   const int C = (Hq / Hkv) * M;
-  const int NT = C <= 8 ? 1 : 2;
-  const int T = (C + 8 * NT - 1) / (8 * NT);
+  int NT = 1, T = (C + 7) / 8;
+  if (T > 8) {
+    NT = 2;
+    T = (C + 15) / 16;
+  }
   if (T > 8) return false;
   for (int HG = 8 / T; HG >= 1; --HG) {
     if (Hkv % HG) continue;
-    if (tc_num_qbuf(HG, C) == 0) continue;
-    if (B > tc_max_batch(HG)) return false;
+    const int S = tc_num_stages(HG, C);
+    if (tc_num_qbuf(HG, C, S) == 0) continue;
+    if (B > tc_max_batch(HG, S)) return false;
     out->HG = HG;
     out->NT = NT;
     out->T = T;
+    out->S = S;
     return true;
   }
   return false;
@@ -271,7 +279,8 @@ int attention_impl(const kvp_pool* pool, int layer, const void* q, int batch, in
     else memset(&ta.tmap, 0, sizeof(ta.tmap));
     ta.kvl_k = layer;
     ta.kvl_v = pool->num_layers + layer;
-    ta.nq = tc_num_qbuf(HG, G * M);
+    ta.nq = tc_num_qbuf(HG, G * M, sh.S);
+    ta.stages = sh.S;
     ta.T = T;
     ta.kv_layer = kv_layer;
     ta.kv_bytes = pool->kv_bytes;

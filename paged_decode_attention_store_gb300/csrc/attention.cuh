@@ -64,6 +64,7 @@ struct TcArgs {
   // columns of a KV head are split over ``tiles`` consumer warps of NT
   // 8-column MMA tiles each; CW = HG * tiles consumer warps in all.
   int M, NT, tiles, CW;
+  int stages;  // ring depth (3 for 8 KV heads per CTA, deeper for fewer)
   float scale_log2;
   int4* merge;
   float* part_ml;
@@ -136,13 +137,15 @@ __device__ __forceinline__ long long block_exclusive_scan(long long x, long long
 // C query columns per KV head (G heads x M tokens) with nq Q buffers (0 if it
 // does not fit), and the number of Q buffers it will use (2 when they fit,
 // else 1; 0 if neither).
-size_t tc_smem_bytes(int HG, int C, int nq);
-int tc_num_qbuf(int HG, int C);
+size_t tc_smem_bytes(int HG, int C, int nq, int S);
+int tc_num_qbuf(int HG, int C, int S);
+// Ring depth for HG KV heads per CTA and C query columns per head.
+int tc_num_stages(int HG, int C);
 // Encode the tensor map of a bf16 pool for HG heads per box; false if the
 // driver refuses it.
 bool tc_encode_tmap(const kvp_pool* pool, int HG, CUtensorMap* out);
-// Largest batch the in-kernel work split can take for HG.
-int tc_max_batch(int HG);
+// Largest batch the in-kernel work split can take for HG and ring depth S.
+int tc_max_batch(int HG, int S);
 // Launch the bf16, head_dim-128 kernel (one CTA per SM) and the combine
 // kernel after it, both as programmatic dependents.
 cudaError_t launch_tc(const TcArgs& a, const CombineArgs& c, cudaStream_t stream, void* ev_before, void* ev_after);

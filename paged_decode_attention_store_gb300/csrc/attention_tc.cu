@@ -61,7 +61,8 @@ namespace kvp {
 namespace {
 
 constexpr int kTok = 16;      // tokens per stage (the MMA M dimension)
-constexpr int kStages = 3;    // ring depth
+constexpr int kMaxStages = 8; // ring depth limit (the depth a.stages is chosen per head group)
+constexpr int kQBars = 8;     // Q-buffer barriers, by piece mod 8 (>= kMaxStages)
 constexpr int kProducers = 2; // producer warps, alternate stages
 constexpr int kAhead = 2;     // own stages whose table entries are fetched ahead of issue
 constexpr int kQueue = 4;     // entry-queue slots per producer (> kAhead)
@@ -78,7 +79,7 @@ struct __align__(16) StageHdr {
   int t0;      // first position of the stage
   int vmask;   // bit j: token t0+j has K/V rows in the stage
   int flags;   // 1 first stage of the piece, 2 last stage, (qbuf << 2), 8 tensor-copy layout,
-               // 16 odd piece (selects the qempty barrier)
+               // (piece % kQBars) << 4 (selects the qempty barrier)
   int b;       // request
   int group;   // KV-head group
   int part;    // partial slot of a split piece, -1 when the piece is the whole request
@@ -116,21 +117,21 @@ __host__ __device__ __forceinline__ int stage_stride(int HG) {
   return (2 * kTok * (HG * 256 + 16) + 1023) & ~1023;
 }
 
-__device__ __forceinline__ SmemMap map_smem(unsigned char* smem, int HG, int C, int nq) {
+__device__ __forceinline__ SmemMap map_smem(unsigned char* smem, int HG, int C, int nq, int S) {
   SmemMap s;
   s.pitch = HG * 256 + 16;
   s.stage_bytes = stage_stride(HG);
   s.qbytes = HG * C * kD * 2;  // C = G * M query columns per KV head
   s.nq = nq;
   s.stages = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem) + 1023) & ~uintptr_t(1023));
-  s.qbuf = s.stages + kStages * s.stage_bytes;
+  s.qbuf = s.stages + S * s.stage_bytes;
   s.meta = reinterpret_cast<StageMeta*>(s.qbuf + nq * s.qbytes);
   s.entries = reinterpret_cast<int*>(s.meta + kProducers * kQueue);
   s.hdr = reinterpret_cast<StageHdr*>(s.entries + kProducers * kQueue * kTok);
-  s.full = reinterpret_cast<uint64_t*>(s.hdr + kStages);
-  s.empty = s.full + kStages;
-  s.qempty = s.empty + kStages;
-  s.abort_flag = reinterpret_cast<volatile int*>(s.qempty + 2);
+  s.full = reinterpret_cast<uint64_t*>(s.hdr + S);
+  s.empty = s.full + S;
+  s.qempty = s.empty + S;
+  s.abort_flag = reinterpret_cast<volatile int*>(s.qempty + kQBars);
   return s;
 }
 
@@ -438,23 +439,25 @@ __device__ void tc_producer(const TcArgs& a, const SmemMap& s, const PlanState& 
     const bool first_stage = m.flags & 1;
     const bool last_stage = m.flags & 2;
     const int qi = m.piece % s.nq;
-    const int st = (int)(gs % kStages);
-    if (gs >= kStages) {
-      ok = __all_sync(0xffffffffu, mbar_wait_bounded(&s.empty[st], (uint32_t)((gs / kStages - 1) & 1),
+    const int S = a.stages;
+    const int st = (int)(gs % S);
+    if (gs >= S) {
+      ok = __all_sync(0xffffffffu, mbar_wait_bounded(&s.empty[st], (uint32_t)((gs / S - 1) & 1),
                                                      s.abort_flag, a.err, kWaitLimitNs));
       if (!ok) break;
     }
     // Q buffer reuse: piece p overwrites the buffer of piece p - nq, so it
     // waits until the consumers have loaded that piece's Q. Consumers
-    // arrive on qempty[piece & 1]; piece p - nq is phase (p - nq) / 2 of
-    // barrier (p - nq) & 1. The parity test is exact because every stage
-    // up to gs - kStages is consumed (the wait above), so the barrier's
-    // previous piece (p - nq - 2, whose first stage is at most gs - 3) has
-    // been loaded and the barrier is at most one phase behind.
+    // arrive on qempty[piece % kQBars]; piece p - nq is phase
+    // (p - nq) / kQBars of barrier (p - nq) % kQBars. The parity test is
+    // exact because every stage up to gs - S is consumed (the wait above)
+    // and the barrier's previous piece, p - nq - kQBars, has its first stage
+    // at most at gs - kQBars <= gs - S: it has been loaded, so the barrier
+    // is at most one phase behind.
     if (first_stage && m.piece >= s.nq) {
       const int pw = m.piece - s.nq;
-      ok = __all_sync(0xffffffffu, mbar_wait_bounded(&s.qempty[pw & 1], (uint32_t)((pw >> 1) & 1), s.abort_flag,
-                                                     a.err, kWaitLimitNs));
+      ok = __all_sync(0xffffffffu, mbar_wait_bounded(&s.qempty[pw % kQBars], (uint32_t)((pw / kQBars) & 1),
+                                                     s.abort_flag, a.err, kWaitLimitNs));
       if (!ok) break;
     }
     const int t = m.t0 + j;
@@ -482,7 +485,7 @@ __device__ void tc_producer(const TcArgs& a, const SmemMap& s, const PlanState& 
         h.live = 1;
         h.t0 = m.t0;
         h.vmask = 0xffff;
-        h.flags = (first_stage ? 1 : 0) | (last_stage ? 2 : 0) | (qi << 2) | 8 | ((m.piece & 1) << 4);
+        h.flags = (first_stage ? 1 : 0) | (last_stage ? 2 : 0) | (qi << 2) | 8 | ((m.piece % kQBars) << 4);
         h.b = m.b;
         h.group = m.group;
         h.part = m.part;
@@ -504,7 +507,7 @@ __device__ void tc_producer(const TcArgs& a, const SmemMap& s, const PlanState& 
         h.live = 1;
         h.t0 = m.t0;
         h.vmask = (int)(copies & copies >> 16 & 0xffffu);
-        h.flags = (first_stage ? 1 : 0) | (last_stage ? 2 : 0) | (qi << 2) | ((m.piece & 1) << 4);
+        h.flags = (first_stage ? 1 : 0) | (last_stage ? 2 : 0) | (qi << 2) | ((m.piece % kQBars) << 4);
         h.b = m.b;
         h.group = m.group;
         h.part = m.part;
@@ -533,9 +536,9 @@ __device__ void tc_producer(const TcArgs& a, const SmemMap& s, const PlanState& 
 
   // The producer that owns the first stage without work tells the consumers.
   if (ok && n_stages >= 0 && (n_stages % kProducers) == pid) {
-    const int st = (int)(n_stages % kStages);
-    if (n_stages >= kStages)
-      ok = __all_sync(0xffffffffu, mbar_wait_bounded(&s.empty[st], (uint32_t)((n_stages / kStages - 1) & 1),
+    const int st = (int)(n_stages % a.stages);
+    if (n_stages >= a.stages)
+      ok = __all_sync(0xffffffffu, mbar_wait_bounded(&s.empty[st], (uint32_t)((n_stages / a.stages - 1) & 1),
                                                      s.abort_flag, a.err, kWaitLimitNs));
     if (ok && lane == 0) {
       s.hdr[st].live = 0;
@@ -545,10 +548,10 @@ __device__ void tc_producer(const TcArgs& a, const SmemMap& s, const PlanState& 
   if (!ok) {
     // Abort: let the copies this warp issued land before the CTA exits.
     *s.abort_flag = 1;
-    for (long long g2 = gs - kProducers; g2 >= 0 && g2 >= gs - kProducers * kStages; g2 -= kProducers) {
-      const int st = (int)(g2 % kStages);
+    for (long long g2 = gs - kProducers; g2 >= 0 && g2 >= gs - kProducers * a.stages; g2 -= kProducers) {
+      const int st = (int)(g2 % a.stages);
       const uint64_t t_start = global_timer_ns();
-      while (!mbar_try_wait(&s.full[st], (uint32_t)((g2 / kStages) & 1))) {
+      while (!mbar_try_wait(&s.full[st], (uint32_t)((g2 / a.stages) & 1))) {
         if (global_timer_ns() - t_start > 100000000ull) break;
       }
     }
@@ -628,8 +631,8 @@ __device__ void tc_consumer(const TcArgs& a, const SmemMap& s, int w, int lane) 
   }
 
   for (long long it = 0;; ++it) {
-    const int st = (int)(it % kStages);
-    if (!__all_sync(0xffffffffu, mbar_wait_bounded(&s.full[st], (uint32_t)((it / kStages) & 1), s.abort_flag,
+    const int st = (int)(it % a.stages);
+    if (!__all_sync(0xffffffffu, mbar_wait_bounded(&s.full[st], (uint32_t)((it / a.stages) & 1), s.abort_flag,
                                                    a.err, kWaitLimitNs)))
       return;
     const volatile StageHdr* vh = &s.hdr[st];
@@ -675,7 +678,7 @@ __device__ void tc_consumer(const TcArgs& a, const SmemMap& s, int w, int lane) 
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s.qempty[(flags >> 4) & 1]);
+      if (lane == 0) mbar_arrive(&s.qempty[(flags >> 4) & (kQBars - 1)]);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         m[nt][0] = m[nt][1] = -INFINITY;
@@ -819,14 +822,14 @@ template <int NT>
 __global__ void __launch_bounds__(32 * (8 + kProducers), 1) tc_decode_kernel(const __grid_constant__ TcArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ PlanState ps;
-  const SmemMap s = map_smem(smem, a.HG, a.G * a.M, a.nq);
+  const SmemMap s = map_smem(smem, a.HG, a.G * a.M, a.nq, a.stages);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < a.stages; ++i) {
       mbar_init(&s.full[i], 1);
       mbar_init(&s.empty[i], a.CW);
     }
-    for (int i = 0; i < 2; ++i) mbar_init(&s.qempty[i], a.CW);
+    for (int i = 0; i < kQBars; ++i) mbar_init(&s.qempty[i], a.CW);
     *s.abort_flag = 0;
     fence_mbar_init();
   }
@@ -894,18 +897,27 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
 
 }  // namespace
 
-size_t tc_smem_bytes(int HG, int C, int nq) {
-  const size_t bytes = kAlignSlack + (size_t)kStages * stage_stride(HG) + (size_t)nq * HG * C * kD * 2 +
-                       kProducers * kQueue * (sizeof(StageMeta) + kTok * sizeof(int)) + kStages * sizeof(StageHdr) +
-                       (2 * kStages + 2) * sizeof(uint64_t) + 16;
+size_t tc_smem_bytes(int HG, int C, int nq, int S) {
+  if (S < 3 || S > kMaxStages) return 0;
+  const size_t bytes = kAlignSlack + (size_t)S * stage_stride(HG) + (size_t)nq * HG * C * kD * 2 +
+                       kProducers * kQueue * (sizeof(StageMeta) + kTok * sizeof(int)) + S * sizeof(StageHdr) +
+                       (2 * S + kQBars) * sizeof(uint64_t) + 16;
   // the dynamic allocation plus the kernel's static shared memory (under
   // kStaticSmemBound) must fit one block
   return bytes <= kMaxDynamicSmem ? bytes : 0;
 }
 
-int tc_num_qbuf(int HG, int C) {
-  if (tc_smem_bytes(HG, C, 2)) return 2;
-  return tc_smem_bytes(HG, C, 1) ? 1 : 0;
+int tc_num_qbuf(int HG, int C, int S) {
+  if (tc_smem_bytes(HG, C, 2, S)) return 2;
+  return tc_smem_bytes(HG, C, 1, S) ? 1 : 0;
+}
+
+int tc_num_stages(int HG, int C) {
+  // about 192 KB of K/V in flight per SM, whatever the group's row size
+  int S = 24 / HG;
+  S = S < 3 ? 3 : (S > kMaxStages ? kMaxStages : S);
+  while (S > 3 && !tc_smem_bytes(HG, C, 1, S)) --S;
+  return S;
 }
 
 bool tc_encode_tmap(const kvp_pool* pool, int HG, CUtensorMap* out) {
@@ -931,15 +943,15 @@ bool tc_encode_tmap(const kvp_pool* pool, int HG, CUtensorMap* out) {
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int tc_max_batch(int HG) {
-  const size_t scratch = (size_t)kStages * stage_stride(HG);
+int tc_max_batch(int HG, int S) {
+  const size_t scratch = (size_t)S * stage_stride(HG);
   return (int)(scratch / kPlanScratchPerRequest);
 }
 
 cudaError_t launch_tc(const TcArgs& a, const CombineArgs& cb, cudaStream_t stream, void* ev_before, void* ev_after) {
-  const size_t smem = tc_smem_bytes(a.HG, a.G * a.M, a.nq);
+  const size_t smem = tc_smem_bytes(a.HG, a.G * a.M, a.nq, a.stages);
   if (smem == 0 || a.NT < 1 || a.NT > 2 || a.CW != a.HG * a.tiles || a.CW > 8 || a.tiles * 8 * a.NT < a.G * a.M ||
-      a.M > 32 || a.B > tc_max_batch(a.HG))
+      a.M > 32 || a.B > tc_max_batch(a.HG, a.stages))
     return cudaErrorInvalidValue;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

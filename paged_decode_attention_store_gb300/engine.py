@@ -154,6 +154,50 @@ class PagedKVCache:
                                      window, scale, out, ws, table_rows=table_rows, table_writes=table_writes,
                                      sinks=sinks)
 
+    def verify(self, layer, q, context_lens, window, scale, out, table_rows=None, sinks=0):
+        """Multi-token verify: q/out [B, M, Hq, D], query j of request b at
+        position context_lens[b] - M + j (the M newest tokens, stored)."""
+        B, M, Hq = q.shape[0], q.shape[1], q.shape[2]
+        key = ("verify", B, M, Hq)
+        if key not in self._ws:
+            self._ws[key] = kb.alloc_verify_workspace(self.pool, B, M, Hq, device=self.dev)
+        kb.paged_verify_attention(self.pool, layer, q, self.table, self.table_mode, context_lens, window, scale,
+                                  out, self._ws[key], table_rows=table_rows, sinks=sinks)
+
+    def rewind(self, rid, n):
+        """Drop the newest n tokens of a request (rejected drafts); returns
+        the number of pages given back."""
+        writes = self.host.rewind(rid, n)
+        self._write_table(writes)
+        self.lengths[rid] -= n
+        return len(writes)
+
+    def verify_step(self, rids, q, k, v, out, window, scale, sinks=0):
+        """One speculative-decoding verify step for requests ``rids`` (ids =
+        table rows), all layers: append the M drafted tokens of each request
+        (host bookkeeping, table writes, copy-on-write), store their K/V rows
+        and verify them. ``q``/``out`` [layers][B, M, Hq, D] and ``k``/``v``
+        [layers][B * M, Hkv, D] (request-major) on the host (pinned) or the
+        device. Returns when ``out`` holds the results; the caller then
+        rewinds the rejected drafts with :meth:`rewind`."""
+        B, M = q[0].shape[0], q[0].shape[1]
+        rr = [int(r) for r in rids for _ in range(M)]
+        ctx = [int(self.lengths[r]) + M for r in rids]
+        out_loc = self.append(rr)
+        lens = self._to_device(ctx)
+        rows = self._to_device([int(r) for r in rids])
+        host_out = not out[0].is_cuda
+        for layer in range(self.layers):
+            qd, kd, vd = (x[layer].to(self.dev, non_blocking=True) for x in (q, k, v))
+            if not q[0].is_cuda:
+                self.h2d_bytes += sum(x[layer].numel() * x[layer].element_size() for x in (q, k, v))
+            self.store(layer, kd, vd, out_loc)
+            od = torch.empty_like(qd) if host_out else out[layer]
+            self.verify(layer, qd, lens, window, scale, od, table_rows=rows, sinks=sinks)
+            if host_out:
+                out[layer].copy_(od, non_blocking=True)
+        torch.cuda.current_stream(self.dev).synchronize()
+
     def check(self):
         """Raise if a device-side error was recorded since the last check."""
         e = kb.kvp_sync_error(self.pool)

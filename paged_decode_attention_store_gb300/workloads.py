@@ -172,6 +172,23 @@ def gqa_decode(seed: int = 0) -> Workload:
                     free_stack_for_order(order), lengths, scale=1.0 / math.sqrt(128))
 
 
+def gqa_verify(seed: int = 0, M: int = 4) -> Workload:
+    """gqa_decode's requests in speculative decoding: every step appends M
+    drafted tokens per request, verifies them at once, accepts a seeded
+    uniform number in [0, M] and rewinds the rest. The pool adds 16 pages
+    per request for the growth over a run."""
+    w = gqa_decode(seed)
+    n_pages = w.num_pages + 16 * len(w.lengths)
+    order = np.random.RandomState(seed * 7919 + 3).permutation(n_pages)
+    return Workload(f"gqa_verify{M}", "bf16", w.Hq, w.Hkv, w.D, w.P, 1, n_pages, free_stack_for_order(order),
+                    list(w.lengths), scale=w.scale, extra={"verify": M})
+
+
+def accepted_drafts(seed: int, step: int, B: int, M: int) -> list:
+    """Drafts accepted per request at a verify step: uniform in [0, M]."""
+    return np.random.RandomState(seed * 7919 + 1000 + step).randint(0, M + 1, size=B).tolist()
+
+
 def sliding_window(seed: int = 0) -> Workload:
     """bf16, 32 q / 8 kv heads, head_dim 128, page 16, batch 32, W = 4096,
     context lengths uniform in [8192, 32768]; pages older than the window are

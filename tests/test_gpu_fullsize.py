@@ -42,7 +42,7 @@ def test_full_size_parity(kb, workload):
     orc = bench.OracleSample(sc, track, layers=layers)
     cache, lens = bench.build_product(sc, dev=DEV)
     steps, _ = bench.prepare_steps(sc, cache, lens, 1, 2, DEV)
-    outs = [torch.empty((len(sc.rids), sc.w.Hq, sc.w.D), dtype=cache.tdt, device=DEV) for _ in range(sc.w.layers)]
+    outs = [torch.empty(bench.out_shape(sc), dtype=cache.tdt, device=DEV) for _ in range(sc.w.layers)]
     for i, st in enumerate(steps):
         bench.run_step(sc, cache, st, outs)
         torch.cuda.synchronize(DEV)
