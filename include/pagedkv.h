@@ -418,6 +418,73 @@ int kvp_host_block_row(const kvp_host* h, int rid, int32_t* out, int cap,
 int kvp_host_refcounts(const kvp_host* h, int32_t* out, int cap);
 int kvp_host_free_list(const kvp_host* h, int32_t* out, int cap, int* n);
 
+/* ------------------------------------------------------------------------
+ * Device-side page allocation: the block-table bookkeeping of kvp_host_*
+ * (chapter 15 "The model": LIFO free list, reference counts, a fresh page
+ * on a page boundary, lazy copy-on-write of a shared tail page, window trim
+ * with sinks, release) kept in device memory, so that a decode step needs
+ * no host decision and no host->device copy of table writes (mini-sglang
+ * code series, part 4: allocate by page, record by token, here both on the
+ * device). Every decision is taken in the order the host bookkeeping takes
+ * it, request after request, so the device state equals kvp_host_*'s for
+ * the same operations.
+ *   state   caller-owned device buffer of kvp_dev_pages_bytes(), 16-byte
+ *           aligned: [top, error word][free stack][ref counts][lengths]
+ *           [released pages][sink pages]. The library keeps the pointer.
+ *   table   the caller's device table (block: page ids; raw: token slots,
+ *           expanded P per page), at least max_requests rows; request id
+ *           = table row.
+ * Each call is one thread block of up to 1024 requests, asynchronous on
+ * ``stream``, and all-or-nothing: a bad request id, a repeated id, a row too
+ * short, a full pool (KVP_ERR_OUT_OF_PAGES) or a short output buffer sets
+ * the state's error word (kvp_dev_sync_error) and changes nothing.
+ * ---------------------------------------------------------------------- */
+typedef struct kvp_dev_pages kvp_dev_pages;
+
+int kvp_dev_pages_bytes(int num_pages, int max_requests, size_t* bytes);
+int kvp_dev_pages_create(int num_pages, int page_size, int max_requests,
+                         void* state, size_t state_bytes, int32_t* table,
+                         int table_rows, int table_cols, int table_mode,
+                         kvp_dev_pages** out);
+int kvp_dev_pages_destroy(kvp_dev_pages* d);
+/* Empty pool: the free stack from free_stack (device int32 [num_pages], the
+ * end handed out first), or num_pages-1 .. 0 when NULL; counts zero. */
+int kvp_dev_pages_init(kvp_dev_pages* d, const int32_t* free_stack,
+                       void* stream);
+/* Start requests rids[0..n) (device int32) with no rows. */
+int kvp_dev_new(kvp_dev_pages* d, const int32_t* rids, int n, void* stream);
+/* Append counts[i] rows (NULL: one) to request rids[i] (device int32 [n],
+ * n <= 1024, distinct ids): new pages popped in call order, a shared tail
+ * page copied first (pairs in cow_src/cow_dst [n], their number in *n_cow,
+ * all device; copy them with copy_pages_device_count before storing), the
+ * table entries written (expanded for a raw table), and the slot of every
+ * new row in out_loc (device int32, request-major, at most max_tokens). */
+int kvp_dev_append(kvp_dev_pages* d, const int32_t* rids,
+                   const int32_t* counts, int n, int32_t* out_loc,
+                   int max_tokens, int32_t* cow_src, int32_t* cow_dst,
+                   int32_t* n_cow, void* stream);
+/* Window trim of requests rids[i] to keep_from[i] (both device int32 [n])
+ * keeping the first ceil(sinks / P) pages, as kvp_host_trim_sinks; the
+ * released entries become -1. At most 4096 pages per call. */
+int kvp_dev_trim(kvp_dev_pages* d, const int32_t* rids, const int32_t* keep_from,
+                 int n, int sinks, void* stream);
+/* End requests rids[0..n): every live page loses a reference (and returns
+ * to the free stack at zero), as kvp_host_release. At most 4096 pages. */
+int kvp_dev_release(kvp_dev_pages* d, const int32_t* rids, int n,
+                    void* stream);
+/* Fork: request dst[i] shares every page of src[i] (one more reference
+ * each) and takes its length (device int32 [n]); the dst ids must be
+ * distinct and none of them a src of the same call. */
+int kvp_dev_fork(kvp_dev_pages* d, const int32_t* src, const int32_t* dst,
+                 int n, void* stream);
+/* Read and clear the state's error word (synchronises the stream). */
+int kvp_dev_sync_error(kvp_dev_pages* d, void* stream, int* err);
+/* copy_pages with the number of pairs read on the device (at most max_n),
+ * for the pairs kvp_dev_append emits. */
+int copy_pages_device_count(const kvp_pool* pool, const int32_t* src,
+                            const int32_t* dst, const int32_t* n_dev,
+                            int max_n, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -68,6 +68,17 @@ SIGNATURES = {
     "kvp_host_block_row": [_vp, _i, _vp, _i, _ip],
     "kvp_host_refcounts": [_vp, _vp, _i],
     "kvp_host_free_list": [_vp, _vp, _i, _ip],
+    "kvp_dev_pages_bytes": [_i, _i, _szp],
+    "kvp_dev_pages_create": [_i, _i, _i, _vp, _sz, _vp, _i, _i, _i, ctypes.POINTER(_vp)],
+    "kvp_dev_pages_destroy": [_vp],
+    "kvp_dev_pages_init": [_vp, _vp, _vp],
+    "kvp_dev_new": [_vp, _vp, _i, _vp],
+    "kvp_dev_append": [_vp, _vp, _vp, _i, _vp, _i, _vp, _vp, _vp, _vp],
+    "kvp_dev_trim": [_vp, _vp, _vp, _i, _i, _vp],
+    "kvp_dev_release": [_vp, _vp, _i, _vp],
+    "kvp_dev_sync_error": [_vp, _vp, _ip],
+    "kvp_dev_fork": [_vp, _vp, _vp, _i, _vp],
+    "copy_pages_device_count": [_vp, _vp, _vp, _vp, _i, _vp],
     "kvp_decode_step": [_vp, _vp, _vp, _i, _i, _i, _vp, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                         _i, _vp, _sz, _vp, _vp],
 }
@@ -189,6 +200,101 @@ def page_table_write(table, rows, cols, vals, expand=1, error_word=None, stream=
         raise ValueError("rows, cols and vals must have the same length")
     _check(lib().page_table_write(_ptr(table), table.shape[0], table.shape[1], _ptr(rows), _ptr(cols), _ptr(vals),
                                   n, expand, _ptr(error_word), _stream(stream)), "page_table_write")
+
+
+class DevicePages:
+    """Device-side page allocation over a caller's device table (see
+    include/pagedkv.h, kvp_dev_*). The state buffer is allocated here with
+    torch and kept alive; every call is asynchronous on the current stream."""
+
+    def __init__(self, num_pages, page_size, max_requests, table, table_mode, free_stack=None, device="cuda"):
+        _dev(table, torch.int32, "table")
+        n = ctypes.c_size_t()
+        _check(lib().kvp_dev_pages_bytes(num_pages, max_requests, ctypes.byref(n)), "kvp_dev_pages_bytes")
+        self.state = torch.zeros(n.value, dtype=torch.uint8, device=device)
+        self.table = table
+        self.num_pages, self.page_size, self.max_requests = num_pages, page_size, max_requests
+        h = ctypes.c_void_p()
+        _check(lib().kvp_dev_pages_create(num_pages, page_size, max_requests, _ptr(self.state), n.value, _ptr(table),
+                                          table.shape[0], table.shape[1], table_mode, ctypes.byref(h)),
+               "kvp_dev_pages_create")
+        self.handle = h
+        fs = None
+        if free_stack is not None:
+            fs = torch.as_tensor(list(free_stack), dtype=torch.int32).to(device)
+            if fs.numel() != num_pages:
+                raise ValueError("free_stack must hold num_pages entries")
+        self._free_stack = fs
+        _check(lib().kvp_dev_pages_init(h, _ptr(fs), _stream(None)), "kvp_dev_pages_init")
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h is not None and _lib is not None:
+            _lib.kvp_dev_pages_destroy(h)
+            self.handle = None
+
+    def new(self, rids, stream=None):
+        _dev(rids, torch.int32, "rids")
+        _check(lib().kvp_dev_new(self.handle, _ptr(rids), rids.numel(), _stream(stream)), "kvp_dev_new")
+
+    def append(self, rids, out_loc, cow_src, cow_dst, n_cow, counts=None, stream=None):
+        for t, nm in ((rids, "rids"), (out_loc, "out_loc"), (cow_src, "cow_src"), (cow_dst, "cow_dst"),
+                      (n_cow, "n_cow")):
+            _dev(t, torch.int32, nm)
+        if counts is not None:
+            _dev(counts, torch.int32, "counts")
+        n = rids.numel()
+        if cow_src.numel() < n or cow_dst.numel() < n:
+            raise ValueError("cow_src/cow_dst need room for one pair per request")
+        _check(lib().kvp_dev_append(self.handle, _ptr(rids), _ptr(counts), n, _ptr(out_loc), out_loc.numel(),
+                                    _ptr(cow_src), _ptr(cow_dst), _ptr(n_cow), _stream(stream)), "kvp_dev_append")
+
+    def trim(self, rids, keep_from, sinks=0, stream=None):
+        _dev(rids, torch.int32, "rids")
+        _dev(keep_from, torch.int32, "keep_from")
+        _check(lib().kvp_dev_trim(self.handle, _ptr(rids), _ptr(keep_from), rids.numel(), int(sinks),
+                                  _stream(stream)), "kvp_dev_trim")
+
+    def release(self, rids, stream=None):
+        _dev(rids, torch.int32, "rids")
+        _check(lib().kvp_dev_release(self.handle, _ptr(rids), rids.numel(), _stream(stream)), "kvp_dev_release")
+
+    def fork(self, src, dst, stream=None):
+        _dev(src, torch.int32, "src")
+        _dev(dst, torch.int32, "dst")
+        if src.numel() != dst.numel():
+            raise ValueError("src and dst must have the same length")
+        _check(lib().kvp_dev_fork(self.handle, _ptr(src), _ptr(dst), src.numel(), _stream(stream)), "kvp_dev_fork")
+
+    def sync_error(self, stream=None):
+        e = ctypes.c_int()
+        _check(lib().kvp_dev_sync_error(self.handle, _stream(stream), ctypes.byref(e)), "kvp_dev_sync_error")
+        return e.value
+
+    def snapshot(self):
+        """(free list, reference counts, lengths, released pages, sink pages) read back to the host."""
+        P, R = self.num_pages, self.max_requests
+        a16 = lambda x: (x + 15) // 16 * 16  # noqa: E731
+        st = self.state.cpu()
+        hdr = st[:16].view(torch.int32).tolist()
+        off = 16
+        stack = st[off:off + 4 * P].view(torch.int32).tolist()
+        off += a16(4 * P)
+        ref = st[off:off + 4 * P].view(torch.int32).tolist()
+        off += a16(4 * P)
+        arr = []
+        for _ in range(3):
+            arr.append(st[off:off + 4 * R].view(torch.int32).tolist())
+            off += a16(4 * R)
+        return stack[:hdr[0]], ref, arr[0], arr[1], arr[2]
+
+
+def copy_pages_device_count(pool, src, dst, n_dev, stream=None):
+    _dev(src, torch.int32, "src")
+    _dev(dst, torch.int32, "dst")
+    _dev(n_dev, torch.int32, "n_dev")
+    _check(lib().copy_pages_device_count(pool.handle, _ptr(src), _ptr(dst), _ptr(n_dev), src.numel(),
+                                         _stream(stream)), "copy_pages_device_count")
 
 
 def copy_pages(pool, src, dst, stream=None):

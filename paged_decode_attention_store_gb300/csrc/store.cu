@@ -35,9 +35,11 @@ __global__ void store_cache_kernel(char* __restrict__ kbase, size_t kv_bytes, co
 
 // Pair p, layer l, K or V: page dst[p] <- page src[p]; one page of one layer
 // is page_size contiguous rows.
+// With n_dev, the number of pairs is read on the device (at most n).
 __global__ void copy_pages_kernel(char* __restrict__ buf, size_t layer_bytes, int num_layers,
                                   const int32_t* __restrict__ src, const int32_t* __restrict__ dst, int n,
-                                  int page_chunks, int num_pages, int32_t* err) {
+                                  const int32_t* __restrict__ n_dev, int page_chunks, int num_pages, int32_t* err) {
+  if (n_dev) n = min(n, max(0, __ldg(n_dev)));
   const long long total = (long long)n * num_layers * 2 * page_chunks;
   for (long long u = blockIdx.x * (long long)blockDim.x + threadIdx.x; u < total;
        u += (long long)gridDim.x * blockDim.x) {
@@ -114,7 +116,20 @@ extern "C" int copy_pages(const kvp_pool* pool, const int32_t* src, const int32_
   const long long work = (long long)n * pool->num_layers * 2 * page_chunks;
   const int threads = 256;
   kvp::copy_pages_kernel<<<kvp::grid_for(work, threads, pool->num_sms), threads, 0, (cudaStream_t)stream>>>(
-      pool->buf, pool->layer_bytes, pool->num_layers, src, dst, n, page_chunks, pool->num_pages, pool->err);
+      pool->buf, pool->layer_bytes, pool->num_layers, src, dst, n, nullptr, page_chunks, pool->num_pages, pool->err);
+  return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
+}
+
+extern "C" int copy_pages_device_count(const kvp_pool* pool, const int32_t* src, const int32_t* dst,
+                                       const int32_t* n_dev, int max_n, void* stream) {
+  if (!pool || max_n < 0 || (max_n > 0 && (!src || !dst || !n_dev))) return KVP_ERR_INVALID_ARG;
+  if (max_n == 0) return KVP_OK;
+  const int page_chunks = (int)(pool->row_bytes * pool->page_size / 16);
+  const long long work = (long long)max_n * pool->num_layers * 2 * page_chunks;
+  const int threads = 256;
+  kvp::copy_pages_kernel<<<kvp::grid_for(work, threads, pool->num_sms), threads, 0, (cudaStream_t)stream>>>(
+      pool->buf, pool->layer_bytes, pool->num_layers, src, dst, max_n, n_dev, page_chunks, pool->num_pages,
+      pool->err);
   return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
 }
 
