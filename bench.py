@@ -51,7 +51,7 @@ UNIT = "GB/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 WORKLOADS = ("gqa_decode", "sliding_window", "sliding_window_sinks", "prefix_sharing", "large_batch_p16",
-             "large_batch_p1", "gqa_verify4")
+             "large_batch_p1", "gqa_verify4", "gqa_decode_devalloc")
 DEFAULT_WORKLOAD = "gqa_decode"
 
 
@@ -62,6 +62,9 @@ class Scenario:
     def __init__(self, name, seed):
         self.name = name
         self.seed = seed
+        self.devalloc = name.endswith("_devalloc")  # page bookkeeping on the device (kvp_dev_*)
+        if self.devalloc:
+            name = name[:-len("_devalloc")]
         if name == "gqa_decode":
             w = wl.gqa_decode(seed)
         elif name == "sliding_window":
@@ -197,10 +200,49 @@ def _i32(xs, dev):
     return torch.tensor(list(xs), dtype=torch.int32, device=dev)
 
 
+def device_twin(sc):
+    """Whether the workload's history is plain appends (no forks, trims or
+    verify steps) and so has a device-bookkeeping twin for the e2e leg."""
+    return (not sc.devalloc and not sc.verify and sc.window <= 0
+            and all(op[0] == "new" or (op[0] == "append" and not op[3] and not op[4]) for op in sc.ops))
+
+
+def build_product_device(sc, dev):
+    """The scenario's history through the device-side bookkeeping: every
+    request's rows appended in one call (pages popped in request order, as
+    the host replays them), then stored layer by layer."""
+    from paged_decode_attention_store_gb300.engine import DevicePagedKVCache
+
+    w = sc.w
+    if any(op[0] not in ("new", "append") for op in sc.ops) or any(op[3] or op[4] for op in sc.ops if op[0] == "append"):
+        raise ValueError("device bookkeeping scenarios build plain histories")
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    cache = DevicePagedKVCache(w.num_pages, w.P, w.Hkv, w.D, w.layers, w.dtype, max_requests=sc.max_requests,
+                               table_mode=w.table_mode, max_seq_len=sc.max_seq_len, free_stack=w.free_order,
+                               device=dev)
+    rids = [op[1] for op in sc.ops if op[0] == "new"]
+    counts = {op[1]: op[2] for op in sc.ops if op[0] == "append"}
+    cache.new(rids)
+    cnt = [counts.get(r, 0) for r in rids]
+    slots = cache.append(rids, counts=cnt)
+    rr = torch.as_tensor([r for r, c in zip(rids, cnt) for _ in range(c)], dtype=torch.int64, device=dev)
+    pos = torch.as_tensor([t for c in cnt for t in range(c)], dtype=torch.int64, device=dev)
+    step = 1 << 18
+    for layer in range(w.layers):
+        for s0 in range(0, rr.numel(), step):
+            k, v = wl.kv_rows(sc.seed, layer, rr[s0:s0 + step], pos[s0:s0 + step], w.Hkv, w.D, dtype=tdt, device=dev)
+            cache.store(layer, k, v, slots[s0:s0 + step].contiguous())
+    torch.cuda.synchronize(dev)
+    cache.check()
+    return cache, [counts.get(r, 0) for r in sc.rids]
+
+
 def build_product(sc, dev):
     from paged_decode_attention_store_gb300.engine import PagedKVCache
 
     w = sc.w
+    if sc.devalloc:
+        return build_product_device(sc, dev)
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     cache = PagedKVCache(w.num_pages, w.P, w.Hkv, w.D, w.layers, w.dtype, max_requests=sc.max_requests,
                          table_mode=w.table_mode, max_seq_len=sc.max_seq_len, free_stack=w.free_order, device=dev)
@@ -275,6 +317,10 @@ def prepare_steps(sc, cache, lens, first_step, n_steps, dev, host_inputs=False):
     steps = []
     lens = list(lens)
     for s in range(first_step, first_step + n_steps):
+        if sc.devalloc:
+            st, lens = _prepare_device_step(sc, lens, s, dev, host_inputs)
+            steps.append(st)
+            continue
         if sc.verify:
             st, lens = _prepare_verify_step(sc, cache, lens, s, dev, host_inputs)
             steps.append(st)
@@ -311,6 +357,34 @@ def prepare_steps(sc, cache, lens, first_step, n_steps, dev, host_inputs=False):
         st.attn_bytes = fused_launch_bytes(sc, lens, st.n_writes, st.n_cows)
         steps.append(st)
     return steps, lens
+
+
+def _prepare_device_step(sc, lens, s, dev, host_inputs):
+    """A decode step whose bookkeeping runs on the device: only q/k/v are
+    prepared (no host decision); the step's table writes are counted from
+    the lengths (a new page on every page boundary)."""
+    w = sc.w
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    st = StepData()
+    st.rids = _i32(sc.rids, dev)
+    st.n_writes = sum(1 for L in lens if L % w.P == 0)
+    st.n_cows = st.n_post = 0
+    st.pre = st.cows = st.post = None
+    positions = list(lens)
+    lens = [L + 1 for L in lens]
+    st.lens_list = list(lens)
+    st.q, st.k, st.v = [], [], []
+    for layer in range(w.layers):
+        q = wl.q_rows(sc.seed, s, layer, sc.rids, w.Hq, w.D, dtype=tdt, device=dev)
+        k, v = wl.kv_rows(sc.seed, layer, sc.rids, positions, w.Hkv, w.D, dtype=tdt, device=dev)
+        if host_inputs:
+            q, k, v = (x.cpu().pin_memory() for x in (q, k, v))
+        st.q.append(q)
+        st.k.append(k)
+        st.v.append(v)
+    st.bytes = step_bytes(sc, lens, st.n_writes, 0, 0)
+    st.attn_bytes = fused_launch_bytes(sc, lens, st.n_writes, 0)
+    return st, lens
 
 
 def _prepare_verify_step(sc, cache, lens, s, dev, host_inputs):
@@ -365,6 +439,11 @@ def run_step(sc, cache, st, outs, events=None):
     w = sc.w
     P = w.P
     n = 0
+    if sc.devalloc:  # device append, fused store + attention (+ combine) per layer, device trim
+        if events is not None:
+            kb.kvp_pool_set_timing_events(cache.pool, *events.pop())
+        cache.decode_step(st.rids, st.q, st.k, st.v, outs, sc.window, w.scale, sinks=sc.sinks)
+        return 1 + 2 * w.layers + (1 if sc.window > 0 else 0) + (1 if cache.may_share else 0)
     if sc.verify:  # table writes, store of the M drafts, verify (+ combine), rewind writes
         if st.pre is not None:
             kb.page_table_write(cache.table, *st.pre, expand=P if sc.raw else 1, error_word=cache.pool.error_word)
@@ -546,7 +625,7 @@ def run_gpu(args, rank, world, local_rank):
     if world > 1:
         torch.distributed.barrier()
 
-    n_attn = K * w.layers
+    n_attn = K if sc.devalloc else K * w.layers  # the native device step times its first layer
     ev_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_attn)]
     for a, b in ev_pairs:  # torch creates the CUDA event at its first record
         a.record()
@@ -563,8 +642,21 @@ def run_gpu(args, rank, world, local_rank):
     timed_tokens = sum(st.accepted for st in steps[W:W + K]) if sc.verify else K * len(sc.rids)
     attn_bytes_mean = statistics.mean(st.attn_bytes for st in steps[W + K:W + 2 * K])
 
-    # end to end through the driver, host buffers
-    e2e = run_e2e(args, sc, cache, lens_after, W + 2 * K + 1, dev)
+    # end to end through the public API, host buffers: the device-side page
+    # bookkeeping (no host decision per step) when the history is plain,
+    # else the host bookkeeping's native step
+    if device_twin(sc):
+        del cache
+        torch.cuda.empty_cache()
+        sc_dev = Scenario(sc.name + "_devalloc", sc.seed)
+        cache, lens_dev = build_product_device(sc_dev, dev)
+        e2e = run_e2e(args, sc_dev, cache, lens_dev, W + 2 * K + 1, dev)
+        e2e["path"] = "DevicePagedKVCache.decode_step (kvp_decode_step_device: page bookkeeping on the device)"
+    else:
+        e2e = run_e2e(args, sc, cache, lens_after, W + 2 * K + 1, dev)
+        e2e["path"] = ("DevicePagedKVCache.decode_step" if sc.devalloc else
+                       "PagedKVCache.verify_step + rewind" if sc.verify else
+                       "PagedKVCache.decode_step (kvp_decode_step: host page bookkeeping)")
     clocks = sampler.stop(t0, t1) if sampler else None
 
     elapsed_ms, total_bytes, tokens, e2e_ms, e2e_bytes = reduce_over_ranks(
@@ -635,6 +727,7 @@ def run_gpu(args, rank, world, local_rank):
             "h2d_bytes_per_step": e2e["h2d"],
             "d2h_bytes_per_step": e2e["d2h"],
             "host_link": e2e["link"],
+            "path": e2e["path"],
         },
         "clocks": clocks,
     }
@@ -651,6 +744,8 @@ def run_e2e(args, sc, cache, lens, first_step, dev):
     K = args.steps
     host_steps = _host_inputs(sc, first_step, K, lens)
     out_host = [torch.empty(out_shape(sc), dtype=cache.tdt, pin_memory=True) for _ in range(w.layers)]
+    if sc.devalloc:
+        return _run_e2e_device(sc, cache, lens, host_steps, out_host, dev)
     rids = np.asarray(sc.rids, np.int32)
     total_bytes = 0
     torch.cuda.synchronize(dev)
@@ -678,6 +773,44 @@ def run_e2e(args, sc, cache, lens, first_step, dev):
     d2h = sum(o.numel() * o.element_size() for o in out_host)
     return {"ms": start.elapsed_time(end), "bytes": total_bytes, "h2d": cache.h2d_bytes // K, "d2h": d2h,
             "link": link_rates(dev)}
+
+
+def _run_e2e_device(sc, cache, lens, host_steps, out_host, dev):
+    """End to end with the bookkeeping on the device: per step the host
+    copies q/k/v in (pinned), launches the native step and reads the output
+    back; no host decision, no table writes from the host."""
+    w = sc.w
+    K = len(host_steps)
+    rids = torch.as_tensor(sc.rids, dtype=torch.int32, device=dev)
+    q_d = [torch.empty_like(x, device=dev) for x in host_steps[0][0]]
+    k_d = [torch.empty_like(x, device=dev) for x in host_steps[0][1]]
+    v_d = [torch.empty_like(x, device=dev) for x in host_steps[0][2]]
+    o_d = [torch.empty(out_shape(sc), dtype=cache.tdt, device=dev) for _ in range(w.layers)]
+    lens = list(lens)
+    total_bytes = h2d = 0
+    stream = torch.cuda.current_stream(dev)
+    torch.cuda.synchronize(dev)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for s in range(K):
+        q_h, k_h, v_h = host_steps[s]
+        for layer in range(w.layers):
+            q_d[layer].copy_(q_h[layer], non_blocking=True)
+            k_d[layer].copy_(k_h[layer], non_blocking=True)
+            v_d[layer].copy_(v_h[layer], non_blocking=True)
+        cache.decode_step(rids, q_d, k_d, v_d, o_d, sc.window, w.scale, sinks=sc.sinks)
+        for layer in range(w.layers):
+            out_host[layer].copy_(o_d[layer], non_blocking=True)
+        stream.synchronize()
+        n_writes = sum(1 for L in lens if L % w.P == 0)
+        lens = [L + 1 for L in lens]
+        total_bytes += step_bytes(sc, lens, n_writes, 0, 0)
+    end.record()
+    torch.cuda.synchronize(dev)
+    cache.check()
+    h2d = sum(x[i].numel() * x[i].element_size() for x in host_steps[0] for i in range(w.layers))
+    d2h = sum(o.numel() * o.element_size() for o in out_host)
+    return {"ms": start.elapsed_time(end), "bytes": total_bytes, "h2d": h2d, "d2h": d2h, "link": link_rates(dev)}
 
 
 def link_rates(dev, nbytes=128 << 20):

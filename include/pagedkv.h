@@ -457,17 +457,21 @@ int kvp_dev_new(kvp_dev_pages* d, const int32_t* rids, int n, void* stream);
  * n <= 1024, distinct ids): new pages popped in call order, a shared tail
  * page copied first (pairs in cow_src/cow_dst [n], their number in *n_cow,
  * all device; copy them with copy_pages_device_count before storing), the
- * table entries written (expanded for a raw table), and the slot of every
- * new row in out_loc (device int32, request-major, at most max_tokens). */
+ * table entries written (expanded for a raw table), the slot of every new
+ * row in out_loc (device int32, request-major, at most max_tokens) and, if
+ * lens_out is not NULL, each request's new length (device int32 [n], the
+ * context_lens of the step's attention). */
 int kvp_dev_append(kvp_dev_pages* d, const int32_t* rids,
                    const int32_t* counts, int n, int32_t* out_loc,
                    int max_tokens, int32_t* cow_src, int32_t* cow_dst,
-                   int32_t* n_cow, void* stream);
+                   int32_t* n_cow, int32_t* lens_out, void* stream);
 /* Window trim of requests rids[i] to keep_from[i] (both device int32 [n])
  * keeping the first ceil(sinks / P) pages, as kvp_host_trim_sinks; the
- * released entries become -1. At most 4096 pages per call. */
+ * released entries become -1. keep_from NULL: each request's own
+ * L + 1 - (window - sinks), what its next decode step reads (0 <= sinks <
+ * window). At most 4096 pages per call. */
 int kvp_dev_trim(kvp_dev_pages* d, const int32_t* rids, const int32_t* keep_from,
-                 int n, int sinks, void* stream);
+                 int n, int window, int sinks, void* stream);
 /* End requests rids[0..n): every live page loses a reference (and returns
  * to the free stack at zero), as kvp_host_release. At most 4096 pages. */
 int kvp_dev_release(kvp_dev_pages* d, const int32_t* rids, int n,
@@ -479,6 +483,29 @@ int kvp_dev_fork(kvp_dev_pages* d, const int32_t* src, const int32_t* dst,
                  int n, void* stream);
 /* Read and clear the state's error word (synchronises the stream). */
 int kvp_dev_sync_error(kvp_dev_pages* d, void* stream, int* err);
+/* kvp_decode_step with the page bookkeeping on the device: for the n
+ * requests rids (DEVICE int32 [n], distinct, ids = table rows),
+ *   1. kvp_dev_append: one row each, slots and new lengths into scratch;
+ *   2. if may_share (requests can hold shared pages after a fork): the
+ *      copy-on-write copies, copy_pages_device_count;
+ *   3. for each layer l: wait for layer_ready[l] (or NULL), one
+ *      store_cache_and_attention(q[l], k[l], v[l] -> out[l]) (per-layer
+ *      DEVICE pointers, as kvp_decode_step), record layer_done[l];
+ *   4. with a window: kvp_dev_trim to each request's L + 1 - (window - sinks).
+ * scratch: device int32 [4n + 1] (slots, lengths, copy pairs, their count),
+ * owned by the caller, in use until the step completes on ``stream``.
+ * Nothing is synchronised; device-detected errors go to the state's error
+ * word (kvp_dev_sync_error) and the pool's (kvp_sync_error). */
+int kvp_decode_step_device(kvp_dev_pages* d, const kvp_pool* pool,
+                           int32_t* table, int table_rows_total,
+                           int table_cols, int table_mode,
+                           const int32_t* rids, int n, int window, int sinks,
+                           int num_q_heads, float scale,
+                           const void* const* q, const void* const* k,
+                           const void* const* v, void* const* out,
+                           void* const* layer_ready, void* const* layer_done,
+                           int32_t* scratch, int may_share, void* workspace,
+                           size_t workspace_bytes, void* stream);
 /* copy_pages with the number of pairs read on the device (at most max_n),
  * for the pairs kvp_dev_append emits. */
 int copy_pages_device_count(const kvp_pool* pool, const int32_t* src,

@@ -73,12 +73,14 @@ SIGNATURES = {
     "kvp_dev_pages_destroy": [_vp],
     "kvp_dev_pages_init": [_vp, _vp, _vp],
     "kvp_dev_new": [_vp, _vp, _i, _vp],
-    "kvp_dev_append": [_vp, _vp, _vp, _i, _vp, _i, _vp, _vp, _vp, _vp],
-    "kvp_dev_trim": [_vp, _vp, _vp, _i, _i, _vp],
+    "kvp_dev_append": [_vp, _vp, _vp, _i, _vp, _i, _vp, _vp, _vp, _vp, _vp],
+    "kvp_dev_trim": [_vp, _vp, _vp, _i, _i, _i, _vp],
     "kvp_dev_release": [_vp, _vp, _i, _vp],
     "kvp_dev_sync_error": [_vp, _vp, _ip],
     "kvp_dev_fork": [_vp, _vp, _vp, _i, _vp],
     "copy_pages_device_count": [_vp, _vp, _vp, _vp, _i, _vp],
+    "kvp_decode_step_device": [_vp, _vp, _vp, _i, _i, _i, _vp, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _vp, _vp,
+                               _vp, _i, _vp, _sz, _vp],
     "kvp_decode_step": [_vp, _vp, _vp, _i, _i, _i, _vp, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                         _i, _vp, _sz, _vp, _vp],
 }
@@ -237,7 +239,7 @@ class DevicePages:
         _dev(rids, torch.int32, "rids")
         _check(lib().kvp_dev_new(self.handle, _ptr(rids), rids.numel(), _stream(stream)), "kvp_dev_new")
 
-    def append(self, rids, out_loc, cow_src, cow_dst, n_cow, counts=None, stream=None):
+    def append(self, rids, out_loc, cow_src, cow_dst, n_cow, counts=None, lens_out=None, stream=None):
         for t, nm in ((rids, "rids"), (out_loc, "out_loc"), (cow_src, "cow_src"), (cow_dst, "cow_dst"),
                       (n_cow, "n_cow")):
             _dev(t, torch.int32, nm)
@@ -246,13 +248,19 @@ class DevicePages:
         n = rids.numel()
         if cow_src.numel() < n or cow_dst.numel() < n:
             raise ValueError("cow_src/cow_dst need room for one pair per request")
+        if lens_out is not None:
+            _dev(lens_out, torch.int32, "lens_out")
         _check(lib().kvp_dev_append(self.handle, _ptr(rids), _ptr(counts), n, _ptr(out_loc), out_loc.numel(),
-                                    _ptr(cow_src), _ptr(cow_dst), _ptr(n_cow), _stream(stream)), "kvp_dev_append")
+                                    _ptr(cow_src), _ptr(cow_dst), _ptr(n_cow), _ptr(lens_out), _stream(stream)),
+               "kvp_dev_append")
 
-    def trim(self, rids, keep_from, sinks=0, stream=None):
+    def trim(self, rids, keep_from=None, sinks=0, window=0, stream=None):
+        """Release what the next step cannot read: below keep_from[i] (device
+        int32), or, without keep_from, below each request's L + 1 - (window - sinks)."""
         _dev(rids, torch.int32, "rids")
-        _dev(keep_from, torch.int32, "keep_from")
-        _check(lib().kvp_dev_trim(self.handle, _ptr(rids), _ptr(keep_from), rids.numel(), int(sinks),
+        if keep_from is not None:
+            _dev(keep_from, torch.int32, "keep_from")
+        _check(lib().kvp_dev_trim(self.handle, _ptr(rids), _ptr(keep_from), rids.numel(), int(window), int(sinks),
                                   _stream(stream)), "kvp_dev_trim")
 
     def release(self, rids, stream=None):

@@ -133,3 +133,42 @@ extern "C" int kvp_decode_step(kvp_host* h, const kvp_pool* pool, int32_t* table
     return rc;
   return KVP_OK;
 }
+
+// kvp_decode_step_device: the same step with the page bookkeeping on the
+// device (kvp_dev_*): nothing is decided on the host and nothing but the
+// caller's q/k/v crosses to the device. The append kernel pops the new
+// pages, writes the table entries and hands the slots and the new lengths
+// to the fused store + attention launches of every layer; the window's
+// trim runs last, on the device too.
+extern "C" int kvp_decode_step_device(kvp_dev_pages* d, const kvp_pool* pool, int32_t* table, int table_rows_total,
+                                      int table_cols, int table_mode, const int32_t* rids, int n, int window,
+                                      int sinks, int num_q_heads, float scale, const void* const* q,
+                                      const void* const* k, const void* const* v, void* const* out,
+                                      void* const* layer_ready, void* const* layer_done, int32_t* scratch,
+                                      int may_share, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!d || !pool || !table || !rids || n <= 0 || !q || !k || !v || !out || !scratch) return KVP_ERR_INVALID_ARG;
+  if (sinks < 0 || (window > 0 && sinks >= window)) return KVP_ERR_INVALID_ARG;
+  if (window <= 0) sinks = 0;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t* out_loc = scratch;
+  int32_t* lens = scratch + n;
+  int32_t* cow_src = scratch + 2 * n;
+  int32_t* cow_dst = scratch + 3 * n;
+  int32_t* n_cow = scratch + 4 * n;
+  int rc = kvp_dev_append(d, rids, nullptr, n, out_loc, n, cow_src, cow_dst, n_cow, lens, stream);
+  if (rc != KVP_OK) return rc;
+  if (may_share && (rc = copy_pages_device_count(pool, cow_src, cow_dst, n_cow, n, stream)) != KVP_OK) return rc;
+  for (int l = 0; l < pool->num_layers; ++l) {
+    if (layer_ready && layer_ready[l] &&
+        cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(layer_ready[l]), 0) != cudaSuccess)
+      return KVP_ERR_CUDA;
+    if ((rc = store_cache_and_attention(pool, l, q[l], k[l], v[l], out_loc, n, num_q_heads, table, table_rows_total,
+                                        table_cols, table_mode, rids, lens, nullptr, nullptr, nullptr, 0, window,
+                                        sinks, scale, out[l], workspace, workspace_bytes, stream)) != KVP_OK)
+      return rc;
+    if (layer_done && layer_done[l] && cudaEventRecord(static_cast<cudaEvent_t>(layer_done[l]), st) != cudaSuccess)
+      return KVP_ERR_CUDA;
+  }
+  if (window > 0 && (rc = kvp_dev_trim(d, rids, nullptr, n, window, sinks, stream)) != KVP_OK) return rc;
+  return KVP_OK;
+}

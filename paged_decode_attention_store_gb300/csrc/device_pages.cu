@@ -126,13 +126,15 @@ __global__ void dev_new_kernel(DevState s, const int32_t* rids, int n) {
 __global__ void __launch_bounds__(kDevThreads) dev_append_kernel(DevState s, const int32_t* rids,
                                                                   const int32_t* counts, int n, int32_t* out_loc,
                                                                   int max_tokens, int32_t* cow_src, int32_t* cow_dst,
-                                                                  int32_t* n_cow) {
+                                                                  int32_t* n_cow, int32_t* lens_out) {
   __shared__ int s_tail[kDevThreads];
   __shared__ int s_rid[kDevThreads];
   const int i = threadIdx.x;
   const int P = s.P;
   bool ok = true;
   int r = -1, L = 0, c = 0, off = 0, tl = -1, tail = -1, ref0 = 0, first_new = 0, b = 0;
+  griddep_wait();  // a programmatic dependent launch: the previous kernels' state is visible from here on
+  griddep_launch_dependents();
   if (i < n) {
     r = rids[i];
     c = counts ? counts[i] : 1;
@@ -202,6 +204,7 @@ __global__ void __launch_bounds__(kDevThreads) dev_append_kernel(DevState s, con
       out_loc[o_tok + k] = page * P + t % P;
     }
     s.len[r] = L + c;
+    if (lens_out) lens_out[i] = L + c;
   }
   __syncthreads();
   if (i == 0) {
@@ -215,8 +218,8 @@ __global__ void __launch_bounds__(kDevThreads) dev_append_kernel(DevState s, con
 // the request. Pages go back in call order, each pushed by the release that
 // drops its count to zero (that is the host's order).
 __global__ void __launch_bounds__(kDevThreads) dev_release_kernel(DevState s, const int32_t* rids,
-                                                                   const int32_t* keep_from, int sinks, int n,
-                                                                   int mode) {
+                                                                   const int32_t* keep_from, int window, int sinks,
+                                                                   int n, int mode) {
   __shared__ int s_page[kMaxReleases];
   __shared__ int s_ref0[kMaxReleases];
   __shared__ int s_rid[kDevThreads];
@@ -224,6 +227,8 @@ __global__ void __launch_bounds__(kDevThreads) dev_release_kernel(DevState s, co
   const int P = s.P;
   bool ok = true;
   int r = -1, cnt = 0, lo = 0, sp = 0, d = 0, pages = 0;
+  griddep_wait();
+  griddep_launch_dependents();
   if (i < n) {
     r = rids[i];
     if ((unsigned)r >= (unsigned)s.max_requests || r >= s.rows) {
@@ -235,7 +240,8 @@ __global__ void __launch_bounds__(kDevThreads) dev_release_kernel(DevState s, co
       if (mode == 0) {
         sp = ceil_div_d(sinks, P);
         if (sinks < 0 || (d > 0 && sp != s.sinkp[r])) ok = false;  // sinks fixed once pages went
-        const int kf = keep_from[i];
+        // without keep_from: what the next decode step reads, L + 1 - (W - S)
+        const int kf = keep_from ? keep_from[i] : L + 1 - (window - sinks);
         const int hi = min(kf > 0 ? kf / P : 0, pages);
         lo = sp + d;
         cnt = max(0, hi - lo);
@@ -334,6 +340,23 @@ __global__ void dev_fork_kernel(DevState s, const int32_t* src, const int32_t* d
   }
 }
 
+// One block of kDevThreads as a programmatic dependent launch: it may start
+// while the previous kernel of the stream finishes, and waits for it
+// (griddep_wait) before touching anything.
+template <typename... Args>
+cudaError_t launch_one_block(void (*kernel)(Args...), cudaStream_t stream, Args... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(kDevThreads);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 }  // namespace
 
 }  // namespace kvp
@@ -402,31 +425,34 @@ extern "C" int kvp_dev_new(kvp_dev_pages* d, const int32_t* rids, int n, void* s
 }
 
 extern "C" int kvp_dev_append(kvp_dev_pages* d, const int32_t* rids, const int32_t* counts, int n, int32_t* out_loc,
-                              int max_tokens, int32_t* cow_src, int32_t* cow_dst, int32_t* n_cow, void* stream) {
+                              int max_tokens, int32_t* cow_src, int32_t* cow_dst, int32_t* n_cow, int32_t* lens_out,
+                              void* stream) {
   if (!d || n < 0 || n > kDevThreads || max_tokens < 0) return KVP_ERR_INVALID_ARG;
   if (n == 0) return KVP_OK;
   if (!rids || !out_loc || !cow_src || !cow_dst) return KVP_ERR_INVALID_ARG;
-  dev_append_kernel<<<1, kDevThreads, 0, static_cast<cudaStream_t>(stream)>>>(state_of(d), rids, counts, n, out_loc,
-                                                                               max_tokens, cow_src, cow_dst, n_cow);
-  return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
+  const cudaError_t e = launch_one_block(dev_append_kernel, static_cast<cudaStream_t>(stream), state_of(d), rids,
+                                         counts, n, out_loc, max_tokens, cow_src, cow_dst, n_cow, lens_out);
+  return e == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
 }
 
-extern "C" int kvp_dev_trim(kvp_dev_pages* d, const int32_t* rids, const int32_t* keep_from, int n, int sinks,
-                            void* stream) {
+extern "C" int kvp_dev_trim(kvp_dev_pages* d, const int32_t* rids, const int32_t* keep_from, int n, int window,
+                            int sinks, void* stream) {
   if (!d || n < 0 || n > kDevThreads || sinks < 0) return KVP_ERR_INVALID_ARG;
+  if (!keep_from && (window <= 0 || sinks >= window)) return KVP_ERR_INVALID_ARG;
   if (n == 0) return KVP_OK;
-  if (!rids || !keep_from) return KVP_ERR_INVALID_ARG;
-  dev_release_kernel<<<1, kDevThreads, 0, static_cast<cudaStream_t>(stream)>>>(state_of(d), rids, keep_from, sinks,
-                                                                                n, 0);
-  return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
+  if (!rids) return KVP_ERR_INVALID_ARG;
+  const cudaError_t e = launch_one_block(dev_release_kernel, static_cast<cudaStream_t>(stream), state_of(d), rids,
+                                         keep_from, window, sinks, n, 0);
+  return e == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
 }
 
 extern "C" int kvp_dev_release(kvp_dev_pages* d, const int32_t* rids, int n, void* stream) {
   if (!d || n < 0 || n > kDevThreads) return KVP_ERR_INVALID_ARG;
   if (n == 0) return KVP_OK;
   if (!rids) return KVP_ERR_INVALID_ARG;
-  dev_release_kernel<<<1, kDevThreads, 0, static_cast<cudaStream_t>(stream)>>>(state_of(d), rids, nullptr, 0, n, 1);
-  return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
+  const cudaError_t e = launch_one_block(dev_release_kernel, static_cast<cudaStream_t>(stream), state_of(d), rids,
+                                         static_cast<const int32_t*>(nullptr), 0, 0, n, 1);
+  return e == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
 }
 
 extern "C" int kvp_dev_fork(kvp_dev_pages* d, const int32_t* src, const int32_t* dst, int n, void* stream) {

@@ -321,3 +321,111 @@ class PagedKVCache:
         torch.cuda.synchronize(self.dev)
         self._steps[key] = st
         return st
+
+
+class DevicePagedKVCache:
+    """A paged KV cache whose page bookkeeping lives on the device (kvp_dev_*).
+
+    The same layout as :class:`PagedKVCache` (mini-sglang's 6-axis buffer, a
+    block table or a raw-location table); the free list, reference counts
+    and lengths are device arrays, so a decode step (:meth:`decode_step`)
+    makes no host decision and copies nothing to the device but q/k/v.
+    Request ids are table rows. Lengths are not mirrored on the host: the
+    caller knows its own schedule.
+    """
+
+    def __init__(self, num_pages, page_size, kv_heads, head_dim, num_layers, dtype="bf16", max_requests=256,
+                 table_mode="block", max_seq_len=None, free_stack=None, device="cuda", zero=True):
+        self.P, self.Hkv, self.D, self.layers = page_size, kv_heads, head_dim, num_layers
+        self.num_pages = num_pages
+        self.tdt, kdt = _DT[dtype]
+        self.raw = table_mode == "raw"
+        self.dev = torch.device(device)
+        extra = 1 if self.raw else 0
+        alloc = torch.zeros if zero else torch.empty
+        self.kv = alloc((2, num_layers, num_pages + extra, page_size, kv_heads, head_dim), dtype=self.tdt,
+                        device=self.dev)
+        self.pool = kb.Pool(self.kv, page_size, kdt)
+        max_seq_len = max_seq_len or num_pages * page_size
+        if self.raw:
+            cols = _align32(min(max_seq_len, num_pages * page_size))
+            self.table = torch.zeros((max_requests + 1, cols), dtype=torch.int32, device=self.dev)
+            self.table[max_requests].fill_(num_pages * page_size)  # dummy row -> dummy page
+        else:
+            cols = -(-max_seq_len // page_size)
+            self.table = torch.full((max_requests, cols), -1, dtype=torch.int32, device=self.dev)
+        self.table_mode = kb.KVP_RAW_LOCATIONS if self.raw else kb.KVP_BLOCK_TABLE
+        self.pages = kb.DevicePages(num_pages, page_size, max_requests, self.table, self.table_mode,
+                                    free_stack=free_stack, device=self.dev)
+        self.may_share = False  # set by fork: appends may then copy shared tail pages
+        self._ws = {}
+        self._scratch = {}
+
+    def _i32(self, xs):
+        return torch.as_tensor(list(xs), dtype=torch.int32).to(self.dev, non_blocking=True)
+
+    def new(self, rids):
+        self.pages.new(self._i32(rids))
+
+    def append(self, rids, counts=None):
+        """Append counts[i] rows (default one) to each request; returns the
+        slots of the new rows on the device (request-major), after copying
+        any shared tail page."""
+        n = len(rids)
+        total = n if counts is None else int(sum(counts))
+        out_loc = torch.empty(max(total, 1), dtype=torch.int32, device=self.dev)
+        cow = torch.empty((2, n), dtype=torch.int32, device=self.dev)
+        n_cow = torch.zeros(1, dtype=torch.int32, device=self.dev)
+        self.pages.append(self._i32(rids), out_loc, cow[0], cow[1], n_cow,
+                          counts=None if counts is None else self._i32(counts))
+        if self.may_share:
+            kb.copy_pages_device_count(self.pool, cow[0], cow[1], n_cow)
+        return out_loc[:total]
+
+    def store(self, layer, k, v, out_loc):
+        kb.store_cache(self.pool, layer, k, v, out_loc)
+
+    def fork(self, src, dst):
+        self.pages.fork(self._i32(src), self._i32(dst))
+        self.may_share = True
+
+    def trim(self, rids, window, sinks=0):
+        self.pages.trim(self._i32(rids), window=window, sinks=sinks)
+
+    def release(self, rids):
+        self.pages.release(self._i32(rids))
+
+    def workspace(self, batch, num_q_heads):
+        key = (batch, num_q_heads)
+        if key not in self._ws:
+            self._ws[key] = kb.alloc_workspace(self.pool, batch, num_q_heads, device=self.dev)
+        return self._ws[key]
+
+    def attend(self, layer, q, context_lens, window, scale, out, table_rows=None, sinks=0):
+        ws = self.workspace(q.shape[0], q.shape[1])
+        kb.paged_decode_attention(self.pool, layer, q, self.table, self.table_mode, context_lens, window, scale,
+                                  out, ws, table_rows=table_rows, sinks=sinks)
+
+    def decode_step(self, rids, q, k, v, out, window, scale, sinks=0):
+        """One decode step, all layers, through kvp_decode_step_device.
+        ``rids``: device int32 [B]; q/k/v/out: per-layer DEVICE tensors
+        ([B, Hq, D] and [B, Hkv, D]). Asynchronous: nothing is synchronised."""
+        n, Hq = rids.numel(), q[0].shape[1]
+        scratch = self._scratch.get(n)
+        if scratch is None:
+            scratch = self._scratch[n] = torch.zeros(4 * n + 1, dtype=torch.int32, device=self.dev)
+        ws = self.workspace(n, Hq)
+        vp = ctypes.c_void_p
+        arr = lambda ts: (vp * self.layers)(*[t.data_ptr() for t in ts])  # noqa: E731
+        stream = torch.cuda.current_stream(self.dev)
+        kb._check(kb.lib().kvp_decode_step_device(
+            self.pages.handle, self.pool.handle, vp(self.table.data_ptr()), self.table.shape[0], self.table.shape[1],
+            self.table_mode, vp(rids.data_ptr()), n, int(window or 0), int(sinks), Hq, float(scale), arr(q), arr(k),
+            arr(v), arr(out), None, None, vp(scratch.data_ptr()), int(self.may_share), vp(ws.data_ptr()),
+            ws.numel(), vp(stream.cuda_stream)), "kvp_decode_step_device")
+
+    def check(self):
+        """Raise if a device-side error was recorded since the last check."""
+        for e, what in ((kb.kvp_sync_error(self.pool), "device"), (self.pages.sync_error(), "device pages")):
+            if e != 0:
+                raise kb.KvpError(e, what)

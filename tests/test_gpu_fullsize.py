@@ -47,7 +47,11 @@ def test_full_size_parity(kb, workload):
         bench.run_step(sc, cache, st, outs)
         torch.cuda.synchronize(DEV)
         ref, slots = orc.step(i + 1, sample, with_slots=True)
-        assert st.out_loc.cpu().tolist() == slots, "decode-step slots differ"
+        if sc.devalloc:  # the slots were chosen on the device, inside the step
+            got_slots = cache._scratch[len(sc.rids)][:len(sc.rids)].cpu().tolist()
+        else:
+            got_slots = st.out_loc.cpu().tolist()
+        assert got_slots == slots, "decode-step slots differ"
         got = {layer: outs[layer].float().cpu().numpy() for layer in layers}
         for r in sample:
             b = sc.rids.index(r)
@@ -58,6 +62,10 @@ def test_full_size_parity(kb, workload):
     for r in sc.rids:
         row = orc.table_row(r)
         assert tab[r, :len(row)].tolist() == row, f"table row {r}"
+    if sc.devalloc:  # the device free list and counts equal the oracle's
+        free, ref, lens_d, _, _ = cache.pages.snapshot()
+        assert free == orc.pt.free and ref == orc.pt.ref
+        assert [lens_d[r] for r in sc.rids] == [orc.pt.length[r] for r in sc.rids]
     cache.check()
     del cache, steps, outs
     gc.collect()
