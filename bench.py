@@ -651,7 +651,8 @@ def run_gpu(args, rank, world, local_rank):
         sc_dev = Scenario(sc.name + "_devalloc", sc.seed)
         cache, lens_dev = build_product_device(sc_dev, dev)
         e2e = run_e2e(args, sc_dev, cache, lens_dev, W + 2 * K + 1, dev)
-        e2e["path"] = "DevicePagedKVCache.decode_step (kvp_decode_step_device: page bookkeeping on the device)"
+        e2e["path"] = ("DevicePagedKVCache.decode_step_host (kvp_decode_step_device_io: page bookkeeping on the "
+                       "device, host copies in the same native call)")
     else:
         e2e = run_e2e(args, sc, cache, lens_after, W + 2 * K + 1, dev)
         e2e["path"] = ("DevicePagedKVCache.decode_step" if sc.devalloc else
@@ -776,32 +777,20 @@ def run_e2e(args, sc, cache, lens, first_step, dev):
 
 
 def _run_e2e_device(sc, cache, lens, host_steps, out_host, dev):
-    """End to end with the bookkeeping on the device: per step the host
-    copies q/k/v in (pinned), launches the native step and reads the output
-    back; no host decision, no table writes from the host."""
+    """End to end with the bookkeeping on the device: per step one native
+    call copies q/k/v in from pinned host memory, runs the step and copies
+    the output back; no host decision, no table writes from the host."""
     w = sc.w
     K = len(host_steps)
     rids = torch.as_tensor(sc.rids, dtype=torch.int32, device=dev)
-    q_d = [torch.empty_like(x, device=dev) for x in host_steps[0][0]]
-    k_d = [torch.empty_like(x, device=dev) for x in host_steps[0][1]]
-    v_d = [torch.empty_like(x, device=dev) for x in host_steps[0][2]]
-    o_d = [torch.empty(out_shape(sc), dtype=cache.tdt, device=dev) for _ in range(w.layers)]
     lens = list(lens)
     total_bytes = h2d = 0
-    stream = torch.cuda.current_stream(dev)
     torch.cuda.synchronize(dev)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record()
     for s in range(K):
         q_h, k_h, v_h = host_steps[s]
-        for layer in range(w.layers):
-            q_d[layer].copy_(q_h[layer], non_blocking=True)
-            k_d[layer].copy_(k_h[layer], non_blocking=True)
-            v_d[layer].copy_(v_h[layer], non_blocking=True)
-        cache.decode_step(rids, q_d, k_d, v_d, o_d, sc.window, w.scale, sinks=sc.sinks)
-        for layer in range(w.layers):
-            out_host[layer].copy_(o_d[layer], non_blocking=True)
-        stream.synchronize()
+        cache.decode_step_host(rids, q_h, k_h, v_h, out_host, sc.window, w.scale, sinks=sc.sinks)
         n_writes = sum(1 for L in lens if L % w.P == 0)
         lens = [L + 1 for L in lens]
         total_bytes += step_bytes(sc, lens, n_writes, 0, 0)

@@ -506,6 +506,25 @@ int kvp_decode_step_device(kvp_dev_pages* d, const kvp_pool* pool,
                            void* const* layer_ready, void* const* layer_done,
                            int32_t* scratch, int may_share, void* workspace,
                            size_t workspace_bytes, void* stream);
+/* kvp_decode_step_device with host buffers: q_host/k_host/v_host (per-layer
+ * HOST pointers, [n, Hq, D] / [n, kv_heads, D], pinned for the copies to
+ * be asynchronous) are copied into the caller's per-layer device staging
+ * q_dev/k_dev/v_dev, the step runs, and each layer's output goes from
+ * out_dev back to out_host. Returns once the outputs are on the host (the
+ * stream is synchronised). One call per step. */
+int kvp_decode_step_device_io(kvp_dev_pages* d, const kvp_pool* pool,
+                              int32_t* table, int table_rows_total,
+                              int table_cols, int table_mode,
+                              const int32_t* rids, int n, int window,
+                              int sinks, int num_q_heads, float scale,
+                              const void* const* q_host,
+                              const void* const* k_host,
+                              const void* const* v_host,
+                              void* const* out_host, void* const* q_dev,
+                              void* const* k_dev, void* const* v_dev,
+                              void* const* out_dev, int32_t* scratch,
+                              int may_share, void* workspace,
+                              size_t workspace_bytes, void* stream);
 /* copy_pages with the number of pairs read on the device (at most max_n),
  * for the pairs kvp_dev_append emits. */
 int copy_pages_device_count(const kvp_pool* pool, const int32_t* src,

@@ -81,6 +81,8 @@ SIGNATURES = {
     "copy_pages_device_count": [_vp, _vp, _vp, _vp, _i, _vp],
     "kvp_decode_step_device": [_vp, _vp, _vp, _i, _i, _i, _vp, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _vp, _vp,
                                _vp, _i, _vp, _sz, _vp],
+    "kvp_decode_step_device_io": [_vp, _vp, _vp, _i, _i, _i, _vp, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _vp, _vp,
+                                  _vp, _vp, _vp, _i, _vp, _sz, _vp],
     "kvp_decode_step": [_vp, _vp, _vp, _i, _i, _i, _vp, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                         _i, _vp, _sz, _vp, _vp],
 }

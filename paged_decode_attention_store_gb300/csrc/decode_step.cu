@@ -172,3 +172,38 @@ extern "C" int kvp_decode_step_device(kvp_dev_pages* d, const kvp_pool* pool, in
   if (window > 0 && (rc = kvp_dev_trim(d, rids, nullptr, n, window, sinks, stream)) != KVP_OK) return rc;
   return KVP_OK;
 }
+
+// kvp_decode_step_device_io: kvp_decode_step_device with host buffers in and
+// out: each layer's q, k, v are copied from host memory into the caller's
+// device staging, the step runs, each layer's output is copied back, and the
+// call returns once the outputs are on the host. One native call per step,
+// so the host issues everything while the first copy is in flight.
+extern "C" int kvp_decode_step_device_io(kvp_dev_pages* d, const kvp_pool* pool, int32_t* table,
+                                         int table_rows_total, int table_cols, int table_mode, const int32_t* rids,
+                                         int n, int window, int sinks, int num_q_heads, float scale,
+                                         const void* const* q_host, const void* const* k_host,
+                                         const void* const* v_host, void* const* out_host, void* const* q_dev,
+                                         void* const* k_dev, void* const* v_dev, void* const* out_dev,
+                                         int32_t* scratch, int may_share, void* workspace, size_t workspace_bytes,
+                                         void* stream) {
+  if (!pool || !q_host || !k_host || !v_host || !out_host || !q_dev || !k_dev || !v_dev || !out_dev || n <= 0 ||
+      num_q_heads <= 0)
+    return KVP_ERR_INVALID_ARG;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t qbytes = (size_t)n * num_q_heads * pool->head_dim * pool->elem;
+  const size_t kvbytes = (size_t)n * pool->row_bytes;
+  for (int l = 0; l < pool->num_layers; ++l) {
+    if (cudaMemcpyAsync(q_dev[l], q_host[l], qbytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaMemcpyAsync(k_dev[l], k_host[l], kvbytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaMemcpyAsync(v_dev[l], v_host[l], kvbytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+      return KVP_ERR_CUDA;
+  }
+  int rc = kvp_decode_step_device(d, pool, table, table_rows_total, table_cols, table_mode, rids, n, window, sinks,
+                                  num_q_heads, scale, q_dev, k_dev, v_dev, out_dev, nullptr, nullptr, scratch,
+                                  may_share, workspace, workspace_bytes, stream);
+  if (rc != KVP_OK) return rc;
+  for (int l = 0; l < pool->num_layers; ++l)
+    if (cudaMemcpyAsync(out_host[l], out_dev[l], qbytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+      return KVP_ERR_CUDA;
+  return cudaStreamSynchronize(st) == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
+}

@@ -360,6 +360,8 @@ class DevicePagedKVCache:
         self.may_share = False  # set by fork: appends may then copy shared tail pages
         self._ws = {}
         self._scratch = {}
+        self._staging = {}
+        self._ptrs = {}
 
     def _i32(self, xs):
         return torch.as_tensor(list(xs), dtype=torch.int32).to(self.dev, non_blocking=True)
@@ -423,6 +425,41 @@ class DevicePagedKVCache:
             self.table_mode, vp(rids.data_ptr()), n, int(window or 0), int(sinks), Hq, float(scale), arr(q), arr(k),
             arr(v), arr(out), None, None, vp(scratch.data_ptr()), int(self.may_share), vp(ws.data_ptr()),
             ws.numel(), vp(stream.cuda_stream)), "kvp_decode_step_device")
+
+    def _ptr_array(self, ts):
+        """ctypes array of the tensors' data pointers, cached by their addresses."""
+        key = tuple(t.data_ptr() for t in ts)
+        arr = self._ptrs.get(key)
+        if arr is None:
+            if len(self._ptrs) > 256:
+                self._ptrs.clear()
+            arr = self._ptrs[key] = (ctypes.c_void_p * len(ts))(*key)
+        return arr
+
+    def decode_step_host(self, rids, q, k, v, out, window, scale, sinks=0):
+        """One decode step with HOST buffers (pinned): ``q``/``k``/``v``/``out``
+        are per-layer host tensors; inputs are copied to device staging, the
+        step runs with the bookkeeping on the device, outputs come back. One
+        native call (kvp_decode_step_device_io); returns when ``out`` holds
+        the results. ``rids``: device int32 [B]."""
+        n, Hq = rids.numel(), q[0].shape[1]
+        key = (n, Hq)
+        stage = self._staging.get(key)
+        if stage is None:
+            mk = lambda t: torch.empty(t.shape, dtype=t.dtype, device=self.dev)  # noqa: E731
+            stage = self._staging[key] = ([mk(t) for t in q], [mk(t) for t in k], [mk(t) for t in v],
+                                          [mk(t) for t in out], torch.zeros(4 * n + 1, dtype=torch.int32,
+                                                                            device=self.dev))
+        qd, kd, vd, od, scratch = stage
+        ws = self.workspace(n, Hq)
+        vp = ctypes.c_void_p
+        pa = self._ptr_array
+        stream = torch.cuda.current_stream(self.dev)
+        kb._check(kb.lib().kvp_decode_step_device_io(
+            self.pages.handle, self.pool.handle, vp(self.table.data_ptr()), self.table.shape[0], self.table.shape[1],
+            self.table_mode, vp(rids.data_ptr()), n, int(window or 0), int(sinks), Hq, float(scale), pa(q), pa(k),
+            pa(v), pa(out), pa(qd), pa(kd), pa(vd), pa(od), vp(scratch.data_ptr()), int(self.may_share),
+            vp(ws.data_ptr()), ws.numel(), vp(stream.cuda_stream)), "kvp_decode_step_device_io")
 
     def check(self):
         """Raise if a device-side error was recorded since the last check."""

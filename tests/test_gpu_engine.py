@@ -84,3 +84,68 @@ def test_decode_step_matches_the_oracle(kb, window, host_io, sinks):
         row = orc.table_row(b)
         assert tab[b, :len(row)].tolist() == row
     cache.check()
+
+
+@pytest.mark.parametrize("window,sinks,host_io,mode", [(0, 0, True, "block"), (40, 2, True, "block"),
+                                                        (0, 0, False, "raw"), (40, 0, False, "block")])
+def test_device_bookkeeping_decode_step_matches_the_oracle(kb, window, sinks, host_io, mode):
+    """DevicePagedKVCache: pages chosen on the device each step (one native
+    call with host or device buffers); outputs, slots, tables and the device
+    free list against the oracle."""
+    from paged_decode_attention_store_gb300.engine import DevicePagedKVCache
+
+    Hq, Hkv, D, P, seed = 32, 8, 128, 16, 73
+    lengths = [300, 17, 64, 5, 1000]
+    B, steps = len(lengths), 20
+    num_pages = sum(-(-(L + steps) // P) for L in lengths) + 8
+    order = wl.free_stack_for_order(wl.permutation(seed, num_pages))
+    w = wl.Workload("devstep", "bf16", Hq, Hkv, D, P, 1, num_pages, order, lengths, window=window, sinks=sinks,
+                    scale=1.0 / math.sqrt(D))
+    cache = DevicePagedKVCache(num_pages, P, Hkv, D, 1, "bf16", max_requests=B, table_mode=mode,
+                               max_seq_len=1100, free_stack=order, device=DEV)
+    orc = OracleSession(w, B, seed=seed, mode=mode, raw_from_pages=True)
+    cache.new(range(B))
+    for b in range(B):
+        orc.new(b)
+    slots = cache.append(list(range(B)), counts=lengths)
+    rr = [b for b in range(B) for _ in range(lengths[b])]
+    pp = [t for L in lengths for t in range(L)]
+    k, v = wl.kv_rows(seed, 0, rr, pp, Hkv, D, device=DEV)
+    cache.store(0, k, v, slots)
+    assert slots.cpu().tolist() == orc.append(rr, pp)
+    if window:
+        cache.trim(list(range(B)), window, sinks)
+        for b in range(B):
+            orc.trim(b, max(0, lengths[b] + 1 - (window - sinks)), sinks=sinks)
+    rids = torch.arange(B, dtype=torch.int32, device=DEV)
+    lens = list(lengths)
+    for step in range(1, steps + 1):
+        q = wl.q_rows(seed, step, 0, list(range(B)), Hq, D, device=DEV)
+        k, v = wl.kv_rows(seed, 0, list(range(B)), lens, Hkv, D, device=DEV)
+        if host_io:
+            qh, kh, vh = (x.cpu().pin_memory() for x in (q, k, v))
+            out = torch.empty((B, Hq, D), dtype=torch.bfloat16, pin_memory=True)
+            cache.decode_step_host(rids, [qh], [kh], [vh], [out], window, w.scale, sinks=sinks)
+        else:
+            out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=DEV)
+            cache.decode_step(rids, [q], [k], [v], [out], window, w.scale, sinks=sinks)
+        want_slots = orc.append(list(range(B)), lens)
+        scratch = cache._staging[(B, Hq)][4] if host_io else cache._scratch[B]
+        assert scratch[:B].cpu().tolist() == want_slots, f"step {step}: slots"
+        lens = [L + 1 for L in lens]
+        got = out.float().cpu().numpy()
+        for b in range(B):
+            assert max_abs(got[b], orc.attend(0, b, lens[b], window, step=step, sinks=sinks)) <= 2e-2, \
+                f"step {step} request {b}"
+        if window:
+            for b in range(B):
+                orc.trim(b, max(0, lens[b] + 1 - (window - sinks)), sinks=sinks)
+    torch.cuda.synchronize()
+    free, ref, lens_d, dropped, _ = cache.pages.snapshot()
+    assert free == orc.pt.free and ref == orc.pt.ref
+    assert lens_d[:B] == lens and dropped[:B] == [orc.pt.dropped[b] for b in range(B)]
+    tab = cache.table.cpu().numpy()
+    for b in range(B):
+        row = orc.table_row(b)
+        assert tab[b, :len(row)].tolist() == row
+    cache.check()
