@@ -204,6 +204,32 @@ int paged_verify_attention(const kvp_pool* pool, int layer, const void* q,
                            void* stream);
 
 /* ------------------------------------------------------------------------
+ * paged_prefill_attention: chunked prefill. Request b's q_lens[b] newest
+ * tokens (NULL: ``chunk`` each; their K/V already stored, L =
+ * context_lens[b] counts them) are queries at once; query j sits at
+ * position L - q_lens[b] + j and attends what a one-token decode step with
+ * that context attends (causal, window and sinks as paged_decode_attention)
+ * - the formula of paged_verify_attention for chunks of any length
+ * ("Week 3 Day 3: Paged KV Cache" of tiny-llm: chunked prefill appends each
+ * chunk to the pages, then attends over them). bf16 pools with head_dim 128
+ * and 128 % (num_q_heads / kv_heads) == 0 run on the tcgen05 tensor cores
+ * (TMEM accumulators), others on the general kernel.
+ *   q    device [batch, chunk, num_q_heads, head_dim], pool dtype,
+ *        16-byte aligned.
+ *   out  device, the same shape; rows j >= q_lens[b] are not written.
+ *   q_lens  device int32 [batch] with 1 <= q_lens[b] <= min(chunk, L), or NULL.
+ * No workspace. Errors as paged_decode_attention (an invalid request's rows
+ * are zero-filled).
+ * ---------------------------------------------------------------------- */
+int paged_prefill_attention(const kvp_pool* pool, int layer, const void* q,
+                            int batch, int chunk, int num_q_heads,
+                            const int32_t* q_lens, const int32_t* table,
+                            int table_rows_total, int table_cols,
+                            int table_mode, const int32_t* table_rows,
+                            const int32_t* context_lens, int window,
+                            int sinks, float scale, void* out, void* stream);
+
+/* ------------------------------------------------------------------------
  * store_cache_and_attention: one layer of a decode step in one launch:
  *     page_table_write(table, tw_rows, tw_cols, tw_vals, n_tw, expand);
  *     store_cache(pool, layer, k, v, out_loc, batch);

@@ -48,6 +48,7 @@ SIGNATURES = {
     "paged_decode_attention": [_vp, _i, _vp, _i, _i, _vp, _i, _i, _i, _vp, _vp, _i, _i, _f, _vp, _vp, _sz, _vp],
     "paged_verify_attention_workspace_size": [_vp, _i, _i, _i, _szp],
     "paged_verify_attention": [_vp, _i, _vp, _i, _i, _i, _vp, _i, _i, _i, _vp, _vp, _i, _i, _f, _vp, _vp, _sz, _vp],
+    "paged_prefill_attention": [_vp, _i, _vp, _i, _i, _i, _vp, _vp, _i, _i, _i, _vp, _vp, _i, _i, _f, _vp, _vp],
     "paged_decode_attention_noalloc": [_vp, _i, _vp, _i, _i, _vp, _i, _i, _i, _vp, _vp, _i, _f, _vp, _vp],
     "store_cache_and_attention": [_vp, _i, _vp, _vp, _vp, _vp, _i, _i, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _i,
                                   _i, _i, _f, _vp, _vp, _sz, _vp],
@@ -378,6 +379,28 @@ def paged_verify_attention(pool, layer, q, table, table_mode, context_lens, wind
                                         table.shape[1], table_mode, _ptr(table_rows), _ptr(context_lens),
                                         int(window or 0), int(sinks), float(scale), _ptr(out), ws_ptr, ws_bytes,
                                         _stream(stream)), "paged_verify_attention")
+
+
+def paged_prefill_attention(pool, layer, q, table, table_mode, context_lens, window, scale, out, q_lens=None,
+                            table_rows=None, stream=None, sinks=0):
+    """Chunked prefill: q/out [B, C, Hq, D]; query j of request b sits at
+    position context_lens[b] - q_lens[b] + j (q_lens NULL: C) and attends
+    causally (see include/pagedkv.h). Rows j >= q_lens[b] are not written."""
+    dt = _TORCH_DTYPE[pool.dtype]
+    _dev(q, dt, "q")
+    _dev(out, dt, "out")
+    _dev(table, torch.int32, "table")
+    _dev(context_lens, torch.int32, "context_lens")
+    for t, nm in ((q_lens, "q_lens"), (table_rows, "table_rows")):
+        if t is not None:
+            _dev(t, torch.int32, nm)
+    if q.dim() != 4 or out.shape != q.shape or context_lens.numel() != q.shape[0]:
+        raise ValueError("q/out must be [B, C, Hq, D] and context_lens [B]")
+    B, C, Hq = q.shape[0], q.shape[1], q.shape[2]
+    _check(lib().paged_prefill_attention(pool.handle, layer, _ptr(q), B, C, Hq, _ptr(q_lens), _ptr(table),
+                                         table.shape[0], table.shape[1], table_mode, _ptr(table_rows),
+                                         _ptr(context_lens), int(window or 0), int(sinks), float(scale), _ptr(out),
+                                         _stream(stream)), "paged_prefill_attention")
 
 
 def store_cache_and_attention(pool, layer, q, k, v, out_loc, table, table_mode, context_lens, window, scale, out,

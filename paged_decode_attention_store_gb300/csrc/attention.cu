@@ -38,6 +38,7 @@ struct GenArgs {
   const int32_t* table_rows;
   int B, Hq, Hkv, D, window, sinks;
   int M;  // query tokens per request (query j at position L - M + j)
+  const int32_t* q_lens;  // per request, <= M (NULL: M); rows j >= q_lens[b] are not written
   float scale_log2;
   int32_t* err;
 };
@@ -59,12 +60,14 @@ __global__ void __launch_bounds__(32 * kGenWarps) generic_decode_kernel(const Ge
   const T* q = static_cast<const T*>(a.q) + ((size_t)bj * a.Hq + h) * D;
   const int Lr = a.context_lens[b];
   const int row = a.table_rows ? a.table_rows[b] : b;
-  if (Lr < a.M || Lr < 1 || Lr > table_capacity(a.T) || row < 0 || row >= a.T.rows_total) {
+  const int Mb = a.q_lens ? a.q_lens[b] : a.M;
+  if (Mb < 1 || Mb > a.M || Lr < Mb || Lr > table_capacity(a.T) || row < 0 || row >= a.T.rows_total) {
     if (h == 0 && j == 0 && lane == 0) set_error(a.err, KVP_ERR_BAD_INDEX);
     for (int d = lane; d < D; d += 32) out[d] = from_f<T>(0.f);
     return;
   }
-  const int L = Lr - a.M + j + 1;  // the query token's own context (causal)
+  if (j >= Mb) return;
+  const int L = Lr - Mb + j + 1;  // the query token's own context (causal)
   for (int d = lane; d < D; d += 32) qs[warp][d] = to_f<T>(q[d]);
   __syncwarp();
   const Span sp = attend_span(L, a.window, a.sinks);
@@ -349,6 +352,7 @@ int attention_impl(const kvp_pool* pool, int layer, const void* q, int batch, in
   ga.window = window;
   ga.sinks = sinks;
   ga.M = M;
+  ga.q_lens = nullptr;
   ga.scale_log2 = scale_log2;
   ga.err = pool->err;
   const long long warps = (long long)batch * M * num_q_heads;
@@ -402,6 +406,53 @@ extern "C" int store_cache_and_attention(const kvp_pool* pool, int layer, const 
   return attention_impl(pool, layer, q, batch, 1, num_q_heads, table, table_rows_total, table_cols, table_mode,
                         table_rows, context_lens, window, sinks, scale, out, workspace, workspace_bytes, stream,
                         &fz);
+}
+
+extern "C" int paged_prefill_attention(const kvp_pool* pool, int layer, const void* q, int batch, int chunk,
+                                       int num_q_heads, const int32_t* q_lens, const int32_t* table,
+                                       int table_rows_total, int table_cols, int table_mode,
+                                       const int32_t* table_rows, const int32_t* context_lens, int window, int sinks,
+                                       float scale, void* out, void* stream) {
+  if (!pool || !q || !table || !context_lens || !out) return KVP_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= pool->num_layers || batch <= 0 || chunk <= 0 || num_q_heads <= 0) return KVP_ERR_INVALID_ARG;
+  if (num_q_heads % pool->kv_heads) return KVP_ERR_INVALID_ARG;
+  if (table_rows_total <= 0 || table_cols <= 0) return KVP_ERR_INVALID_ARG;
+  if (table_mode != KVP_BLOCK_TABLE && table_mode != KVP_RAW_LOCATIONS) return KVP_ERR_INVALID_ARG;
+  if (!(scale == scale)) return KVP_ERR_INVALID_ARG;
+  if (sinks < 0 || (window > 0 && sinks >= window)) return KVP_ERR_INVALID_ARG;
+  if (window <= 0) sinks = 0;
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 15) return KVP_ERR_INVALID_ARG;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const TableRef T = make_table(pool, table, table_rows_total, table_cols, table_mode);
+  if (prefill_tc_eligible(pool, num_q_heads, chunk))
+    return launch_prefill_tc(pool, layer, q, batch, chunk, num_q_heads, q_lens, T, table_rows, context_lens, window,
+                             sinks, scale, out, st);
+  if (pool->head_dim > kGenMaxD) return KVP_ERR_INVALID_ARG;
+  GenArgs ga;
+  ga.T = T;
+  ga.kv_layer = pool->buf + (size_t)layer * pool->layer_bytes;
+  ga.kv_bytes = pool->kv_bytes;
+  ga.q = q;
+  ga.out = out;
+  ga.context_lens = context_lens;
+  ga.table_rows = table_rows;
+  ga.B = batch;
+  ga.Hq = num_q_heads;
+  ga.Hkv = pool->kv_heads;
+  ga.D = pool->head_dim;
+  ga.window = window;
+  ga.sinks = sinks;
+  ga.M = chunk;
+  ga.q_lens = q_lens;
+  ga.scale_log2 = scale * 1.4426950408889634f;
+  ga.err = pool->err;
+  const long long warps = (long long)batch * chunk * num_q_heads;
+  const unsigned blocks = (unsigned)((warps + kGenWarps - 1) / kGenWarps);
+  if (pool->dtype == KVP_F32)
+    generic_decode_kernel<float><<<blocks, 32 * kGenWarps, 0, st>>>(ga);
+  else
+    generic_decode_kernel<__nv_bfloat16><<<blocks, 32 * kGenWarps, 0, st>>>(ga);
+  return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
 }
 
 extern "C" int gather_indices(const kvp_pool* pool, const int32_t* table, int table_rows_total, int table_cols,

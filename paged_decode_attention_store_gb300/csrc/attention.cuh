@@ -146,6 +146,12 @@ int tc_num_stages(int HG, int C);
 bool tc_encode_tmap(const kvp_pool* pool, int HG, CUtensorMap* out);
 // Largest batch the in-kernel work split can take for HG and ring depth S.
 int tc_max_batch(int HG, int S);
+// Chunked prefill on tcgen05 (prefill_tc.cu): whether a pool and query-head
+// count take it, and its launch over batch requests of up to C new tokens.
+bool prefill_tc_eligible(const kvp_pool* pool, int Hq, int C);
+int launch_prefill_tc(const kvp_pool* pool, int layer, const void* q, int batch, int C, int Hq, const int32_t* q_lens,
+                      const TableRef& T, const int32_t* table_rows, const int32_t* context_lens, int window, int sinks,
+                      float scale, void* out, cudaStream_t stream);
 // Launch the bf16, head_dim-128 kernel (one CTA per SM) and the combine
 // kernel after it, both as programmatic dependents.
 cudaError_t launch_tc(const TcArgs& a, const CombineArgs& c, cudaStream_t stream, void* ev_before, void* ev_after);

@@ -39,6 +39,7 @@ extern "C" int kv_pool_create(int num_pages, int page_size, int kv_heads, int he
   p->ev_before = nullptr;
   p->ev_after = nullptr;
   p->tmap_hg = 0;
+  p->tmap1_state = 0;
   *out = p;
   return KVP_OK;
 }
