@@ -51,7 +51,7 @@ UNIT = "GB/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 WORKLOADS = ("gqa_decode", "sliding_window", "sliding_window_sinks", "prefix_sharing", "large_batch_p16",
-             "large_batch_p1", "gqa_verify4", "gqa_decode_devalloc")
+             "large_batch_p1", "gqa_verify4", "gqa_decode_devalloc", "gqa_prefill512")
 DEFAULT_WORKLOAD = "gqa_decode"
 
 
@@ -71,6 +71,8 @@ class Scenario:
             w = wl.sliding_window(seed)
         elif name == "sliding_window_sinks":
             w = wl.sliding_window_sinks(seed)
+        elif name.startswith("gqa_prefill"):
+            w = wl.gqa_prefill(seed, chunk=int(name[len("gqa_prefill"):]))
         elif name.startswith("gqa_verify"):
             w = wl.gqa_verify(seed, M=int(name[len("gqa_verify"):]))
         elif name == "prefix_sharing":
@@ -121,10 +123,14 @@ class Scenario:
                 else:
                     self.ops.append(("append", b, L, 0, 0))
         self.raw = w.table_mode == "raw"
-        self.max_seq_len = w.extra.get("max_seq_len") if self.raw else max(self.lengths) + 512
+        # room for the steps' growth: one token a step, or a chunk a step for prefill (72 steps)
+        growth = max(512, 72 * w.extra.get("prefill", 0))
+        self.max_seq_len = w.extra.get("max_seq_len") if self.raw else max(self.lengths) + growth
         self.window = w.window
         self.sinks = w.sinks
         self.verify = w.extra.get("verify", 0)  # drafted tokens verified per request and step (0: decode)
+        self.prefill = w.extra.get("prefill", 0)  # chunk tokens prefilled per request and step (0: decode)
+        self.multi = self.verify or self.prefill  # query tokens per request and step, when more than one
 
 
 def attended_span(sc, L):
@@ -133,7 +139,7 @@ def attended_span(sc, L):
     W, S = sc.w.window, sc.w.sinks
     if W <= 0:
         return 0, 0
-    lo = max(0, L - (W + max(sc.verify, 1) - 1 - S))
+    lo = max(0, L - (W + max(sc.multi, 1) - 1 - S))
     se = min(S, lo)
     return (0, 0) if se == lo else (se, lo)
 
@@ -141,7 +147,25 @@ def attended_span(sc, L):
 def out_shape(sc):
     """Attention output of one layer: [B, Hq, D], or [B, M, Hq, D] for verify steps."""
     B, w = len(sc.rids), sc.w
-    return (B, sc.verify, w.Hq, w.D) if sc.verify else (B, w.Hq, w.D)
+    return (B, sc.multi, w.Hq, w.D) if sc.multi else (B, w.Hq, w.D)
+
+
+def attention_flops(sc, lens):
+    """Algorithmic flops of one multi-token attention launch: for every query
+    token j (context L - M + j + 1) and query head, 2 D flops per attended key
+    for Q K^T and as many for P V (masked work inside tiles not counted)."""
+    w, M = sc.w, max(sc.multi, 1)
+    keys = 0
+    for L in lens:
+        for j in range(M):
+            Lj = L - M + j + 1
+            if w.window > 0:
+                lo = max(0, Lj - (w.window - w.sinks))
+                se = min(w.sinks, lo)
+                keys += (Lj - lo) + (se if se < lo else 0)
+            else:
+                keys += Lj
+    return 4 * w.D * w.Hq * keys
 
 
 def attended_count(sc, L):
@@ -161,7 +185,7 @@ def attention_bytes(sc, lens):
         n = se + L - lo
         kv += n * row_kv
         tab += 4 * (n if sc.raw else (-(-se // w.P) + -(-L // w.P) - lo // w.P))
-    qo = 2 * len(lens) * max(sc.verify, 1) * w.Hq * w.D * elem
+    qo = 2 * len(lens) * max(sc.multi, 1) * w.Hq * w.D * elem
     return kv + qo + tab + 4 * len(lens)
 
 
@@ -181,7 +205,7 @@ def step_bytes(sc, lens, n_writes, n_cows, n_trim_writes):
     w = sc.w
     row = w.Hkv * w.D * (2 if w.dtype == "bf16" else 4)
     copies = n_cows * w.layers * 2 * 2 * w.P * row
-    return (w.layers * (attention_bytes(sc, lens) + store_bytes(sc, len(lens) * max(sc.verify, 1)))
+    return (w.layers * (attention_bytes(sc, lens) + store_bytes(sc, len(lens) * max(sc.multi, 1)))
             + table_write_bytes(sc, n_writes + n_trim_writes) + copies)
 
 
@@ -203,7 +227,7 @@ def _i32(xs, dev):
 def device_twin(sc):
     """Whether the workload's history is plain appends (no forks, trims or
     verify steps) and so has a device-bookkeeping twin for the e2e leg."""
-    return (not sc.devalloc and not sc.verify and sc.window <= 0
+    return (not sc.devalloc and not sc.multi and sc.window <= 0
             and all(op[0] == "new" or (op[0] == "append" and not op[3] and not op[4]) for op in sc.ops))
 
 
@@ -321,7 +345,7 @@ def prepare_steps(sc, cache, lens, first_step, n_steps, dev, host_inputs=False):
             st, lens = _prepare_device_step(sc, lens, s, dev, host_inputs)
             steps.append(st)
             continue
-        if sc.verify:
+        if sc.multi:
             st, lens = _prepare_verify_step(sc, cache, lens, s, dev, host_inputs)
             steps.append(st)
             continue
@@ -388,9 +412,10 @@ def _prepare_device_step(sc, lens, s, dev, host_inputs):
 
 
 def _prepare_verify_step(sc, cache, lens, s, dev, host_inputs):
-    """A speculative step: M drafted tokens per request appended and stored,
-    verified at once, a seeded number accepted, the rest rewound."""
-    w, M = sc.w, sc.verify
+    """A multi-token step: M tokens per request appended and stored, then
+    attended at once. A speculative (verify) step then accepts a seeded
+    number of the M drafts and rewinds the rest; a prefill step keeps all."""
+    w, M = sc.w, sc.multi
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     st = StepData()
     rr = [r for r in sc.rids for _ in range(M)]
@@ -404,11 +429,12 @@ def _prepare_verify_step(sc, cache, lens, s, dev, host_inputs):
     ctx = [L + M for L in lens]
     st.lens_list = list(ctx)
     st.lens = _i32(ctx, dev)
-    acc = wl.accepted_drafts(sc.seed, s, len(sc.rids), M)
+    acc = wl.accepted_drafts(sc.seed, s, len(sc.rids), M) if sc.verify else [M] * len(sc.rids)
     post = []
     for r, a in zip(sc.rids, acc):
-        post += cache.host.rewind(r, M - a)
-        cache.lengths[r] -= M - a
+        if a < M:
+            post += cache.host.rewind(r, M - a)
+            cache.lengths[r] -= M - a
     st.n_post = len(post)
     st.post = None if not post else tuple(_i32(x, dev) for x in zip(*post))
     st.q, st.k, st.v = [], [], []
@@ -423,6 +449,7 @@ def _prepare_verify_step(sc, cache, lens, s, dev, host_inputs):
         st.v.append(v)
     st.bytes = step_bytes(sc, ctx, st.n_writes, st.n_cows, st.n_post)
     st.attn_bytes = attention_bytes(sc, ctx)
+    st.attn_flops = attention_flops(sc, ctx)
     st.accepted = sum(acc)
     return st, [L + a for L, a in zip(lens, acc)]
 
@@ -444,7 +471,7 @@ def run_step(sc, cache, st, outs, events=None):
             kb.kvp_pool_set_timing_events(cache.pool, *events.pop())
         cache.decode_step(st.rids, st.q, st.k, st.v, outs, sc.window, w.scale, sinks=sc.sinks)
         return 1 + 2 * w.layers + (1 if sc.window > 0 else 0) + (1 if cache.may_share else 0)
-    if sc.verify:  # table writes, store of the M drafts, verify (+ combine), rewind writes
+    if sc.multi:  # table writes, store of the M rows, verify (+ combine) or prefill, rewind writes
         if st.pre is not None:
             kb.page_table_write(cache.table, *st.pre, expand=P if sc.raw else 1, error_word=cache.pool.error_word)
             n += 1
@@ -455,8 +482,12 @@ def run_step(sc, cache, st, outs, events=None):
             cache.store(layer, st.k[layer], st.v[layer], st.out_loc)
             if events is not None:
                 kb.kvp_pool_set_timing_events(cache.pool, *events.pop())
-            cache.verify(layer, st.q[layer], st.lens, sc.window, w.scale, outs[layer], sinks=sc.sinks)
-            n += 3
+            if sc.verify:
+                cache.verify(layer, st.q[layer], st.lens, sc.window, w.scale, outs[layer], sinks=sc.sinks)
+                n += 3
+            else:
+                cache.prefill(layer, st.q[layer], st.lens, sc.window, w.scale, outs[layer], sinks=sc.sinks)
+                n += 2
         if st.post is not None:
             kb.page_table_write(cache.table, *st.post, expand=P if sc.raw else 1, error_word=cache.pool.error_word)
             n += 1
@@ -531,14 +562,14 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(inside)}
 
 
-def measured_peak():
+def measured_peak(key="hbm_gbs", fallback=None):
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), "measured"
+        return float(d[key]), "measured"
     except (OSError, KeyError, ValueError):
-        return FALLBACK_HBM_GBS, "fallback"
+        return (FALLBACK_HBM_GBS if fallback is None else fallback), "fallback"
 
 
 def ncu_traffic(workload):
@@ -602,7 +633,7 @@ def run_gpu(args, rank, world, local_rank):
     soak_window = sc.window - 1 if sc.window > 0 else 0
     while time.time() - t_soak < args.soak:
         for layer in range(w.layers):
-            q0 = steps[0].q[layer][:, 0].contiguous() if sc.verify else steps[0].q[layer]
+            q0 = steps[0].q[layer][:, 0].contiguous() if sc.multi else steps[0].q[layer]
             cache.attend(layer, q0, _i32(lens, dev), soak_window, w.scale, soak_out, sinks=sc.sinks)
         torch.cuda.synchronize(dev)
     for i in range(W):
@@ -639,7 +670,7 @@ def run_gpu(args, rank, world, local_rank):
     attn_ms = [a.elapsed_time(b) for a, b in ev_pairs]
     total_bytes = sum(st.bytes for st in steps[W:W + K])
     # tokens a step adds: one per request, or the accepted drafts of a verify step
-    timed_tokens = sum(st.accepted for st in steps[W:W + K]) if sc.verify else K * len(sc.rids)
+    timed_tokens = sum(st.accepted for st in steps[W:W + K]) if sc.multi else K * len(sc.rids)
     attn_bytes_mean = statistics.mean(st.attn_bytes for st in steps[W + K:W + 2 * K])
 
     # end to end through the public API, host buffers: the device-side page
@@ -657,6 +688,7 @@ def run_gpu(args, rank, world, local_rank):
         e2e = run_e2e(args, sc, cache, lens_after, W + 2 * K + 1, dev)
         e2e["path"] = ("DevicePagedKVCache.decode_step" if sc.devalloc else
                        "PagedKVCache.verify_step + rewind" if sc.verify else
+                       "PagedKVCache.prefill_step" if sc.prefill else
                        "PagedKVCache.decode_step (kvp_decode_step: host page bookkeeping)")
     clocks = sampler.stop(t0, t1) if sampler else None
 
@@ -669,6 +701,28 @@ def run_gpu(args, rank, world, local_rank):
     value = total_bytes / (elapsed_ms * 1e-3) / 1e9
     achieved = attn_bytes_mean / (statistics.mean(attn_ms) * 1e-3) / 1e9
     traffic = ncu_traffic(sc.name)
+    roofline = {
+        "bound": "hbm",
+        "kernel": "tc_decode_kernel",
+        "achieved": round(achieved, 1),
+        "peak": peak,
+        "peak_kind": f"{peak_kind} hbm_gbs (copy, burst)",
+        "unit": "GB/s",
+        "frac": round(achieved / peak, 4),
+        "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
+        "traffic": traffic,
+        "algorithmic_bytes_per_launch": int(attn_bytes_mean),
+        "mean_launch_us": round(1e3 * statistics.mean(attn_ms), 2),
+        "launches_timed": len(attn_ms),
+    }
+    if sc.prefill:  # a dense contraction: flops against the measured bf16 tensor peak
+        flops_mean = statistics.mean(st.attn_flops for st in steps[W + K:W + 2 * K])
+        tf = flops_mean / (statistics.mean(attn_ms) * 1e-3) / 1e12
+        tpeak, tkind = measured_peak("bf16_tflops", 1900.0)
+        roofline.update({"bound": "tensor", "kernel": "prefill_tc_kernel", "achieved": round(tf, 1), "peak": tpeak,
+                         "peak_kind": f"{tkind} bf16_tflops (cuBLAS, burst)", "unit": "TFLOP/s",
+                         "frac": round(tf / tpeak, 4), "frac_of_nominal_8tbs": None,
+                         "algorithmic_flops_per_launch": int(flops_mean), "attention_gbps": round(achieved, 1)})
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -693,6 +747,7 @@ def run_gpu(args, rank, world, local_rank):
             "window": w.window,
             "sinks": w.sinks,
             "verify_tokens": sc.verify,
+            "prefill_chunk": sc.prefill,
             "table": "raw token locations" if sc.raw else "block table",
             "mean_attended_tokens": round(statistics.mean(
                 attended_count(sc, L) for L in steps[W].lens_list), 1),
@@ -706,20 +761,7 @@ def run_gpu(args, rank, world, local_rank):
         "pct_of_peak": round(100.0 * value / peak, 2),
         "pct_of_nominal_8tbs": round(100.0 * value / NOMINAL_HBM_GBS, 2),
         "gpu_launches": launches,
-        "roofline": {
-            "bound": "hbm",
-            "kernel": "tc_decode_kernel",
-            "achieved": round(achieved, 1),
-            "peak": peak,
-            "peak_kind": f"{peak_kind} hbm_gbs (copy, burst)",
-            "unit": "GB/s",
-            "frac": round(achieved / peak, 4),
-            "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
-            "traffic": traffic,
-            "algorithmic_bytes_per_launch": int(attn_bytes_mean),
-            "mean_launch_us": round(1e3 * statistics.mean(attn_ms), 2),
-            "launches_timed": len(attn_ms),
-        },
+        "roofline": roofline,
         "e2e": {
             "value": round(e2e_bytes / (e2e_ms * 1e-3) / 1e9, 2),
             "unit": UNIT,
@@ -755,6 +797,11 @@ def run_e2e(args, sc, cache, lens, first_step, dev):
     start.record()
     for s in range(K):
         q_h, k_h, v_h = host_steps[s]
+        if sc.prefill:  # a chunk per request: append, store, attend
+            cache.prefill_step(rids, q_h, k_h, v_h, out_host, sc.window, w.scale, sinks=sc.sinks)
+            total_bytes += step_bytes(sc, [int(x) for x in cache.lengths[rids]], cache.last_writes,
+                                      cache.last_copies, 0)
+            continue
         if sc.verify:  # draft M, verify, accept the seeded count, rewind the rest
             M = sc.verify
             cache.verify_step(rids, q_h, k_h, v_h, out_host, sc.window, w.scale, sinks=sc.sinks)
@@ -826,8 +873,8 @@ def _host_inputs(sc, first_step, K, lens):
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     dev = torch.device("cuda", torch.cuda.current_device())
     out = []
-    if sc.verify:
-        M = sc.verify
+    if sc.multi:
+        M = sc.multi
         lens = list(lens)
         rr = [r for r in sc.rids for _ in range(M)]
         for s in range(first_step, first_step + K):
@@ -841,7 +888,8 @@ def _host_inputs(sc, first_step, K, lens):
                 ks.append(k.cpu().pin_memory())
                 vs.append(v.cpu().pin_memory())
             out.append((qs, ks, vs))
-            lens = [L + a for L, a in zip(lens, wl.accepted_drafts(sc.seed, s, len(sc.rids), M))]
+            acc = wl.accepted_drafts(sc.seed, s, len(sc.rids), M) if sc.verify else [M] * len(sc.rids)
+            lens = [L + a for L, a in zip(lens, acc)]
         return out
     for i, s in enumerate(range(first_step, first_step + K)):
         positions = [L + i for L in lens]
@@ -945,7 +993,7 @@ class OracleSample:
         """A speculative step: M drafts appended per request, the ones of
         ``attend_rids`` stored and verified, the seeded acceptance applied by
         rewinding the rest."""
-        sc, w, OA, M = self.sc, self.sc.w, self.OA, self.sc.verify
+        sc, w, OA, M = self.sc, self.sc.w, self.OA, self.sc.multi
         pos0 = {r: self.pt.length[r] for r in sc.rids}
         rr = [r for r in sc.rids for _ in range(M)]
         slots = self._append(rr)
@@ -963,15 +1011,16 @@ class OracleSample:
                     sl = [s for p in pos for s in OA.gather_block(row, w.P, p, p + 1)]
                     per_q.append(OA.attend_request(self.stores[layer], q.float().numpy(), sl, w.scale))
                 outs[(r, layer)] = np.stack(per_q)
-        for r, a in zip(sc.rids, wl.accepted_drafts(sc.seed, step_index, len(sc.rids), M)):
-            self.pt.rewind(r, M - a)
+        if sc.verify:
+            for r, a in zip(sc.rids, wl.accepted_drafts(sc.seed, step_index, len(sc.rids), M)):
+                self.pt.rewind(r, M - a)
         return (outs, slots) if with_slots else outs
 
     def step(self, step_index, attend_rids, with_slots=False):
         """One decode step: bookkeeping for every request, store + attention for ``attend_rids``.
 
         Returns {(rid, layer): output}, and also the step's slots when ``with_slots``."""
-        if self.sc.verify:
+        if self.sc.multi:
             return self._verify_step(step_index, attend_rids, with_slots)
         sc, w, OA = self.sc, self.sc.w, self.OA
         pos = [self.pt.length[r] for r in sc.rids]

@@ -424,9 +424,17 @@ extern "C" int paged_prefill_attention(const kvp_pool* pool, int layer, const vo
   if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 15) return KVP_ERR_INVALID_ARG;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   const TableRef T = make_table(pool, table, table_rows_total, table_cols, table_mode);
-  if (prefill_tc_eligible(pool, num_q_heads, chunk))
-    return launch_prefill_tc(pool, layer, q, batch, chunk, num_q_heads, q_lens, T, table_rows, context_lens, window,
-                             sinks, scale, out, st);
+  kvp_pool* mp = const_cast<kvp_pool*>(pool);
+  if (prefill_tc_eligible(pool, num_q_heads, chunk)) {
+    if (mp->ev_before && cudaEventRecord(static_cast<cudaEvent_t>(mp->ev_before), st) != cudaSuccess)
+      return KVP_ERR_CUDA;
+    const int rc = launch_prefill_tc(pool, layer, q, batch, chunk, num_q_heads, q_lens, T, table_rows, context_lens,
+                                     window, sinks, scale, out, st);
+    if (rc == KVP_OK && mp->ev_after && cudaEventRecord(static_cast<cudaEvent_t>(mp->ev_after), st) != cudaSuccess)
+      return KVP_ERR_CUDA;
+    mp->ev_before = mp->ev_after = nullptr;
+    return rc;
+  }
   if (pool->head_dim > kGenMaxD) return KVP_ERR_INVALID_ARG;
   GenArgs ga;
   ga.T = T;

@@ -172,6 +172,20 @@ class PagedKVCache:
         self.lengths[rid] -= n
         return len(writes)
 
+    def prefill(self, layer, q, context_lens, window, scale, out, q_lens=None, table_rows=None, sinks=0):
+        """Chunked prefill: q/out [B, C, Hq, D], query j of request b at
+        position context_lens[b] - q_lens[b] + j (the chunk's rows stored)."""
+        kb.paged_prefill_attention(self.pool, layer, q, self.table, self.table_mode, context_lens, window, scale,
+                                   out, q_lens=q_lens, table_rows=table_rows, sinks=sinks)
+
+    def prefill_step(self, rids, q, k, v, out, window, scale, sinks=0):
+        """One chunked-prefill step for ``rids``, all layers: append each
+        request's C new tokens (host bookkeeping, table writes, copy-on-write),
+        store their K/V and attend them at once. ``q``/``out`` [layers][B, C,
+        Hq, D], ``k``/``v`` [layers][B * C, Hkv, D] (request-major), on the host
+        (pinned) or the device; returns when ``out`` holds the results."""
+        self._multi_step("prefill", rids, q, k, v, out, window, scale, sinks)
+
     def verify_step(self, rids, q, k, v, out, window, scale, sinks=0):
         """One speculative-decoding verify step for requests ``rids`` (ids =
         table rows), all layers: append the M drafted tokens of each request
@@ -180,6 +194,9 @@ class PagedKVCache:
         [layers][B * M, Hkv, D] (request-major) on the host (pinned) or the
         device. Returns when ``out`` holds the results; the caller then
         rewinds the rejected drafts with :meth:`rewind`."""
+        self._multi_step("verify", rids, q, k, v, out, window, scale, sinks)
+
+    def _multi_step(self, kind, rids, q, k, v, out, window, scale, sinks):
         B, M = q[0].shape[0], q[0].shape[1]
         rr = [int(r) for r in rids for _ in range(M)]
         ctx = [int(self.lengths[r]) + M for r in rids]
@@ -193,7 +210,10 @@ class PagedKVCache:
                 self.h2d_bytes += sum(x[layer].numel() * x[layer].element_size() for x in (q, k, v))
             self.store(layer, kd, vd, out_loc)
             od = torch.empty_like(qd) if host_out else out[layer]
-            self.verify(layer, qd, lens, window, scale, od, table_rows=rows, sinks=sinks)
+            if kind == "verify":
+                self.verify(layer, qd, lens, window, scale, od, table_rows=rows, sinks=sinks)
+            else:
+                self.prefill(layer, qd, lens, window, scale, od, table_rows=rows, sinks=sinks)
             if host_out:
                 out[layer].copy_(od, non_blocking=True)
         torch.cuda.current_stream(self.dev).synchronize()

@@ -184,6 +184,20 @@ def gqa_verify(seed: int = 0, M: int = 4) -> Workload:
                     list(w.lengths), scale=w.scale, extra={"verify": M})
 
 
+def gqa_prefill(seed: int = 0, chunk: int = 512) -> Workload:
+    """Chunked prefill with gqa_decode's heads: bf16, 32 q / 8 kv heads,
+    head_dim 128, page 16, 16 requests with a prefix uniform in [0, 2048];
+    every step appends a chunk of ``chunk`` tokens per request, stores it and
+    attends it at once (causal). The pool holds 72 chunks of growth."""
+    P, B = 16, 16
+    rs = np.random.RandomState(seed * 7919 + 12)
+    lengths = rs.randint(0, 2048 + 1, size=B).tolist()
+    n_pages = sum(-(-(L + 72 * chunk) // P) for L in lengths) + B
+    order = np.random.RandomState(seed * 7919 + 13).permutation(n_pages)
+    return Workload(f"gqa_prefill{chunk}", "bf16", 32, 8, 128, P, 1, n_pages, free_stack_for_order(order), lengths,
+                    scale=1.0 / math.sqrt(128), extra={"prefill": chunk})
+
+
 def accepted_drafts(seed: int, step: int, B: int, M: int) -> list:
     """Drafts accepted per request at a verify step: uniform in [0, M]."""
     return np.random.RandomState(seed * 7919 + 1000 + step).randint(0, M + 1, size=B).tolist()
