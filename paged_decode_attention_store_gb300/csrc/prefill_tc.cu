@@ -24,9 +24,11 @@
 //   rescaled (read, scaled, written back in TMEM) only when the row maximum
 //   grows by more than 8, so P = 2^(x - m) <= 256 always fits bf16 and the
 //   normalisation stays exact (numerator and denominator use the same m).
-// * P (bf16, K-major, 128-byte swizzle) goes to shared memory and
-//   O += P V (V as the MN-major operand) accumulates in TMEM columns
-//   128-255. The epilogue divides by the row sum and stores bf16.
+// * P (bf16, K-major, 128-byte swizzle) goes to shared memory, in K's
+//   place, and O += P V (V as the MN-major operand) accumulates in TMEM
+//   columns 128-255. The epilogue divides by the row sum and stores bf16.
+// * 97 KB of shared memory and 256 TMEM columns per CTA: two CTAs share an
+//   SM, so one's loads and softmax overlap the other's MMAs.
 // * Every wait is bounded (2 s): on timeout the CTA records KVP_ERR_TIMEOUT,
 //   issues nothing more, waits (bounded) for what it issued and frees TMEM.
 #include <cudaTypedefs.h>
@@ -127,7 +129,7 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
 // Byte offset of 16-byte chunk c (0..7) of row r in a 128-byte-swizzled operand half.
 __device__ __forceinline__ uint32_t sw128(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
 
-__global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_constant__ PrefillArgs a) {
+__global__ void __launch_bounds__(kPThreads, 2) prefill_tc_kernel(const __grid_constant__ PrefillArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ uint64_t bar_q, bar_kv, bar_mma;
   __shared__ uint32_t s_taddr;
@@ -136,7 +138,9 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_c
   unsigned char* sQ = smem;              // [2 halves][128 rows][128 B]
   unsigned char* sK = smem + 2 * kHalf;  // [2 halves][128 keys][128 B]
   unsigned char* sV = smem + 4 * kHalf;
-  unsigned char* sP = smem + 6 * kHalf;  // [2 key halves][128 rows][128 B]
+  // P [2 key halves][128 rows][128 B] takes K's place once S = Q K^T is done
+  // with it, so that a CTA needs 97 KB and two fit on an SM
+  unsigned char* sP = sK;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   volatile int* abort_flag = &s_abort;
 
@@ -382,7 +386,7 @@ bool encode_qmap(const void* q, int B, int C, int Hq, int G, CUtensorMap* out) {
 
 }  // namespace
 
-constexpr size_t kPrefillSmem = 8 * kHalf + 1024;
+constexpr size_t kPrefillSmem = 6 * kHalf + 1024;
 
 bool prefill_tc_eligible(const kvp_pool* pool, int Hq, int C) {
   if (pool->dtype != KVP_BF16 || pool->head_dim != kPD || Hq % pool->kv_heads) return false;
