@@ -425,7 +425,7 @@ extern "C" int paged_prefill_attention(const kvp_pool* pool, int layer, const vo
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   const TableRef T = make_table(pool, table, table_rows_total, table_cols, table_mode);
   kvp_pool* mp = const_cast<kvp_pool*>(pool);
-  if (prefill_tc_eligible(pool, num_q_heads, chunk)) {
+  if (prefill_tc_eligible(pool, num_q_heads, chunk, scale)) {
     if (mp->ev_before && cudaEventRecord(static_cast<cudaEvent_t>(mp->ev_before), st) != cudaSuccess)
       return KVP_ERR_CUDA;
     const int rc = launch_prefill_tc(pool, layer, q, batch, chunk, num_q_heads, q_lens, T, table_rows, context_lens,

@@ -148,7 +148,7 @@ bool tc_encode_tmap(const kvp_pool* pool, int HG, CUtensorMap* out);
 int tc_max_batch(int HG, int S);
 // Chunked prefill on tcgen05 (prefill_tc.cu): whether a pool and query-head
 // count take it, and its launch over batch requests of up to C new tokens.
-bool prefill_tc_eligible(const kvp_pool* pool, int Hq, int C);
+bool prefill_tc_eligible(const kvp_pool* pool, int Hq, int C, float scale);
 int launch_prefill_tc(const kvp_pool* pool, int layer, const void* q, int batch, int C, int Hq, const int32_t* q_lens,
                       const TableRef& T, const int32_t* table_rows, const int32_t* context_lens, int window, int sinks,
                       float scale, void* out, cudaStream_t stream);

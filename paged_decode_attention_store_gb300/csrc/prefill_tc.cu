@@ -9,7 +9,7 @@
 // attends (causal, the same window and sinks; chapter 15, "The model", and
 // its exercise "Attention sinks"), reading K/V in place through the table.
 //
-// How (one CTA of four warps per 128-row query tile):
+// How (one CTA of six warps per 128-row query tile):
 // * A tile is 128 / G consecutive query tokens of one request times the G
 //   query heads of one KV head: 128 rows of Q, loaded once by TMA (128-byte
 //   swizzle, two 64-element halves of head_dim).
@@ -18,17 +18,24 @@
 //   comes by TMA (K and V, two halves each), any other key row is copied by
 //   its thread into the same swizzled layout.
 // * S = Q K^T (M 128, N 128, K 128: eight kind::f16 MMAs, both operands
-//   K-major) accumulates in TMEM columns 0-127. Each thread owns one query
-//   row: it reads its 128 scores from TMEM, masks them (causal, window,
-//   sinks, block end), and keeps an online softmax in log2 units. O is
-//   rescaled (read, scaled, written back in TMEM) only when the row maximum
-//   grows by more than 8, so P = 2^(x - m) <= 256 always fits bf16 and the
-//   normalisation stays exact (numerator and denominator use the same m).
-// * P (bf16, K-major, 128-byte swizzle) goes to shared memory, in K's
-//   place, and O += P V (V as the MN-major operand) accumulates in TMEM
-//   columns 128-255. The epilogue divides by the row sum and stores bf16.
-// * 97 KB of shared memory and 256 TMEM columns per CTA: two CTAs share an
-//   SM, so one's loads and softmax overlap the other's MMAs.
+//   K-major) accumulates in a TMEM S buffer. Each thread owns one query row:
+//   it reads its 128 scores from TMEM and keeps an online softmax in log2
+//   units. A block that no row of the warp masks (causal, window, sinks,
+//   block end) skips the mask; the row maximum is taken on unscaled scores
+//   and P = 2^(s * scale - m) is one FMA and one ex2 per score. O is rescaled
+//   (read, scaled, written back in TMEM) only when the row maximum grows by
+//   more than 8, so P <= 256 always fits bf16 and the normalisation stays
+//   exact (numerator and denominator use the same m).
+// * P (bf16, K-major, 128-byte swizzle) goes to shared memory and
+//   O += P V (V as the MN-major operand) accumulates in TMEM. The epilogue
+//   divides by the row sum and stores bf16.
+// * Warp-specialised pipeline: a loader warp fills two-stage K and V rings,
+//   K one block ahead of V (K stage s is free once S has read it, V stage s
+//   once P V has), with the table lookups of a block done before its waits;
+//   an MMA warp issues S(i) into one of two TMEM S buffers and then
+//   O += P(i-1) V(i-1); four softmax warps turn S(i) into P(i) (two P
+//   buffers). The tensor core computes the next block's S while the softmax
+//   works on this one. mbarriers carry every hand-off.
 // * Every wait is bounded (2 s): on timeout the CTA records KVP_ERR_TIMEOUT,
 //   issues nothing more, waits (bounded) for what it issued and frees TMEM.
 #include <cudaTypedefs.h>
@@ -42,7 +49,7 @@ namespace {
 constexpr int kPM = 128;  // query rows per tile
 constexpr int kPN = 128;  // keys per block
 constexpr int kPD = 128;  // head_dim
-constexpr int kPThreads = 128;
+constexpr int kPThreads = 192;  // warps: loader, MMA, four softmax
 constexpr uint32_t kHalf = 16384;  // one 64-element half of a 128-row operand: 128 rows x 128 B
 constexpr uint64_t kPWaitNs = 2000000000ull;
 
@@ -126,23 +133,81 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
       : "memory");
 }
 
+// 2^x by the PTX approximate base-2 exponential (flush-to-zero; 2^-inf = +0).
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Byte offset of 16-byte chunk c (0..7) of row r in a 128-byte-swizzled operand half.
 __device__ __forceinline__ uint32_t sw128(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
 
-__global__ void __launch_bounds__(kPThreads, 2) prefill_tc_kernel(const __grid_constant__ PrefillArgs a) {
+// Barriers and flags of one CTA (static shared memory).
+struct PrefillBars {
+  uint64_t q_full;
+  uint64_t k_full[2];   // loader -> MMA: K block in K stage s (TMA bytes and thread copies)
+  uint64_t v_full[2];   // loader -> MMA: V block in V stage s
+  uint64_t s_full[2];   // MMA -> softmax: S = Q K^T of the block in TMEM buffer s
+  uint64_t s_empty[2];  // softmax (4 warps) -> MMA: S buffer s read
+  uint64_t p_full[2];   // softmax (4 warps) -> MMA: P of the block in buffer s
+  uint64_t pv_done[2];  // MMA -> all: O += P V of the block in stage s done (V stage and P buffer free)
+  uint64_t drain;       // MMA -> all: everything it issued is done
+  uint32_t taddr;
+  int abort;
+  int slots[2][kPN];    // the loader's slots of the blocks in stage s
+};
+
+// Wait for phase ``k`` of ``bar`` (parity k & 1), bounded.
+__device__ __forceinline__ bool pwait(uint64_t* bar, int k, volatile int* abort_flag, int32_t* err) {
+  return mbar_wait_bounded(bar, (uint32_t)(k & 1), abort_flag, err, kPWaitNs);
+}
+
+// The loader warp fills one 128-key operand (K, or V when ``is_v``, of head
+// group g) from ``slots``: 16-slot groups flagged in ``tm`` by one TMA
+// copy per 64-column half, the others by plain 16-byte copies (zeros for slots
+// < 0); ``bar`` (count 1) gets the arrival and the TMA byte count.
+__device__ __forceinline__ void load_rows(const PrefillArgs& a, unsigned char* dst, const int* slots, unsigned tm,
+                                          int g, bool is_v, uint64_t* bar, int lane) {
+  const size_t base = is_v ? a.kv_bytes : 0;
+  const int kvl = is_v ? a.kvl_v : a.kvl_k;
+  for (int gi = 0; gi < 8; ++gi) {
+    if ((tm >> gi) & 1) continue;
+    for (int x = lane; x < 16 * 16; x += 32) {
+      const int key = 16 * gi + x / 16, c = x % 16;
+      const int sl = slots[key];
+      uint4 val = make_uint4(0u, 0u, 0u, 0u);
+      if (sl >= 0)
+        val = __ldg(reinterpret_cast<const uint4*>(a.kv_layer + base + (size_t)sl * a.row_bytes +
+                                                   (size_t)g * kPD * 2) + c);
+      *reinterpret_cast<uint4*>(dst + (c >> 3) * kHalf + sw128(key, c & 7)) = val;
+    }
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)__popc(tm) * 2u * 2048u);
+  __syncwarp();
+  if (lane < 8 && ((tm >> lane) & 1)) {
+    const int s0 = slots[16 * lane];
+    const uint32_t off = (uint32_t)lane * 16u * 128u;
+    tma_load_4d(dst + off, &a.kvmap, 0, s0, g, kvl, bar);
+    tma_load_4d(dst + kHalf + off, &a.kvmap, 64, s0, g, kvl, bar);
+  }
+  __syncwarp();
+}
+
+// Warp roles: 0 loads (Q once, then K and V blocks into two-stage rings),
+// 1 issues the MMAs (lane 0), 2..5 run the softmax, one query row per
+// thread (TMEM lane quadrant = warp % 4), and the epilogue.
+__global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_constant__ PrefillArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  __shared__ uint64_t bar_q, bar_kv, bar_mma;
-  __shared__ uint32_t s_taddr;
-  __shared__ int s_abort;
+  __shared__ PrefillBars sb;
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  unsigned char* sQ = smem;              // [2 halves][128 rows][128 B]
-  unsigned char* sK = smem + 2 * kHalf;  // [2 halves][128 keys][128 B]
-  unsigned char* sV = smem + 4 * kHalf;
-  // P [2 key halves][128 rows][128 B] takes K's place once S = Q K^T is done
-  // with it, so that a CTA needs 97 KB and two fit on an SM
-  unsigned char* sP = sK;
+  unsigned char* sQ = smem;                          // [2 halves][128 rows][128 B]
+  unsigned char* sKV = smem + 2 * kHalf;             // K stage s at s * 2 kHalf, V stage s at (4 + 2 s) kHalf
+  unsigned char* sPb = smem + 10 * kHalf;            // P buffer s at s * 2 kHalf
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  volatile int* abort_flag = &s_abort;
+  volatile int* abort_flag = &sb.abort;
 
   // Tile order: the last tiles of the requests (the most keys) first.
   const int per_tile = a.B * a.Hkv;
@@ -154,11 +219,13 @@ __global__ void __launch_bounds__(kPThreads, 2) prefill_tc_kernel(const __grid_c
   const int ql = a.q_lens ? a.q_lens[b] : a.C;
   const int row = a.table_rows ? a.table_rows[b] : b;
   const bool valid = ql >= 1 && ql <= a.C && ql <= L && L <= table_capacity(a.T) && row >= 0 && row < a.T.rows_total;
-  const int rt = tid / a.G, hh = tid % a.G;  // this thread's query row: token j0 + rt, head hh of the group
+  // softmax threads: query row r = 32 * (warp % 4) + lane: token j0 + r / G, head r % G of the group
+  const int r = 32 * (warp & 3) + lane;
+  const int rt = r / a.G, hh = r % a.G;
   __nv_bfloat16* orow = a.out + (((size_t)b * a.C + j0 + rt) * a.Hq + (size_t)g * a.G + hh) * kPD;
   if (!valid) {
     if (tid == 0 && g == 0 && tile == 0) set_error(a.err, KVP_ERR_BAD_INDEX);
-    if (j0 + rt < a.C)
+    if (warp >= 2 && j0 + rt < a.C)
       for (int d = 0; d < kPD; d += 8) *reinterpret_cast<uint4*>(orow + d) = make_uint4(0u, 0u, 0u, 0u);
     return;
   }
@@ -169,197 +236,248 @@ __global__ void __launch_bounds__(kPThreads, 2) prefill_tc_kernel(const __grid_c
   const Span u = attend_span(p_last + 1, a.window > 0 ? a.window + (p_last - p_first) : 0, a.sinks);
   const int n_keys = u.se + (p_last + 1 - u.lo);
   const int nblk = (n_keys + kPN - 1) / kPN;
-  const bool rv = rt < jn;
-  const int pr = p_first + rt;
-  const Span sr = attend_span(pr + 1, a.window, a.sinks);
 
   if (tid == 0) {
-    mbar_init(&bar_q, 1);
-    mbar_init(&bar_kv, 1);
-    mbar_init(&bar_mma, 1);
-    s_abort = 0;
+    mbar_init(&sb.q_full, 1);
+    for (int s2 = 0; s2 < 2; ++s2) {
+      mbar_init(&sb.k_full[s2], 1);
+      mbar_init(&sb.v_full[s2], 1);
+      mbar_init(&sb.s_full[s2], 1);
+      mbar_init(&sb.s_empty[s2], 4);
+      mbar_init(&sb.p_full[s2], 4);
+      mbar_init(&sb.pv_done[s2], 1);
+    }
+    mbar_init(&sb.drain, 1);
+    sb.abort = 0;
     fence_mbar_init();
   }
   if (warp == 0) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 256;" ::"r"(smem_u32(&s_taddr))
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(&sb.taddr))
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tS = s_taddr, tO = s_taddr + 128;
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;  // this warp's 32 TMEM lanes = its 32 query rows
+  const uint32_t tS0 = sb.taddr, tO = sb.taddr + 256;  // S buffers at columns 0 and 128, O at 256
 
-  if (tid == 0) {
-    mbar_arrive_expect_tx(&bar_q, 2 * kHalf);
-    tma_load_4d(sQ, &a.qmap, 0, g * a.G, j0, b, &bar_q);
-    tma_load_4d(sQ + kHalf, &a.qmap, 64, g * a.G, j0, b, &bar_q);
-  }
-
-  const uint32_t qa = smem_u32(sQ), ka = smem_u32(sK), va = smem_u32(sV), pa = smem_u32(sP);
-  const uint32_t id_s = umma_idesc(0), id_o = umma_idesc(1);
-  float m_used = -INFINITY, lsum = 0.f;
-  uint32_t ph_mma = 0;
-  bool issued_unwaited = false;
-
-  for (int blk = 0; blk < nblk; ++blk) {
-    // ---- keys o0 .. o0 + 127: one per thread -------------------------------
-    const int o0 = blk * kPN, o = o0 + tid;
-    const int slot = o < n_keys ? resolve_slot(a.T, row, span_pos(u, o), a.err) : -1;
-    const int slot0 = __shfl_sync(0xffffffffu, slot, lane & 16);
-    const unsigned okm = __ballot_sync(0xffffffffu, slot >= 0 && slot == slot0 + (lane & 15));
-    const unsigned halfm = (lane & 16) ? 0xffff0000u : 0x0000ffffu;
-    const bool grp_tma = a.use_kvmap && slot0 >= 0 && (slot0 & 15) == 0 && (okm & halfm) == halfm;
-    const int n_tma = __syncthreads_count(grp_tma && (lane & 15) == 0);
-    if (tid == 0) mbar_arrive_expect_tx(&bar_kv, (uint32_t)n_tma * 4u * 2048u);
-    __syncthreads();
-    if (grp_tma && (lane & 15) == 0) {
-      const uint32_t off = (uint32_t)(tid >> 4) * 16u * 128u;  // the group's 16 key rows
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        tma_load_4d(sK + h * kHalf + off, &a.kvmap, h * 64, slot0, g, a.kvl_k, &bar_kv);
-        tma_load_4d(sV + h * kHalf + off, &a.kvmap, h * 64, slot0, g, a.kvl_v, &bar_kv);
-      }
+  if (warp == 0) {
+    // ======================= loader ===========================================
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&sb.q_full, 2 * kHalf);
+      tma_load_4d(sQ, &a.qmap, 0, g * a.G, j0, b, &sb.q_full);
+      tma_load_4d(sQ + kHalf, &a.qmap, 64, g * a.G, j0, b, &sb.q_full);
     }
-    if (!grp_tma) {  // this key's rows by plain loads, into the same swizzled places (zeros past the end)
-      const uint4* ks = slot >= 0 ? reinterpret_cast<const uint4*>(a.kv_layer + (size_t)slot * a.row_bytes +
-                                                                   (size_t)g * kPD * 2)
-                                  : nullptr;
-      const uint4* vs = slot >= 0 ? reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(ks) + a.kv_bytes)
-                                  : nullptr;
+    // Iteration i resolves block i's slots, loads K(i) once S(i - 2) has read
+    // K stage i % 2, then V(i - 1) once P V(i - 3) has read V stage (i - 1) % 2:
+    // K runs a block ahead of V, so the S of the next block never waits on P V.
+    unsigned tm_prev = 0;  // TMA groups of block i - 1
+    for (int i = 0; i <= nblk; ++i) {
+      unsigned tm = 0;
+      if (i < nblk) {
+        const int st = i & 1;
+        const int o0 = i * kPN;
+        // lane l resolves keys 4l .. 4l+3 (four independent table reads); group
+        // gi (lanes 4gi .. 4gi+3) goes by one TMA copy when its 16 slots are
+        // contiguous and 16-aligned
+        int sl[4];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const uint4 kx = ks ? __ldg(ks + c) : make_uint4(0u, 0u, 0u, 0u);
-        const uint4 vx = vs ? __ldg(vs + c) : make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4*>(sK + (c >> 3) * kHalf + sw128(tid, c & 7)) = kx;
-        *reinterpret_cast<uint4*>(sV + (c >> 3) * kHalf + sw128(tid, c & 7)) = vx;
+        for (int k = 0; k < 4; ++k) {
+          const int o = o0 + 4 * lane + k;
+          sl[k] = o < n_keys ? resolve_slot(a.T, row, span_pos(u, o), a.err) : -1;
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) sb.slots[st][4 * lane + k] = sl[k];
+        const int g0 = __shfl_sync(0xffffffffu, sl[0], lane & ~3);
+        const bool mine = a.use_kvmap && sl[0] >= 0 && sl[1] == sl[0] + 1 && sl[2] == sl[0] + 2 &&
+                          sl[3] == sl[0] + 3 && sl[0] == g0 + 4 * (lane & 3) && (g0 & 15) == 0;
+        const unsigned okb = __ballot_sync(0xffffffffu, mine);
+#pragma unroll
+        for (int gi = 0; gi < 8; ++gi)
+          if (((okb >> (4 * gi)) & 0xFu) == 0xFu) tm |= 1u << gi;
+        __syncwarp();
+        if (i >= 2 && !__all_sync(0xffffffffu, pwait(&sb.s_full[st], (i - 2) >> 1, abort_flag, a.err))) break;
+        load_rows(a, sKV + st * 2 * kHalf, sb.slots[st], tm, g, false, &sb.k_full[st], lane);
+      }
+      if (i >= 1) {
+        const int k = i - 1, st = k & 1;
+        if (k >= 2 && !__all_sync(0xffffffffu, pwait(&sb.pv_done[st], (k - 2) >> 1, abort_flag, a.err))) break;
+        load_rows(a, sKV + (4 + st * 2) * kHalf, sb.slots[st], tm_prev, g, true, &sb.v_full[st], lane);
+      }
+      tm_prev = tm;
+    }
+  } else if (warp == 1) {
+    // ======================= MMA issuer =======================================
+    // The whole warp walks the schedule and waits (no divergent spin beside the
+    // issuing lane); lane 0 alone issues the MMAs and the commits.
+    {
+      const bool issuer = lane == 0;
+      const uint32_t qa = smem_u32(sQ);
+      const uint32_t id_s = umma_idesc(0), id_o = umma_idesc(1);
+      bool ok = __all_sync(0xffffffffu, pwait(&sb.q_full, 0, abort_flag, a.err));
+      for (int i = 0; ok && i <= nblk; ++i) {
+        if (i < nblk) {  // S(i) = Q K(i)^T into S buffer i % 2
+          const int st = i & 1;
+          ok = __all_sync(0xffffffffu, pwait(&sb.k_full[st], i >> 1, abort_flag, a.err));
+          if (ok && i >= 2) ok = __all_sync(0xffffffffu, pwait(&sb.s_empty[st], (i - 2) >> 1, abort_flag, a.err));
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t ka = smem_u32(sKV + st * 2 * kHalf);
+#pragma unroll
+          for (int ks = 0; ks < 8 && issuer; ++ks) {
+            const uint32_t koff = (uint32_t)(ks >> 2) * kHalf + (uint32_t)(ks & 3) * 32u;
+            umma_f16(tS0 + (uint32_t)st * 128u, umma_desc(qa + koff, 16, 1024), umma_desc(ka + koff, 16, 1024), id_s,
+                     ks > 0);
+          }
+          if (issuer) umma_commit(&sb.s_full[st]);
+          __syncwarp();
+        }
+        if (i >= 1) {  // O += P(i-1) V(i-1)
+          const int k = i - 1, st = k & 1;
+          ok = __all_sync(0xffffffffu, pwait(&sb.p_full[st], k >> 1, abort_flag, a.err));
+          if (ok) ok = __all_sync(0xffffffffu, pwait(&sb.v_full[st], k >> 1, abort_flag, a.err));
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t pa = smem_u32(sPb + st * 2 * kHalf), va = smem_u32(sKV + (4 + st * 2) * kHalf);
+#pragma unroll
+          for (int ks = 0; ks < 8 && issuer; ++ks) {
+            const uint32_t poff = (uint32_t)(ks >> 2) * kHalf + (uint32_t)(ks & 3) * 32u;
+            umma_f16(tO, umma_desc(pa + poff, 16, 1024), umma_desc(va + (uint32_t)ks * 2048u, kHalf, 1024), id_o,
+                     (k > 0 || ks > 0) ? 1u : 0u);
+          }
+          if (issuer) umma_commit(&sb.pv_done[st]);
+          __syncwarp();
+        }
+      }
+      if (issuer) umma_commit(&sb.drain);  // arrives once everything issued above is done
+      __syncwarp();
+    }
+  } else {
+    // ======================= softmax warps =====================================
+    const bool rv = rt < jn;
+    const int pr = p_first + rt;
+    const Span sr0 = attend_span(pr + 1, a.window, a.sinks);
+    // In key offsets of the chunk's span u: the row's sink rows are offsets
+    // [0, sr.se) (when u keeps a sink segment its width is the row's; when it
+    // does not, u starts at position 0 and offsets are positions), and its
+    // window [sr.lo, pr] starts at or after u.lo. Rows past the chunk keep nothing.
+    const Span sr = rv ? sr0 : Span{0, 0};
+    const int wb0 = rv ? u.se + (sr.lo - u.lo) : 1 << 30, we0 = rv ? u.se + (pr - u.lo) : -1;
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    const float sl2 = a.scale_log2;
+    float m_used = -INFINITY, lsum = 0.f;  // m in scaled log2 units
+    bool ok = true;
+    for (int i = 0; i < nblk; ++i) {
+      const int st = i & 1;
+      ok = __all_sync(0xffffffffu, pwait(&sb.s_full[st], i >> 1, abort_flag, a.err));
+      if (!ok) break;
+      tc_fence_after();
+      float sv[kPN];
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) tmem_ld32(tS0 + (uint32_t)st * 128u + lane_base + c4 * 32, sv + c4 * 32);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sb.s_empty[st]);
+      // The row attends key offsets [0, ea) (its sink rows) and [wb, we] (its
+      // window), relative to this block's first offset.
+      const int o0 = i * kPN;
+      // The maximum is taken on unscaled scores (scale > 0) and scaled once.
+      const int ea = sr.se - o0, wb = wb0 - o0, we = we0 - o0;
+      float rmax = -INFINITY;
+      if (__all_sync(0xffffffffu, wb <= 0 && we >= kPN - 1)) {  // no row of the warp masks in this block
+#pragma unroll
+        for (int c = 0; c < kPN; ++c) rmax = fmaxf(rmax, sv[c]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < kPN; ++c) {
+          const bool keep = c < ea || (c >= wb && c <= we);
+          sv[c] = keep ? sv[c] : -INFINITY;
+          rmax = fmaxf(rmax, sv[c]);
+        }
+      }
+      rmax *= sl2;
+      const bool grow = rmax > m_used + 8.f;  // also when nothing was kept before
+      const bool scale_o = grow && lsum > 0.f;
+      const float f = scale_o ? exp2f(m_used - rmax) : 1.f;
+      if (grow) m_used = rmax;
+      const float msub = m_used == -INFINITY ? 0.f : m_used;  // masked scores give 2^-inf = 0 either way
+      // P buffer st is free once the P V of block i - 2 is done
+      if (i >= 2) {
+        ok = __all_sync(0xffffffffu, pwait(&sb.pv_done[st], (i - 2) >> 1, abort_flag, a.err));
+        if (!ok) break;
+      }
+      unsigned char* sP = sPb + st * 2 * kHalf;
+      float psum = 0.f;
+#pragma unroll
+      for (int c8 = 0; c8 < kPN / 8; ++c8) {
+        uint32_t w[4];
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          const float x0 = sv[c8 * 8 + 2 * x], x1 = sv[c8 * 8 + 2 * x + 1];
+          const float p0 = ex2_ftz(fmaf(x0, sl2, -msub));
+          const float p1 = ex2_ftz(fmaf(x1, sl2, -msub));
+          w[x] = pack_bf16(p0, p1);
+          psum += bf16_lo(w[x]) + bf16_hi(w[x]);
+        }
+        *reinterpret_cast<uint4*>(sP + (c8 >> 3) * kHalf + sw128(r, c8 & 7)) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      lsum = lsum * f + psum;
+      if (__any_sync(0xffffffffu, scale_o)) {
+        // O holds blocks < i in the old maximum: rescale it once P V(i - 1) is
+        // in, before P V(i) may start (a warp-wide TMEM read and write)
+        ok = __all_sync(0xffffffffu, pwait(&sb.pv_done[(i - 1) & 1], (i - 1) >> 1, abort_flag, a.err));
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          float ov[32];
+          tmem_ld32(tO + lane_base + c4 * 32, ov);
+#pragma unroll
+          for (int x = 0; x < 32; ++x) ov[x] *= f;
+          tmem_st32(tO + lane_base + c4 * 32, ov);
+        }
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       }
       fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sb.p_full[st]);
     }
-    __syncthreads();
-    bool okw = mbar_wait_bounded(&bar_kv, (uint32_t)(blk & 1), abort_flag, a.err, kPWaitNs);
-    if (blk == 0) okw = okw && mbar_wait_bounded(&bar_q, 0u, abort_flag, a.err, kPWaitNs);
-    if (!okw) *abort_flag = 1;
-    __syncthreads();
-    if (*abort_flag) break;
-
-    // ---- S = Q K^T ---------------------------------------------------------
-    tc_fence_after();
-    if (tid == 0) {
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t koff = (uint32_t)(ks >> 2) * kHalf + (uint32_t)(ks & 3) * 32u;
-        umma_f16(tS, umma_desc(qa + koff, 16, 1024), umma_desc(ka + koff, 16, 1024), id_s, ks > 0);
-      }
-      umma_commit(&bar_mma);
-    }
-    issued_unwaited = true;
-    if (!mbar_wait_bounded(&bar_mma, ph_mma & 1, abort_flag, a.err, kPWaitNs)) *abort_flag = 1;
-    __syncthreads();
-    if (*abort_flag) break;
-    ++ph_mma;
-    issued_unwaited = false;
-    tc_fence_after();
-
-    // ---- online softmax of this thread's row ------------------------------
-    float s[kPN];
-#pragma unroll
-    for (int c4 = 0; c4 < 4; ++c4) tmem_ld32(tS + lane_base + c4 * 32, s + c4 * 32);
-    float rmax = -INFINITY;
-#pragma unroll
-    for (int c = 0; c < kPN; ++c) {
-      const int oc = o0 + c;
-      bool keep = rv && oc < n_keys;
-      if (keep) {
-        const int t = span_pos(u, oc);
-        keep = t <= pr && (t >= sr.lo || t < sr.se);
-      }
-      s[c] = keep ? s[c] * a.scale_log2 : -INFINITY;
-      rmax = fmaxf(rmax, s[c]);
-    }
-    const bool grow = rmax > m_used + 8.f;  // also when nothing was kept before
-    if (__any_sync(0xffffffffu, grow && lsum > 0.f)) {  // rescale O (a warp-wide TMEM read and write)
-      const float f = (grow && lsum > 0.f) ? exp2f(m_used - rmax) : 1.f;
+    // ---- epilogue: O / l -> bf16, once the last P V is in O ------------------
+    if (ok) ok = __all_sync(0xffffffffu, pwait(&sb.pv_done[(nblk - 1) & 1], (nblk - 1) >> 1, abort_flag, a.err));
+    if (ok) {
+      tc_fence_after();
+      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
 #pragma unroll
       for (int c4 = 0; c4 < 4; ++c4) {
         float ov[32];
         tmem_ld32(tO + lane_base + c4 * 32, ov);
+        if (rv) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) ov[i] *= f;
-        tmem_st32(tO + lane_base + c4 * 32, ov);
-      }
-      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-      lsum *= f;
-    }
-    if (grow) m_used = rmax;
-    float psum = 0.f;
-#pragma unroll
-    for (int c8 = 0; c8 < kPN / 8; ++c8) {
-      uint32_t w[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float x0 = s[c8 * 8 + 2 * i], x1 = s[c8 * 8 + 2 * i + 1];
-        const float p0 = m_used == -INFINITY ? 0.f : exp2f(x0 - m_used);
-        const float p1 = m_used == -INFINITY ? 0.f : exp2f(x1 - m_used);
-        w[i] = pack_bf16(p0, p1);
-        psum += bf16_lo(w[i]) + bf16_hi(w[i]);
-      }
-      *reinterpret_cast<uint4*>(sP + (c8 >> 3) * kHalf + sw128(tid, c8 & 7)) = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-    lsum += psum;
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-
-    // ---- O += P V ----------------------------------------------------------
-    if (tid == 0) {
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t poff = (uint32_t)(ks >> 2) * kHalf + (uint32_t)(ks & 3) * 32u;
-        umma_f16(tO, umma_desc(pa + poff, 16, 1024), umma_desc(va + (uint32_t)ks * 2048u, kHalf, 1024), id_o,
-                 (blk > 0 || ks > 0) ? 1u : 0u);
-      }
-      umma_commit(&bar_mma);
-    }
-    issued_unwaited = true;
-    if (!mbar_wait_bounded(&bar_mma, ph_mma & 1, abort_flag, a.err, kPWaitNs)) *abort_flag = 1;
-    __syncthreads();
-    if (*abort_flag) break;
-    ++ph_mma;
-    issued_unwaited = false;
-    tc_fence_after();
-  }
-
-  if (!*abort_flag) {
-    // ---- epilogue: O / l -> bf16 -------------------------------------------
-    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-#pragma unroll
-    for (int c4 = 0; c4 < 4; ++c4) {
-      float ov[32];
-      tmem_ld32(tO + lane_base + c4 * 32, ov);
-      if (rv) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint4 w;
-          w.x = pack_bf16(ov[8 * q + 0] * inv, ov[8 * q + 1] * inv);
-          w.y = pack_bf16(ov[8 * q + 2] * inv, ov[8 * q + 3] * inv);
-          w.z = pack_bf16(ov[8 * q + 4] * inv, ov[8 * q + 5] * inv);
-          w.w = pack_bf16(ov[8 * q + 6] * inv, ov[8 * q + 7] * inv);
-          *reinterpret_cast<uint4*>(orow + c4 * 32 + q * 8) = w;
+          for (int q = 0; q < 4; ++q) {
+            uint4 w;
+            w.x = pack_bf16(ov[8 * q + 0] * inv, ov[8 * q + 1] * inv);
+            w.y = pack_bf16(ov[8 * q + 2] * inv, ov[8 * q + 3] * inv);
+            w.z = pack_bf16(ov[8 * q + 4] * inv, ov[8 * q + 5] * inv);
+            w.w = pack_bf16(ov[8 * q + 6] * inv, ov[8 * q + 7] * inv);
+            *reinterpret_cast<uint4*>(orow + c4 * 32 + q * 8) = w;
+          }
         }
       }
     }
-  } else if (issued_unwaited) {
-    // let the MMAs in flight finish (bounded) before their TMEM goes back
+  }
+  // Everything the MMA lane issued is done (bounded) before TMEM goes back.
+  {
     const uint64_t t0 = global_timer_ns();
-    while (!mbar_try_wait(&bar_mma, ph_mma & 1))
-      if (global_timer_ns() - t0 > 100000000ull) break;
+    while (!mbar_try_wait(&sb.drain, 0u))
+      if (global_timer_ns() - t0 > 2 * kPWaitNs) {
+        set_error(a.err, KVP_ERR_TIMEOUT);
+        break;
+      }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 256;" ::"r"(tS) : "memory");
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tS0) : "memory");
 }
 
 bool encode_qmap(const void* q, int B, int C, int Hq, int G, CUtensorMap* out) {
@@ -386,10 +504,11 @@ bool encode_qmap(const void* q, int B, int C, int Hq, int G, CUtensorMap* out) {
 
 }  // namespace
 
-constexpr size_t kPrefillSmem = 6 * kHalf + 1024;
+constexpr size_t kPrefillSmem = 14 * kHalf + 1024;  // Q, two K/V stages, two P buffers
 
-bool prefill_tc_eligible(const kvp_pool* pool, int Hq, int C) {
-  if (pool->dtype != KVP_BF16 || pool->head_dim != kPD || Hq % pool->kv_heads) return false;
+bool prefill_tc_eligible(const kvp_pool* pool, int Hq, int C, float scale) {
+  // the row maximum is taken on unscaled scores, which needs scale > 0
+  if (!(scale > 0.f) || pool->dtype != KVP_BF16 || pool->head_dim != kPD || Hq % pool->kv_heads) return false;
   const int G = Hq / pool->kv_heads;
   return G >= 1 && G <= kPM && kPM % G == 0 && C >= 1;
 }
