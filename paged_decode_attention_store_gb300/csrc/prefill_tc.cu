@@ -29,9 +29,9 @@
 // * P (bf16, K-major, 128-byte swizzle) goes to shared memory and
 //   O += P V (V as the MN-major operand) accumulates in TMEM. The epilogue
 //   divides by the row sum and stores bf16.
-// * Warp-specialised pipeline: a loader warp fills two-stage K and V rings,
-//   K one block ahead of V (K stage s is free once S has read it, V stage s
-//   once P V has), with the table lookups of a block done before its waits;
+// * Warp-specialised pipeline: two loader warps fill two-stage K and V rings
+//   (K stage s is free once S has read it, V stage s once P V has), each
+//   resolving its own slots, so K never waits behind V;
 //   an MMA warp issues S(i) into one of two TMEM S buffers and then
 //   O += P(i-1) V(i-1); four softmax warps turn S(i) into P(i) (two P
 //   buffers). The tensor core computes the next block's S while the softmax
@@ -49,7 +49,8 @@ namespace {
 constexpr int kPM = 128;  // query rows per tile
 constexpr int kPN = 128;  // keys per block
 constexpr int kPD = 128;  // head_dim
-constexpr int kPThreads = 192;  // warps: loader, MMA, four softmax
+constexpr int kPThreads = 224;  // warps: K loader, MMA, four softmax, V loader
+constexpr int kVWarp = 6;
 constexpr uint32_t kHalf = 16384;  // one 64-element half of a 128-row operand: 128 rows x 128 B
 constexpr uint64_t kPWaitNs = 2000000000ull;
 
@@ -155,7 +156,7 @@ struct PrefillBars {
   uint64_t drain;       // MMA -> all: everything it issued is done
   uint32_t taddr;
   int abort;
-  int slots[2][kPN];    // the loader's slots of the blocks in stage s
+  int slots[2][kPN];    // the K and the V loader's slots of the block being loaded
 };
 
 // Wait for phase ``k`` of ``bar`` (parity k & 1), bounded.
@@ -196,9 +197,9 @@ __device__ __forceinline__ void load_rows(const PrefillArgs& a, unsigned char* d
   __syncwarp();
 }
 
-// Warp roles: 0 loads (Q once, then K and V blocks into two-stage rings),
-// 1 issues the MMAs (lane 0), 2..5 run the softmax, one query row per
-// thread (TMEM lane quadrant = warp % 4), and the epilogue.
+// Warp roles: 0 loads Q once, then K blocks into a two-stage ring; 6 loads
+// V blocks into theirs; 1 issues the MMAs (lane 0); 2..5 run the softmax,
+// one query row per thread (TMEM lane quadrant = warp % 4), and the epilogue.
 __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_constant__ PrefillArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ PrefillBars sb;
@@ -225,7 +226,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_c
   __nv_bfloat16* orow = a.out + (((size_t)b * a.C + j0 + rt) * a.Hq + (size_t)g * a.G + hh) * kPD;
   if (!valid) {
     if (tid == 0 && g == 0 && tile == 0) set_error(a.err, KVP_ERR_BAD_INDEX);
-    if (warp >= 2 && j0 + rt < a.C)
+    if (warp >= 2 && warp < 6 && j0 + rt < a.C)
       for (int d = 0; d < kPD; d += 8) *reinterpret_cast<uint4*>(orow + d) = make_uint4(0u, 0u, 0u, 0u);
     return;
   }
@@ -261,50 +262,47 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_c
   tc_fence_after();
   const uint32_t tS0 = sb.taddr, tO = sb.taddr + 256;  // S buffers at columns 0 and 128, O at 256
 
-  if (warp == 0) {
-    // ======================= loader ===========================================
-    if (lane == 0) {
+  if (warp == 0 || warp == kVWarp) {
+    // ======================= loaders ==========================================
+    // Warp 0 loads Q, then K(i) once S(i - 2) has read K stage i % 2; warp
+    // kVWarp loads V(i) once P V(i - 2) has read V stage i % 2. Each resolves
+    // its own slots, so neither waits on the other's ring.
+    const bool is_v = warp == kVWarp;
+    if (!is_v && lane == 0) {
       mbar_arrive_expect_tx(&sb.q_full, 2 * kHalf);
       tma_load_4d(sQ, &a.qmap, 0, g * a.G, j0, b, &sb.q_full);
       tma_load_4d(sQ + kHalf, &a.qmap, 64, g * a.G, j0, b, &sb.q_full);
     }
-    // Iteration i resolves block i's slots, loads K(i) once S(i - 2) has read
-    // K stage i % 2, then V(i - 1) once P V(i - 3) has read V stage (i - 1) % 2:
-    // K runs a block ahead of V, so the S of the next block never waits on P V.
-    unsigned tm_prev = 0;  // TMA groups of block i - 1
-    for (int i = 0; i <= nblk; ++i) {
+    int* slots = sb.slots[is_v ? 1 : 0];
+    for (int i = 0; i < nblk; ++i) {
+      const int st = i & 1;
+      const int o0 = i * kPN;
+      // lane l resolves keys 4l .. 4l+3 (four independent table reads); group
+      // gi (lanes 4gi .. 4gi+3) goes by one TMA copy when its 16 slots are
+      // contiguous and 16-aligned
+      int sl[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int o = o0 + 4 * lane + k;
+        sl[k] = o < n_keys ? resolve_slot(a.T, row, span_pos(u, o), a.err) : -1;
+      }
+      __syncwarp();  // the previous block's copies have read the slot list
+#pragma unroll
+      for (int k = 0; k < 4; ++k) slots[4 * lane + k] = sl[k];
+      const int g0 = __shfl_sync(0xffffffffu, sl[0], lane & ~3);
+      const bool mine = a.use_kvmap && sl[0] >= 0 && sl[1] == sl[0] + 1 && sl[2] == sl[0] + 2 &&
+                        sl[3] == sl[0] + 3 && sl[0] == g0 + 4 * (lane & 3) && (g0 & 15) == 0;
+      const unsigned okb = __ballot_sync(0xffffffffu, mine);
       unsigned tm = 0;
-      if (i < nblk) {
-        const int st = i & 1;
-        const int o0 = i * kPN;
-        // lane l resolves keys 4l .. 4l+3 (four independent table reads); group
-        // gi (lanes 4gi .. 4gi+3) goes by one TMA copy when its 16 slots are
-        // contiguous and 16-aligned
-        int sl[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int o = o0 + 4 * lane + k;
-          sl[k] = o < n_keys ? resolve_slot(a.T, row, span_pos(u, o), a.err) : -1;
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) sb.slots[st][4 * lane + k] = sl[k];
-        const int g0 = __shfl_sync(0xffffffffu, sl[0], lane & ~3);
-        const bool mine = a.use_kvmap && sl[0] >= 0 && sl[1] == sl[0] + 1 && sl[2] == sl[0] + 2 &&
-                          sl[3] == sl[0] + 3 && sl[0] == g0 + 4 * (lane & 3) && (g0 & 15) == 0;
-        const unsigned okb = __ballot_sync(0xffffffffu, mine);
-#pragma unroll
-        for (int gi = 0; gi < 8; ++gi)
-          if (((okb >> (4 * gi)) & 0xFu) == 0xFu) tm |= 1u << gi;
-        __syncwarp();
-        if (i >= 2 && !__all_sync(0xffffffffu, pwait(&sb.s_full[st], (i - 2) >> 1, abort_flag, a.err))) break;
-        load_rows(a, sKV + st * 2 * kHalf, sb.slots[st], tm, g, false, &sb.k_full[st], lane);
-      }
-      if (i >= 1) {
-        const int k = i - 1, st = k & 1;
-        if (k >= 2 && !__all_sync(0xffffffffu, pwait(&sb.pv_done[st], (k - 2) >> 1, abort_flag, a.err))) break;
-        load_rows(a, sKV + (4 + st * 2) * kHalf, sb.slots[st], tm_prev, g, true, &sb.v_full[st], lane);
-      }
-      tm_prev = tm;
+      for (int gi = 0; gi < 8; ++gi)
+        if (((okb >> (4 * gi)) & 0xFu) == 0xFu) tm |= 1u << gi;
+      __syncwarp();
+      if (i >= 2 && !__all_sync(0xffffffffu, pwait(is_v ? &sb.pv_done[st] : &sb.s_full[st], (i - 2) >> 1,
+                                                    abort_flag, a.err)))
+        break;
+      load_rows(a, sKV + (is_v ? 4 + st * 2 : st * 2) * kHalf, slots, tm, g, is_v,
+                is_v ? &sb.v_full[st] : &sb.k_full[st], lane);
     }
   } else if (warp == 1) {
     // ======================= MMA issuer =======================================
@@ -352,7 +350,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_c
       if (issuer) umma_commit(&sb.drain);  // arrives once everything issued above is done
       __syncwarp();
     }
-  } else {
+  } else if (warp < kVWarp) {
     // ======================= softmax warps =====================================
     const bool rv = rt < jn;
     const int pr = p_first + rt;
