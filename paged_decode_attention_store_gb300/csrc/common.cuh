@@ -28,7 +28,7 @@ struct kvp_pool {
   void* ev_after;
   CUtensorMap tmap;  // tensor map of the whole buffer for the tensor-core kernel,
   int tmap_hg;       // heads per box it was encoded for (0: none yet, -HG: refused for HG)
-  CUtensorMap tmap1; // the same map with one head per box, for the prefill kernel
+  CUtensorMap tmap1; // the buffer as (d % 64, slot, d / 64, head, K/V x layer), for the prefill kernel
   int tmap1_state;   // 0: not encoded yet, 1: encoded, -1: refused
 };
 

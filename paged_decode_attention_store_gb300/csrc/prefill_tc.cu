@@ -9,24 +9,25 @@
 // attends (causal, the same window and sinks; chapter 15, "The model", and
 // its exercise "Attention sinks"), reading K/V in place through the table.
 //
-// How (one CTA of six warps per 128-row query tile):
+// How (one CTA of seven warps per 128-row query tile):
 // * A tile is 128 / G consecutive query tokens of one request times the G
 //   query heads of one KV head: 128 rows of Q, loaded once by TMA (128-byte
 //   swizzle, two 64-element halves of head_dim).
 // * The keys the tile needs (the union of its queries' spans) stream in
 //   blocks of 128: a 16-slot group whose slots are contiguous and 16-aligned
-//   comes by TMA (K and V, two halves each), any other key row is copied by
-//   its thread into the same swizzled layout.
-// * S = Q K^T (M 128, N 128, K 128: eight kind::f16 MMAs, both operands
-//   K-major) accumulates in a TMEM S buffer. Each thread owns one query row:
-//   it reads its 128 scores from TMEM and keeps an online softmax in log2
-//   units. A block that no row of the warp masks (causal, window, sinks,
+//   comes by one TMA copy (both halves of head_dim, 4 KB), any other key row
+//   is copied by the loader warp into the same swizzled layout.
+// * S = Q K^T (M 128, K 128, both operands K-major) accumulates in a TMEM
+//   S buffer as two N 64 halves (rows 0-7 and 8-15 of the eight key groups),
+//   so S column c holds key 16 (c % 64 / 8) + 8 (c / 64) + c % 8. Each
+//   thread owns one query row: it reads its 128 scores from TMEM and keeps
+//   an online softmax in log2 units. A block that no row of the warp masks (causal, window, sinks,
 //   block end) skips the mask; the row maximum is taken on unscaled scores
 //   and P = 2^(s * scale - m) is one FMA and one ex2 per score. O is rescaled
 //   (read, scaled, written back in TMEM) only when the row maximum grows by
 //   more than 8, so P <= 256 always fits bf16 and the normalisation stays
 //   exact (numerator and denominator use the same m).
-// * P (bf16, K-major, 128-byte swizzle) goes to shared memory and
+// * P (bf16, K-major, 128-byte swizzle, columns in key order) goes to shared memory and
 //   O += P V (V as the MN-major operand) accumulates in TMEM. The epilogue
 //   divides by the row sum and stores bf16.
 // * Warp-specialised pipeline: two loader warps fill two-stage K and V rings
@@ -52,11 +53,12 @@ constexpr int kPD = 128;  // head_dim
 constexpr int kPThreads = 224;  // warps: K loader, MMA, four softmax, V loader
 constexpr int kVWarp = 6;
 constexpr uint32_t kHalf = 16384;  // one 64-element half of a 128-row operand: 128 rows x 128 B
+constexpr uint32_t kGroupBytes = 4096;  // K or V of one 16-key group: 2 halves x 16 rows x 128 B
 constexpr uint64_t kPWaitNs = 2000000000ull;
 
 struct PrefillArgs {
   CUtensorMap qmap;   // q as (d, head, token, request), box (64, G, 128 / G, 1)
-  CUtensorMap kvmap;  // the KV buffer as (d, slot, kv head, K/V x layer), box (64, 16, 1, 1)
+  CUtensorMap kvmap;  // the KV buffer as (d % 64, slot, d / 64, kv head, K/V x layer), box (64, 16, 2, 1, 1)
   int use_kvmap;
   int kvl_k, kvl_v;
   TableRef T;
@@ -79,9 +81,9 @@ __device__ __forceinline__ uint64_t umma_desc(uint32_t addr, uint32_t lbo, uint3
          ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
-// kind::f16 instruction descriptor: fp32 accumulate, bf16 A and B, M 128, N 128.
-__host__ __device__ constexpr uint32_t umma_idesc(int b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn_major << 16) | ((uint32_t)(kPN >> 3) << 17) |
+// kind::f16 instruction descriptor: fp32 accumulate, bf16 A and B, M 128, N n.
+__host__ __device__ constexpr uint32_t umma_idesc(int b_mn_major, int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn_major << 16) | ((uint32_t)(n >> 3) << 17) |
          ((uint32_t)(kPM >> 4) << 24);
 }
 
@@ -141,6 +143,10 @@ __device__ __forceinline__ float ex2_ftz(float x) {
   return y;
 }
 
+// Key offset (within its 128-key block) of S column c: columns 0..63 are
+// rows 0..7 of the eight 16-key groups, columns 64..127 their rows 8..15.
+__host__ __device__ constexpr int key_of_col(int c) { return 16 * ((c & 63) >> 3) + 8 * (c >> 6) + (c & 7); }
+
 // Byte offset of 16-byte chunk c (0..7) of row r in a 128-byte-swizzled operand half.
 __device__ __forceinline__ uint32_t sw128(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
 
@@ -164,10 +170,22 @@ __device__ __forceinline__ bool pwait(uint64_t* bar, int k, volatile int* abort_
   return mbar_wait_bounded(bar, (uint32_t)(k & 1), abort_flag, err, kPWaitNs);
 }
 
+// 5-D tiled TMA load (coordinates innermost first) completing on ``bar``.
+__device__ __forceinline__ void tma_load_5d(void* dst, const void* tmap, int c0, int c1, int c2, int c3, int c4,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, "
+      "%6}], [%7];" ::"r"(smem_u32(dst)),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // The loader warp fills one 128-key operand (K, or V when ``is_v``, of head
 // group g) from ``slots``: 16-slot groups flagged in ``tm`` by one TMA
-// copy per 64-column half, the others by plain 16-byte copies (zeros for slots
-// < 0); ``bar`` (count 1) gets the arrival and the TMA byte count.
+// copy each (both 64-column halves), the others by plain 16-byte copies
+// (zeros for slots < 0); ``bar`` (count 1) gets the arrival and the TMA byte
+// count. Layout: group gi (keys 16 gi .. 16 gi + 15) at gi * 4 KB, its half h
+// at + h * 2 KB, key row r of the group at + r * 128 B (128-byte swizzle).
 __device__ __forceinline__ void load_rows(const PrefillArgs& a, unsigned char* dst, const int* slots, unsigned tm,
                                           int g, bool is_v, uint64_t* bar, int lane) {
   const size_t base = is_v ? a.kv_bytes : 0;
@@ -181,19 +199,16 @@ __device__ __forceinline__ void load_rows(const PrefillArgs& a, unsigned char* d
       if (sl >= 0)
         val = __ldg(reinterpret_cast<const uint4*>(a.kv_layer + base + (size_t)sl * a.row_bytes +
                                                    (size_t)g * kPD * 2) + c);
-      *reinterpret_cast<uint4*>(dst + (c >> 3) * kHalf + sw128(key, c & 7)) = val;
+      *reinterpret_cast<uint4*>(dst + gi * kGroupBytes + (c >> 3) * (kGroupBytes / 2) + sw128(key & 15, c & 7)) =
+          val;
     }
   }
   fence_proxy_async_smem();
   __syncwarp();
-  if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)__popc(tm) * 2u * 2048u);
+  if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)__popc(tm) * kGroupBytes);
   __syncwarp();
-  if (lane < 8 && ((tm >> lane) & 1)) {
-    const int s0 = slots[16 * lane];
-    const uint32_t off = (uint32_t)lane * 16u * 128u;
-    tma_load_4d(dst + off, &a.kvmap, 0, s0, g, kvl, bar);
-    tma_load_4d(dst + kHalf + off, &a.kvmap, 64, s0, g, kvl, bar);
-  }
+  if (lane < 8 && ((tm >> lane) & 1))
+    tma_load_5d(dst + lane * kGroupBytes, &a.kvmap, 0, slots[16 * lane], 0, g, kvl, bar);
   __syncwarp();
 }
 
@@ -311,7 +326,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_c
     {
       const bool issuer = lane == 0;
       const uint32_t qa = smem_u32(sQ);
-      const uint32_t id_s = umma_idesc(0), id_o = umma_idesc(1);
+      const uint32_t id_s = umma_idesc(0, kPN / 2), id_o = umma_idesc(1, kPN);
       bool ok = __all_sync(0xffffffffu, pwait(&sb.q_full, 0, abort_flag, a.err));
       for (int i = 0; ok && i <= nblk; ++i) {
         if (i < nblk) {  // S(i) = Q K(i)^T into S buffer i % 2
@@ -321,11 +336,15 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_c
           if (!ok) break;
           tc_fence_after();
           const uint32_t ka = smem_u32(sKV + st * 2 * kHalf);
+          // S columns 0..63 are rows 0..7 of the eight key groups, columns
+          // 64..127 their rows 8..15 (N 64 each, 8-row atoms 4 KB apart)
 #pragma unroll
           for (int ks = 0; ks < 8 && issuer; ++ks) {
-            const uint32_t koff = (uint32_t)(ks >> 2) * kHalf + (uint32_t)(ks & 3) * 32u;
-            umma_f16(tS0 + (uint32_t)st * 128u, umma_desc(qa + koff, 16, 1024), umma_desc(ka + koff, 16, 1024), id_s,
-                     ks > 0);
+            const uint32_t qoff = (uint32_t)(ks >> 2) * kHalf + (uint32_t)(ks & 3) * 32u;
+            const uint32_t koff = (uint32_t)(ks >> 2) * (kGroupBytes / 2) + (uint32_t)(ks & 3) * 32u;
+            const uint64_t qd = umma_desc(qa + qoff, 16, 1024);
+            umma_f16(tS0 + (uint32_t)st * 128u, qd, umma_desc(ka + koff, 16, kGroupBytes), id_s, ks > 0);
+            umma_f16(tS0 + (uint32_t)st * 128u + 64u, qd, umma_desc(ka + koff + 1024u, 16, kGroupBytes), id_s, ks > 0);
           }
           if (issuer) umma_commit(&sb.s_full[st]);
           __syncwarp();
@@ -340,7 +359,9 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_c
 #pragma unroll
           for (int ks = 0; ks < 8 && issuer; ++ks) {
             const uint32_t poff = (uint32_t)(ks >> 2) * kHalf + (uint32_t)(ks & 3) * 32u;
-            umma_f16(tO, umma_desc(pa + poff, 16, 1024), umma_desc(va + (uint32_t)ks * 2048u, kHalf, 1024), id_o,
+            // keys 16 ks .. 16 ks + 15 are V group ks: halves of d 2 KB apart, 8-key atoms 1 KB
+            umma_f16(tO, umma_desc(pa + poff, 16, 1024),
+                     umma_desc(va + (uint32_t)ks * kGroupBytes, kGroupBytes / 2, 1024), id_o,
                      (k > 0 || ks > 0) ? 1u : 0u);
           }
           if (issuer) umma_commit(&sb.pv_done[st]);
@@ -388,7 +409,8 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_c
       } else {
 #pragma unroll
         for (int c = 0; c < kPN; ++c) {
-          const bool keep = c < ea || (c >= wb && c <= we);
+          const int oc = key_of_col(c);
+          const bool keep = oc < ea || (oc >= wb && oc <= we);
           sv[c] = keep ? sv[c] : -INFINITY;
           rmax = fmaxf(rmax, sv[c]);
         }
@@ -417,7 +439,9 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_c
           w[x] = pack_bf16(p0, p1);
           psum += bf16_lo(w[x]) + bf16_hi(w[x]);
         }
-        *reinterpret_cast<uint4*>(sP + (c8 >> 3) * kHalf + sw128(r, c8 & 7)) = make_uint4(w[0], w[1], w[2], w[3]);
+        // P column k is key k of the block: S chunk c8 holds keys 16 (c8 % 8) + 8 (c8 / 8) + 0..7
+        const int j8 = 2 * (c8 & 7) + (c8 >> 3);
+        *reinterpret_cast<uint4*>(sP + (j8 >> 3) * kHalf + sw128(r, j8 & 7)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
       lsum = lsum * f + psum;
       if (__any_sync(0xffffffffu, scale_o)) {
@@ -478,7 +502,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_c
   if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tS0) : "memory");
 }
 
-bool encode_qmap(const void* q, int B, int C, int Hq, int G, CUtensorMap* out) {
+PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   static bool looked_up = false;
   if (!looked_up) {
@@ -490,6 +514,26 @@ bool encode_qmap(const void* q, int B, int C, int Hq, int G, CUtensorMap* out) {
       encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     looked_up = true;
   }
+  return encode;
+}
+
+// The K/V buffer as (d % 64, slot, d / 64, kv head, K/V x layer): one box
+// (64, 16, 2, 1, 1) is a 16-slot group of one head with both halves of d.
+bool encode_kvmap(const kvp_pool* pool, CUtensorMap* out) {
+  const auto encode = tmap_encoder();
+  if (!encode || pool->dtype != KVP_BF16 || pool->head_dim != kPD) return false;
+  cuuint64_t dims[5] = {64, (cuuint64_t)pool->num_slots, 2, (cuuint64_t)pool->kv_heads,
+                        (cuuint64_t)(2 * pool->num_layers)};
+  cuuint64_t strides[4] = {(cuuint64_t)pool->row_bytes, 128, (cuuint64_t)kPD * 2, (cuuint64_t)pool->layer_bytes};
+  cuuint32_t box[5] = {64, 16, 2, 1, 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return encode(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, pool->buf, dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_qmap(const void* q, int B, int C, int Hq, int G, CUtensorMap* out) {
+  const auto encode = tmap_encoder();
   if (!encode) return false;
   cuuint64_t dims[4] = {(cuuint64_t)kPD, (cuuint64_t)Hq, (cuuint64_t)C, (cuuint64_t)B};
   cuuint64_t strides[3] = {(cuuint64_t)kPD * 2, (cuuint64_t)Hq * kPD * 2, (cuuint64_t)C * Hq * kPD * 2};
@@ -518,7 +562,7 @@ int launch_prefill_tc(const kvp_pool* pool, int layer, const void* q, int batch,
   PrefillArgs a;
   const int G = Hq / pool->kv_heads;
   if (!encode_qmap(q, batch, C, Hq, G, &a.qmap)) return KVP_ERR_CUDA;
-  if (mp->tmap1_state == 0) mp->tmap1_state = tc_encode_tmap(pool, 1, &mp->tmap1) ? 1 : -1;
+  if (mp->tmap1_state == 0) mp->tmap1_state = encode_kvmap(pool, &mp->tmap1) ? 1 : -1;
   a.use_kvmap = mp->tmap1_state == 1;
   if (a.use_kvmap) a.kvmap = mp->tmap1;
   else memset(&a.kvmap, 0, sizeof(a.kvmap));
