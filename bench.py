@@ -572,13 +572,13 @@ def measured_peak(key="hbm_gbs", fallback=None):
         return (FALLBACK_HBM_GBS if fallback is None else fallback), "fallback"
 
 
-def ncu_traffic(workload):
-    """DRAM bytes per launch of the attention kernel from the committed ncu
-    summary, if it was taken on the current kernel source."""
+def ncu_summary(kernel, source, workload):
+    """The ``key: value`` lines of the committed ncu summary of ``kernel`` on
+    ``workload``, if it was taken on the current source of that kernel."""
     import hashlib
 
-    src = os.path.join(ROOT, "paged_decode_attention_store_gb300", "csrc", "attention_tc.cu")
-    path = os.path.join(ROOT, "profiles", f"tc_decode_kernel_{workload}.txt")
+    src = os.path.join(ROOT, "paged_decode_attention_store_gb300", "csrc", source)
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.txt")
     try:
         digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
         vals = {}
@@ -586,10 +586,28 @@ def ncu_traffic(workload):
             if ":" in line:
                 k, v = line.split(":", 1)
                 vals[k.strip()] = v.strip()
-        if vals.get("kernel_source_sha256_16") != digest:
-            return None
-        return float(vals["dram_bytes_per_launch"])
-    except (OSError, KeyError, ValueError):
+    except OSError:
+        return None
+    return vals if vals.get("kernel_source_sha256_16") == digest else None
+
+
+def ncu_traffic(workload):
+    """DRAM bytes per launch of the decode attention kernel from its ncu summary."""
+    vals = ncu_summary("tc_decode_kernel", "attention_tc.cu", workload)
+    try:
+        return float(vals["dram_bytes_per_launch"]) if vals else None
+    except (KeyError, ValueError):
+        return None
+
+
+def ncu_prefill_traffic(workload, flops):
+    """DRAM bytes of a prefill launch of ``flops`` algorithmic flops: the
+    captured launch's bytes scaled by flops (both grow with the tiles' key
+    counts; the L2 hit rate falls as contexts grow, so this is a lower bound)."""
+    vals = ncu_summary("prefill_tc_kernel", "prefill_tc.cu", workload)
+    try:
+        return round(float(vals["dram_bytes_per_launch"]) * flops / float(vals["algorithmic_flops_per_launch"]))
+    except (TypeError, KeyError, ValueError, ZeroDivisionError):
         return None
 
 
@@ -722,6 +740,7 @@ def run_gpu(args, rank, world, local_rank):
         roofline.update({"bound": "tensor", "kernel": "prefill_tc_kernel", "achieved": round(tf, 1), "peak": tpeak,
                          "peak_kind": f"{tkind} bf16_tflops (cuBLAS, burst)", "unit": "TFLOP/s",
                          "frac": round(tf / tpeak, 4), "frac_of_nominal_8tbs": None,
+                         "traffic": ncu_prefill_traffic(sc.name, flops_mean),
                          "algorithmic_flops_per_launch": int(flops_mean), "attention_gbps": round(achieved, 1)})
     line = {
         "metric": METRIC,
