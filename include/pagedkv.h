@@ -537,7 +537,12 @@ int kvp_decode_step_device(kvp_dev_pages* d, const kvp_pool* pool,
  * be asynchronous) are copied into the caller's per-layer device staging
  * q_dev/k_dev/v_dev, the step runs, and each layer's output goes from
  * out_dev back to out_host. Returns once the outputs are on the host (the
- * stream is synchronised). One call per step. */
+ * stream is synchronised). One call per step.
+ * The input copies run on a copy stream of the page state, after the work
+ * already queued on ``stream``, while the page append runs on ``stream``;
+ * layer l's attention waits for layer l's copies only. The first call
+ * creates that stream and num_layers + 1 events; kvp_dev_pages_destroy
+ * releases them (no device memory is allocated). */
 int kvp_decode_step_device_io(kvp_dev_pages* d, const kvp_pool* pool,
                               int32_t* table, int table_rows_total,
                               int table_cols, int table_mode,

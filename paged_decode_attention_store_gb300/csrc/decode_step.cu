@@ -173,11 +173,15 @@ extern "C" int kvp_decode_step_device(kvp_dev_pages* d, const kvp_pool* pool, in
   return KVP_OK;
 }
 
+// The page state's copy stream and events (device_pages.cu).
+int kvp_dev_io_resources(kvp_dev_pages* d, int nevents, void** stream, void*** events);
+
 // kvp_decode_step_device_io: kvp_decode_step_device with host buffers in and
-// out: each layer's q, k, v are copied from host memory into the caller's
-// device staging, the step runs, each layer's output is copied back, and the
-// call returns once the outputs are on the host. One native call per step,
-// so the host issues everything while the first copy is in flight.
+// out. Each layer's q, k, v are copied from host memory into the caller's
+// device staging on the state's copy stream, while the page append runs on
+// ``stream``; layer l's attention waits for layer l's copies only. Each
+// layer's output is copied back on ``stream`` and the call returns once the
+// outputs are on the host. One native call per step.
 extern "C" int kvp_decode_step_device_io(kvp_dev_pages* d, const kvp_pool* pool, int32_t* table,
                                          int table_rows_total, int table_cols, int table_mode, const int32_t* rids,
                                          int n, int window, int sinks, int num_q_heads, float scale,
@@ -186,23 +190,37 @@ extern "C" int kvp_decode_step_device_io(kvp_dev_pages* d, const kvp_pool* pool,
                                          void* const* k_dev, void* const* v_dev, void* const* out_dev,
                                          int32_t* scratch, int may_share, void* workspace, size_t workspace_bytes,
                                          void* stream) {
-  if (!pool || !q_host || !k_host || !v_host || !out_host || !q_dev || !k_dev || !v_dev || !out_dev || n <= 0 ||
-      num_q_heads <= 0)
+  if (!d || !pool || !q_host || !k_host || !v_host || !out_host || !q_dev || !k_dev || !v_dev || !out_dev ||
+      n <= 0 || num_q_heads <= 0)
     return KVP_ERR_INVALID_ARG;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int layers = pool->num_layers;
+  void* io = nullptr;
+  void** ev = nullptr;
+  int rc = kvp_dev_io_resources(d, layers + 1, &io, &ev);
+  if (rc != KVP_OK) return rc;
+  const cudaStream_t cs = static_cast<cudaStream_t>(io);
   const size_t qbytes = (size_t)n * num_q_heads * pool->head_dim * pool->elem;
   const size_t kvbytes = (size_t)n * pool->row_bytes;
-  for (int l = 0; l < pool->num_layers; ++l) {
-    if (cudaMemcpyAsync(q_dev[l], q_host[l], qbytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
-        cudaMemcpyAsync(k_dev[l], k_host[l], kvbytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
-        cudaMemcpyAsync(v_dev[l], v_host[l], kvbytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+  // the copies start after the work already on ``stream`` (the staging may still be read there)
+  if (cudaEventRecord(static_cast<cudaEvent_t>(ev[0]), st) != cudaSuccess ||
+      cudaStreamWaitEvent(cs, static_cast<cudaEvent_t>(ev[0]), 0) != cudaSuccess)
+    return KVP_ERR_CUDA;
+  for (int l = 0; l < layers; ++l) {
+    if (cudaMemcpyAsync(q_dev[l], q_host[l], qbytes, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
+        cudaMemcpyAsync(k_dev[l], k_host[l], kvbytes, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
+        cudaMemcpyAsync(v_dev[l], v_host[l], kvbytes, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
+        cudaEventRecord(static_cast<cudaEvent_t>(ev[1 + l]), cs) != cudaSuccess)
       return KVP_ERR_CUDA;
   }
-  int rc = kvp_decode_step_device(d, pool, table, table_rows_total, table_cols, table_mode, rids, n, window, sinks,
-                                  num_q_heads, scale, q_dev, k_dev, v_dev, out_dev, nullptr, nullptr, scratch,
-                                  may_share, workspace, workspace_bytes, stream);
-  if (rc != KVP_OK) return rc;
-  for (int l = 0; l < pool->num_layers; ++l)
+  rc = kvp_decode_step_device(d, pool, table, table_rows_total, table_cols, table_mode, rids, n, window, sinks,
+                              num_q_heads, scale, q_dev, k_dev, v_dev, out_dev, ev + 1, nullptr, scratch, may_share,
+                              workspace, workspace_bytes, stream);
+  if (rc != KVP_OK) {
+    cudaStreamSynchronize(cs);  // the host buffers stay in use until the copies are done
+    return rc;
+  }
+  for (int l = 0; l < layers; ++l)
     if (cudaMemcpyAsync(out_host[l], out_dev[l], qbytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
       return KVP_ERR_CUDA;
   return cudaStreamSynchronize(st) == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;

@@ -33,6 +33,11 @@ struct kvp_dev_pages {
   int32_t* sinkp;
   int32_t* table;
   int rows, cols, raw;
+  // host-to-device copy stream and events of kvp_decode_step_device_io,
+  // created on its first call: [0] the step's start, [1 + l] layer l's inputs
+  void* io_stream;
+  void** io_events;
+  int io_nevents;
 };
 
 namespace kvp {
@@ -400,12 +405,46 @@ extern "C" int kvp_dev_pages_create(int num_pages, int page_size, int max_reques
   d->rows = table_rows;
   d->cols = table_cols;
   d->raw = table_mode == KVP_RAW_LOCATIONS;
+  d->io_stream = nullptr;
+  d->io_events = nullptr;
+  d->io_nevents = 0;
   *out = d;
   return KVP_OK;
 }
 
 extern "C" int kvp_dev_pages_destroy(kvp_dev_pages* d) {
+  if (!d) return KVP_OK;
+  for (int i = 0; i < d->io_nevents; ++i)
+    if (d->io_events[i]) cudaEventDestroy(static_cast<cudaEvent_t>(d->io_events[i]));
+  delete[] d->io_events;
+  if (d->io_stream) cudaStreamDestroy(static_cast<cudaStream_t>(d->io_stream));
   delete d;
+  return KVP_OK;
+}
+
+// The copy stream and ``nevents`` events of the host-buffer step (created
+// once, kept until kvp_dev_pages_destroy).
+int kvp_dev_io_resources(kvp_dev_pages* d, int nevents, void** stream, void*** events) {
+  if (!d->io_stream) {
+    cudaStream_t s;
+    if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return KVP_ERR_CUDA;
+    d->io_stream = s;
+  }
+  if (d->io_nevents < nevents) {
+    void** ev = new (std::nothrow) void*[nevents];
+    if (!ev) return KVP_ERR_INVALID_ARG;
+    for (int i = 0; i < d->io_nevents; ++i) ev[i] = d->io_events[i];
+    delete[] d->io_events;
+    d->io_events = ev;
+    for (int i = d->io_nevents; i < nevents; ++i) {
+      cudaEvent_t e;
+      if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return KVP_ERR_CUDA;
+      d->io_events[i] = e;
+      d->io_nevents = i + 1;
+    }
+  }
+  *stream = d->io_stream;
+  *events = d->io_events;
   return KVP_OK;
 }
 
