@@ -41,6 +41,15 @@ def test_argument_checks_fail_before_launch():
     assert lib.paged_decode_attention(null, 0, null, 1, 1, null, 1, 1, 0, null, null, 0, 0, 1.0, null, null, 0,
                                       null) == kb.KVP_ERR_INVALID_ARG
     assert lib.gather_indices(null, null, 1, 1, 0, null, null, 1, 0, 0, null, 1, null) == kb.KVP_ERR_INVALID_ARG
+    BT = kb.KVP_BLOCK_TABLE
+    assert lib.paged_prefill_attention(null, 0, null, 1, 1, 1, null, null, 1, 1, BT, null, null, 0, 0, 1.0, null,
+                                       null) == kb.KVP_ERR_INVALID_ARG
+    assert lib.paged_verify_attention(null, 0, null, 1, 1, 1, null, 1, 1, BT, null, null, 0, 0, 1.0, null, null, 0,
+                                      null) == kb.KVP_ERR_INVALID_ARG
+    assert lib.store_cache_and_attention(null, 0, null, null, null, null, 1, 1, null, 1, 1, BT, null, null, null,
+                                         null, null, 0, 0, 0, 1.0, null, null, 0, null) == kb.KVP_ERR_INVALID_ARG
+    assert lib.kvp_decode_step_device_io(null, null, null, 1, 1, BT, null, 1, 0, 0, 1, 1.0, null, null, null, null,
+                                         null, null, null, null, null, 0, null, 0, null) == kb.KVP_ERR_INVALID_ARG
     out = ctypes.c_void_p()
     # misaligned buffer and bad dtype are rejected before any CUDA call
     assert lib.kv_pool_create(4, 4, 1, 16, 1, 1, ctypes.c_void_p(8), ctypes.c_void_p(64),

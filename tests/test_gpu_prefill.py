@@ -40,6 +40,9 @@ CASES = [
     ("bf16", 32, 8, 128, 16, "block", 256, [700, 40], [256, 256], 200, 2),                # window with sinks
     ("bf16", 64, 4, 128, 4, "block", 64, [90, 3], [64, 40], 0, 0),                        # GQA 16, page 4
     ("f32", 4, 2, 16, 4, "block", 20, [5, 30], [20, 7], 12, 2),                           # general kernel
+    ("bf16", 32, 8, 128, 16, "raw", 200, [500, 33], [200, 150], 0, 0),                    # raw table, page 16 (TMA)
+    ("bf16", 32, 8, 128, 16, "block", 300, [1000, 0], [300, 300], 128, 0),                # window, no sinks
+    ("bf16", 16, 8, 128, 16, "block", 96, [70, 0], [96, 5], 0, 0),                        # GQA 2: 64 tokens per tile
 ]
 
 
@@ -104,3 +107,34 @@ def test_prefill_single_token_equals_decode(kb):
     torch.cuda.synchronize()
     assert (out[:, 0].float() - dec.float()).abs().max().item() <= 2e-2
     assert prod.error() == 0
+
+
+def test_prefill_bad_lengths_zero_the_request(kb):
+    """A request whose chunk is longer than its context records
+    KVP_ERR_BAD_INDEX and gets zero rows; the other request is unaffected."""
+    Hq, Hkv, D, P, C = 32, 8, 128, 16, 128
+    lens, q_lens = [300, 40], [128, 64]
+    B = len(lens)
+    num_pages = sum(-(-L // P) for L in lens) + 8
+    order = wl.free_stack_for_order(wl.permutation(77, num_pages))
+    w = wl.Workload("pbad", "bf16", Hq, Hkv, D, P, 1, num_pages, order, [0, 0], scale=1.0 / math.sqrt(D))
+    prod = ProductSession(kb, w, DEV, max_requests=B, cols=-(-max(lens) // P) + 2, seed=5)
+    orc = OracleSession(w, B, seed=5)
+    for b in range(B):
+        prod.new(b)
+        orc.new(b)
+        assert prod.append([b] * lens[b], list(range(lens[b]))) == orc.append([b] * lens[b], list(range(lens[b])))
+    i32 = lambda xs: torch.tensor(list(xs), dtype=torch.int32, device=DEV)  # noqa: E731
+    q = torch.stack([wl.q_rows(9, 700 + j, 0, list(range(B)), Hq, D, dtype=prod.dt, device=DEV) for j in range(C)],
+                    dim=1).contiguous()
+    out = torch.full_like(q, 7.0)
+    kb.paged_prefill_attention(prod.pool, 0, q, prod.table, kb.KVP_BLOCK_TABLE, i32(lens), 0, w.scale, out,
+                               q_lens=i32(q_lens), table_rows=i32(range(B)))
+    torch.cuda.synchronize()
+    assert prod.error() == kb.KVP_ERR_BAD_INDEX
+    assert (out[1] == 0).all(), "the invalid request's rows are not zero"
+    got = out.float().cpu().numpy()
+    for j, pos in enumerate(OA.verify_positions(lens[0], q_lens[0], None, 0)):
+        sl = [s_ for p_ in pos for s_ in orc.slots(0, p_, p_ + 1)]
+        ref = OA.attend_request(orc.stores[0], q[0, j].float().cpu().numpy(), sl, w.scale)
+        assert max_abs(got[0, j], ref) <= tol_for("bf16"), f"query {j}"
