@@ -315,6 +315,17 @@ int gather_indices(const kvp_pool* pool, const int32_t* table,
  * into *err (0 = none) and clear it. */
 int kvp_sync_error(const kvp_pool* pool, void* stream, int* err);
 
+/* kvp_selftest_wait: checks, on the device, the bounded wait behind every
+ * pipeline wait of the library's kernels (mbarrier try-wait against the
+ * global timer, then an error code instead of a hang). One warp waits on a
+ * shared-memory mbarrier for at most limit_ns (1 .. 1e9 ns). arrive = 0:
+ * nothing arrives, the wait gives up after limit_ns and KVP_ERR_TIMEOUT is
+ * recorded in *err (DEVICE int32, first error wins, as the pool's error
+ * word). arrive = 1: the barrier is satisfied first and nothing is recorded.
+ * Asynchronous on ``stream``; KVP_ERR_INVALID_ARG for a NULL err or a limit
+ * or mode out of range. No kernel traps or hangs either way. */
+int kvp_selftest_wait(long long limit_ns, int arrive, int32_t* err, void* stream);
+
 /* kvp_pool_set_timing_events: measurement hook. When both events are
  * non-NULL (cudaEvent_t, caller-owned), the next paged_decode_attention call
  * on this pool records ``before`` on its stream just before its main

@@ -54,6 +54,7 @@ SIGNATURES = {
                                   _i, _i, _f, _vp, _vp, _sz, _vp],
     "gather_indices": [_vp, _vp, _i, _i, _i, _vp, _vp, _i, _i, _i, _vp, _i, _vp],
     "kvp_sync_error": [_vp, _vp, _ip],
+    "kvp_selftest_wait": [ctypes.c_longlong, _i, _vp, _vp],
     "kvp_pool_set_timing_events": [_vp, _vp, _vp],
     "kvp_host_create": [_i, _i, _i, _vp, ctypes.POINTER(_vp)],
     "kvp_host_destroy": [_vp],
@@ -477,6 +478,12 @@ def kvp_sync_error(pool, stream=None):
     e = ctypes.c_int()
     _check(lib().kvp_sync_error(pool.handle, _stream(stream), ctypes.byref(e)), "kvp_sync_error")
     return e.value
+
+
+def kvp_selftest_wait(limit_ns, arrive, err, stream=None):
+    """One bounded mbarrier wait on the device (kvp_selftest_wait): ``err`` is
+    a device int32 tensor that receives KVP_ERR_TIMEOUT when nothing arrives."""
+    _check(lib().kvp_selftest_wait(int(limit_ns), int(arrive), _ptr(err), _stream(stream)), "kvp_selftest_wait")
 
 
 # ---------------------------------------------------------------------------

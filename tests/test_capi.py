@@ -41,6 +41,10 @@ def test_argument_checks_fail_before_launch():
     assert lib.paged_decode_attention(null, 0, null, 1, 1, null, 1, 1, 0, null, null, 0, 0, 1.0, null, null, 0,
                                       null) == kb.KVP_ERR_INVALID_ARG
     assert lib.gather_indices(null, null, 1, 1, 0, null, null, 1, 0, 0, null, 1, null) == kb.KVP_ERR_INVALID_ARG
+    assert lib.kvp_selftest_wait(1000, 0, null, null) == kb.KVP_ERR_INVALID_ARG
+    assert lib.kvp_selftest_wait(0, 0, ctypes.c_void_p(16), null) == kb.KVP_ERR_INVALID_ARG
+    assert lib.kvp_selftest_wait(2_000_000_000, 0, ctypes.c_void_p(16), null) == kb.KVP_ERR_INVALID_ARG
+    assert lib.kvp_selftest_wait(1000, 2, ctypes.c_void_p(16), null) == kb.KVP_ERR_INVALID_ARG
     BT = kb.KVP_BLOCK_TABLE
     assert lib.paged_prefill_attention(null, 0, null, 1, 1, 1, null, null, 1, 1, BT, null, null, 0, 0, 1.0, null,
                                        null) == kb.KVP_ERR_INVALID_ARG
