@@ -1008,10 +1008,11 @@ class OracleSample:
         elif kind == "release":
             self.pt.release(op[1])
 
-    def _verify_step(self, step_index, attend_rids, with_slots):
+    def _verify_step(self, step_index, attend_rids, with_slots, queries=None):
         """A speculative step: M drafts appended per request, the ones of
         ``attend_rids`` stored and verified, the seeded acceptance applied by
-        rewinding the rest."""
+        rewinding the rest. ``queries``: the query indices j to attend (all
+        when None; a timed sample of a long chunk takes a subset)."""
         sc, w, OA, M = self.sc, self.sc.w, self.OA, self.sc.multi
         pos0 = {r: self.pt.length[r] for r in sc.rids}
         rr = [r for r in sc.rids for _ in range(M)]
@@ -1026,6 +1027,8 @@ class OracleSample:
             for layer in self.layers:
                 per_q = []
                 for j, pos in enumerate(OA.verify_positions(L, M, sc.window, sc.sinks)):
+                    if queries is not None and j not in queries:
+                        continue
                     q = wl.q_rows(sc.seed, step_index * M + j, layer, [r], w.Hq, w.D, dtype=self.tdt)[0]
                     sl = [s for p in pos for s in OA.gather_block(row, w.P, p, p + 1)]
                     per_q.append(OA.attend_request(self.stores[layer], q.float().numpy(), sl, w.scale))
@@ -1035,12 +1038,12 @@ class OracleSample:
                 self.pt.rewind(r, M - a)
         return (outs, slots) if with_slots else outs
 
-    def step(self, step_index, attend_rids, with_slots=False):
+    def step(self, step_index, attend_rids, with_slots=False, queries=None):
         """One decode step: bookkeeping for every request, store + attention for ``attend_rids``.
 
         Returns {(rid, layer): output}, and also the step's slots when ``with_slots``."""
         if self.sc.multi:
-            return self._verify_step(step_index, attend_rids, with_slots)
+            return self._verify_step(step_index, attend_rids, with_slots, queries)
         sc, w, OA = self.sc, self.sc.w, self.OA
         pos = [self.pt.length[r] for r in sc.rids]
         slots = self._append(sc.rids)
@@ -1078,27 +1081,41 @@ def _sample_rids(sc, n):
     return [sc.rids[i] for i in idx]
 
 
+def timed_queries(sc):
+    """Query tokens a timed oracle sample attends per request: all of a decode
+    or verify step; 16 evenly spaced ones of a long prefill chunk, whose bytes
+    are then credited in proportion. Returns (indices or None, fraction)."""
+    M = max(sc.multi, 1)
+    if M <= 32:
+        return None, 1.0
+    js = sorted({round(k * (M - 1) / 15) for k in range(16)})
+    return set(js), len(js) / M
+
+
 def cpu_baseline(sc, seconds):
     """The oracle, as it stands, on one host core: decode steps of a sample of
     requests of the same workload, timed for about ``seconds``."""
     n = 4 if sc.w.layers == 1 else 2
     sample = _sample_rids(sc, n)
     orc = OracleSample(sc, sample)
+    queries, frac = timed_queries(sc)
     done_bytes, t_total, steps = 0, 0.0, 0
     while t_total < seconds or steps == 0:
         steps += 1
         t = time.perf_counter()
-        orc.step(10_000 + steps, sample)
+        orc.step(10_000 + steps, sample, queries=queries)
         t_total += time.perf_counter() - t
         lens = [orc.pt.length[r] for r in sample]
-        done_bytes += sc.w.layers * attention_bytes(sc, lens)
+        done_bytes += frac * sc.w.layers * attention_bytes(sc, lens)
     return {
         "value": round(done_bytes / t_total / 1e9, 6),
         "unit": UNIT,
         "cores": 1,
         "kind": "oracle",
         "sample": f"{steps} decode steps of {len(sample)} of {len(sc.rids)} requests (all {sc.w.layers} layers); "
-                  f"bookkeeping for every request, store + float64 attention for the sample",
+                  f"bookkeeping for every request, store + float64 attention for the sample"
+                  + (f" ({len(queries)} of {sc.multi} query tokens each, bytes credited in proportion)"
+                     if queries else ""),
         "seconds": round(t_total, 2),
     }
 
@@ -1109,13 +1126,14 @@ def run_reference(args):
     n = 2 if sc.w.layers == 1 else 1
     sample = _sample_rids(sc, n)
     orc = OracleSample(sc, sample)
+    queries, frac = timed_queries(sc)
     for i in range(args.warmup):
-        orc.step(1 + i, sample)
+        orc.step(1 + i, sample, queries=queries)
     t = time.perf_counter()
     done = 0
     for i in range(args.steps):
-        orc.step(1 + args.warmup + i, sample)
-        done += sc.w.layers * attention_bytes(sc, [orc.pt.length[r] for r in sample])
+        orc.step(1 + args.warmup + i, sample, queries=queries)
+        done += frac * sc.w.layers * attention_bytes(sc, [orc.pt.length[r] for r in sample])
     el = time.perf_counter() - t
     value = done / el / 1e9
     return {
@@ -1135,7 +1153,9 @@ def run_reference(args):
         "config": {"workload": sc.name, "batch": len(sc.rids), "sampled_requests": len(sample),
                    "layers": sc.w.layers, "seed": args.seed},
         "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"{len(sample)} of {len(sc.rids)} requests per step, all layers"},
+                         "sample": f"{len(sample)} of {len(sc.rids)} requests per step, all layers"
+                                   + (f", {len(queries)} of {sc.multi} query tokens each (bytes credited in "
+                                      f"proportion)" if queries else "")},
         "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
