@@ -211,9 +211,11 @@ int paged_verify_attention(const kvp_pool* pool, int layer, const void* q,
  * that context attends (causal, window and sinks as paged_decode_attention)
  * - the formula of paged_verify_attention for chunks of any length
  * ("Week 3 Day 3: Paged KV Cache" of tiny-llm: chunked prefill appends each
- * chunk to the pages, then attends over them). bf16 pools with head_dim 128
- * and 128 % (num_q_heads / kv_heads) == 0 run on the tcgen05 tensor cores
- * (TMEM accumulators), others on the general kernel.
+ * chunk to the pages, then attends over them). bf16 pools with head_dim 128,
+ * 128 % (num_q_heads / kv_heads) == 0 and scale > 0 run on the tcgen05
+ * tensor cores (TMEM accumulators), others on the general kernel. The
+ * tcgen05 kernel keeps the pool's tensor map (built on first use) in the
+ * pool descriptor; ``q`` is mapped per call.
  *   q    device [batch, chunk, num_q_heads, head_dim], pool dtype,
  *        16-byte aligned.
  *   out  device, the same shape; rows j >= q_lens[b] are not written.
