@@ -259,6 +259,22 @@ def test_verify_equals_masked_sdpa():
     assert check_verify_library_sdpa() == []
 
 
+def test_whole_sequence_prefill_equals_causal_sdpa():
+    """A chunk that is the whole sequence (L0 = 0: every token a query) is
+    textbook causal attention: torch SDPA with its own is_causal mask
+    (float64, GQA), no mask written here."""
+    for page, M in ((4, 21), (1, 7), (16, 40)):
+        Hq, Hkv, D, seed = 4, 2, 16, 11
+        got, k, v = _verify_oracle(None, 0, page, M, L0=0, seed=seed, Hq=Hq, Hkv=Hkv, D=D)
+        q = torch.stack([wl.q_rows(seed, j + 1, 0, [0], Hq, D, dtype=torch.float64)[0] for j in range(M)])
+        qt = q.permute(1, 0, 2)[None]
+        kt = torch.as_tensor(k, dtype=torch.float64).permute(1, 0, 2)[None]
+        vt = torch.as_tensor(v, dtype=torch.float64).permute(1, 0, 2)[None]
+        ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, is_causal=True, scale=1.0 / math.sqrt(D),
+                                                               enable_gqa=True)[0].permute(1, 0, 2).numpy()
+        assert np.max(np.abs(ref - got)) <= 1e-12, f"page {page}, {M} tokens"
+
+
 def test_verify_positions_readings():
     # context 10, 3 verify tokens, no window: causal prefixes
     assert A.verify_positions(10, 3, None) == [list(range(8)), list(range(9)), list(range(10))]
