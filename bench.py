@@ -794,7 +794,15 @@ def run_gpu(args, rank, world, local_rank):
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(sc, args.cpu_seconds)
+        single = cpu_baseline(sc, args.cpu_seconds)
+        line["cpu_baseline"] = single
+        if sc.w.layers == 1:  # the one-layer oracle state is small enough to hold once per core
+            try:
+                allc = cpu_baseline_all_cores(sc, args.cpu_seconds, min(os.cpu_count() or 1, 16))
+                line["cpu_baseline"] = dict(single, value=allc["value"], cores=allc["cores"], sample=allc["sample"],
+                                            single_core={"value": single["value"], "sample": single["sample"]})
+            except Exception as e:  # keep the single-core figure, and say why
+                line["cpu_baseline"]["all_cores_unavailable"] = repr(e)[:200]
     return line
 
 
@@ -1117,6 +1125,71 @@ def cpu_baseline(sc, seconds):
                   + (f" ({len(queries)} of {sc.multi} query tokens each, bytes credited in proportion)"
                      if queries else ""),
         "seconds": round(t_total, 2),
+    }
+
+
+def _oracle_worker(name, seed, sample, seconds, barrier, out_q):
+    """One process of the all-cores oracle timing: builds the workload's
+    oracle state, waits for the others, then times decode steps of its own
+    sample of requests for about ``seconds``."""
+    try:
+        sc = Scenario(name, seed)
+        orc = OracleSample(sc, sample)
+        queries, frac = timed_queries(sc)
+        barrier.wait(timeout=300)
+        done, t_total, steps = 0.0, 0.0, 0
+        while t_total < seconds or steps == 0:
+            steps += 1
+            t = time.perf_counter()
+            orc.step(10_000 + steps, sample, queries=queries)
+            t_total += time.perf_counter() - t
+            done += frac * sc.w.layers * attention_bytes(sc, [orc.pt.length[r] for r in sample])
+        out_q.put((done, t_total, steps, len(sample)))
+    except Exception as e:  # reported to the parent, which then keeps the single-core figure
+        out_q.put(repr(e))
+
+
+def cpu_baseline_all_cores(sc, seconds, workers):
+    """The oracle on ``workers`` host cores at once: one spawned process per
+    core, each on its own sample of requests (disjoint, spread over the
+    batch), timed together; the value is the sum of their rates."""
+    import multiprocessing as mp
+
+    ctx = mp.get_context("spawn")  # safe after CUDA has been initialised
+    B = len(sc.rids)
+    per = max(1, min(4, B // workers))
+    samples = [s for s in ([sc.rids[i] for i in range(w, B, workers)][:per] for w in range(workers)) if s]
+    barrier, out_q = ctx.Barrier(len(samples)), ctx.Queue()
+    procs = [ctx.Process(target=_oracle_worker, args=(sc.name, sc.seed, smp, seconds, barrier, out_q), daemon=True)
+             for smp in samples]
+    import queue
+
+    for p in procs:
+        p.start()
+    res = []
+    try:
+        deadline = time.time() + 900
+        while len(res) < len(procs):
+            try:
+                res.append(out_q.get(timeout=1.0))
+            except queue.Empty:
+                # a process that died without reporting would leave the others at the barrier
+                if any(p.exitcode not in (None, 0) for p in procs) or time.time() > deadline:
+                    raise RuntimeError("an oracle process ended without a result")
+    finally:
+        for p in procs:
+            p.join(timeout=5)
+            if p.is_alive():
+                p.kill()
+    bad = [r for r in res if isinstance(r, str)]
+    if bad:
+        raise RuntimeError(bad[0])
+    rate = sum(d / t for d, t, _, _ in res)
+    return {
+        "value": round(rate / 1e9, 6),
+        "cores": len(procs),
+        "sample": f"{len(procs)} processes, each {min(r[2] for r in res)}+ decode steps of its own {per} of {B} "
+                  f"requests (all {sc.w.layers} layers), timed together; rates summed",
     }
 
 

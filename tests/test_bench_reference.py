@@ -44,3 +44,10 @@ def test_timed_queries_sample_long_chunks_only():
     js, frac = bench.timed_queries(bench.Scenario("gqa_prefill512", 0))
     assert len(js) == 16 and 0 in js and 511 in js
     assert frac == 16 / 512
+
+
+def test_all_cores_oracle_timing_runs_processes_together():
+    sc = bench.Scenario("gqa_decode", 0)
+    r = bench.cpu_baseline_all_cores(sc, 0.5, 2)
+    assert r["cores"] == 2 and r["value"] > 0
+    assert "2 processes" in r["sample"]
