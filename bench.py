@@ -52,16 +52,25 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 WORKLOADS = ("gqa_decode", "sliding_window", "sliding_window_sinks", "prefix_sharing", "large_batch_p16",
              "large_batch_p1", "gqa_verify4", "gqa_decode_devalloc", "gqa_prefill512")
-DEFAULT_WORKLOAD = "gqa_decode"
+DEFAULT_WORKLOAD = "large_batch_p16"
+# a second workload timed in the same run and reported under "legs"
+EXTRA_LEGS = {"large_batch_p16": ("large_batch_p1",)}
 
 
 # ---------------------------------------------------------------------------
 # Workloads as host-operation scripts, replayed by the product and the oracle.
 # ---------------------------------------------------------------------------
 class Scenario:
-    def __init__(self, name, seed):
+    """A workload as a script of host operations. ``layers`` overrides the
+    layer count of the 32-layer workloads (a one-layer variant launches the
+    same per-layer kernels on the same lengths, for captures that must stay
+    small); ``inputs`` is the generator of q/k/v rows (``kv_rows`` and
+    ``q_rows`` as in the workloads module, the default)."""
+
+    def __init__(self, name, seed, layers=None, inputs=None, lengths=None):
         self.name = name
         self.seed = seed
+        self.inputs = wl if inputs is None else inputs
         self.devalloc = name.endswith("_devalloc")  # page bookkeeping on the device (kvp_dev_*)
         if self.devalloc:
             name = name[:-len("_devalloc")]
@@ -78,7 +87,7 @@ class Scenario:
         elif name == "prefix_sharing":
             w = wl.prefix_sharing(seed)
         elif name.startswith("large_batch_p"):
-            w = wl.large_batch(seed, P=int(name[len("large_batch_p"):]))
+            w = wl.large_batch(seed, P=int(name[len("large_batch_p"):]), layers=layers or 32, lengths=lengths)
         else:
             raise ValueError(f"unknown workload {name}")
         self.w = w
@@ -131,6 +140,7 @@ class Scenario:
         self.verify = w.extra.get("verify", 0)  # drafted tokens verified per request and step (0: decode)
         self.prefill = w.extra.get("prefill", 0)  # chunk tokens prefilled per request and step (0: decode)
         self.multi = self.verify or self.prefill  # query tokens per request and step, when more than one
+        self.l2_resident = name == "prefix_sharing"  # most attended rows are a shared prefix held in L2
 
 
 def attended_span(sc, L):
@@ -254,7 +264,7 @@ def build_product_device(sc, dev):
     step = 1 << 18
     for layer in range(w.layers):
         for s0 in range(0, rr.numel(), step):
-            k, v = wl.kv_rows(sc.seed, layer, rr[s0:s0 + step], pos[s0:s0 + step], w.Hkv, w.D, dtype=tdt, device=dev)
+            k, v = sc.inputs.kv_rows(sc.seed, layer, rr[s0:s0 + step], pos[s0:s0 + step], w.Hkv, w.D, dtype=tdt, device=dev)
             cache.store(layer, k, v, slots[s0:s0 + step].contiguous())
     torch.cuda.synchronize(dev)
     cache.check()
@@ -282,7 +292,7 @@ def build_product(sc, dev):
         step = 1 << 18
         for layer in range(w.layers):
             for s in range(0, rids.numel(), step):
-                k, v = wl.kv_rows(sc.seed, layer, rids[s:s + step], pos[s:s + step], w.Hkv, w.D, dtype=tdt,
+                k, v = sc.inputs.kv_rows(sc.seed, layer, rids[s:s + step], pos[s:s + step], w.Hkv, w.D, dtype=tdt,
                                   device=dev)
                 cache.store(layer, k, v, slots[s:s + step].contiguous())
         pend.clear()
@@ -363,15 +373,13 @@ def prepare_steps(sc, cache, lens, first_step, n_steps, dev, host_inputs=False):
         post = []
         if sc.window > 0:
             for r, L in zip(sc.rids, lens):
-                wr = cache.host.trim(r, max(0, L + 1 - (sc.window - sc.sinks)), sinks=sc.sinks)
-                cache.dropped[r] += len(wr)
-                post += wr
+                post += cache.host.trim(r, max(0, L + 1 - (sc.window - sc.sinks)), sinks=sc.sinks)
         st.n_post = len(post)
         st.post = None if not post else tuple(_i32(x, dev) for x in zip(*post))
         st.q, st.k, st.v = [], [], []
         for layer in range(w.layers):
-            q = wl.q_rows(sc.seed, s, layer, sc.rids, w.Hq, w.D, dtype=tdt, device=dev)
-            k, v = wl.kv_rows(sc.seed, layer, sc.rids, positions, w.Hkv, w.D, dtype=tdt, device=dev)
+            q = sc.inputs.q_rows(sc.seed, s, layer, sc.rids, w.Hq, w.D, dtype=tdt, device=dev)
+            k, v = sc.inputs.kv_rows(sc.seed, layer, sc.rids, positions, w.Hkv, w.D, dtype=tdt, device=dev)
             if host_inputs:
                 q, k, v = (x.cpu().pin_memory() for x in (q, k, v))
             st.q.append(q)
@@ -399,8 +407,8 @@ def _prepare_device_step(sc, lens, s, dev, host_inputs):
     st.lens_list = list(lens)
     st.q, st.k, st.v = [], [], []
     for layer in range(w.layers):
-        q = wl.q_rows(sc.seed, s, layer, sc.rids, w.Hq, w.D, dtype=tdt, device=dev)
-        k, v = wl.kv_rows(sc.seed, layer, sc.rids, positions, w.Hkv, w.D, dtype=tdt, device=dev)
+        q = sc.inputs.q_rows(sc.seed, s, layer, sc.rids, w.Hq, w.D, dtype=tdt, device=dev)
+        k, v = sc.inputs.kv_rows(sc.seed, layer, sc.rids, positions, w.Hkv, w.D, dtype=tdt, device=dev)
         if host_inputs:
             q, k, v = (x.cpu().pin_memory() for x in (q, k, v))
         st.q.append(q)
@@ -439,9 +447,9 @@ def _prepare_verify_step(sc, cache, lens, s, dev, host_inputs):
     st.post = None if not post else tuple(_i32(x, dev) for x in zip(*post))
     st.q, st.k, st.v = [], [], []
     for layer in range(w.layers):
-        q = torch.stack([wl.q_rows(sc.seed, s * M + j, layer, sc.rids, w.Hq, w.D, dtype=tdt, device=dev)
+        q = torch.stack([sc.inputs.q_rows(sc.seed, s * M + j, layer, sc.rids, w.Hq, w.D, dtype=tdt, device=dev)
                          for j in range(M)], dim=1).contiguous()
-        k, v = wl.kv_rows(sc.seed, layer, rr, positions, w.Hkv, w.D, dtype=tdt, device=dev)
+        k, v = sc.inputs.kv_rows(sc.seed, layer, rr, positions, w.Hkv, w.D, dtype=tdt, device=dev)
         if host_inputs:
             q, k, v = (x.cpu().pin_memory() for x in (q, k, v))
         st.q.append(q)
@@ -624,13 +632,37 @@ def reduce_over_ranks(elapsed_ms, total_bytes, tokens, e2e_ms, e2e_bytes, world,
 
 
 def run_gpu(args, rank, world, local_rank):
+    """The headline workload's line, with the extra legs of the same run
+    (each timed the same way, one after the other) under ``legs``."""
+    line = measure(args, args.workload, rank, world, local_rank, with_cpu=True)
+    if args.no_extra:
+        return line
+    for name in EXTRA_LEGS.get(args.workload, ()):
+        gc_cuda()
+        leg = measure(args, name, rank, world, local_rank, with_cpu=False)
+        if line is not None:
+            line.setdefault("legs", {})[name] = {k: leg[k] for k in (
+                "value", "unit", "ms_per_step", "tokens_per_s", "pct_of_peak", "pct_of_nominal_8tbs", "gpu_launches",
+                "roofline", "e2e", "clocks", "config")}
+    return line
+
+
+def gc_cuda():
+    import gc
+
+    gc.collect()
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+def measure(args, name, rank, world, local_rank, with_cpu):
     from paged_decode_attention_store_gb300 import binding as kb
     from paged_decode_attention_store_gb300.engine import PagedKVCache  # noqa: F401  (fail loudly if missing)
 
     kb.lib()
     dev = torch.device(f"cuda:{local_rank}")
     torch.cuda.set_device(dev)
-    sc = Scenario(args.workload, args.seed + rank)
+    sc = Scenario(name, args.seed + rank, layers=args.layers)
     w = sc.w
     cache, lens = build_product(sc, dev)
     K, W = args.steps, args.warmup
@@ -697,7 +729,7 @@ def run_gpu(args, rank, world, local_rank):
     if device_twin(sc):
         del cache
         torch.cuda.empty_cache()
-        sc_dev = Scenario(sc.name + "_devalloc", sc.seed)
+        sc_dev = Scenario(sc.name + "_devalloc", sc.seed, layers=args.layers)
         cache, lens_dev = build_product_device(sc_dev, dev)
         e2e = run_e2e(args, sc_dev, cache, lens_dev, W + 2 * K + 1, dev)
         e2e["path"] = ("DevicePagedKVCache.decode_step_host (kvp_decode_step_device_io: page bookkeeping on the "
@@ -719,6 +751,7 @@ def run_gpu(args, rank, world, local_rank):
     value = total_bytes / (elapsed_ms * 1e-3) / 1e9
     achieved = attn_bytes_mean / (statistics.mean(attn_ms) * 1e-3) / 1e9
     traffic = ncu_traffic(sc.name)
+    launch_s = statistics.mean(attn_ms) * 1e-3
     roofline = {
         "bound": "hbm",
         "kernel": "tc_decode_kernel",
@@ -729,10 +762,26 @@ def run_gpu(args, rank, world, local_rank):
         "frac": round(achieved / peak, 4),
         "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
         "traffic": traffic,
+        "basis": "algorithmic bytes per launch / CUDA-event launch time",
+        "dram_gbs": None if traffic is None else round(traffic / launch_s / 1e9, 1),
         "algorithmic_bytes_per_launch": int(attn_bytes_mean),
         "mean_launch_us": round(1e3 * statistics.mean(attn_ms), 2),
         "launches_timed": len(attn_ms),
     }
+    if sc.l2_resident:
+        # most of the logical bytes are the shared prefix, served from L2: the
+        # fraction of the HBM peak is taken on the DRAM bytes ncu counted for
+        # one launch of this workload, the logical rate reported beside it
+        dram = None if traffic is None else traffic / launch_s / 1e9
+        roofline.update({
+            "achieved": None if dram is None else round(dram, 1),
+            "frac": None if dram is None else round(dram / peak, 4),
+            "frac_of_nominal_8tbs": None if dram is None else round(dram / NOMINAL_HBM_GBS, 4),
+            "logical_gbs": round(achieved, 1),
+            "basis": ("ncu DRAM bytes per launch (dram__bytes_read + write) / CUDA-event launch time" if dram is not None
+                      else "no ncu summary of the current kernel source: DRAM bytes unknown (logical bytes are "
+                           "mostly L2 hits and would overstate the HBM rate)"),
+        })
     if sc.prefill:  # a dense contraction: flops against the measured bf16 tensor peak
         flops_mean = statistics.mean(st.attn_flops for st in steps[W + K:W + 2 * K])
         tf = flops_mean / (statistics.mean(attn_ms) * 1e-3) / 1e12
@@ -772,7 +821,9 @@ def run_gpu(args, rank, world, local_rank):
                 attended_count(sc, L) for L in steps[W].lens_list), 1),
             "kv_bytes_per_step": int(sum(attended_count(sc, L) for L in steps[W].lens_list)
                                      * 2 * w.Hkv * w.D * 2 * w.layers),
-            "l2": "no flush: inputs larger than L2 (K/V read per step >> 129 MB)",
+            "l2": ("no flush: the shared prefix (8 x 129 pages, 67.6 MB) stays L2-resident by design; roofline.frac "
+                   "uses ncu DRAM bytes" if sc.l2_resident else
+                   "no flush: inputs larger than L2 (K/V read per step >> 129 MB)"),
             "seed": args.seed,
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
         },
@@ -793,16 +844,15 @@ def run_gpu(args, rank, world, local_rank):
         },
         "clocks": clocks,
     }
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and with_cpu and not args.no_cpu_baseline:
         single = cpu_baseline(sc, args.cpu_seconds)
         line["cpu_baseline"] = single
-        if sc.w.layers == 1:  # the one-layer oracle state is small enough to hold once per core
-            try:
-                allc = cpu_baseline_all_cores(sc, args.cpu_seconds, min(os.cpu_count() or 1, 16))
-                line["cpu_baseline"] = dict(single, value=allc["value"], cores=allc["cores"], sample=allc["sample"],
-                                            single_core={"value": single["value"], "sample": single["sample"]})
-            except Exception as e:  # keep the single-core figure, and say why
-                line["cpu_baseline"]["all_cores_unavailable"] = repr(e)[:200]
+        try:
+            allc = cpu_baseline_all_cores(sc, args.cpu_seconds, min(os.cpu_count() or 1, 16))
+            line["cpu_baseline"] = dict(single, value=allc["value"], cores=allc["cores"], sample=allc["sample"],
+                                        single_core={"value": single["value"], "sample": single["sample"]})
+        except Exception as e:  # keep the single-core figure, and say why
+            line["cpu_baseline"]["all_cores_unavailable"] = repr(e)[:200]
     return line
 
 
@@ -908,9 +958,9 @@ def _host_inputs(sc, first_step, K, lens):
             positions = [L + j for L in lens for j in range(M)]
             qs, ks, vs = [], [], []
             for layer in range(w.layers):
-                q = torch.stack([wl.q_rows(sc.seed, s * M + j, layer, sc.rids, w.Hq, w.D, dtype=tdt, device=dev)
+                q = torch.stack([sc.inputs.q_rows(sc.seed, s * M + j, layer, sc.rids, w.Hq, w.D, dtype=tdt, device=dev)
                                  for j in range(M)], dim=1)
-                k, v = wl.kv_rows(sc.seed, layer, rr, positions, w.Hkv, w.D, dtype=tdt, device=dev)
+                k, v = sc.inputs.kv_rows(sc.seed, layer, rr, positions, w.Hkv, w.D, dtype=tdt, device=dev)
                 qs.append(q.cpu().pin_memory())
                 ks.append(k.cpu().pin_memory())
                 vs.append(v.cpu().pin_memory())
@@ -922,8 +972,8 @@ def _host_inputs(sc, first_step, K, lens):
         positions = [L + i for L in lens]
         qs, ks, vs = [], [], []
         for layer in range(w.layers):
-            q = wl.q_rows(sc.seed, s, layer, sc.rids, w.Hq, w.D, dtype=tdt, device=dev)
-            k, v = wl.kv_rows(sc.seed, layer, sc.rids, positions, w.Hkv, w.D, dtype=tdt, device=dev)
+            q = sc.inputs.q_rows(sc.seed, s, layer, sc.rids, w.Hq, w.D, dtype=tdt, device=dev)
+            k, v = sc.inputs.kv_rows(sc.seed, layer, sc.rids, positions, w.Hkv, w.D, dtype=tdt, device=dev)
             qs.append(q.cpu().pin_memory())
             ks.append(k.cpu().pin_memory())
             vs.append(v.cpu().pin_memory())
@@ -961,7 +1011,7 @@ class OracleSample:
             return
         w = self.sc.w
         for layer in self.layers:
-            k, v = wl.kv_rows(self.sc.seed, layer, rid, positions, w.Hkv, w.D, dtype=self.tdt)
+            k, v = self.sc.inputs.kv_rows(self.sc.seed, layer, rid, positions, w.Hkv, w.D, dtype=self.tdt)
             self.stores[layer].store_cache(slots, k.float().numpy(), v.float().numpy())
 
     def _append(self, rids):
@@ -1037,7 +1087,7 @@ class OracleSample:
                 for j, pos in enumerate(OA.verify_positions(L, M, sc.window, sc.sinks)):
                     if queries is not None and j not in queries:
                         continue
-                    q = wl.q_rows(sc.seed, step_index * M + j, layer, [r], w.Hq, w.D, dtype=self.tdt)[0]
+                    q = sc.inputs.q_rows(sc.seed, step_index * M + j, layer, [r], w.Hq, w.D, dtype=self.tdt)[0]
                     sl = [s for p in pos for s in OA.gather_block(row, w.P, p, p + 1)]
                     per_q.append(OA.attend_request(self.stores[layer], q.float().numpy(), sl, w.scale))
                 outs[(r, layer)] = np.stack(per_q)
@@ -1064,7 +1114,7 @@ class OracleSample:
             L = self.pt.length[r]
             pos = OA.attended_positions(L, sc.window, sc.sinks)
             for layer in self.layers:
-                q = wl.q_rows(sc.seed, step_index, layer, [r], w.Hq, w.D, dtype=self.tdt)[0].float().numpy()
+                q = sc.inputs.q_rows(sc.seed, step_index, layer, [r], w.Hq, w.D, dtype=self.tdt)[0].float().numpy()
                 if self.raw is not None:
                     row = self.raw.page_table[r]
                     sl = [s for p in pos for s in OA.gather_raw(row, p, p + 1)]
@@ -1128,22 +1178,22 @@ def cpu_baseline(sc, seconds):
     }
 
 
-def _oracle_worker(name, seed, sample, seconds, barrier, out_q):
+def _oracle_worker(name, seed, n_layers, layers, sample, seconds, barrier, out_q):
     """One process of the all-cores oracle timing: builds the workload's
-    oracle state, waits for the others, then times decode steps of its own
-    sample of requests for about ``seconds``."""
+    oracle state for its layers, waits for the others, then times decode
+    steps of its own sample of requests for about ``seconds``."""
     try:
-        sc = Scenario(name, seed)
-        orc = OracleSample(sc, sample)
+        sc = Scenario(name, seed, layers=n_layers)
+        orc = OracleSample(sc, sample, layers=layers)
         queries, frac = timed_queries(sc)
-        barrier.wait(timeout=300)
+        barrier.wait(timeout=600)
         done, t_total, steps = 0.0, 0.0, 0
         while t_total < seconds or steps == 0:
             steps += 1
             t = time.perf_counter()
             orc.step(10_000 + steps, sample, queries=queries)
             t_total += time.perf_counter() - t
-            done += frac * sc.w.layers * attention_bytes(sc, [orc.pt.length[r] for r in sample])
+            done += frac * len(orc.layers) * attention_bytes(sc, [orc.pt.length[r] for r in sample])
         out_q.put((done, t_total, steps, len(sample)))
     except Exception as e:  # reported to the parent, which then keeps the single-core figure
         out_q.put(repr(e))
@@ -1151,24 +1201,32 @@ def _oracle_worker(name, seed, sample, seconds, barrier, out_q):
 
 def cpu_baseline_all_cores(sc, seconds, workers):
     """The oracle on ``workers`` host cores at once: one spawned process per
-    core, each on its own sample of requests (disjoint, spread over the
-    batch), timed together; the value is the sum of their rates."""
+    core, timed together; the value is the sum of their rates. One-layer
+    workloads give each process its own sample of requests (disjoint, spread
+    over the batch); multi-layer workloads give each its own layers (the
+    same two requests, every layer taken by one process), whose oracle state
+    stays small."""
     import multiprocessing as mp
 
     ctx = mp.get_context("spawn")  # safe after CUDA has been initialised
-    B = len(sc.rids)
-    per = max(1, min(4, B // workers))
-    samples = [s for s in ([sc.rids[i] for i in range(w, B, workers)][:per] for w in range(workers)) if s]
-    barrier, out_q = ctx.Barrier(len(samples)), ctx.Queue()
-    procs = [ctx.Process(target=_oracle_worker, args=(sc.name, sc.seed, smp, seconds, barrier, out_q), daemon=True)
-             for smp in samples]
+    B, NL = len(sc.rids), sc.w.layers
+    if NL == 1:
+        per = max(1, min(4, B // workers))
+        jobs = [([0], s) for s in ([sc.rids[i] for i in range(w, B, workers)][:per] for w in range(workers)) if s]
+    else:
+        per = 2
+        sample = _sample_rids(sc, per)
+        jobs = [(list(range(w, NL, workers)), sample) for w in range(min(workers, NL))]
+    barrier, out_q = ctx.Barrier(len(jobs)), ctx.Queue()
+    procs = [ctx.Process(target=_oracle_worker, args=(sc.name, sc.seed, NL, lay, smp, seconds, barrier, out_q),
+                         daemon=True) for lay, smp in jobs]
     import queue
 
     for p in procs:
         p.start()
     res = []
     try:
-        deadline = time.time() + 900
+        deadline = time.time() + 1200
         while len(res) < len(procs):
             try:
                 res.append(out_q.get(timeout=1.0))
@@ -1185,17 +1243,20 @@ def cpu_baseline_all_cores(sc, seconds, workers):
     if bad:
         raise RuntimeError(bad[0])
     rate = sum(d / t for d, t, _, _ in res)
+    steps = min(r[2] for r in res)
     return {
         "value": round(rate / 1e9, 6),
         "cores": len(procs),
-        "sample": f"{len(procs)} processes, each {min(r[2] for r in res)}+ decode steps of its own {per} of {B} "
-                  f"requests (all {sc.w.layers} layers), timed together; rates summed",
+        "sample": (f"{len(procs)} processes, each {steps}+ decode steps of its own {per} of {B} requests, timed "
+                   f"together; rates summed" if NL == 1 else
+                   f"{len(procs)} processes, each {steps}+ decode steps of the same {per} of {B} requests on its own "
+                   f"{len(jobs[0][0])} of {NL} layers (every layer taken once), timed together; rates summed"),
     }
 
 
 def run_reference(args):
     """--impl reference: the CPU oracle on the same workload, metric and unit."""
-    sc = Scenario(args.workload, args.seed)
+    sc = Scenario(args.workload, args.seed, layers=args.layers)
     n = 2 if sc.w.layers == 1 else 1
     sample = _sample_rids(sc, n)
     orc = OracleSample(sc, sample)
@@ -1244,6 +1305,9 @@ def main():
     ap.add_argument("--soak", type=float, default=1.0, help="seconds of untimed attention before warm-up")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the extra legs of the headline workload")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="layer count of the 32-layer workloads (a small variant for ncu captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -275,16 +275,20 @@ int store_cache_and_attention(const kvp_pool* pool, int layer, const void* q,
  * reservations, callers that may not enter an allocator from their thread,
  * plug-in hosts that only receive their input and output buffers). There is
  * no counterpart in the source pages: it is an interface convenience.
- * Same arguments and results as paged_decode_attention minus the workspace:
- * the split-K scratch is a fixed 12 MiB array in the library's own device
- * memory, held by every GPU that loads it until the process exits.
+ * Same arguments (window and sinks included) and results as
+ * paged_decode_attention minus the workspace: the split-K scratch is a fixed
+ * 12 MiB array in the library's own device memory, held by every GPU that
+ * loads it until the process exits.
  *  - The pool's device must be current. The first call on a device looks up
- *    the array's device address (cudaGetSymbolAddress) and keeps it; make
- *    that first call before any stream capture.
+ *    the array's device address (cudaGetSymbolAddress) and keeps it with the
+ *    CUDA context it belongs to; make that first call before any stream
+ *    capture. After a device reset a call finds another context current and
+ *    looks the address up again (outside a capture, as the first call).
  *  - No allocation of any kind (no cudaMalloc/cudaFree, no library
  *    allocator) happens in any call.
  *  - A shape whose scratch would exceed 12 MiB is rejected with
- *    KVP_ERR_INVALID_ARG and nothing is launched.
+ *    KVP_ERR_INVALID_ARG and nothing is launched; so is a pool of another
+ *    device than the current one.
  *  - Every call on a device shares the one array: calls that overlap on the
  *    GPU (different streams, or different pools on the same device) race and
  *    must be serialised by the caller. The array keeps the last call's
@@ -296,7 +300,8 @@ int paged_decode_attention_noalloc(const kvp_pool* pool, int layer,
                                    int table_cols, int table_mode,
                                    const int32_t* table_rows,
                                    const int32_t* context_lens, int window,
-                                   float scale, void* out, void* stream);
+                                   int sinks, float scale, void* out,
+                                   void* stream);
 
 /* ------------------------------------------------------------------------
  * gather_indices: the slots paged_decode_attention would read, for

@@ -23,7 +23,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from .attention import SlotStore, attend_request, gather_block, gather_raw, window_lo
+from .attention import SlotStore, attend_request, gather_block, window_lo
 
 
 def _span(L: int, window, sinks: int):
@@ -93,11 +93,3 @@ class BlockDecoder:
                 self._trim(rid)
         return slots, cows, np.stack(outs)
 
-
-def attend_raw(store: SlotStore, raw_row, q, L: int, window, scale: float, sinks: int = 0):
-    """Decode attention of one request through a raw-location table row."""
-    if sinks:
-        sink_end, lo, _ = _span(L, window, sinks)
-        return attend_request(store, q, gather_raw(raw_row, 0, sink_end) + gather_raw(raw_row, lo, L), scale)
-    lo = window_lo(L, window)
-    return attend_request(store, q, gather_raw(raw_row, lo, L), scale)

@@ -49,7 +49,7 @@ SIGNATURES = {
     "paged_verify_attention_workspace_size": [_vp, _i, _i, _i, _szp],
     "paged_verify_attention": [_vp, _i, _vp, _i, _i, _i, _vp, _i, _i, _i, _vp, _vp, _i, _i, _f, _vp, _vp, _sz, _vp],
     "paged_prefill_attention": [_vp, _i, _vp, _i, _i, _i, _vp, _vp, _i, _i, _i, _vp, _vp, _i, _i, _f, _vp, _vp],
-    "paged_decode_attention_noalloc": [_vp, _i, _vp, _i, _i, _vp, _i, _i, _i, _vp, _vp, _i, _f, _vp, _vp],
+    "paged_decode_attention_noalloc": [_vp, _i, _vp, _i, _i, _vp, _i, _i, _i, _vp, _vp, _i, _i, _f, _vp, _vp],
     "store_cache_and_attention": [_vp, _i, _vp, _vp, _vp, _vp, _i, _i, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _i,
                                   _i, _i, _f, _vp, _vp, _sz, _vp],
     "gather_indices": [_vp, _vp, _i, _i, _i, _vp, _vp, _i, _i, _i, _vp, _i, _vp],
@@ -437,7 +437,7 @@ def store_cache_and_attention(pool, layer, q, k, v, out_loc, table, table_mode, 
 
 
 def paged_decode_attention_noalloc(pool, layer, q, table, table_mode, context_lens, window, scale, out,
-                                   table_rows=None, stream=None):
+                                   table_rows=None, stream=None, sinks=0):
     """paged_decode_attention without a workspace argument, for callers that
     cannot allocate: the library uses a fixed scratch array of its own (see
     include/pagedkv.h). Overlapping calls on one device must be serialised."""
@@ -453,7 +453,8 @@ def paged_decode_attention_noalloc(pool, layer, q, table, table_mode, context_le
         raise ValueError("q/out must be [B, Hq, D] and context_lens [B]")
     _check(lib().paged_decode_attention_noalloc(pool.handle, layer, _ptr(q), B, Hq, _ptr(table), table.shape[0],
                                                 table.shape[1], table_mode, _ptr(table_rows), _ptr(context_lens),
-                                                int(window or 0), float(scale), _ptr(out), _stream(stream)),
+                                                int(window or 0), int(sinks), float(scale), _ptr(out),
+                                                _stream(stream)),
            "paged_decode_attention_noalloc")
 
 

@@ -60,8 +60,7 @@ class PagedKVCache:
         self.table_mode = kb.KVP_RAW_LOCATIONS if self.raw else kb.KVP_BLOCK_TABLE
         self._ws = {}
         self._steps = {}
-        self.lengths = np.zeros(max_requests, np.int64)  # rows stored, per request (mirrors the host table)
-        self.dropped = np.zeros(max_requests, np.int64)  # pages released by the window, per request
+        self.lengths = np.zeros(max_requests, np.int64)  # tokens appended, per request (the caller's count)
         self.copies = 0
         self.h2d_bytes = 0  # bytes this driver has copied host -> device
 
@@ -85,22 +84,21 @@ class PagedKVCache:
     # -- request lifecycle ---------------------------------------------------
     def new(self, rid):
         self.host.new(rid)
-        self.lengths[rid] = self.dropped[rid] = 0
+        self.lengths[rid] = 0
 
     def fork(self, src, dst):
         self._write_table(self.host.fork(src, dst))
-        self.lengths[dst], self.dropped[dst] = self.lengths[src], self.dropped[src]
+        self.lengths[dst] = self.lengths[src]
 
     def release(self, rid):
         self.host.release(rid)
-        self.lengths[rid] = self.dropped[rid] = 0
+        self.lengths[rid] = 0
 
     def trim(self, rid, keep_from, sinks=0):
         """Release the pages below keep_from (except the first ceil(sinks / P));
         returns the number of table writes."""
         writes = self.host.trim(rid, keep_from, sinks=sinks)
         self._write_table(writes)
-        self.dropped[rid] += len(writes)
         return len(writes)
 
     def append(self, rids):
@@ -285,15 +283,6 @@ class PagedKVCache:
         self.last_writes, self.last_copies, self.last_trims = info.n_table_writes, info.n_copies, info.n_trim_writes
         self.copies += info.n_copies
         np.add.at(self.lengths, rids, 1)
-        if window and window > 0 and info.n_trim_writes:
-            # mirror the released pages: the native call releases every page that
-            # lies wholly below keep_from = L + 1 - (window - sinks), after the
-            # first ceil(sinks / P)
-            Lr = self.lengths[rids]
-            keep = Lr + 1 - (window - sinks)
-            sp = -(-sinks // self.P)
-            to = np.minimum(np.maximum(keep, 0) // self.P, -(-Lr // self.P))
-            self.dropped[rids] = np.maximum(self.dropped[rids], to - sp)
         if host_io:
             if side:
                 with torch.cuda.stream(st["d2h"]):

@@ -15,15 +15,18 @@ device, in any order, bit-identically. The recipe:
    ``mix32`` is the "lowbias32" integer hash published by C. Wellons (hash
    prospector): ``x ^= x>>16; x *= 0x7feb352d; x ^= x>>15; x *= 0x846ca68b;
    x ^= x>>16`` (mod 2^32).
-2. The three low bytes of ``h`` are summed (Irwin-Hall with three terms),
-   centred and scaled: ``(b0 + b1 + b2 - 382) / 128``. The result has mean
-   ~0.004, standard deviation 1.000 and support [-2.98, 3.0]: a bounded
-   stand-in for N(0, 1) that is exact in float32.
+2. The top 16 bits ``i = h >> 16`` pick one of 2^16 equiprobable levels of
+   N(0, 1) by inverse transform sampling: the value is the standard normal
+   quantile at the level's midpoint, ``Phi^-1((i + 0.5) / 2^16)``, from a
+   table computed once in float64 (``statistics.NormalDist().inv_cdf``) and
+   rounded to float32. The result is N(0, 1) up to a discretisation far
+   below bf16 resolution; its support is +-4.33 (the standard normal puts
+   1.5e-5 of its mass beyond that).
 3. bf16 workloads round that float32 value to bf16 (round to nearest even).
 
 All integer steps run in int64 tensors holding 32-bit values, with the
-32-bit products split in 16-bit halves so that no step overflows; torch
-gives the same bits on CPU and CUDA.
+32-bit products split in 16-bit halves so that no step overflows, and the
+quantile step is a table gather; torch gives the same bits on CPU and CUDA.
 
 Element indices
 ---------------
@@ -37,6 +40,7 @@ stream numpy keeps frozen across versions).
 from __future__ import annotations
 
 import math
+import statistics
 from dataclasses import dataclass, field
 
 import numpy as np
@@ -68,14 +72,32 @@ def _mix32_i(x: int) -> int:
     return x ^ (x >> 16)
 
 
+_LEVELS = 1 << 16
+_QUANTILES = {}
+
+
+def _quantile_table(device) -> torch.Tensor:
+    """Standard normal quantiles at the midpoints of 2^16 equiprobable
+    levels, float32, cached per device (built on the host, then copied)."""
+    key = str(torch.device(device))
+    t = _QUANTILES.get(key)
+    if t is None:
+        if "cpu" not in _QUANTILES:
+            nd = statistics.NormalDist()
+            _QUANTILES["cpu"] = torch.tensor([nd.inv_cdf((i + 0.5) / _LEVELS) for i in range(_LEVELS)],
+                                             dtype=torch.float64).to(torch.float32)
+        t = _QUANTILES["cpu"].to(device)
+        _QUANTILES[key] = t
+    return t
+
+
 def hash_normal(seed: int, stream: int, idx: torch.Tensor) -> torch.Tensor:
-    """float32 approximately-N(0,1) value for each int64 element index."""
+    """float32 N(0,1) value (2^16-level inverse transform) for each int64 element index."""
     key = _mix32_i(_mix32_i(seed * 0x9E3779B9 + 0x632BE5AB) ^ (stream * 0x85EBCA77))
     lo = idx & _M32
     hi = idx >> 32
     h = _mix32_t(lo ^ _mix32_t((hi + key) & _M32))
-    s = (h & 255) + ((h >> 8) & 255) + ((h >> 16) & 255) - 382
-    return s.to(torch.float32) * (1.0 / 128.0)
+    return _quantile_table(idx.device)[h >> 16]
 
 
 def _as_index(x, device) -> torch.Tensor:
@@ -249,20 +271,65 @@ def prefix_sharing(seed: int = 0) -> Workload:
                            "prompt_len": prompt_len, "suffix": suffix})
 
 
-def large_batch(seed: int = 0, P: int = 16, headroom: int = 256) -> Workload:
+def large_batch(seed: int = 0, P: int = 16, headroom: int = 256, layers: int = 32, lengths=None) -> Workload:
     """mini-sglang layout: bf16, 64 q / 8 kv heads, head_dim 128, batch 256,
     32 layers, context lengths lognormal (median 1024, sigma 0.8) capped at
     16384 (minus ``headroom`` decode steps), raw token-location page table of
-    shape (257, align32(16384)), run at page 16 and page 1."""
+    shape (257, align32(16384)), run at page 16 and page 1. ``layers`` and
+    ``lengths`` (a replacement list of 256 lengths) make variants of it."""
     B, max_seq = 256, 16384
     rs = np.random.RandomState(seed * 7919 + 8)
     draw = rs.lognormal(mean=math.log(1024.0), sigma=0.8, size=B)
-    lengths = [int(min(max_seq - headroom, max(1, math.floor(x + 0.5)))) for x in draw]
+    if lengths is None:
+        lengths = [int(min(max_seq - headroom, max(1, math.floor(x + 0.5)))) for x in draw]
+    lengths = [int(L) for L in lengths]
+    assert len(lengths) == B and all(1 <= L <= max_seq - headroom for L in lengths)
     need = sum(-(-(L + headroom) // P) for L in lengths)
     n_pages = int(math.ceil(need * 1.1))
     order = np.random.RandomState(seed * 7919 + 9 + P).permutation(n_pages)
-    return Workload(f"large_batch_p{P}", "bf16", 64, 8, 128, P, 32, n_pages,
+    return Workload(f"large_batch_p{P}", "bf16", 64, 8, 128, P, layers, n_pages,
                     free_stack_for_order(order), lengths, scale=1.0 / math.sqrt(128),
                     table_mode="raw",
                     extra={"max_running_req": B, "max_seq_len": max_seq,
                            "headroom": headroom})
+
+
+class CodedInputs:
+    """Structured inputs whose attention outputs show which K/V rows were read.
+
+    K and the odd query heads come from the seeded generator above; the even
+    query heads are zero, so their scores are all equal. Each V row holds
+    two ones and zeros elsewhere, placed by the token's position ``t`` over
+    the ``Hkv * D`` entries of a row (``half = D / 2`` entries per head):
+
+    - row code: entry ``(h, d)`` with ``h * half + d = t mod (Hkv * half)``;
+    - stage code: entry ``(h, half + d)`` with ``h * half + d = (t div 16)
+      mod (Hkv * half)``, one entry per 16-position group.
+
+    The values are exact in bf16. Every output entry is then a weighted count
+    of the attended rows of one residue class, so a row or a 16-row group that
+    is read twice, skipped or taken from another position moves an entry by a
+    whole row's weight.
+    """
+
+    STAGE = 16
+
+    def kv_rows(self, seed, layer, rid, pos, Hkv, D, dtype=torch.bfloat16, device="cpu"):
+        k, _ = kv_rows(seed, layer, rid, pos, Hkv, D, dtype=dtype, device=device)
+        rid = _as_index(rid, device)
+        pos = _as_index(pos, device)
+        rid, pos = torch.broadcast_tensors(rid, pos)
+        half = D // 2
+        n = pos.numel()
+        v = torch.zeros((n, Hkv * D), dtype=dtype, device=device)
+        rows = torch.arange(n, device=device)
+        c = pos % (Hkv * half)
+        v[rows, (c // half) * D + c % half] = 1
+        c = (pos // self.STAGE) % (Hkv * half)
+        v[rows, (c // half) * D + half + c % half] = 1
+        return k, v.view(n, Hkv, D)
+
+    def q_rows(self, seed, step, layer, rid, Hq, D, dtype=torch.bfloat16, device="cpu"):
+        q = q_rows(seed, step, layer, rid, Hq, D, dtype=dtype, device=device)
+        q[:, 0::2, :] = 0
+        return q

@@ -16,7 +16,7 @@ import pytest
 import torch
 
 import oracle.attention as OA
-from gpu_harness import OracleSession, ProductSession, max_abs, tol_for
+from gpu_harness import OracleSession, ProductSession, close
 from libbuild import ensure_built
 from paged_decode_attention_store_gb300 import workloads as wl
 
@@ -75,13 +75,11 @@ def test_prefill_chunk_matches_the_oracle(kb, case):
     torch.cuda.synchronize()
     assert prod.error() == 0
     got = out.float().cpu().numpy()
-    tol = tol_for(dtype)
     for b in range(B):
         for j, pos in enumerate(OA.verify_positions(lens[b], q_lens[b], W if W else None, S)):
             sl = [s for p in pos for s in orc.slots(b, p, p + 1)]
             ref = OA.attend_request(orc.stores[0], q[b, j].float().cpu().numpy(), sl, w.scale)
-            d = max_abs(got[b, j], ref)
-            assert d <= tol, f"request {b} query {j} (L={lens[b]}, q_len={q_lens[b]}): {d}"
+            close(got[b, j], ref, dtype, f"request {b} query {j} (L={lens[b]}, q_len={q_lens[b]})")
         assert (got[b, q_lens[b]:] == 7.0).all(), f"request {b}: rows past the chunk were written"
 
 
@@ -137,4 +135,4 @@ def test_prefill_bad_lengths_zero_the_request(kb):
     for j, pos in enumerate(OA.verify_positions(lens[0], q_lens[0], None, 0)):
         sl = [s_ for p_ in pos for s_ in orc.slots(0, p_, p_ + 1)]
         ref = OA.attend_request(orc.stores[0], q[0, j].float().cpu().numpy(), sl, w.scale)
-        assert max_abs(got[0, j], ref) <= tol_for("bf16"), f"query {j}"
+        close(got[0, j], ref, "bf16", f"query {j}")

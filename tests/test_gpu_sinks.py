@@ -16,7 +16,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_harness import OracleSession, ProductSession, max_abs, tol_for
+from gpu_harness import OracleSession, ProductSession, close
 from libbuild import ensure_built
 from paged_decode_attention_store_gb300 import workloads as wl
 
@@ -89,7 +89,6 @@ def test_sink_decode_parity(kb, case):
     assert prod.host.used() == orc.pt.used()
     lens = list(lengths)
     rids = list(range(B))
-    tol = tol_for(dtype)
     for step in range(1, steps + 1):
         assert prod.append(rids, lens) == orc.append(rids, lens)
         lens = [L + 1 for L in lens]
@@ -99,8 +98,7 @@ def test_sink_decode_parity(kb, case):
             want = orc.span_slots(b, lens[b], W, S)
             assert len(want) == min(lens[b], W)
             assert got[b, :len(want)].tolist() == want and (got[b, len(want):] == -1).all()
-            d = max_abs(out[b], orc.attend(0, b, lens[b], W, step=step, sinks=S))
-            assert d <= tol, f"step {step} request {b} (L={lens[b]}): {d}"
+            close(out[b], orc.attend(0, b, lens[b], W, step=step, sinks=S), dtype, f"step {step} request {b} (L={lens[b]})")
         for b in rids:
             prod.trim(b, max(0, lens[b] + 1 - (W - S)), sinks=S)
             orc.trim(b, max(0, lens[b] + 1 - (W - S)), sinks=S)
@@ -141,7 +139,7 @@ def test_sink_fused_step_equals_separate_calls(kb, case):
         assert torch.equal(out_f, out_s), f"step {step}: fused output differs"
         got = out_f.float().cpu().numpy()
         for b in rids:
-            assert max_abs(got[b], orc.attend(0, b, new_lens[b], W, step=step, sinks=S)) <= tol_for(dtype)
+            close(got[b], orc.attend(0, b, new_lens[b], W, step=step, sinks=S), dtype, f"step {step} request {b}")
         for b in rids:
             kf = max(0, new_lens[b] + 1 - (W - S))
             sep.trim(b, kf, sinks=S)

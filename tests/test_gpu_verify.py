@@ -16,7 +16,7 @@ import pytest
 import torch
 
 import oracle.attention as OA
-from gpu_harness import OracleSession, ProductSession, max_abs, tol_for
+from gpu_harness import OracleSession, ProductSession, close
 from libbuild import ensure_built
 from paged_decode_attention_store_gb300 import workloads as wl
 
@@ -70,7 +70,6 @@ def test_speculative_steps_match_the_oracle(kb, case):
     R = random.Random(case)
     rids = list(range(B))
     lens = list(lengths)
-    tol = tol_for(dtype)
     i32 = lambda xs: torch.tensor(list(xs), dtype=torch.int32, device=DEV)  # noqa: E731
     for step in range(1, steps + 1):
         # M drafted tokens per request, stored before the verify
@@ -89,8 +88,7 @@ def test_speculative_steps_match_the_oracle(kb, case):
                 qj = q[b, j].float().cpu().numpy()
                 sl = [s for p in pos for s in orc.slots(b, p, p + 1)]
                 ref = OA.attend_request(orc.stores[0], qj, sl, w.scale)
-                d = max_abs(got[b, j], ref)
-                assert d <= tol, f"step {step} request {b} query {j} (L={ctx[b]}): {d}"
+                close(got[b, j], ref, dtype, f"step {step} request {b} query {j} (L={ctx[b]})")
         # accept a random number of drafts, rewind the rest, trim for the next step
         for b in rids:
             acc = R.randrange(0, M + 1)
