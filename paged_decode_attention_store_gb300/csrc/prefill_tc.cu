@@ -9,34 +9,45 @@
 // attends (causal, the same window and sinks; chapter 15, "The model", and
 // its exercise "Attention sinks"), reading K/V in place through the table.
 //
-// How (one CTA of seven warps per 128-row query tile):
+// How (one CTA of eleven warps per pair of 128-row query tiles):
 // * A tile is 128 / G consecutive query tokens of one request times the G
 //   query heads of one KV head: 128 rows of Q, loaded once by TMA (128-byte
-//   swizzle, two 64-element halves of head_dim).
-// * The keys the tile needs (the union of its queries' spans) stream in
+//   swizzle, two 64-element halves of head_dim). A CTA takes two adjacent
+//   tiles (A and B) of the same request and KV head, so every K/V block it
+//   loads serves 256 query rows.
+// * The keys the pair needs (the union of its queries' spans) stream in
 //   blocks of 128: a 16-slot group whose slots are contiguous and 16-aligned
 //   comes by one TMA copy (both halves of head_dim, 4 KB), any other key row
 //   is copied by the loader warp into the same swizzled layout.
-// * S = Q K^T (M 128, K 128, both operands K-major) accumulates in a TMEM
-//   S buffer as two N 64 halves (rows 0-7 and 8-15 of the eight key groups),
-//   so S column c holds key 16 (c % 64 / 8) + 8 (c / 64) + c % 8. Each
-//   thread owns one query row: it reads its 128 scores from TMEM and keeps
-//   an online softmax in log2 units. A block that no row of the warp masks (causal, window, sinks,
-//   block end) skips the mask; the row maximum is taken on unscaled scores
-//   and P = 2^(s * scale - m) is one FMA and one ex2 per score. O is rescaled
-//   (read, scaled, written back in TMEM) only when the row maximum grows by
-//   more than 8, so P <= 256 always fits bf16 and the normalisation stays
-//   exact (numerator and denominator use the same m).
-// * P (bf16, K-major, 128-byte swizzle, columns in key order) goes to shared memory and
-//   O += P V (V as the MN-major operand) accumulates in TMEM. The epilogue
-//   divides by the row sum and stores bf16.
-// * Warp-specialised pipeline: two loader warps fill two-stage K and V rings
-//   (K stage s is free once S has read it, V stage s once P V has), each
-//   resolving its own slots, so K never waits behind V;
-//   an MMA warp issues S(i) into one of two TMEM S buffers and then
-//   O += P(i-1) V(i-1); four softmax warps turn S(i) into P(i) (two P
-//   buffers). The tensor core computes the next block's S while the softmax
-//   works on this one. mbarriers carry every hand-off.
+// * A 128-key block is taken as two half-blocks of 64 keys: rows 0-7 of its
+//   eight 16-key groups (h = 0) and rows 8-15 (h = 1), which is how the
+//   groups lie in shared memory (8-row atoms, 4 KB from group to group).
+//   S = Q K^T of a half-block (M 128, N 64, K 128, both operands K-major)
+//   accumulates in TMEM sub-buffer h of the tile's S region, so its column c
+//   holds key 16 (c / 8) + 8 h + c % 8 of the block. Each softmax thread owns
+//   one query row: it reads the half-block's 64 scores from TMEM and keeps an
+//   online softmax in log2 units. A half-block that no row of the warp masks
+//   (causal, window, sinks, block end) skips the mask; the row maximum is
+//   taken on unscaled scores and P = 2^(s * scale - m) is one FMA and one ex2
+//   per score. O is rescaled (read, scaled, written back in TMEM) only when
+//   the row maximum grows by more than 8, so P <= 256 always fits bf16 and
+//   the normalisation stays exact (numerator and denominator use the same m
+//   and the same rounded P).
+// * P (bf16, two per 32-bit column, in S-column order) is written back into
+//   the first 32 columns of its sub-buffer and is the A operand, read from
+//   TMEM, of O += P V. V is the MN-major B operand in shared memory: the K
+//   step over P columns 16 m .. 16 m + 15 takes rows 8 h .. 8 h + 7 of groups
+//   2 m and 2 m + 1, one 8-row atom each, 4 KB apart. The epilogue divides
+//   by the row sum and stores bf16.
+// * Warp-specialised pipeline: two loader warps fill a three-stage K ring
+//   and a two-stage V ring (a K stage is free once both tiles' S have read
+//   it, a V stage once both P V have), each resolving its own slots; an MMA
+//   warp issues, per half-block j, P_A(j) V and P_B(j) V, then S_A(j + 2)
+//   and S_B(j + 2); two groups of four softmax warps turn the scores of each
+//   tile into P. S_X(j + 1) sits in the other sub-buffer, so the tensor core
+//   computes it while the softmax works on half-block j; S_X(j + 2)
+//   overwrites P_X(j) and is issued once P_X(j) V is done. mbarriers carry
+//   every hand-off.
 // * Every wait is bounded (2 s): on timeout the CTA records KVP_ERR_TIMEOUT,
 //   issues nothing more, waits (bounded) for what it issued and frees TMEM.
 #include <cudaTypedefs.h>
@@ -50,8 +61,10 @@ namespace {
 constexpr int kPM = 128;  // query rows per tile
 constexpr int kPN = 128;  // keys per block
 constexpr int kPD = 128;  // head_dim
-constexpr int kPThreads = 224;  // warps: K loader, MMA, four softmax, V loader
-constexpr int kVWarp = 6;
+constexpr int kPThreads = 352;  // warps: K loader, MMA, four softmax (tile A), four softmax (tile B), V loader
+constexpr int kVWarp = 10;
+constexpr int kKS = 3;  // K ring stages
+constexpr int kVS = 2;  // V ring stages
 constexpr uint32_t kHalf = 16384;  // one 64-element half of a 128-row operand: 128 rows x 128 B
 constexpr uint32_t kGroupBytes = 4096;  // K or V of one 16-key group: 2 halves x 16 rows x 128 B
 constexpr uint64_t kPWaitNs = 2000000000ull;
@@ -136,6 +149,40 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
       : "memory");
 }
 
+// 16 consecutive fp32 columns of this thread's TMEM lane (no wait).
+__device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// 16 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+
+// D (TMEM) (+)= A (TMEM, K-major, two bf16 per column) * B (shared-memory descriptor).
+__device__ __forceinline__ void umma_f16_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t b, uint32_t idesc,
+                                            uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
 // 2^x by the PTX approximate base-2 exponential (flush-to-zero; 2^-inf = +0).
 __device__ __forceinline__ float ex2_ftz(float x) {
   float y;
@@ -143,26 +190,26 @@ __device__ __forceinline__ float ex2_ftz(float x) {
   return y;
 }
 
-// Key offset (within its 128-key block) of S column c: columns 0..63 are
-// rows 0..7 of the eight 16-key groups, columns 64..127 their rows 8..15.
-__host__ __device__ constexpr int key_of_col(int c) { return 16 * ((c & 63) >> 3) + 8 * (c >> 6) + (c & 7); }
 
 // Byte offset of 16-byte chunk c (0..7) of row r in a 128-byte-swizzled operand half.
 __device__ __forceinline__ uint32_t sw128(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
 
-// Barriers and flags of one CTA (static shared memory).
+// Barriers and flags of one CTA (static shared memory). Per-tile barriers
+// are indexed by the tile (0: A, 1: B) and complete once per key block.
 struct PrefillBars {
   uint64_t q_full;
-  uint64_t k_full[2];   // loader -> MMA: K block in K stage s (TMA bytes and thread copies)
-  uint64_t v_full[2];   // loader -> MMA: V block in V stage s
-  uint64_t s_full[2];   // MMA -> softmax: S = Q K^T of the block in TMEM buffer s
-  uint64_t s_empty[2];  // softmax (4 warps) -> MMA: S buffer s read
-  uint64_t p_full[2];   // softmax (4 warps) -> MMA: P of the block in buffer s
-  uint64_t pv_done[2];  // MMA -> all: O += P V of the block in stage s done (V stage and P buffer free)
-  uint64_t drain;       // MMA -> all: everything it issued is done
+  uint64_t k_full[kKS];   // loader -> MMA: K block in K stage s (TMA bytes and thread copies)
+  uint64_t k_empty[kKS];  // MMA -> loader: both tiles' S have read K stage s
+  uint64_t v_full[kVS];   // loader -> MMA: V block in V stage s
+  uint64_t v_empty[kVS];  // MMA -> loader: both tiles' P V have read V stage s
+  // [tile X][half h]: the half-blocks of tile X in TMEM sub-buffer h (one phase per key block)
+  uint64_t s_full[2][2];  // MMA -> softmax of tile X: S of the half-block in sub-buffer h
+  uint64_t p_full[2][2];  // softmax of tile X (4 warps) -> MMA: P of the half-block in sub-buffer h
+  uint64_t pv_done[2][2]; // MMA -> all: O_X += P V of the half-block done (sub-buffer h free again)
+  uint64_t drain;         // MMA -> all: everything it issued is done
   uint32_t taddr;
   int abort;
-  int slots[2][kPN];    // the K and the V loader's slots of the block being loaded
+  int slots[2][kPN];      // the K and the V loader's slots of the block being loaded
 };
 
 // Wait for phase ``k`` of ``bar`` (parity k & 1), bounded.
@@ -212,57 +259,70 @@ __device__ __forceinline__ void load_rows(const PrefillArgs& a, unsigned char* d
   __syncwarp();
 }
 
-// Warp roles: 0 loads Q once, then K blocks into a two-stage ring; 6 loads
-// V blocks into theirs; 1 issues the MMAs (lane 0); 2..5 run the softmax,
-// one query row per thread (TMEM lane quadrant = warp % 4), and the epilogue.
+// Warp roles: 0 loads Q once, then K blocks into a three-stage ring; 10
+// loads V blocks into a two-stage ring; 1 issues the MMAs (lane 0); 2..5 run
+// the softmax of tile A and 6..9 that of tile B, one query row per thread
+// (TMEM lane quadrant = warp % 4), and their epilogues.
 __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_constant__ PrefillArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ PrefillBars sb;
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  unsigned char* sQ = smem;                          // [2 halves][128 rows][128 B]
-  unsigned char* sKV = smem + 2 * kHalf;             // K stage s at s * 2 kHalf, V stage s at (4 + 2 s) kHalf
-  unsigned char* sPb = smem + 10 * kHalf;            // P buffer s at s * 2 kHalf
+  unsigned char* sQ = smem;                   // tile X's Q at X * 2 kHalf: [2 halves][128 rows][128 B]
+  unsigned char* sK = smem + 4 * kHalf;       // K stage s at s * 2 kHalf
+  unsigned char* sV = sK + kKS * 2 * kHalf;   // V stage s at s * 2 kHalf
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   volatile int* abort_flag = &sb.abort;
 
-  // Tile order: the last tiles of the requests (the most keys) first.
-  const int per_tile = a.B * a.Hkv;
-  const int tile = a.tiles - 1 - (int)(blockIdx.x / per_tile);
-  const int b = (int)(blockIdx.x % per_tile) / a.Hkv, g = (int)(blockIdx.x % per_tile) % a.Hkv;
+  // CTA order: request and KV head major, the pair with the most keys first,
+  // so that the pairs reading the same K/V run side by side (L2 serves all
+  // but the first of them).
+  const int pairs = (a.tiles + 1) >> 1;
+  const int pair = pairs - 1 - (int)(blockIdx.x % pairs);
+  const int bg = (int)(blockIdx.x / pairs);
+  const int b = bg / a.Hkv, g = bg % a.Hkv;
   const int TT = kPM / a.G;  // query tokens per tile
-  const int j0 = tile * TT;
+  const int j0 = 2 * pair * TT;  // first token of tile A; tile B starts at j0 + TT
   const int L = a.context_lens[b];
   const int ql = a.q_lens ? a.q_lens[b] : a.C;
   const int row = a.table_rows ? a.table_rows[b] : b;
   const bool valid = ql >= 1 && ql <= a.C && ql <= L && L <= table_capacity(a.T) && row >= 0 && row < a.T.rows_total;
-  // softmax threads: query row r = 32 * (warp % 4) + lane: token j0 + r / G, head r % G of the group
+  // softmax threads: tile X = (warp - 2) / 4, query row r = 32 * (warp % 4) + lane: token j0 + X TT + r / G,
+  // head r % G of the group
+  const int X = warp >= 6 ? 1 : 0;
   const int r = 32 * (warp & 3) + lane;
-  const int rt = r / a.G, hh = r % a.G;
+  const int rt = X * TT + r / a.G, hh = r % a.G;  // token offset from j0, head in the group
   __nv_bfloat16* orow = a.out + (((size_t)b * a.C + j0 + rt) * a.Hq + (size_t)g * a.G + hh) * kPD;
   if (!valid) {
-    if (tid == 0 && g == 0 && tile == 0) set_error(a.err, KVP_ERR_BAD_INDEX);
-    if (warp >= 2 && warp < 6 && j0 + rt < a.C)
+    if (tid == 0 && g == 0 && pair == 0) set_error(a.err, KVP_ERR_BAD_INDEX);
+    if (warp >= 2 && warp < kVWarp && j0 + rt < a.C)
       for (int d = 0; d < kPD; d += 8) *reinterpret_cast<uint4*>(orow + d) = make_uint4(0u, 0u, 0u, 0u);
     return;
   }
-  if (j0 >= ql) return;  // no query of this request falls in the tile
-  const int jn = min(TT, ql - j0);
+  if (j0 >= ql) return;  // no query of this request falls in the pair
+  const int jn = min(2 * TT, ql - j0);  // query tokens of the pair
+  const bool has_b = jn > TT;
   const int p_first = L - ql + j0, p_last = p_first + jn - 1;
-  // the union of the tile's spans: the first query reaches furthest back
+  // the union of the pair's spans: the first query reaches furthest back
   const Span u = attend_span(p_last + 1, a.window > 0 ? a.window + (p_last - p_first) : 0, a.sinks);
   const int n_keys = u.se + (p_last + 1 - u.lo);
   const int nblk = (n_keys + kPN - 1) / kPN;
 
   if (tid == 0) {
     mbar_init(&sb.q_full, 1);
-    for (int s2 = 0; s2 < 2; ++s2) {
+    for (int s2 = 0; s2 < kKS; ++s2) {
       mbar_init(&sb.k_full[s2], 1);
-      mbar_init(&sb.v_full[s2], 1);
-      mbar_init(&sb.s_full[s2], 1);
-      mbar_init(&sb.s_empty[s2], 4);
-      mbar_init(&sb.p_full[s2], 4);
-      mbar_init(&sb.pv_done[s2], 1);
+      mbar_init(&sb.k_empty[s2], 1);
     }
+    for (int s2 = 0; s2 < kVS; ++s2) {
+      mbar_init(&sb.v_full[s2], 1);
+      mbar_init(&sb.v_empty[s2], 1);
+    }
+    for (int x = 0; x < 2; ++x)
+      for (int h = 0; h < 2; ++h) {
+        mbar_init(&sb.s_full[x][h], 1);
+        mbar_init(&sb.p_full[x][h], 4);
+        mbar_init(&sb.pv_done[x][h], 1);
+      }
     mbar_init(&sb.drain, 1);
     sb.abort = 0;
     fence_mbar_init();
@@ -275,22 +335,30 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_c
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tS0 = sb.taddr, tO = sb.taddr + 256;  // S buffers at columns 0 and 128, O at 256
+  // TMEM: S_A at columns 0, S_B at 128, O_A at 256, O_B at 384. A tile's S
+  // region holds two 64-column sub-buffers, one per half-block (below); the
+  // P of a half-block goes to the first 32 columns of its sub-buffer.
+  const uint32_t tbase = sb.taddr;
 
   if (warp == 0 || warp == kVWarp) {
     // ======================= loaders ==========================================
-    // Warp 0 loads Q, then K(i) once S(i - 2) has read K stage i % 2; warp
-    // kVWarp loads V(i) once P V(i - 2) has read V stage i % 2. Each resolves
-    // its own slots, so neither waits on the other's ring.
+    // Warp 0 loads Q, then K(i) once both S of block i - kKS have read its
+    // stage; warp kVWarp loads V(i) once both P V of block i - kVS have. Each
+    // resolves its own slots, so neither waits on the other's ring.
     const bool is_v = warp == kVWarp;
+    const int NS = is_v ? kVS : kKS;
     if (!is_v && lane == 0) {
-      mbar_arrive_expect_tx(&sb.q_full, 2 * kHalf);
+      mbar_arrive_expect_tx(&sb.q_full, (has_b ? 4u : 2u) * kHalf);
       tma_load_4d(sQ, &a.qmap, 0, g * a.G, j0, b, &sb.q_full);
       tma_load_4d(sQ + kHalf, &a.qmap, 64, g * a.G, j0, b, &sb.q_full);
+      if (has_b) {
+        tma_load_4d(sQ + 2 * kHalf, &a.qmap, 0, g * a.G, j0 + TT, b, &sb.q_full);
+        tma_load_4d(sQ + 3 * kHalf, &a.qmap, 64, g * a.G, j0 + TT, b, &sb.q_full);
+      }
     }
     int* slots = sb.slots[is_v ? 1 : 0];
     for (int i = 0; i < nblk; ++i) {
-      const int st = i & 1;
+      const int st = i % NS;
       const int o0 = i * kPN;
       // lane l resolves keys 4l .. 4l+3 (four independent table reads); group
       // gi (lanes 4gi .. 4gi+3) goes by one TMA copy when its 16 slots are
@@ -313,167 +381,181 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_c
       for (int gi = 0; gi < 8; ++gi)
         if (((okb >> (4 * gi)) & 0xFu) == 0xFu) tm |= 1u << gi;
       __syncwarp();
-      if (i >= 2 && !__all_sync(0xffffffffu, pwait(is_v ? &sb.pv_done[st] : &sb.s_full[st], (i - 2) >> 1,
+      if (i >= NS && !__all_sync(0xffffffffu, pwait(is_v ? &sb.v_empty[st] : &sb.k_empty[st], (i - NS) / NS,
                                                     abort_flag, a.err)))
         break;
-      load_rows(a, sKV + (is_v ? 4 + st * 2 : st * 2) * kHalf, slots, tm, g, is_v,
-                is_v ? &sb.v_full[st] : &sb.k_full[st], lane);
+      load_rows(a, (is_v ? sV : sK) + st * 2 * kHalf, slots, tm, g, is_v, is_v ? &sb.v_full[st] : &sb.k_full[st],
+                lane);
     }
   } else if (warp == 1) {
     // ======================= MMA issuer =======================================
-    // The whole warp walks the schedule and waits (no divergent spin beside the
-    // issuing lane); lane 0 alone issues the MMAs and the commits.
+    // A 128-key block is two half-blocks: h = 0 holds rows 0-7 of its eight
+    // 16-key groups, h = 1 rows 8-15 (one N 64 MMA per 16-wide K step each,
+    // B's 8-row atoms 4 KB apart). Half-block j = 2 i + h of tile X lives in
+    // TMEM sub-buffer h of S_X, so S_X(j + 1) is computed while the softmax
+    // works on S_X(j); S_X(j + 2) overwrites P_X(j) and waits for P_X(j) V.
+    // Issue order per half-block j: P_A(j) V, P_B(j) V, S_A(j + 2), S_B(j + 2).
+    // The whole warp walks the schedule and waits (no divergent spin beside
+    // the issuing lane); lane 0 alone issues the MMAs and the commits.
     {
       const bool issuer = lane == 0;
-      const uint32_t qa = smem_u32(sQ);
+      const int ntile = has_b ? 2 : 1;
+      const int nsub = 2 * nblk;
       const uint32_t id_s = umma_idesc(0, kPN / 2), id_o = umma_idesc(1, kPN);
-      bool ok = __all_sync(0xffffffffu, pwait(&sb.q_full, 0, abort_flag, a.err));
-      for (int i = 0; ok && i <= nblk; ++i) {
-        if (i < nblk) {  // S(i) = Q K(i)^T into S buffer i % 2
-          const int st = i & 1;
-          ok = __all_sync(0xffffffffu, pwait(&sb.k_full[st], i >> 1, abort_flag, a.err));
-          if (ok && i >= 2) ok = __all_sync(0xffffffffu, pwait(&sb.s_empty[st], (i - 2) >> 1, abort_flag, a.err));
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t ka = smem_u32(sKV + st * 2 * kHalf);
-          // S columns 0..63 are rows 0..7 of the eight key groups, columns
-          // 64..127 their rows 8..15 (N 64 each, 8-row atoms 4 KB apart)
+      auto issue_s = [&](int x, int j) {  // S of half-block j of tile x, K of block j / 2
+        const int h = j & 1, blk = j >> 1;
+        const uint32_t qa = smem_u32(sQ + x * 2 * kHalf), tS = tbase + (uint32_t)x * 128u + (uint32_t)h * 64u;
+        const uint32_t ka = smem_u32(sK + (blk % kKS) * 2 * kHalf) + (uint32_t)h * 1024u;
+        if (issuer) {
 #pragma unroll
-          for (int ks = 0; ks < 8 && issuer; ++ks) {
+          for (int ks = 0; ks < 8; ++ks) {
             const uint32_t qoff = (uint32_t)(ks >> 2) * kHalf + (uint32_t)(ks & 3) * 32u;
             const uint32_t koff = (uint32_t)(ks >> 2) * (kGroupBytes / 2) + (uint32_t)(ks & 3) * 32u;
-            const uint64_t qd = umma_desc(qa + qoff, 16, 1024);
-            umma_f16(tS0 + (uint32_t)st * 128u, qd, umma_desc(ka + koff, 16, kGroupBytes), id_s, ks > 0);
-            umma_f16(tS0 + (uint32_t)st * 128u + 64u, qd, umma_desc(ka + koff + 1024u, 16, kGroupBytes), id_s, ks > 0);
+            umma_f16(tS, umma_desc(qa + qoff, 16, 1024), umma_desc(ka + koff, 16, kGroupBytes), id_s, ks > 0);
           }
-          if (issuer) umma_commit(&sb.s_full[st]);
-          __syncwarp();
+          umma_commit(&sb.s_full[x][h]);
+          if (h == 1 && x == ntile - 1) umma_commit(&sb.k_empty[blk % kKS]);  // both tiles' S read the stage
         }
-        if (i >= 1) {  // O += P(i-1) V(i-1)
-          const int k = i - 1, st = k & 1;
-          ok = __all_sync(0xffffffffu, pwait(&sb.p_full[st], k >> 1, abort_flag, a.err));
-          if (ok) ok = __all_sync(0xffffffffu, pwait(&sb.v_full[st], k >> 1, abort_flag, a.err));
+        __syncwarp();
+      };
+      bool ok = __all_sync(0xffffffffu, pwait(&sb.q_full, 0, abort_flag, a.err));
+      if (ok) ok = __all_sync(0xffffffffu, pwait(&sb.k_full[0], 0, abort_flag, a.err));
+      if (ok) {
+        tc_fence_after();
+        for (int x = 0; x < ntile; ++x) {
+          issue_s(x, 0);
+          issue_s(x, 1);
+        }
+      }
+      for (int j = 0; ok && j < nsub; ++j) {
+        const int h = j & 1, blk = j >> 1, sv = blk % kVS;
+        if (h == 0) ok = __all_sync(0xffffffffu, pwait(&sb.v_full[sv], blk / kVS, abort_flag, a.err));
+        // O_X += P_X(j) V: P from TMEM (8 columns per 16 keys, in S-column
+        // order), V the MN-major B operand: K step m covers rows 8h .. 8h + 7
+        // of groups 2m and 2m + 1 (atoms 4 KB apart), the halves of d 2 KB apart
+        const uint32_t va = smem_u32(sV + sv * 2 * kHalf) + (uint32_t)h * 1024u;
+        for (int x = 0; ok && x < ntile; ++x) {
+          ok = __all_sync(0xffffffffu, pwait(&sb.p_full[x][h], blk, abort_flag, a.err));
           if (!ok) break;
           tc_fence_after();
-          const uint32_t pa = smem_u32(sPb + st * 2 * kHalf), va = smem_u32(sKV + (4 + st * 2) * kHalf);
+          const uint32_t tP = tbase + (uint32_t)x * 128u + (uint32_t)h * 64u, tO = tbase + 256u + (uint32_t)x * 128u;
+          if (issuer) {
 #pragma unroll
-          for (int ks = 0; ks < 8 && issuer; ++ks) {
-            const uint32_t poff = (uint32_t)(ks >> 2) * kHalf + (uint32_t)(ks & 3) * 32u;
-            // keys 16 ks .. 16 ks + 15 are V group ks: halves of d 2 KB apart, 8-key atoms 1 KB
-            umma_f16(tO, umma_desc(pa + poff, 16, 1024),
-                     umma_desc(va + (uint32_t)ks * kGroupBytes, kGroupBytes / 2, 1024), id_o,
-                     (k > 0 || ks > 0) ? 1u : 0u);
+            for (int m = 0; m < 4; ++m)
+              umma_f16_ts(tO, tP + (uint32_t)m * 8u, umma_desc(va + (uint32_t)m * 2u * kGroupBytes, kGroupBytes / 2,
+                                                               kGroupBytes),
+                          id_o, (j > 0 || m > 0) ? 1u : 0u);
+            umma_commit(&sb.pv_done[x][h]);
+            if (h == 1 && x == ntile - 1) umma_commit(&sb.v_empty[sv]);  // both tiles' P V read the stage
           }
-          if (issuer) umma_commit(&sb.pv_done[st]);
           __syncwarp();
+        }
+        if (ok && j + 2 < nsub) {
+          if (h == 0) ok = __all_sync(0xffffffffu, pwait(&sb.k_full[(blk + 1) % kKS], (blk + 1) / kKS, abort_flag, a.err));
+          for (int x = 0; ok && x < ntile; ++x) {
+            ok = __all_sync(0xffffffffu, pwait(&sb.pv_done[x][h], blk, abort_flag, a.err));
+            if (!ok) break;
+            tc_fence_after();
+            issue_s(x, j + 2);
+          }
         }
       }
       if (issuer) umma_commit(&sb.drain);  // arrives once everything issued above is done
       __syncwarp();
     }
-  } else if (warp < kVWarp) {
-    // ======================= softmax warps =====================================
+  } else if (warp < kVWarp && (X == 0 || has_b)) {
+    // ======================= softmax warps (tile X) ============================
     const bool rv = rt < jn;
     const int pr = p_first + rt;
     const Span sr0 = attend_span(pr + 1, a.window, a.sinks);
-    // In key offsets of the chunk's span u: the row's sink rows are offsets
+    // In key offsets of the pair's span u: the row's sink rows are offsets
     // [0, sr.se) (when u keeps a sink segment its width is the row's; when it
     // does not, u starts at position 0 and offsets are positions), and its
     // window [sr.lo, pr] starts at or after u.lo. Rows past the chunk keep nothing.
     const Span sr = rv ? sr0 : Span{0, 0};
     const int wb0 = rv ? u.se + (sr.lo - u.lo) : 1 << 30, we0 = rv ? u.se + (pr - u.lo) : -1;
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    const uint32_t tS = tbase + (uint32_t)X * 128u + lane_base, tO = tbase + 256u + (uint32_t)X * 128u + lane_base;
     const float sl2 = a.scale_log2;
     float m_used = -INFINITY, lsum = 0.f;  // m in scaled log2 units
     bool ok = true;
-    for (int i = 0; i < nblk; ++i) {
-      const int st = i & 1;
-      ok = __all_sync(0xffffffffu, pwait(&sb.s_full[st], i >> 1, abort_flag, a.err));
+    const int nsub = 2 * nblk;
+    for (int j = 0; j < nsub; ++j) {
+      const int h = j & 1, blk = j >> 1;
+      ok = __all_sync(0xffffffffu, pwait(&sb.s_full[X][h], blk, abort_flag, a.err));
       if (!ok) break;
       tc_fence_after();
-      float sv[kPN];
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) tmem_ld32(tS0 + (uint32_t)st * 128u + lane_base + c4 * 32, sv + c4 * 32);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sb.s_empty[st]);
+      // S column c (0..63) of half-block h is key 16 (c / 8) + 8 h + c % 8 of the block
+      float sv[64];
+      tmem_ld16_nowait(tS + 64 * h, sv);
+      tmem_ld16_nowait(tS + 64 * h + 16, sv + 16);
+      tmem_ld16_nowait(tS + 64 * h + 32, sv + 32);
+      tmem_ld16_nowait(tS + 64 * h + 48, sv + 48);
+      tmem_wait_ld();
       // The row attends key offsets [0, ea) (its sink rows) and [wb, we] (its
       // window), relative to this block's first offset.
-      const int o0 = i * kPN;
-      // The maximum is taken on unscaled scores (scale > 0) and scaled once.
+      const int o0 = blk * kPN;
       const int ea = sr.se - o0, wb = wb0 - o0, we = we0 - o0;
-      float rmax = -INFINITY;
-      if (__all_sync(0xffffffffu, wb <= 0 && we >= kPN - 1)) {  // no row of the warp masks in this block
+      const bool unmasked = __all_sync(0xffffffffu, wb <= 0 && we >= kPN - 1);  // no row of the warp masks
+      if (!unmasked) {
 #pragma unroll
-        for (int c = 0; c < kPN; ++c) rmax = fmaxf(rmax, sv[c]);
-      } else {
-#pragma unroll
-        for (int c = 0; c < kPN; ++c) {
-          const int oc = key_of_col(c);
-          const bool keep = oc < ea || (oc >= wb && oc <= we);
-          sv[c] = keep ? sv[c] : -INFINITY;
-          rmax = fmaxf(rmax, sv[c]);
+        for (int c = 0; c < 64; ++c) {
+          const int oc = 16 * (c >> 3) + 8 * h + (c & 7);
+          if (!(oc < ea || (oc >= wb && oc <= we))) sv[c] = -INFINITY;
         }
       }
+      // the maximum is taken on unscaled scores (scale > 0) and scaled once
+      float rmax = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) rmax = fmaxf(rmax, sv[c]);
       rmax *= sl2;
       const bool grow = rmax > m_used + 8.f;  // also when nothing was kept before
       const bool scale_o = grow && lsum > 0.f;
       const float f = scale_o ? exp2f(m_used - rmax) : 1.f;
       if (grow) m_used = rmax;
       const float msub = m_used == -INFINITY ? 0.f : m_used;  // masked scores give 2^-inf = 0 either way
-      // P buffer st is free once the P V of block i - 2 is done
-      if (i >= 2) {
-        ok = __all_sync(0xffffffffu, pwait(&sb.pv_done[st], (i - 2) >> 1, abort_flag, a.err));
-        if (!ok) break;
-      }
-      unsigned char* sP = sPb + st * 2 * kHalf;
+      // P in S-column order, two per 32-bit column, over the first 32 columns
+      // of the sub-buffer (S_X(j + 2) is issued only after this P's P V is done)
+      uint32_t w[32];
       float psum = 0.f;
 #pragma unroll
-      for (int c8 = 0; c8 < kPN / 8; ++c8) {
-        uint32_t w[4];
-#pragma unroll
-        for (int x = 0; x < 4; ++x) {
-          const float x0 = sv[c8 * 8 + 2 * x], x1 = sv[c8 * 8 + 2 * x + 1];
-          const float p0 = ex2_ftz(fmaf(x0, sl2, -msub));
-          const float p1 = ex2_ftz(fmaf(x1, sl2, -msub));
-          w[x] = pack_bf16(p0, p1);
-          psum += bf16_lo(w[x]) + bf16_hi(w[x]);
-        }
-        // P column k is key k of the block: S chunk c8 holds keys 16 (c8 % 8) + 8 (c8 / 8) + 0..7
-        const int j8 = 2 * (c8 & 7) + (c8 >> 3);
-        *reinterpret_cast<uint4*>(sP + (j8 >> 3) * kHalf + sw128(r, j8 & 7)) = make_uint4(w[0], w[1], w[2], w[3]);
+      for (int x = 0; x < 32; ++x) {
+        w[x] = pack_bf16(ex2_ftz(fmaf(sv[2 * x], sl2, -msub)), ex2_ftz(fmaf(sv[2 * x + 1], sl2, -msub)));
+        psum += bf16_lo(w[x]) + bf16_hi(w[x]);
       }
+      tmem_st16(tS + 64 * h, w);
+      tmem_st16(tS + 64 * h + 16, w + 16);
       lsum = lsum * f + psum;
       if (__any_sync(0xffffffffu, scale_o)) {
-        // O holds blocks < i in the old maximum: rescale it once P V(i - 1) is
-        // in, before P V(i) may start (a warp-wide TMEM read and write)
-        ok = __all_sync(0xffffffffu, pwait(&sb.pv_done[(i - 1) & 1], (i - 1) >> 1, abort_flag, a.err));
+        // O_X holds the half-blocks < j in the old maximum: rescale it once the
+        // P V of half-block j - 1 is in, before this one's may start (a
+        // warp-wide TMEM read and write)
+        ok = __all_sync(0xffffffffu, pwait(&sb.pv_done[X][h ^ 1], (j - 1) >> 1, abort_flag, a.err));
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) {
           float ov[32];
-          tmem_ld32(tO + lane_base + c4 * 32, ov);
+          tmem_ld32(tO + c4 * 32, ov);
 #pragma unroll
           for (int x = 0; x < 32; ++x) ov[x] *= f;
-          tmem_st32(tO + lane_base + c4 * 32, ov);
+          tmem_st32(tO + c4 * 32, ov);
         }
-        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       }
-      fence_proxy_async_smem();
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sb.p_full[st]);
+      if (lane == 0) mbar_arrive(&sb.p_full[X][h]);
     }
     // ---- epilogue: O / l -> bf16, once the last P V is in O ------------------
-    if (ok) ok = __all_sync(0xffffffffu, pwait(&sb.pv_done[(nblk - 1) & 1], (nblk - 1) >> 1, abort_flag, a.err));
+    if (ok) ok = __all_sync(0xffffffffu, pwait(&sb.pv_done[X][(nsub - 1) & 1], (nsub - 1) >> 1, abort_flag, a.err));
     if (ok) {
       tc_fence_after();
       const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
 #pragma unroll
       for (int c4 = 0; c4 < 4; ++c4) {
         float ov[32];
-        tmem_ld32(tO + lane_base + c4 * 32, ov);
+        tmem_ld32(tO + c4 * 32, ov);
         if (rv) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -499,7 +581,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_c
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tS0) : "memory");
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tbase) : "memory");
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
@@ -546,7 +628,7 @@ bool encode_qmap(const void* q, int B, int C, int Hq, int G, CUtensorMap* out) {
 
 }  // namespace
 
-constexpr size_t kPrefillSmem = 14 * kHalf + 1024;  // Q, two K/V stages, two P buffers
+constexpr size_t kPrefillSmem = (4 + 2 * kKS + 2 * kVS) * kHalf + 1024;  // two Q tiles, the K and V rings
 
 bool prefill_tc_eligible(const kvp_pool* pool, int Hq, int C, float scale) {
   // the row maximum is taken on unscaled scores, which needs scale > 0
@@ -593,7 +675,7 @@ int launch_prefill_tc(const kvp_pool* pool, int layer, const void* q, int batch,
       return KVP_ERR_CUDA;
     attr = true;
   }
-  const long long grid = (long long)a.tiles * batch * pool->kv_heads;
+  const long long grid = (long long)((a.tiles + 1) / 2) * batch * pool->kv_heads;
   if (grid <= 0 || grid > 0x7fffffffLL) return KVP_ERR_INVALID_ARG;
   prefill_tc_kernel<<<(unsigned)grid, kPThreads, kPrefillSmem, stream>>>(a);
   return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
