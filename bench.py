@@ -235,40 +235,93 @@ def _i32(xs, dev):
 
 
 def device_twin(sc):
-    """Whether the workload's history is plain appends (no forks, trims or
-    verify steps) and so has a device-bookkeeping twin for the e2e leg."""
-    return (not sc.devalloc and not sc.multi and sc.window <= 0
-            and all(op[0] == "new" or (op[0] == "append" and not op[3] and not op[4]) for op in sc.ops))
+    """Whether the workload's e2e leg runs through the device-side page
+    bookkeeping (every decode and verify workload; chunked prefill keeps the
+    host bookkeeping)."""
+    return not sc.devalloc and not sc.prefill
 
 
 def build_product_device(sc, dev):
-    """The scenario's history through the device-side bookkeeping: every
-    request's rows appended in one call (pages popped in request order, as
-    the host replays them), then stored layer by layer."""
+    """The scenario's history through the device-side bookkeeping, in the
+    order the host replays it: plain histories append every request's rows
+    in one call (pages popped in request order); others replay each
+    operation (appends, window trims, forks, the first suffix token of a
+    batch, releases). The rows are stored layer by layer."""
     from paged_decode_attention_store_gb300.engine import DevicePagedKVCache
 
     w = sc.w
-    if any(op[0] not in ("new", "append") for op in sc.ops) or any(op[3] or op[4] for op in sc.ops if op[0] == "append"):
-        raise ValueError("device bookkeeping scenarios build plain histories")
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     cache = DevicePagedKVCache(w.num_pages, w.P, w.Hkv, w.D, w.layers, w.dtype, max_requests=sc.max_requests,
                                table_mode=w.table_mode, max_seq_len=sc.max_seq_len, free_stack=w.free_order,
                                device=dev)
-    rids = [op[1] for op in sc.ops if op[0] == "new"]
-    counts = {op[1]: op[2] for op in sc.ops if op[0] == "append"}
-    cache.new(rids)
-    cnt = [counts.get(r, 0) for r in rids]
-    slots = cache.append(rids, counts=cnt)
-    rr = torch.as_tensor([r for r, c in zip(rids, cnt) for _ in range(c)], dtype=torch.int64, device=dev)
-    pos = torch.as_tensor([t for c in cnt for t in range(c)], dtype=torch.int64, device=dev)
-    step = 1 << 18
-    for layer in range(w.layers):
-        for s0 in range(0, rr.numel(), step):
-            k, v = sc.inputs.kv_rows(sc.seed, layer, rr[s0:s0 + step], pos[s0:s0 + step], w.Hkv, w.D, dtype=tdt, device=dev)
-            cache.store(layer, k, v, slots[s0:s0 + step].contiguous())
+    pend = []  # (rids, positions, slots) waiting to be stored
+
+    def flush():
+        if not pend:
+            return
+        rr = torch.cat([p[0] for p in pend])
+        pos = torch.cat([p[1] for p in pend])
+        slots = torch.cat([p[2] for p in pend])
+        step = 1 << 18
+        for layer in range(w.layers):
+            for s0 in range(0, rr.numel(), step):
+                k, v = sc.inputs.kv_rows(sc.seed, layer, rr[s0:s0 + step], pos[s0:s0 + step], w.Hkv, w.D, dtype=tdt,
+                                         device=dev)
+                cache.store(layer, k, v, slots[s0:s0 + step].contiguous())
+        pend.clear()
+
+    def add_store(rid_list, pos_list, slots):
+        pend.append((torch.as_tensor(rid_list, dtype=torch.int64, device=dev),
+                     torch.as_tensor(pos_list, dtype=torch.int64, device=dev), slots))
+
+    plain = all(op[0] == "new" or (op[0] == "append" and not op[3] and not op[4]) for op in sc.ops)
+    lengths = {}
+    if plain:
+        rids = [op[1] for op in sc.ops if op[0] == "new"]
+        counts = {op[1]: op[2] for op in sc.ops if op[0] == "append"}
+        cache.new(rids)
+        cnt = [counts.get(r, 0) for r in rids]
+        slots = cache.append(rids, counts=cnt)
+        add_store([r for r, c in zip(rids, cnt) for _ in range(c)], [t for c in cnt for t in range(c)], slots)
+        lengths = dict(zip(rids, cnt))
+    else:
+        for op in sc.ops:
+            kind = op[0]
+            if kind == "new":
+                cache.new([op[1]])
+                lengths[op[1]] = 0
+            elif kind == "append":
+                _, rid, n, store_from, store_below = op
+                L0 = lengths[rid]
+                slots = cache.append([rid], counts=[n])
+                lengths[rid] = L0 + n
+                first = max(store_from, L0)
+                if first < L0 + n:
+                    add_store([rid] * (L0 + n - first), list(range(first, L0 + n)), slots[first - L0:])
+                sink_end = min(store_below, first, L0 + n)
+                if L0 < sink_end:
+                    add_store([rid] * (sink_end - L0), list(range(L0, sink_end)), slots[:sink_end - L0])
+            elif kind == "batch":
+                flush()
+                slots = cache.append(op[1])
+                add_store(op[1], [lengths[r] for r in op[1]], slots)
+                for r in op[1]:
+                    lengths[r] += 1
+            elif kind == "trim":
+                cache.pages.trim(cache._i32([op[1]]), keep_from=cache._i32([op[2]]), sinks=op[3])
+            elif kind == "fork":
+                flush()
+                cache.fork([op[1]], [op[2]])
+                lengths[op[2]] = lengths[op[1]]
+            elif kind == "release":
+                cache.release([op[1]])
+                del lengths[op[1]]
+            if not sc.accumulate:
+                flush()
+    flush()
     torch.cuda.synchronize(dev)
     cache.check()
-    return cache, [counts.get(r, 0) for r in sc.rids]
+    return cache, [lengths[r] for r in sc.rids]
 
 
 def build_product(sc, dev):
@@ -716,6 +769,10 @@ def measure(args, name, rank, world, local_rank, with_cpu):
     for i in range(W + K, W + 2 * K):
         run_step(sc, cache, steps[i], outs, events=pending)
     torch.cuda.synchronize(dev)
+    # the clock record covers the device-timed region; nvidia-smi's polling
+    # is stopped before the end-to-end leg, whose per-step host
+    # synchronisation it would otherwise slow down
+    clocks = sampler.stop(t0, t1) if sampler else None
     cache.check()
     attn_ms = [a.elapsed_time(b) for a, b in ev_pairs]
     total_bytes = sum(st.bytes for st in steps[W:W + K])
@@ -732,15 +789,17 @@ def measure(args, name, rank, world, local_rank, with_cpu):
         sc_dev = Scenario(sc.name + "_devalloc", sc.seed, layers=args.layers)
         cache, lens_dev = build_product_device(sc_dev, dev)
         e2e = run_e2e(args, sc_dev, cache, lens_dev, W + 2 * K + 1, dev)
-        e2e["path"] = ("DevicePagedKVCache.decode_step_host (kvp_decode_step_device_io: page bookkeeping on the "
-                       "device, host copies in the same native call)")
+        e2e["path"] = ("DevicePagedKVCache.verify_step_host (kvp_verify_step_device_io: drafts appended, stored, "
+                       "verified and the rejected ones rewound with the page bookkeeping on the device, host copies "
+                       "in the same native call)" if sc.verify else
+                       "DevicePagedKVCache.decode_step_host (kvp_decode_step_device_io: page bookkeeping, window "
+                       "trim included, on the device, host copies in the same native call)")
     else:
         e2e = run_e2e(args, sc, cache, lens_after, W + 2 * K + 1, dev)
         e2e["path"] = ("DevicePagedKVCache.decode_step" if sc.devalloc else
                        "PagedKVCache.verify_step + rewind" if sc.verify else
                        "PagedKVCache.prefill_step" if sc.prefill else
                        "PagedKVCache.decode_step (kvp_decode_step: host page bookkeeping)")
-    clocks = sampler.stop(t0, t1) if sampler else None
 
     elapsed_ms, total_bytes, tokens, e2e_ms, e2e_bytes = reduce_over_ranks(
         elapsed_ms, float(total_bytes), float(timed_tokens), e2e["ms"], float(e2e["bytes"]), world, dev)
@@ -865,7 +924,7 @@ def run_e2e(args, sc, cache, lens, first_step, dev):
     host_steps = _host_inputs(sc, first_step, K, lens)
     out_host = [torch.empty(out_shape(sc), dtype=cache.tdt, pin_memory=True) for _ in range(w.layers)]
     if sc.devalloc:
-        return _run_e2e_device(sc, cache, lens, host_steps, out_host, dev)
+        return _run_e2e_device(sc, cache, lens, host_steps, out_host, dev, first_step)
     rids = np.asarray(sc.rids, np.int32)
     total_bytes = 0
     torch.cuda.synchronize(dev)
@@ -900,30 +959,50 @@ def run_e2e(args, sc, cache, lens, first_step, dev):
             "link": link_rates(dev)}
 
 
-def _run_e2e_device(sc, cache, lens, host_steps, out_host, dev):
+def _run_e2e_device(sc, cache, lens, host_steps, out_host, dev, first_step):
     """End to end with the bookkeeping on the device: per step one native
-    call copies q/k/v in from pinned host memory, runs the step and copies
-    the output back; no host decision, no table writes from the host."""
+    call copies q/k/v in from pinned host memory, runs the step (a decode
+    step, or a verify step that rewinds the rejected drafts) and copies the
+    output back; no host decision, no table writes from the host. The step's
+    table writes are counted for the bytes from the lengths."""
     w = sc.w
     K = len(host_steps)
+    P = w.P
     rids = torch.as_tensor(sc.rids, dtype=torch.int32, device=dev)
     lens = list(lens)
-    total_bytes = h2d = 0
+    M = max(sc.verify, 1)
+    back = [[M - a for a in wl.accepted_drafts(sc.seed, first_step + s, len(sc.rids), M)] for s in range(K)] \
+        if sc.verify else None
+    total_bytes = 0
     torch.cuda.synchronize(dev)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record()
     for s in range(K):
         q_h, k_h, v_h = host_steps[s]
+        if sc.verify:
+            cache.verify_step_host(rids, q_h, k_h, v_h, back[s], out_host, sc.window, w.scale, sinks=sc.sinks)
+            ctx = [L + M for L in lens]
+            n_writes = sum(-(-c // P) - -(-L // P) for L, c in zip(lens, ctx))
+            after = [c - nb for c, nb in zip(ctx, back[s])]
+            n_back = sum(-(-c // P) - -(-a // P) for c, a in zip(ctx, after))
+            total_bytes += step_bytes(sc, ctx, n_writes, 0, n_back)
+            lens = after
+            continue
         cache.decode_step_host(rids, q_h, k_h, v_h, out_host, sc.window, w.scale, sinks=sc.sinks)
-        n_writes = sum(1 for L in lens if L % w.P == 0)
+        n_writes = sum(1 for L in lens if L % P == 0)
         lens = [L + 1 for L in lens]
-        total_bytes += step_bytes(sc, lens, n_writes, 0, 0)
+        n_trim = 0
+        if sc.window > 0:  # pages the step's trim releases: those that fall wholly below L + 1 - (W - S)
+            kf = lambda L: max(0, L + 1 - (sc.window - sc.sinks)) // P  # noqa: E731
+            n_trim = sum(max(0, kf(L) - kf(L - 1)) for L in lens)
+        total_bytes += step_bytes(sc, lens, n_writes, 0, n_trim)
     end.record()
     torch.cuda.synchronize(dev)
     cache.check()
     h2d = sum(x[i].numel() * x[i].element_size() for x in host_steps[0] for i in range(w.layers))
     d2h = sum(o.numel() * o.element_size() for o in out_host)
-    return {"ms": start.elapsed_time(end), "bytes": total_bytes, "h2d": h2d, "d2h": d2h, "link": link_rates(dev)}
+    return {"ms": start.elapsed_time(end), "bytes": total_bytes, "h2d": h2d + (4 * len(sc.rids) if sc.verify else 0),
+            "d2h": d2h, "link": link_rates(dev)}
 
 
 def link_rates(dev, nbytes=128 << 20):

@@ -28,8 +28,9 @@ struct kvp_pool {
   void* ev_after;
   CUtensorMap tmap;  // tensor map of the whole buffer for the tensor-core kernel,
   int tmap_hg;       // heads per box it was encoded for (0: none yet, -HG: refused for HG)
-  CUtensorMap tmap1; // the buffer as (d % 64, slot, d / 64, head, K/V x layer), for the prefill kernel
-  int tmap1_state;   // 0: not encoded yet, 1: encoded, -1: refused
+  CUtensorMap tmap1; // the buffer as (d % 64, slot, d / 64, head, K/V x layer), for the prefill kernel:
+  CUtensorMap tmap2; //   box (64, 16, 2, 1, 1) (tmap1, V) and box (64, 16, 1, 1, 1) (tmap2, K halves)
+  int tmap1_state;   // 0: not encoded yet, 1: both encoded, -1: refused
 };
 
 namespace kvp {

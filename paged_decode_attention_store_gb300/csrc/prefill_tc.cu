@@ -16,38 +16,36 @@
 //   tiles (A and B) of the same request and KV head, so every K/V block it
 //   loads serves 256 query rows.
 // * The keys the pair needs (the union of its queries' spans) stream in
-//   blocks of 128: a 16-slot group whose slots are contiguous and 16-aligned
-//   comes by one TMA copy (both halves of head_dim, 4 KB), any other key row
-//   is copied by the loader warp into the same swizzled layout.
-// * A 128-key block is taken as two half-blocks of 64 keys: rows 0-7 of its
-//   eight 16-key groups (h = 0) and rows 8-15 (h = 1), which is how the
-//   groups lie in shared memory (8-row atoms, 4 KB from group to group).
-//   S = Q K^T of a half-block (M 128, N 64, K 128, both operands K-major)
-//   accumulates in TMEM sub-buffer h of the tile's S region, so its column c
-//   holds key 16 (c / 8) + 8 h + c % 8 of the block. Each softmax thread owns
-//   one query row: it reads the half-block's 64 scores from TMEM and keeps an
-//   online softmax in log2 units. A half-block that no row of the warp masks
-//   (causal, window, sinks, block end) skips the mask; the row maximum is
-//   taken on unscaled scores and P = 2^(s * scale - m) is one FMA and one ex2
-//   per score. O is rescaled (read, scaled, written back in TMEM) only when
-//   the row maximum grows by more than 8, so P <= 256 always fits bf16 and
-//   the normalisation stays exact (numerator and denominator use the same m
-//   and the same rounded P).
-// * P (bf16, two per 32-bit column, in S-column order) is written back into
-//   the first 32 columns of its sub-buffer and is the A operand, read from
-//   TMEM, of O += P V. V is the MN-major B operand in shared memory: the K
-//   step over P columns 16 m .. 16 m + 15 takes rows 8 h .. 8 h + 7 of groups
-//   2 m and 2 m + 1, one 8-row atom each, 4 KB apart. The epilogue divides
-//   by the row sum and stores bf16.
+//   blocks of 128. A 16-slot group whose slots are contiguous and 16-aligned
+//   comes by TMA copies (4 KB of K or V), any other key row is copied by the
+//   loader warp into the same layout. K lies half-major (each half of d is
+//   128 key rows of 128 B, 8-row atoms 1 KB apart: two copies per group), so
+//   that S = Q K^T of a block is eight MMAs of N 128; V lies group-major
+//   (one copy per group), the B operand of O += P V.
+// * The tensor cores take the same time per MMA instruction for any N up to
+//   256 (measured), so the kernel keeps N large: S_X = Q_X K^T (M 128, N 128,
+//   K 128, both operands K-major) accumulates in the tile's 128-column TMEM
+//   S buffer, column c holding key c of the block. Each softmax thread owns
+//   one query row: it reads its 128 scores from TMEM (once for the maximum,
+//   once for P) and keeps an online softmax in log2 units. A block that no
+//   row of the warp masks (causal, window, sinks, block end) skips the mask;
+//   the row maximum is taken on unscaled scores and P = 2^(s * scale - m) is
+//   one FMA and one ex2 per score. O is rescaled (read, scaled, written back
+//   in TMEM) only when the row maximum grows by more than 8, so P <= 256
+//   always fits bf16 and the normalisation stays exact (numerator and
+//   denominator use the same m and the same rounded P).
+// * P (bf16, two per 32-bit column, keys in order) is written back into the
+//   first 64 columns of S_X and is the A operand, read from TMEM, of O += P V
+//   (V the MN-major operand in shared memory, one 16-key group per K step).
+//   The epilogue divides by the row sum and stores bf16.
 // * Warp-specialised pipeline: two loader warps fill a three-stage K ring
 //   and a two-stage V ring (a K stage is free once both tiles' S have read
 //   it, a V stage once both P V have), each resolving its own slots; an MMA
-//   warp issues, per half-block j, P_A(j) V and P_B(j) V, then S_A(j + 2)
-//   and S_B(j + 2); two groups of four softmax warps turn the scores of each
-//   tile into P. S_X(j + 1) sits in the other sub-buffer, so the tensor core
-//   computes it while the softmax works on half-block j; S_X(j + 2)
-//   overwrites P_X(j) and is issued once P_X(j) V is done. mbarriers carry
-//   every hand-off.
+//   warp issues S_A(0), S_B(0), then per block i: P_A(i) V, P_B(i) V,
+//   S_A(i + 1), S_B(i + 1); two groups of four softmax warps turn each tile's
+//   scores into P. While one tile's softmax runs the tensor core works on the
+//   other tile. S_X(i + 1) overwrites P_X(i), so it is issued once P_X(i) V
+//   is done. mbarriers carry every hand-off.
 // * Every wait is bounded (2 s): on timeout the CTA records KVP_ERR_TIMEOUT,
 //   issues nothing more, waits (bounded) for what it issued and frees TMEM.
 #include <cudaTypedefs.h>
@@ -72,6 +70,7 @@ constexpr uint64_t kPWaitNs = 2000000000ull;
 struct PrefillArgs {
   CUtensorMap qmap;   // q as (d, head, token, request), box (64, G, 128 / G, 1)
   CUtensorMap kvmap;  // the KV buffer as (d % 64, slot, d / 64, kv head, K/V x layer), box (64, 16, 2, 1, 1)
+  CUtensorMap kmap;   // the same view, box (64, 16, 1, 1, 1): one half of d of a 16-slot group
   int use_kvmap;
   int kvl_k, kvl_v;
   TableRef T;
@@ -202,10 +201,9 @@ struct PrefillBars {
   uint64_t k_empty[kKS];  // MMA -> loader: both tiles' S have read K stage s
   uint64_t v_full[kVS];   // loader -> MMA: V block in V stage s
   uint64_t v_empty[kVS];  // MMA -> loader: both tiles' P V have read V stage s
-  // [tile X][half h]: the half-blocks of tile X in TMEM sub-buffer h (one phase per key block)
-  uint64_t s_full[2][2];  // MMA -> softmax of tile X: S of the half-block in sub-buffer h
-  uint64_t p_full[2][2];  // softmax of tile X (4 warps) -> MMA: P of the half-block in sub-buffer h
-  uint64_t pv_done[2][2]; // MMA -> all: O_X += P V of the half-block done (sub-buffer h free again)
+  uint64_t s_full[2];     // MMA -> softmax of tile X: S_X = Q_X K^T of the block in TMEM
+  uint64_t p_full[2];     // softmax of tile X (4 warps) -> MMA: P_X of the block in TMEM
+  uint64_t pv_done[2];    // MMA -> all: O_X += P_X V of the block done (S_X's columns free again)
   uint64_t drain;         // MMA -> all: everything it issued is done
   uint32_t taddr;
   int abort;
@@ -227,12 +225,16 @@ __device__ __forceinline__ void tma_load_5d(void* dst, const void* tmap, int c0,
       : "memory");
 }
 
-// The loader warp fills one 128-key operand (K, or V when ``is_v``, of head
-// group g) from ``slots``: 16-slot groups flagged in ``tm`` by one TMA
-// copy each (both 64-column halves), the others by plain 16-byte copies
-// (zeros for slots < 0); ``bar`` (count 1) gets the arrival and the TMA byte
-// count. Layout: group gi (keys 16 gi .. 16 gi + 15) at gi * 4 KB, its half h
-// at + h * 2 KB, key row r of the group at + r * 128 B (128-byte swizzle).
+// The loader warp fills one 128-key operand from ``slots``: 16-slot groups
+// flagged in ``tm`` by TMA copies, the others by plain 16-byte copies (zeros
+// for slots < 0); ``bar`` (count 1) gets the arrival and the TMA byte count.
+// Both layouts use the 128-byte swizzle with 8-row atoms of 1 KB.
+//  - K (``is_v`` false), half-major: half h of d at h * 16 KB, key row k at
+//    + k * 128 B, so the 128 keys of a half are 16 evenly spaced atoms (the
+//    N 128 B operand of S = Q K^T). A group is two copies (one per half).
+//  - V, group-major: group gi (keys 16 gi .. 16 gi + 15) at gi * 4 KB, its
+//    half h at + h * 2 KB, key row r at + r * 128 B (the MN-major B operand
+//    of O += P V, one group per 16-key K step). A group is one copy.
 __device__ __forceinline__ void load_rows(const PrefillArgs& a, unsigned char* dst, const int* slots, unsigned tm,
                                           int g, bool is_v, uint64_t* bar, int lane) {
   const size_t base = is_v ? a.kv_bytes : 0;
@@ -246,16 +248,22 @@ __device__ __forceinline__ void load_rows(const PrefillArgs& a, unsigned char* d
       if (sl >= 0)
         val = __ldg(reinterpret_cast<const uint4*>(a.kv_layer + base + (size_t)sl * a.row_bytes +
                                                    (size_t)g * kPD * 2) + c);
-      *reinterpret_cast<uint4*>(dst + gi * kGroupBytes + (c >> 3) * (kGroupBytes / 2) + sw128(key & 15, c & 7)) =
-          val;
+      const uint32_t off = is_v ? gi * kGroupBytes + (c >> 3) * (kGroupBytes / 2) + sw128(key & 15, c & 7)
+                                : (c >> 3) * kHalf + sw128(key, c & 7);
+      *reinterpret_cast<uint4*>(dst + off) = val;
     }
   }
   fence_proxy_async_smem();
   __syncwarp();
   if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)__popc(tm) * kGroupBytes);
   __syncwarp();
-  if (lane < 8 && ((tm >> lane) & 1))
-    tma_load_5d(dst + lane * kGroupBytes, &a.kvmap, 0, slots[16 * lane], 0, g, kvl, bar);
+  if (is_v) {
+    if (lane < 8 && ((tm >> lane) & 1))
+      tma_load_5d(dst + lane * kGroupBytes, &a.kvmap, 0, slots[16 * lane], 0, g, kvl, bar);
+  } else if (lane < 16 && ((tm >> (lane & 7)) & 1)) {  // lane = group + 8 * half
+    const int gi = lane & 7, h = lane >> 3;
+    tma_load_5d(dst + h * kHalf + gi * (kGroupBytes / 2), &a.kmap, 0, slots[16 * gi], h, g, kvl, bar);
+  }
   __syncwarp();
 }
 
@@ -317,12 +325,11 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_c
       mbar_init(&sb.v_full[s2], 1);
       mbar_init(&sb.v_empty[s2], 1);
     }
-    for (int x = 0; x < 2; ++x)
-      for (int h = 0; h < 2; ++h) {
-        mbar_init(&sb.s_full[x][h], 1);
-        mbar_init(&sb.p_full[x][h], 4);
-        mbar_init(&sb.pv_done[x][h], 1);
-      }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&sb.s_full[x], 1);
+      mbar_init(&sb.p_full[x], 4);
+      mbar_init(&sb.pv_done[x], 1);
+    }
     mbar_init(&sb.drain, 1);
     sb.abort = 0;
     fence_mbar_init();
@@ -335,9 +342,8 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_c
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // TMEM: S_A at columns 0, S_B at 128, O_A at 256, O_B at 384. A tile's S
-  // region holds two 64-column sub-buffers, one per half-block (below); the
-  // P of a half-block goes to the first 32 columns of its sub-buffer.
+  // TMEM: S_A at columns 0, S_B at 128, O_A at 256, O_B at 384; P_X in the
+  // first 64 columns of S_X
   const uint32_t tbase = sb.taddr;
 
   if (warp == 0 || warp == kVWarp) {
@@ -389,32 +395,28 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_c
     }
   } else if (warp == 1) {
     // ======================= MMA issuer =======================================
-    // A 128-key block is two half-blocks: h = 0 holds rows 0-7 of its eight
-    // 16-key groups, h = 1 rows 8-15 (one N 64 MMA per 16-wide K step each,
-    // B's 8-row atoms 4 KB apart). Half-block j = 2 i + h of tile X lives in
-    // TMEM sub-buffer h of S_X, so S_X(j + 1) is computed while the softmax
-    // works on S_X(j); S_X(j + 2) overwrites P_X(j) and waits for P_X(j) V.
-    // Issue order per half-block j: P_A(j) V, P_B(j) V, S_A(j + 2), S_B(j + 2).
-    // The whole warp walks the schedule and waits (no divergent spin beside
-    // the issuing lane); lane 0 alone issues the MMAs and the commits.
+    // S_X(i) = Q_X K(i)^T is eight N 128 MMAs (one per 16-wide K step of d),
+    // so S column c is key c of the block. S_X(i + 1) overwrites P_X(i), so
+    // it waits for P_X(i) V. Issue order: S_A(0), S_B(0), then per block i:
+    // P_A(i) V, P_B(i) V, S_A(i + 1), S_B(i + 1): while one tile's softmax
+    // runs, the tensor core works on the other tile. The whole warp walks
+    // the schedule and waits (no divergent spin beside the issuing lane);
+    // lane 0 alone issues the MMAs and the commits.
     {
       const bool issuer = lane == 0;
       const int ntile = has_b ? 2 : 1;
-      const int nsub = 2 * nblk;
-      const uint32_t id_s = umma_idesc(0, kPN / 2), id_o = umma_idesc(1, kPN);
-      auto issue_s = [&](int x, int j) {  // S of half-block j of tile x, K of block j / 2
-        const int h = j & 1, blk = j >> 1;
-        const uint32_t qa = smem_u32(sQ + x * 2 * kHalf), tS = tbase + (uint32_t)x * 128u + (uint32_t)h * 64u;
-        const uint32_t ka = smem_u32(sK + (blk % kKS) * 2 * kHalf) + (uint32_t)h * 1024u;
+      const uint32_t id_n128 = umma_idesc(0, kPN), id_o = umma_idesc(1, kPN);
+      auto issue_s = [&](int x, int blk) {
+        const uint32_t qa = smem_u32(sQ + x * 2 * kHalf), tS = tbase + (uint32_t)x * 128u;
+        const uint32_t ka = smem_u32(sK + (blk % kKS) * 2 * kHalf);
         if (issuer) {
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t qoff = (uint32_t)(ks >> 2) * kHalf + (uint32_t)(ks & 3) * 32u;
-            const uint32_t koff = (uint32_t)(ks >> 2) * (kGroupBytes / 2) + (uint32_t)(ks & 3) * 32u;
-            umma_f16(tS, umma_desc(qa + qoff, 16, 1024), umma_desc(ka + koff, 16, kGroupBytes), id_s, ks > 0);
+            const uint32_t off = (uint32_t)(ks >> 2) * kHalf + (uint32_t)(ks & 3) * 32u;
+            umma_f16(tS, umma_desc(qa + off, 16, 1024), umma_desc(ka + off, 16, 1024), id_n128, ks > 0);
           }
-          umma_commit(&sb.s_full[x][h]);
-          if (h == 1 && x == ntile - 1) umma_commit(&sb.k_empty[blk % kKS]);  // both tiles' S read the stage
+          umma_commit(&sb.s_full[x]);
+          if (x == ntile - 1) umma_commit(&sb.k_empty[blk % kKS]);  // both tiles' S have read the K stage
         }
         __syncwarp();
       };
@@ -422,41 +424,36 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_c
       if (ok) ok = __all_sync(0xffffffffu, pwait(&sb.k_full[0], 0, abort_flag, a.err));
       if (ok) {
         tc_fence_after();
-        for (int x = 0; x < ntile; ++x) {
-          issue_s(x, 0);
-          issue_s(x, 1);
-        }
+        for (int x = 0; x < ntile; ++x) issue_s(x, 0);
       }
-      for (int j = 0; ok && j < nsub; ++j) {
-        const int h = j & 1, blk = j >> 1, sv = blk % kVS;
-        if (h == 0) ok = __all_sync(0xffffffffu, pwait(&sb.v_full[sv], blk / kVS, abort_flag, a.err));
-        // O_X += P_X(j) V: P from TMEM (8 columns per 16 keys, in S-column
-        // order), V the MN-major B operand: K step m covers rows 8h .. 8h + 7
-        // of groups 2m and 2m + 1 (atoms 4 KB apart), the halves of d 2 KB apart
-        const uint32_t va = smem_u32(sV + sv * 2 * kHalf) + (uint32_t)h * 1024u;
+      for (int i = 0; ok && i < nblk; ++i) {
+        const int sv = i % kVS;
+        ok = __all_sync(0xffffffffu, pwait(&sb.v_full[sv], i / kVS, abort_flag, a.err));
+        // O_X += P_X(i) V(i): P_X from TMEM (8 columns per 16 keys), V group m
+        // the MN-major B operand of K step m (halves of d 2 KB apart, 8-key atoms 1 KB)
+        const uint32_t va = smem_u32(sV + sv * 2 * kHalf);
         for (int x = 0; ok && x < ntile; ++x) {
-          ok = __all_sync(0xffffffffu, pwait(&sb.p_full[x][h], blk, abort_flag, a.err));
+          ok = __all_sync(0xffffffffu, pwait(&sb.p_full[x], i, abort_flag, a.err));
           if (!ok) break;
           tc_fence_after();
-          const uint32_t tP = tbase + (uint32_t)x * 128u + (uint32_t)h * 64u, tO = tbase + 256u + (uint32_t)x * 128u;
+          const uint32_t tP = tbase + (uint32_t)x * 128u, tO = tbase + 256u + (uint32_t)x * 128u;
           if (issuer) {
 #pragma unroll
-            for (int m = 0; m < 4; ++m)
-              umma_f16_ts(tO, tP + (uint32_t)m * 8u, umma_desc(va + (uint32_t)m * 2u * kGroupBytes, kGroupBytes / 2,
-                                                               kGroupBytes),
-                          id_o, (j > 0 || m > 0) ? 1u : 0u);
-            umma_commit(&sb.pv_done[x][h]);
-            if (h == 1 && x == ntile - 1) umma_commit(&sb.v_empty[sv]);  // both tiles' P V read the stage
+            for (int m = 0; m < 8; ++m)
+              umma_f16_ts(tO, tP + (uint32_t)m * 8u, umma_desc(va + (uint32_t)m * kGroupBytes, kGroupBytes / 2, 1024),
+                          id_o, (i > 0 || m > 0) ? 1u : 0u);
+            umma_commit(&sb.pv_done[x]);
+            if (x == ntile - 1) umma_commit(&sb.v_empty[sv]);  // both tiles' P V have read the V stage
           }
           __syncwarp();
         }
-        if (ok && j + 2 < nsub) {
-          if (h == 0) ok = __all_sync(0xffffffffu, pwait(&sb.k_full[(blk + 1) % kKS], (blk + 1) / kKS, abort_flag, a.err));
+        if (ok && i + 1 < nblk) {
+          ok = __all_sync(0xffffffffu, pwait(&sb.k_full[(i + 1) % kKS], (i + 1) / kKS, abort_flag, a.err));
           for (int x = 0; ok && x < ntile; ++x) {
-            ok = __all_sync(0xffffffffu, pwait(&sb.pv_done[x][h], blk, abort_flag, a.err));
+            ok = __all_sync(0xffffffffu, pwait(&sb.pv_done[x], i, abort_flag, a.err));
             if (!ok) break;
             tc_fence_after();
-            issue_s(x, j + 2);
+            issue_s(x, i + 1);
           }
         }
       }
@@ -479,58 +476,79 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_c
     const float sl2 = a.scale_log2;
     float m_used = -INFINITY, lsum = 0.f;  // m in scaled log2 units
     bool ok = true;
-    const int nsub = 2 * nblk;
-    for (int j = 0; j < nsub; ++j) {
-      const int h = j & 1, blk = j >> 1;
-      ok = __all_sync(0xffffffffu, pwait(&sb.s_full[X][h], blk, abort_flag, a.err));
+    for (int i = 0; i < nblk; ++i) {
+      ok = __all_sync(0xffffffffu, pwait(&sb.s_full[X], i, abort_flag, a.err));
       if (!ok) break;
       tc_fence_after();
-      // S column c (0..63) of half-block h is key 16 (c / 8) + 8 h + c % 8 of the block
-      float sv[64];
-      tmem_ld16_nowait(tS + 64 * h, sv);
-      tmem_ld16_nowait(tS + 64 * h + 16, sv + 16);
-      tmem_ld16_nowait(tS + 64 * h + 32, sv + 32);
-      tmem_ld16_nowait(tS + 64 * h + 48, sv + 48);
-      tmem_wait_ld();
       // The row attends key offsets [0, ea) (its sink rows) and [wb, we] (its
-      // window), relative to this block's first offset.
-      const int o0 = blk * kPN;
+      // window), relative to this block's first offset; S column c is key c.
+      const int o0 = i * kPN;
       const int ea = sr.se - o0, wb = wb0 - o0, we = we0 - o0;
       const bool unmasked = __all_sync(0xffffffffu, wb <= 0 && we >= kPN - 1);  // no row of the warp masks
-      if (!unmasked) {
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const int oc = 16 * (c >> 3) + 8 * h + (c & 7);
-          if (!(oc < ea || (oc >= wb && oc <= we))) sv[c] = -INFINITY;
-        }
-      }
-      // the maximum is taken on unscaled scores (scale > 0) and scaled once
+      // pass 1: the row maximum, taken on unscaled scores (scale > 0) and scaled once
       float rmax = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 64; ++c) rmax = fmaxf(rmax, sv[c]);
+      for (int q = 0; q < 2; ++q) {
+        float sv[64];
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) tmem_ld16_nowait(tS + 64 * q + 16 * c4, sv + 16 * c4);
+        tmem_wait_ld();
+        if (unmasked) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) rmax = fmaxf(rmax, sv[c]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
+            const int oc = 64 * q + c;
+            if (oc < ea || (oc >= wb && oc <= we)) rmax = fmaxf(rmax, sv[c]);
+          }
+        }
+      }
       rmax *= sl2;
       const bool grow = rmax > m_used + 8.f;  // also when nothing was kept before
       const bool scale_o = grow && lsum > 0.f;
       const float f = scale_o ? exp2f(m_used - rmax) : 1.f;
       if (grow) m_used = rmax;
       const float msub = m_used == -INFINITY ? 0.f : m_used;  // masked scores give 2^-inf = 0 either way
-      // P in S-column order, two per 32-bit column, over the first 32 columns
-      // of the sub-buffer (S_X(j + 2) is issued only after this P's P V is done)
-      uint32_t w[32];
+      // pass 2: P_X(i), keys in order, two per 32-bit column, over the first 64
+      // columns of S_X: keys 64 q .. 64 q + 63 go to columns 32 q .. 32 q + 31,
+      // which hold scores this pass has already read (S_X(i + 1) is issued
+      // only after P_X(i) V(i) is done)
       float psum = 0.f;
 #pragma unroll
-      for (int x = 0; x < 32; ++x) {
-        w[x] = pack_bf16(ex2_ftz(fmaf(sv[2 * x], sl2, -msub)), ex2_ftz(fmaf(sv[2 * x + 1], sl2, -msub)));
-        psum += bf16_lo(w[x]) + bf16_hi(w[x]);
+      for (int q = 0; q < 2; ++q) {
+        float sv[64];
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) tmem_ld16_nowait(tS + 64 * q + 16 * c4, sv + 16 * c4);
+        tmem_wait_ld();
+        uint32_t w[32];
+        if (unmasked) {
+#pragma unroll
+          for (int x = 0; x < 32; ++x) {
+            w[x] = pack_bf16(ex2_ftz(fmaf(sv[2 * x], sl2, -msub)), ex2_ftz(fmaf(sv[2 * x + 1], sl2, -msub)));
+            psum += bf16_lo(w[x]) + bf16_hi(w[x]);
+          }
+        } else {
+#pragma unroll
+          for (int x = 0; x < 32; ++x) {
+            float pp[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int oc = 64 * q + 2 * x + e;
+              pp[e] = (oc < ea || (oc >= wb && oc <= we)) ? ex2_ftz(fmaf(sv[2 * x + e], sl2, -msub)) : 0.f;
+            }
+            w[x] = pack_bf16(pp[0], pp[1]);
+            psum += bf16_lo(w[x]) + bf16_hi(w[x]);
+          }
+        }
+        tmem_st16(tS + 32 * q, w);
+        tmem_st16(tS + 32 * q + 16, w + 16);
       }
-      tmem_st16(tS + 64 * h, w);
-      tmem_st16(tS + 64 * h + 16, w + 16);
       lsum = lsum * f + psum;
       if (__any_sync(0xffffffffu, scale_o)) {
-        // O_X holds the half-blocks < j in the old maximum: rescale it once the
-        // P V of half-block j - 1 is in, before this one's may start (a
-        // warp-wide TMEM read and write)
-        ok = __all_sync(0xffffffffu, pwait(&sb.pv_done[X][h ^ 1], (j - 1) >> 1, abort_flag, a.err));
+        // O_X holds blocks < i in the old maximum: rescale it once P V(i - 1) is
+        // in, before P V(i) may start (a warp-wide TMEM read and write)
+        ok = __all_sync(0xffffffffu, pwait(&sb.pv_done[X], i - 1, abort_flag, a.err));
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
@@ -545,10 +563,10 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_c
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sb.p_full[X][h]);
+      if (lane == 0) mbar_arrive(&sb.p_full[X]);
     }
     // ---- epilogue: O / l -> bf16, once the last P V is in O ------------------
-    if (ok) ok = __all_sync(0xffffffffu, pwait(&sb.pv_done[X][(nsub - 1) & 1], (nsub - 1) >> 1, abort_flag, a.err));
+    if (ok) ok = __all_sync(0xffffffffu, pwait(&sb.pv_done[X], nblk - 1, abort_flag, a.err));
     if (ok) {
       tc_fence_after();
       const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
@@ -600,14 +618,15 @@ PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
 }
 
 // The K/V buffer as (d % 64, slot, d / 64, kv head, K/V x layer): one box
-// (64, 16, 2, 1, 1) is a 16-slot group of one head with both halves of d.
-bool encode_kvmap(const kvp_pool* pool, CUtensorMap* out) {
+// (64, 16, halves, 1, 1) is a 16-slot group of one head with ``halves`` (2:
+// both, 1: one) halves of d.
+bool encode_kvmap(const kvp_pool* pool, int halves, CUtensorMap* out) {
   const auto encode = tmap_encoder();
   if (!encode || pool->dtype != KVP_BF16 || pool->head_dim != kPD) return false;
   cuuint64_t dims[5] = {64, (cuuint64_t)pool->num_slots, 2, (cuuint64_t)pool->kv_heads,
                         (cuuint64_t)(2 * pool->num_layers)};
   cuuint64_t strides[4] = {(cuuint64_t)pool->row_bytes, 128, (cuuint64_t)kPD * 2, (cuuint64_t)pool->layer_bytes};
-  cuuint32_t box[5] = {64, 16, 2, 1, 1};
+  cuuint32_t box[5] = {64, 16, (cuuint32_t)halves, 1, 1};
   cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   return encode(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, pool->buf, dims, strides, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -644,10 +663,16 @@ int launch_prefill_tc(const kvp_pool* pool, int layer, const void* q, int batch,
   PrefillArgs a;
   const int G = Hq / pool->kv_heads;
   if (!encode_qmap(q, batch, C, Hq, G, &a.qmap)) return KVP_ERR_CUDA;
-  if (mp->tmap1_state == 0) mp->tmap1_state = encode_kvmap(pool, &mp->tmap1) ? 1 : -1;
+  if (mp->tmap1_state == 0)
+    mp->tmap1_state = encode_kvmap(pool, 2, &mp->tmap1) && encode_kvmap(pool, 1, &mp->tmap2) ? 1 : -1;
   a.use_kvmap = mp->tmap1_state == 1;
-  if (a.use_kvmap) a.kvmap = mp->tmap1;
-  else memset(&a.kvmap, 0, sizeof(a.kvmap));
+  if (a.use_kvmap) {
+    a.kvmap = mp->tmap1;
+    a.kmap = mp->tmap2;
+  } else {
+    memset(&a.kvmap, 0, sizeof(a.kvmap));
+    memset(&a.kmap, 0, sizeof(a.kmap));
+  }
   a.kvl_k = layer;
   a.kvl_v = pool->num_layers + layer;
   a.T = T;
