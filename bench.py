@@ -899,6 +899,8 @@ def measure(args, name, rank, world, local_rank, with_cpu):
             "h2d_bytes_per_step": e2e["h2d"],
             "d2h_bytes_per_step": e2e["d2h"],
             "host_link": e2e["link"],
+            "pinned_input_sets": e2e["input_sets"],
+            "warmup_steps": e2e["warmup"],
             "path": e2e["path"],
         },
         "clocks": clocks,
@@ -915,29 +917,32 @@ def measure(args, name, rank, world, local_rank, with_cpu):
     return line
 
 
+E2E_INPUT_SETS = 4  # distinct pinned input sets the end-to-end leg cycles through
+
+
 def run_e2e(args, sc, cache, lens, first_step, dev):
-    """K steps through PagedKVCache.decode_step with pinned host q/k/v and
-    outputs: host bookkeeping, all copies and the output read-back (the call
-    returns once the step's output is on the host) are inside the timing."""
+    """W untimed and K timed steps through the public driver with pinned
+    host q/k/v and outputs: bookkeeping, all copies and the output read-back
+    (each call returns once the step's output is on the host) are inside the
+    timing. The steps cycle through E2E_INPUT_SETS distinct pinned input sets,
+    as a caller reuses its staging buffers (one pinned set per step of a long
+    run would make the copies slower as the GPU's translation of host memory
+    runs out: a step over 20 distinct 160 MB sets took 15-29 ms against 8.8 ms
+    over a reused few)."""
     w = sc.w
-    K = args.steps
-    host_steps = _host_inputs(sc, first_step, K, lens)
+    K, W = args.steps, args.warmup
+    R = min(K + W, E2E_INPUT_SETS)
+    host_sets = _host_inputs(sc, first_step, R, lens)
     out_host = [torch.empty(out_shape(sc), dtype=cache.tdt, pin_memory=True) for _ in range(w.layers)]
     if sc.devalloc:
-        return _run_e2e_device(sc, cache, lens, host_steps, out_host, dev, first_step)
+        return _run_e2e_device(sc, cache, lens, host_sets, out_host, dev, first_step, K, W)
     rids = np.asarray(sc.rids, np.int32)
-    total_bytes = 0
-    torch.cuda.synchronize(dev)
-    cache.h2d_bytes = 0
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    start.record()
-    for s in range(K):
-        q_h, k_h, v_h = host_steps[s]
+
+    def step(s):
+        q_h, k_h, v_h = host_sets[s % R]
         if sc.prefill:  # a chunk per request: append, store, attend
             cache.prefill_step(rids, q_h, k_h, v_h, out_host, sc.window, w.scale, sinks=sc.sinks)
-            total_bytes += step_bytes(sc, [int(x) for x in cache.lengths[rids]], cache.last_writes,
-                                      cache.last_copies, 0)
-            continue
+            return step_bytes(sc, [int(x) for x in cache.lengths[rids]], cache.last_writes, cache.last_copies, 0)
         if sc.verify:  # draft M, verify, accept the seeded count, rewind the rest
             M = sc.verify
             cache.verify_step(rids, q_h, k_h, v_h, out_host, sc.window, w.scale, sinks=sc.sinks)
@@ -946,48 +951,53 @@ def run_e2e(args, sc, cache, lens, first_step, dev):
             n_back = 0
             for r, a in zip(sc.rids, wl.accepted_drafts(sc.seed, first_step + s, len(sc.rids), M)):
                 n_back += cache.rewind(r, M - a)
-            total_bytes += step_bytes(sc, ctx, n_writes, n_cows, n_back)
-            continue
+            return step_bytes(sc, ctx, n_writes, n_cows, n_back)
         cache.decode_step(rids, q_h, k_h, v_h, out_host, sc.window, w.scale, sinks=sc.sinks)
-        total_bytes += step_bytes(sc, [int(x) for x in cache.lengths[rids]], cache.last_writes, cache.last_copies,
-                                  cache.last_trims)
+        return step_bytes(sc, [int(x) for x in cache.lengths[rids]], cache.last_writes, cache.last_copies,
+                          cache.last_trims)
+
+    for s in range(W):
+        step(s)
+    total_bytes = 0
+    torch.cuda.synchronize(dev)
+    cache.h2d_bytes = 0
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for s in range(W, W + K):
+        total_bytes += step(s)
     end.record()
     torch.cuda.synchronize(dev)
     cache.check()
     d2h = sum(o.numel() * o.element_size() for o in out_host)
     return {"ms": start.elapsed_time(end), "bytes": total_bytes, "h2d": cache.h2d_bytes // K, "d2h": d2h,
-            "link": link_rates(dev)}
+            "link": link_rates(dev), "input_sets": R, "warmup": W}
 
 
-def _run_e2e_device(sc, cache, lens, host_steps, out_host, dev, first_step):
+def _run_e2e_device(sc, cache, lens, host_sets, out_host, dev, first_step, K, W):
     """End to end with the bookkeeping on the device: per step one native
     call copies q/k/v in from pinned host memory, runs the step (a decode
     step, or a verify step that rewinds the rejected drafts) and copies the
     output back; no host decision, no table writes from the host. The step's
-    table writes are counted for the bytes from the lengths."""
+    table writes are counted for the bytes from the lengths. W untimed steps
+    first, then K timed ones."""
     w = sc.w
-    K = len(host_steps)
+    R = len(host_sets)
     P = w.P
     rids = torch.as_tensor(sc.rids, dtype=torch.int32, device=dev)
     lens = list(lens)
     M = max(sc.verify, 1)
-    back = [[M - a for a in wl.accepted_drafts(sc.seed, first_step + s, len(sc.rids), M)] for s in range(K)] \
-        if sc.verify else None
     total_bytes = 0
-    torch.cuda.synchronize(dev)
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    start.record()
-    for s in range(K):
-        q_h, k_h, v_h = host_steps[s]
+
+    def step(s, lens):
+        q_h, k_h, v_h = host_sets[s % R]
         if sc.verify:
-            cache.verify_step_host(rids, q_h, k_h, v_h, back[s], out_host, sc.window, w.scale, sinks=sc.sinks)
+            back = [M - a for a in wl.accepted_drafts(sc.seed, first_step + s, len(sc.rids), M)]
+            cache.verify_step_host(rids, q_h, k_h, v_h, back, out_host, sc.window, w.scale, sinks=sc.sinks)
             ctx = [L + M for L in lens]
             n_writes = sum(-(-c // P) - -(-L // P) for L, c in zip(lens, ctx))
-            after = [c - nb for c, nb in zip(ctx, back[s])]
+            after = [c - nb for c, nb in zip(ctx, back)]
             n_back = sum(-(-c // P) - -(-a // P) for c, a in zip(ctx, after))
-            total_bytes += step_bytes(sc, ctx, n_writes, 0, n_back)
-            lens = after
-            continue
+            return step_bytes(sc, ctx, n_writes, 0, n_back), after
         cache.decode_step_host(rids, q_h, k_h, v_h, out_host, sc.window, w.scale, sinks=sc.sinks)
         n_writes = sum(1 for L in lens if L % P == 0)
         lens = [L + 1 for L in lens]
@@ -995,14 +1005,23 @@ def _run_e2e_device(sc, cache, lens, host_steps, out_host, dev, first_step):
         if sc.window > 0:  # pages the step's trim releases: those that fall wholly below L + 1 - (W - S)
             kf = lambda L: max(0, L + 1 - (sc.window - sc.sinks)) // P  # noqa: E731
             n_trim = sum(max(0, kf(L) - kf(L - 1)) for L in lens)
-        total_bytes += step_bytes(sc, lens, n_writes, 0, n_trim)
+        return step_bytes(sc, lens, n_writes, 0, n_trim), lens
+
+    for s in range(W):
+        _, lens = step(s, lens)
+    torch.cuda.synchronize(dev)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for s in range(W, W + K):
+        b, lens = step(s, lens)
+        total_bytes += b
     end.record()
     torch.cuda.synchronize(dev)
     cache.check()
-    h2d = sum(x[i].numel() * x[i].element_size() for x in host_steps[0] for i in range(w.layers))
+    h2d = sum(x[i].numel() * x[i].element_size() for x in host_sets[0] for i in range(w.layers))
     d2h = sum(o.numel() * o.element_size() for o in out_host)
     return {"ms": start.elapsed_time(end), "bytes": total_bytes, "h2d": h2d + (4 * len(sc.rids) if sc.verify else 0),
-            "d2h": d2h, "link": link_rates(dev)}
+            "d2h": d2h, "link": link_rates(dev), "input_sets": R, "warmup": W}
 
 
 def link_rates(dev, nbytes=128 << 20):

@@ -59,8 +59,9 @@ namespace {
 constexpr int kPM = 128;  // query rows per tile
 constexpr int kPN = 128;  // keys per block
 constexpr int kPD = 128;  // head_dim
-constexpr int kPThreads = 352;  // warps: K loader, MMA, four softmax (tile A), four softmax (tile B), V loader
+constexpr int kPThreads = 384;  // warps: K loader, MMA (tile A), 4 softmax (tile A), 4 softmax (tile B), V loader, MMA (tile B)
 constexpr int kVWarp = 10;
+constexpr int kMmaWarpB = 11;
 constexpr int kKS = 3;  // K ring stages
 constexpr int kVS = 2;  // V ring stages
 constexpr uint32_t kHalf = 16384;  // one 64-element half of a 128-row operand: 128 rows x 128 B
@@ -198,13 +199,13 @@ __device__ __forceinline__ uint32_t sw128(int r, int c) { return (uint32_t)(r * 
 struct PrefillBars {
   uint64_t q_full;
   uint64_t k_full[kKS];   // loader -> MMA: K block in K stage s (TMA bytes and thread copies)
-  uint64_t k_empty[kKS];  // MMA -> loader: both tiles' S have read K stage s
+  uint64_t k_empty[kKS];  // MMA (one commit per tile) -> loader: both tiles' S have read K stage s
   uint64_t v_full[kVS];   // loader -> MMA: V block in V stage s
-  uint64_t v_empty[kVS];  // MMA -> loader: both tiles' P V have read V stage s
+  uint64_t v_empty[kVS];  // MMA (one commit per tile) -> loader: both tiles' P V have read V stage s
   uint64_t s_full[2];     // MMA -> softmax of tile X: S_X = Q_X K^T of the block in TMEM
   uint64_t p_full[2];     // softmax of tile X (4 warps) -> MMA: P_X of the block in TMEM
   uint64_t pv_done[2];    // MMA -> all: O_X += P_X V of the block done (S_X's columns free again)
-  uint64_t drain;         // MMA -> all: everything it issued is done
+  uint64_t drain;         // MMA (one commit per tile) -> all: everything issued is done
   uint32_t taddr;
   int abort;
   int slots[2][kPN];      // the K and the V loader's slots of the block being loaded
@@ -268,9 +269,10 @@ __device__ __forceinline__ void load_rows(const PrefillArgs& a, unsigned char* d
 }
 
 // Warp roles: 0 loads Q once, then K blocks into a three-stage ring; 10
-// loads V blocks into a two-stage ring; 1 issues the MMAs (lane 0); 2..5 run
-// the softmax of tile A and 6..9 that of tile B, one query row per thread
-// (TMEM lane quadrant = warp % 4), and their epilogues.
+// loads V blocks into a two-stage ring; 1 issues tile A's MMAs and 11 tile
+// B's (lane 0 each: one issuing thread cannot keep the tensor core busy);
+// 2..5 run the softmax of tile A and 6..9 that of tile B, one query row per
+// thread (TMEM lane quadrant = warp % 4), and their epilogues.
 __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_constant__ PrefillArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ PrefillBars sb;
@@ -295,8 +297,8 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_c
   const int row = a.table_rows ? a.table_rows[b] : b;
   const bool valid = ql >= 1 && ql <= a.C && ql <= L && L <= table_capacity(a.T) && row >= 0 && row < a.T.rows_total;
   // softmax threads: tile X = (warp - 2) / 4, query row r = 32 * (warp % 4) + lane: token j0 + X TT + r / G,
-  // head r % G of the group
-  const int X = warp >= 6 ? 1 : 0;
+  // head r % G of the group (the MMA warps: tile X = warp == kMmaWarpB)
+  const int X = warp >= 6 ? (warp == kVWarp ? 0 : 1) : 0;
   const int r = 32 * (warp & 3) + lane;
   const int rt = X * TT + r / a.G, hh = r % a.G;  // token offset from j0, head in the group
   __nv_bfloat16* orow = a.out + (((size_t)b * a.C + j0 + rt) * a.Hq + (size_t)g * a.G + hh) * kPD;
@@ -317,20 +319,21 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_c
 
   if (tid == 0) {
     mbar_init(&sb.q_full, 1);
+    const uint32_t ntile = has_b ? 2 : 1;
     for (int s2 = 0; s2 < kKS; ++s2) {
       mbar_init(&sb.k_full[s2], 1);
-      mbar_init(&sb.k_empty[s2], 1);
+      mbar_init(&sb.k_empty[s2], ntile);
     }
     for (int s2 = 0; s2 < kVS; ++s2) {
       mbar_init(&sb.v_full[s2], 1);
-      mbar_init(&sb.v_empty[s2], 1);
+      mbar_init(&sb.v_empty[s2], ntile);
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(&sb.s_full[x], 1);
       mbar_init(&sb.p_full[x], 4);
       mbar_init(&sb.pv_done[x], 1);
     }
-    mbar_init(&sb.drain, 1);
+    mbar_init(&sb.drain, ntile);
     sb.abort = 0;
     fence_mbar_init();
   }
@@ -393,30 +396,34 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_c
       load_rows(a, (is_v ? sV : sK) + st * 2 * kHalf, slots, tm, g, is_v, is_v ? &sb.v_full[st] : &sb.k_full[st],
                 lane);
     }
-  } else if (warp == 1) {
-    // ======================= MMA issuer =======================================
+  } else if (warp == 1 || warp == kMmaWarpB) {
+    // ======================= MMA issuers (one per tile) ========================
     // S_X(i) = Q_X K(i)^T is eight N 128 MMAs (one per 16-wide K step of d),
     // so S column c is key c of the block. S_X(i + 1) overwrites P_X(i), so
-    // it waits for P_X(i) V. Issue order: S_A(0), S_B(0), then per block i:
-    // P_A(i) V, P_B(i) V, S_A(i + 1), S_B(i + 1): while one tile's softmax
-    // runs, the tensor core works on the other tile. The whole warp walks
-    // the schedule and waits (no divergent spin beside the issuing lane);
-    // lane 0 alone issues the MMAs and the commits.
-    {
+    // it waits for P_X(i) V. Per block i: P_X(i) V, then S_X(i + 1); the two
+    // tiles' issuers run side by side, so while one tile's softmax runs the
+    // tensor core works on the other tile. The whole warp walks the schedule
+    // and waits (no divergent spin beside the issuing lane); lane 0 alone
+    // issues the MMAs and the commits. A K (V) stage is free once both
+    // tiles' issuers have committed their S (P V) of it.
+    if (X == 0 || has_b) {
       const bool issuer = lane == 0;
-      const int ntile = has_b ? 2 : 1;
       const uint32_t id_n128 = umma_idesc(0, kPN), id_o = umma_idesc(1, kPN);
-      auto issue_s = [&](int x, int blk) {
-        const uint32_t qa = smem_u32(sQ + x * 2 * kHalf), tS = tbase + (uint32_t)x * 128u;
-        const uint32_t ka = smem_u32(sK + (blk % kKS) * 2 * kHalf);
+      const uint32_t tS = tbase + (uint32_t)X * 128u, tO = tbase + 256u + (uint32_t)X * 128u;
+      // descriptors of the operands' starts; a K step adds its byte offset >> 4
+      const uint64_t dq = umma_desc(smem_u32(sQ + X * 2 * kHalf), 16, 1024);
+      const uint64_t dk0 = umma_desc(smem_u32(sK), 16, 1024);
+      const uint64_t dv0 = umma_desc(smem_u32(sV), kGroupBytes / 2, 1024);
+      auto issue_s = [&](int blk) {
+        const uint64_t dk = dk0 + (uint64_t)(((blk % kKS) * 2 * kHalf) >> 4);
         if (issuer) {
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t off = (uint32_t)(ks >> 2) * kHalf + (uint32_t)(ks & 3) * 32u;
-            umma_f16(tS, umma_desc(qa + off, 16, 1024), umma_desc(ka + off, 16, 1024), id_n128, ks > 0);
+            const uint64_t off = (uint64_t)((((ks >> 2) * kHalf) + (ks & 3) * 32) >> 4);
+            umma_f16(tS, dq + off, dk + off, id_n128, ks > 0);
           }
-          umma_commit(&sb.s_full[x]);
-          if (x == ntile - 1) umma_commit(&sb.k_empty[blk % kKS]);  // both tiles' S have read the K stage
+          umma_commit(&sb.s_full[X]);
+          umma_commit(&sb.k_empty[blk % kKS]);
         }
         __syncwarp();
       };
@@ -424,40 +431,35 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_c
       if (ok) ok = __all_sync(0xffffffffu, pwait(&sb.k_full[0], 0, abort_flag, a.err));
       if (ok) {
         tc_fence_after();
-        for (int x = 0; x < ntile; ++x) issue_s(x, 0);
+        issue_s(0);
       }
       for (int i = 0; ok && i < nblk; ++i) {
         const int sv = i % kVS;
         ok = __all_sync(0xffffffffu, pwait(&sb.v_full[sv], i / kVS, abort_flag, a.err));
+        if (ok) ok = __all_sync(0xffffffffu, pwait(&sb.p_full[X], i, abort_flag, a.err));
+        if (!ok) break;
+        tc_fence_after();
         // O_X += P_X(i) V(i): P_X from TMEM (8 columns per 16 keys), V group m
         // the MN-major B operand of K step m (halves of d 2 KB apart, 8-key atoms 1 KB)
-        const uint32_t va = smem_u32(sV + sv * 2 * kHalf);
-        for (int x = 0; ok && x < ntile; ++x) {
-          ok = __all_sync(0xffffffffu, pwait(&sb.p_full[x], i, abort_flag, a.err));
+        const uint64_t dv = dv0 + (uint64_t)((sv * 2 * kHalf) >> 4);
+        if (issuer) {
+#pragma unroll
+          for (int m = 0; m < 8; ++m)
+            umma_f16_ts(tO, tS + (uint32_t)m * 8u, dv + (uint64_t)((m * kGroupBytes) >> 4), id_o,
+                        (i > 0 || m > 0) ? 1u : 0u);
+          umma_commit(&sb.pv_done[X]);
+          umma_commit(&sb.v_empty[sv]);
+        }
+        __syncwarp();
+        if (i + 1 < nblk) {
+          ok = __all_sync(0xffffffffu, pwait(&sb.k_full[(i + 1) % kKS], (i + 1) / kKS, abort_flag, a.err));
+          if (ok) ok = __all_sync(0xffffffffu, pwait(&sb.pv_done[X], i, abort_flag, a.err));
           if (!ok) break;
           tc_fence_after();
-          const uint32_t tP = tbase + (uint32_t)x * 128u, tO = tbase + 256u + (uint32_t)x * 128u;
-          if (issuer) {
-#pragma unroll
-            for (int m = 0; m < 8; ++m)
-              umma_f16_ts(tO, tP + (uint32_t)m * 8u, umma_desc(va + (uint32_t)m * kGroupBytes, kGroupBytes / 2, 1024),
-                          id_o, (i > 0 || m > 0) ? 1u : 0u);
-            umma_commit(&sb.pv_done[x]);
-            if (x == ntile - 1) umma_commit(&sb.v_empty[sv]);  // both tiles' P V have read the V stage
-          }
-          __syncwarp();
-        }
-        if (ok && i + 1 < nblk) {
-          ok = __all_sync(0xffffffffu, pwait(&sb.k_full[(i + 1) % kKS], (i + 1) / kKS, abort_flag, a.err));
-          for (int x = 0; ok && x < ntile; ++x) {
-            ok = __all_sync(0xffffffffu, pwait(&sb.pv_done[x], i, abort_flag, a.err));
-            if (!ok) break;
-            tc_fence_after();
-            issue_s(x, i + 1);
-          }
+          issue_s(i + 1);
         }
       }
-      if (issuer) umma_commit(&sb.drain);  // arrives once everything issued above is done
+      if (issuer) umma_commit(&sb.drain);  // arrives once everything this warp issued is done
       __syncwarp();
     }
   } else if (warp < kVWarp && (X == 0 || has_b)) {
