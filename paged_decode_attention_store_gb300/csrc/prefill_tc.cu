@@ -32,8 +32,8 @@
 //   the row maximum is taken on unscaled scores and P = 2^(s * scale - m) is
 //   one FMA and one ex2 per score. O is rescaled (read, scaled, written back
 //   in TMEM) only when the row maximum grows by more than 8, so P <= 256
-//   always fits bf16 and the normalisation stays exact (numerator and
-//   denominator use the same m and the same rounded P).
+//   always fits bf16 (numerator and denominator use the same m; the row sum
+//   adds the fp32 exponentials, P V their bf16 roundings).
 // * P (bf16, two per 32-bit column, keys in order) is written back into the
 //   first 64 columns of S_X and is the A operand, read from TMEM, of O += P V
 //   (V the MN-major operand in shared memory, one 16-key group per K step).
@@ -41,11 +41,14 @@
 // * Warp-specialised pipeline: two loader warps fill a three-stage K ring
 //   and a two-stage V ring (a K stage is free once both tiles' S have read
 //   it, a V stage once both P V have), each resolving its own slots; an MMA
-//   warp issues S_A(0), S_B(0), then per block i: P_A(i) V, P_B(i) V,
-//   S_A(i + 1), S_B(i + 1); two groups of four softmax warps turn each tile's
-//   scores into P. While one tile's softmax runs the tensor core works on the
-//   other tile. S_X(i + 1) overwrites P_X(i), so it is issued once P_X(i) V
-//   is done. mbarriers carry every hand-off.
+//   warp per tile issues S_X(0), then per block i: P_X(i) V and S_X(i + 1)
+//   (one issuing thread cannot keep the tensor core busy: measured); two
+//   groups of four softmax warps turn each tile's scores into P. S_X(i + 1)
+//   overwrites P_X(i), so it is issued once P_X(i) V is done. mbarriers carry
+//   every hand-off.
+// * The softmax is bound by instruction issue: the scale-and-shift of a pair
+//   of scores is one packed fma.rn.f32x2, their row sum one packed
+//   add.rn.f32x2 (of the fp32 exponentials, before the bf16 rounding of P).
 // * Every wait is bounded (2 s): on timeout the CTA records KVP_ERR_TIMEOUT,
 //   issues nothing more, waits (bounded) for what it issued and frees TMEM.
 #include <cudaTypedefs.h>
@@ -181,6 +184,21 @@ __device__ __forceinline__ void umma_f16_ts(uint32_t tmem_d, uint32_t tmem_a, ui
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
       "r"(tmem_a), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
+}
+
+// (d0, d1) = (a0, a1) * (b, b) + (c, c) and (d0, d1) += (a0, a1): Blackwell's
+// packed fp32 instructions, one issue for two lanes of work.
+__device__ __forceinline__ void fma2_bc(float& d0, float& d1, float a0, float a1, float b, float c) {
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %4};\n\t"
+      "mov.b64 rc, {%5, %5};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+__device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1) {
+  asm("{\n\t.reg .b64 ra, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rd, {%0, %1};\n\t"
+      "add.rn.f32x2 rd, rd, ra;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1));
 }
 
 // 2^x by the PTX approximate base-2 exponential (flush-to-zero; 2^-inf = +0).
@@ -516,7 +534,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_c
       // columns of S_X: keys 64 q .. 64 q + 63 go to columns 32 q .. 32 q + 31,
       // which hold scores this pass has already read (S_X(i + 1) is issued
       // only after P_X(i) V(i) is done)
-      float psum = 0.f;
+      float ps0 = 0.f, ps1 = 0.f;  // the row sum, two lanes of a packed add
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
         float sv[64];
@@ -527,8 +545,11 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_c
         if (unmasked) {
 #pragma unroll
           for (int x = 0; x < 32; ++x) {
-            w[x] = pack_bf16(ex2_ftz(fmaf(sv[2 * x], sl2, -msub)), ex2_ftz(fmaf(sv[2 * x + 1], sl2, -msub)));
-            psum += bf16_lo(w[x]) + bf16_hi(w[x]);
+            float x0, x1;
+            fma2_bc(x0, x1, sv[2 * x], sv[2 * x + 1], sl2, -msub);
+            const float p0 = ex2_ftz(x0), p1 = ex2_ftz(x1);
+            w[x] = pack_bf16(p0, p1);
+            add2(ps0, ps1, p0, p1);
           }
         } else {
 #pragma unroll
@@ -540,13 +561,13 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_c
               pp[e] = (oc < ea || (oc >= wb && oc <= we)) ? ex2_ftz(fmaf(sv[2 * x + e], sl2, -msub)) : 0.f;
             }
             w[x] = pack_bf16(pp[0], pp[1]);
-            psum += bf16_lo(w[x]) + bf16_hi(w[x]);
+            add2(ps0, ps1, pp[0], pp[1]);
           }
         }
         tmem_st16(tS + 32 * q, w);
         tmem_st16(tS + 32 * q + 16, w + 16);
       }
-      lsum = lsum * f + psum;
+      lsum = lsum * f + (ps0 + ps1);
       if (__any_sync(0xffffffffu, scale_o)) {
         // O_X holds blocks < i in the old maximum: rescale it once P V(i - 1) is
         // in, before P V(i) may start (a warp-wide TMEM read and write)
