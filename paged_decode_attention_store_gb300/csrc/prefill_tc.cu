@@ -26,9 +26,9 @@
 //   256 (measured), so the kernel keeps N large: S_X = Q_X K^T (M 128, N 128,
 //   K 128, both operands K-major) accumulates in the tile's 128-column TMEM
 //   S buffer, column c holding key c of the block. Each softmax thread owns
-//   one query row: it reads its 128 scores from TMEM (once for the maximum,
-//   once for P) and keeps an online softmax in log2 units. A block that no
-//   row of the warp masks (causal, window, sinks, block end) skips the mask;
+//   one query row: it reads its 128 scores from TMEM (one wait for all) and
+//   keeps an online softmax in log2 units. A block that no row of the warp
+//   masks (causal, window, sinks, block end) skips the mask;
 //   the row maximum is taken on unscaled scores and P = 2^(s * scale - m) is
 //   one FMA and one ex2 per score. O is rescaled (read, scaled, written back
 //   in TMEM) only when the row maximum grows by more than 8, so P <= 256
@@ -505,67 +505,41 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_c
       const int o0 = i * kPN;
       const int ea = sr.se - o0, wb = wb0 - o0, we = we0 - o0;
       const bool unmasked = __all_sync(0xffffffffu, wb <= 0 && we >= kPN - 1);  // no row of the warp masks
-      // pass 1: the row maximum, taken on unscaled scores (scale > 0) and scaled once
+      // The row's 128 scores, read from TMEM once (one wait for four loads).
+      float sv[128];
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8) tmem_ld16_nowait(tS + 16 * c8, sv + 16 * c8);
+      tmem_wait_ld();
+      if (!unmasked) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (!(c < ea || (c >= wb && c <= we))) sv[c] = -INFINITY;
+      }
+      // the row maximum, taken on unscaled scores (scale > 0) and scaled once
       float rmax = -INFINITY;
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        float sv[64];
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) tmem_ld16_nowait(tS + 64 * q + 16 * c4, sv + 16 * c4);
-        tmem_wait_ld();
-        if (unmasked) {
-#pragma unroll
-          for (int c = 0; c < 64; ++c) rmax = fmaxf(rmax, sv[c]);
-        } else {
-#pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            const int oc = 64 * q + c;
-            if (oc < ea || (oc >= wb && oc <= we)) rmax = fmaxf(rmax, sv[c]);
-          }
-        }
-      }
+      for (int c = 0; c < 128; ++c) rmax = fmaxf(rmax, sv[c]);
       rmax *= sl2;
       const bool grow = rmax > m_used + 8.f;  // also when nothing was kept before
       const bool scale_o = grow && lsum > 0.f;
       const float f = scale_o ? exp2f(m_used - rmax) : 1.f;
       if (grow) m_used = rmax;
       const float msub = m_used == -INFINITY ? 0.f : m_used;  // masked scores give 2^-inf = 0 either way
-      // pass 2: P_X(i), keys in order, two per 32-bit column, over the first 64
-      // columns of S_X: keys 64 q .. 64 q + 63 go to columns 32 q .. 32 q + 31,
-      // which hold scores this pass has already read (S_X(i + 1) is issued
-      // only after P_X(i) V(i) is done)
+      // P_X(i), keys in order, two per 32-bit column, over the first 64
+      // columns of S_X (S_X(i + 1) is issued only after P_X(i) V(i) is done)
       float ps0 = 0.f, ps1 = 0.f;  // the row sum, two lanes of a packed add
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        float sv[64];
+      for (int q = 0; q < 4; ++q) {
+        uint32_t w[16];
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) tmem_ld16_nowait(tS + 64 * q + 16 * c4, sv + 16 * c4);
-        tmem_wait_ld();
-        uint32_t w[32];
-        if (unmasked) {
-#pragma unroll
-          for (int x = 0; x < 32; ++x) {
-            float x0, x1;
-            fma2_bc(x0, x1, sv[2 * x], sv[2 * x + 1], sl2, -msub);
-            const float p0 = ex2_ftz(x0), p1 = ex2_ftz(x1);
-            w[x] = pack_bf16(p0, p1);
-            add2(ps0, ps1, p0, p1);
-          }
-        } else {
-#pragma unroll
-          for (int x = 0; x < 32; ++x) {
-            float pp[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int oc = 64 * q + 2 * x + e;
-              pp[e] = (oc < ea || (oc >= wb && oc <= we)) ? ex2_ftz(fmaf(sv[2 * x + e], sl2, -msub)) : 0.f;
-            }
-            w[x] = pack_bf16(pp[0], pp[1]);
-            add2(ps0, ps1, pp[0], pp[1]);
-          }
+        for (int x = 0; x < 16; ++x) {
+          float x0, x1;
+          fma2_bc(x0, x1, sv[32 * q + 2 * x], sv[32 * q + 2 * x + 1], sl2, -msub);
+          const float p0 = ex2_ftz(x0), p1 = ex2_ftz(x1);
+          w[x] = pack_bf16(p0, p1);
+          add2(ps0, ps1, p0, p1);
         }
-        tmem_st16(tS + 32 * q, w);
-        tmem_st16(tS + 32 * q + 16, w + 16);
+        tmem_st16(tS + 16 * q, w);
       }
       lsum = lsum * f + (ps0 + ps1);
       if (__any_sync(0xffffffffu, scale_o)) {
