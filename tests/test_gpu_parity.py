@@ -49,6 +49,11 @@ def test_generator_identical_on_cpu_and_gpu(kb):
 
 @pytest.mark.parametrize("dtype,Hkv,D", [("bf16", 8, 128), ("f32", 2, 16), ("bf16", 1, 64)])
 def test_store_cache_bit_exact(kb, dtype, Hkv, D):
+    """Every slot of the written layer equals the oracle's SlotStore after
+    the same store_cache (mini-sglang part 4: row i at slot out_loc[i]);
+    slots never written stay zero, other layers are untouched."""
+    import oracle.attention as OA
+
     tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
     P, pages, layers = 16, 40, 3
     kv = torch.zeros((2, layers, pages, P, Hkv, D), dtype=tdt, device=DEV)
@@ -59,13 +64,16 @@ def test_store_cache_bit_exact(kb, dtype, Hkv, D):
     kb.store_cache(pool, 1, k, v, torch.tensor(slots, dtype=torch.int32, device=DEV))
     torch.cuda.synchronize()
     assert kb.kvp_sync_error(pool) == 0
-    flatK = kv[0, 1].reshape(pages * P, Hkv, D)
-    flatV = kv[1, 1].reshape(pages * P, Hkv, D)
-    idx = torch.tensor(slots, device=DEV)
-    assert torch.equal(flatK[idx], k) and torch.equal(flatV[idx], v)
-    mask = torch.ones(pages * P, dtype=torch.bool, device=DEV)
-    mask[idx] = False
-    assert not flatK[mask].any() and not flatV[mask].any()
+    store = OA.SlotStore()
+    kc, vc = wl.kv_rows(1, 1, 0, list(range(300)), Hkv, D, dtype=tdt)
+    store.store_cache(slots, kc.double().numpy(), vc.double().numpy())
+    gotK = kv[0, 1].reshape(pages * P, Hkv, D).double().cpu().numpy()
+    gotV = kv[1, 1].reshape(pages * P, Hkv, D).double().cpu().numpy()
+    for sl in range(pages * P):
+        if sl in store.k:
+            assert np.array_equal(gotK[sl], store.k[sl]) and np.array_equal(gotV[sl], store.v[sl]), f"slot {sl}"
+        else:
+            assert not gotK[sl].any() and not gotV[sl].any(), f"slot {sl} was written"
     assert not kv[:, 0].any() and not kv[:, 2].any()  # other layers untouched
 
 
@@ -134,17 +142,32 @@ def test_page_table_write_block_and_raw(kb, P):
 
 
 def test_copy_pages_bit_exact(kb):
-    P, pages, layers = 16, 12, 2
-    kv = torch.randn((2, layers, pages, P, 8, 128), device=DEV).to(torch.bfloat16)
-    ref = kv.clone()
+    """copy_pages equals the oracle's whole-page copy (chapter 15, "The
+    model": a shared tail page is copied before a private write) on every
+    layer, K and V."""
+    import oracle.attention as OA
+
+    P, pages, layers, Hkv, D = 16, 12, 2, 8, 128
+    kv = torch.randn((2, layers, pages, P, Hkv, D), device=DEV).to(torch.bfloat16)
+    stores = []
+    for layer in range(layers):  # the oracle's view of the pool, every slot written
+        st = OA.SlotStore()
+        st.store_cache(list(range(pages * P)), kv[0, layer].reshape(-1, Hkv, D).double().cpu().numpy(),
+                       kv[1, layer].reshape(-1, Hkv, D).double().cpu().numpy())
+        stores.append(st)
     pool = kb.Pool(kv, P, kb.KVP_BF16)
     src, dst = [1, 5, 7], [2, 9, 0]
     kb.copy_pages(pool, torch.tensor(src, dtype=torch.int32, device=DEV), torch.tensor(dst, dtype=torch.int32, device=DEV))
     torch.cuda.synchronize()
-    for s, d in zip(src, dst):
-        ref[:, :, d] = ref[:, :, s]
-    assert torch.equal(kv, ref)
     assert kb.kvp_sync_error(pool) == 0
+    for st in stores:
+        for s_, d_ in zip(src, dst):
+            st.copy_page(s_, d_, P)
+    for layer, st in enumerate(stores):
+        gotK = kv[0, layer].reshape(-1, Hkv, D).double().cpu().numpy()
+        gotV = kv[1, layer].reshape(-1, Hkv, D).double().cpu().numpy()
+        for sl in range(pages * P):
+            assert np.array_equal(gotK[sl], st.k[sl]) and np.array_equal(gotV[sl], st.v[sl]), f"layer {layer} slot {sl}"
 
 
 # ---------------------------------------------------------------------------
