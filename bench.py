@@ -939,34 +939,35 @@ def run_e2e(args, sc, cache, lens, first_step, dev):
     rids = np.asarray(sc.rids, np.int32)
 
     def step(s):
+        """One step; returns what its bytes are computed from (after the timing)."""
         q_h, k_h, v_h = host_sets[s % R]
         if sc.prefill:  # a chunk per request: append, store, attend
             cache.prefill_step(rids, q_h, k_h, v_h, out_host, sc.window, w.scale, sinks=sc.sinks)
-            return step_bytes(sc, [int(x) for x in cache.lengths[rids]], cache.last_writes, cache.last_copies, 0)
+            return cache.lengths[rids].copy(), cache.last_writes, cache.last_copies, 0
         if sc.verify:  # draft M, verify, accept the seeded count, rewind the rest
             M = sc.verify
             cache.verify_step(rids, q_h, k_h, v_h, out_host, sc.window, w.scale, sinks=sc.sinks)
-            ctx = [int(x) for x in cache.lengths[rids]]
+            ctx = cache.lengths[rids].copy()
             n_writes, n_cows = cache.last_writes, cache.last_copies
             n_back = 0
             for r, a in zip(sc.rids, wl.accepted_drafts(sc.seed, first_step + s, len(sc.rids), M)):
                 n_back += cache.rewind(r, M - a)
-            return step_bytes(sc, ctx, n_writes, n_cows, n_back)
+            return ctx, n_writes, n_cows, n_back
         cache.decode_step(rids, q_h, k_h, v_h, out_host, sc.window, w.scale, sinks=sc.sinks)
-        return step_bytes(sc, [int(x) for x in cache.lengths[rids]], cache.last_writes, cache.last_copies,
-                          cache.last_trims)
+        return cache.lengths[rids].copy(), cache.last_writes, cache.last_copies, cache.last_trims
 
     for s in range(W):
         step(s)
-    total_bytes = 0
     torch.cuda.synchronize(dev)
     cache.h2d_bytes = 0
+    records = []
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record()
     for s in range(W, W + K):
-        total_bytes += step(s)
+        records.append(step(s))
     end.record()
     torch.cuda.synchronize(dev)
+    total_bytes = sum(step_bytes(sc, [int(x) for x in lens_], nw, nc, nt) for lens_, nw, nc, nt in records)
     cache.check()
     d2h = sum(o.numel() * o.element_size() for o in out_host)
     return {"ms": start.elapsed_time(end), "bytes": total_bytes, "h2d": cache.h2d_bytes // K, "d2h": d2h,
@@ -986,37 +987,45 @@ def _run_e2e_device(sc, cache, lens, host_sets, out_host, dev, first_step, K, W)
     rids = torch.as_tensor(sc.rids, dtype=torch.int32, device=dev)
     lens = list(lens)
     M = max(sc.verify, 1)
-    total_bytes = 0
 
-    def step(s, lens):
-        q_h, k_h, v_h = host_sets[s % R]
+    # every step's inputs and byte count are known before the timing starts
+    backs, step_b = [], []
+    for s in range(W + K):
         if sc.verify:
             back = [M - a for a in wl.accepted_drafts(sc.seed, first_step + s, len(sc.rids), M)]
-            cache.verify_step_host(rids, q_h, k_h, v_h, back, out_host, sc.window, w.scale, sinks=sc.sinks)
             ctx = [L + M for L in lens]
             n_writes = sum(-(-c // P) - -(-L // P) for L, c in zip(lens, ctx))
             after = [c - nb for c, nb in zip(ctx, back)]
             n_back = sum(-(-c // P) - -(-a // P) for c, a in zip(ctx, after))
-            return step_bytes(sc, ctx, n_writes, 0, n_back), after
-        cache.decode_step_host(rids, q_h, k_h, v_h, out_host, sc.window, w.scale, sinks=sc.sinks)
+            backs.append(back)
+            step_b.append(step_bytes(sc, ctx, n_writes, 0, n_back))
+            lens = after
+            continue
         n_writes = sum(1 for L in lens if L % P == 0)
         lens = [L + 1 for L in lens]
         n_trim = 0
         if sc.window > 0:  # pages the step's trim releases: those that fall wholly below L + 1 - (W - S)
             kf = lambda L: max(0, L + 1 - (sc.window - sc.sinks)) // P  # noqa: E731
             n_trim = sum(max(0, kf(L) - kf(L - 1)) for L in lens)
-        return step_bytes(sc, lens, n_writes, 0, n_trim), lens
+        step_b.append(step_bytes(sc, lens, n_writes, 0, n_trim))
+
+    def step(s):
+        q_h, k_h, v_h = host_sets[s % R]
+        if sc.verify:
+            cache.verify_step_host(rids, q_h, k_h, v_h, backs[s], out_host, sc.window, w.scale, sinks=sc.sinks)
+        else:
+            cache.decode_step_host(rids, q_h, k_h, v_h, out_host, sc.window, w.scale, sinks=sc.sinks)
 
     for s in range(W):
-        _, lens = step(s, lens)
+        step(s)
     torch.cuda.synchronize(dev)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record()
     for s in range(W, W + K):
-        b, lens = step(s, lens)
-        total_bytes += b
+        step(s)
     end.record()
     torch.cuda.synchronize(dev)
+    total_bytes = sum(step_b[W:])
     cache.check()
     h2d = sum(x[i].numel() * x[i].element_size() for x in host_sets[0] for i in range(w.layers))
     d2h = sum(o.numel() * o.element_size() for o in out_host)
