@@ -520,6 +520,13 @@ int kvp_dev_trim(kvp_dev_pages* d, const int32_t* rids, const int32_t* keep_from
  * to the free stack at zero), as kvp_host_release. At most 4096 pages. */
 int kvp_dev_release(kvp_dev_pages* d, const int32_t* rids, int n,
                     void* stream);
+/* Rewind (kvp_host_rewind on the device): request rids[i] drops its newest
+ * n_back[i] rows (both device int32 [n], n <= 1024); the pages past the new
+ * length go, tail first, and their entries become -1. A rewind below the
+ * rows a window or its sinks released, or n_back[i] outside [0, length],
+ * sets KVP_ERR_INVALID_ARG in the state's error word and changes nothing. */
+int kvp_dev_rewind(kvp_dev_pages* d, const int32_t* rids, const int32_t* n_back,
+                   int n, void* stream);
 /* Fork: request dst[i] shares every page of src[i] (one more reference
  * each) and takes its length (device int32 [n]); the dst ids must be
  * distinct and none of them a src of the same call. */
@@ -569,6 +576,41 @@ int kvp_decode_step_device_io(kvp_dev_pages* d, const kvp_pool* pool,
                               const void* const* q_host,
                               const void* const* k_host,
                               const void* const* v_host,
+                              void* const* out_host, void* const* q_dev,
+                              void* const* k_dev, void* const* v_dev,
+                              void* const* out_dev, int32_t* scratch,
+                              int may_share, void* workspace,
+                              size_t workspace_bytes, void* stream);
+/* kvp_verify_step_device_io: one speculative-decoding verify step with the
+ * page bookkeeping on the device and host buffers ("Week 3 Day 3: Paged KV
+ * Cache" of tiny-llm names speculative decoding as the user of rewind(n)):
+ *   1. the inputs go to the caller's device staging on the page state's copy
+ *      stream: per layer q_host[l] [n, M, Hq, D] -> q_dev[l], k_host[l] and
+ *      v_host[l] [n * M, kv_heads, D] (request-major) -> k_dev[l], v_dev[l],
+ *      and n_back_host (host int32 [n], 0 <= n_back[i] <= M) into scratch;
+ *   2. kvp_dev_append: M rows for each of the n requests rids (DEVICE int32
+ *      [n], distinct, ids = table rows); if may_share, the copy-on-write
+ *      copies;
+ *   3. for each layer, once its inputs are in: store_cache of the n * M
+ *      rows, paged_verify_attention(q_dev[l] -> out_dev[l]) with the new
+ *      lengths;
+ *   4. kvp_dev_rewind of n_back[i] rows per request (the rejected drafts),
+ *      then with a window kvp_dev_trim to L + 1 - (window - sinks);
+ *   5. out_dev[l] -> out_host[l]; returns once the outputs are on the host.
+ * scratch: device int32 [n * M + 4 n + 1]; workspace as
+ * paged_verify_attention_workspace_size(pool, n, M, Hq). Host buffers
+ * should be pinned for the copies to be asynchronous. Errors as the calls
+ * it makes; device-detected ones go to the state's and the pool's error
+ * words. */
+int kvp_verify_step_device_io(kvp_dev_pages* d, const kvp_pool* pool,
+                              int32_t* table, int table_rows_total,
+                              int table_cols, int table_mode,
+                              const int32_t* rids, int n, int num_q_tokens,
+                              int window, int sinks, int num_q_heads,
+                              float scale, const void* const* q_host,
+                              const void* const* k_host,
+                              const void* const* v_host,
+                              const int32_t* n_back_host,
                               void* const* out_host, void* const* q_dev,
                               void* const* k_dev, void* const* v_dev,
                               void* const* out_dev, int32_t* scratch,

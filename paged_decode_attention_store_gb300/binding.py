@@ -80,6 +80,9 @@ SIGNATURES = {
     "kvp_dev_release": [_vp, _vp, _i, _vp],
     "kvp_dev_sync_error": [_vp, _vp, _ip],
     "kvp_dev_fork": [_vp, _vp, _vp, _i, _vp],
+    "kvp_dev_rewind": [_vp, _vp, _vp, _i, _vp],
+    "kvp_verify_step_device_io": [_vp, _vp, _vp, _i, _i, _i, _vp, _i, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _vp,
+                                  _vp, _vp, _vp, _vp, _vp, _i, _vp, _sz, _vp],
     "copy_pages_device_count": [_vp, _vp, _vp, _vp, _i, _vp],
     "kvp_decode_step_device": [_vp, _vp, _vp, _i, _i, _i, _vp, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _vp, _vp,
                                _vp, _i, _vp, _sz, _vp],
@@ -277,6 +280,15 @@ class DevicePages:
         if src.numel() != dst.numel():
             raise ValueError("src and dst must have the same length")
         _check(lib().kvp_dev_fork(self.handle, _ptr(src), _ptr(dst), src.numel(), _stream(stream)), "kvp_dev_fork")
+
+    def rewind(self, rids, n_back, stream=None):
+        """Drop the newest n_back[i] rows of request rids[i] (both device int32)."""
+        _dev(rids, torch.int32, "rids")
+        _dev(n_back, torch.int32, "n_back")
+        if rids.numel() != n_back.numel():
+            raise ValueError("rids and n_back must have the same length")
+        _check(lib().kvp_dev_rewind(self.handle, _ptr(rids), _ptr(n_back), rids.numel(), _stream(stream)),
+               "kvp_dev_rewind")
 
     def sync_error(self, stream=None):
         e = ctypes.c_int()

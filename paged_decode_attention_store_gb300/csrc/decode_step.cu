@@ -225,3 +225,85 @@ extern "C" int kvp_decode_step_device_io(kvp_dev_pages* d, const kvp_pool* pool,
       return KVP_ERR_CUDA;
   return cudaStreamSynchronize(st) == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
 }
+
+// kvp_dev_append for ``count`` rows of every request (device_pages.cu).
+int kvp_dev_append_uniform(kvp_dev_pages* d, const int32_t* rids, int count, int n, int32_t* out_loc, int max_tokens,
+                           int32_t* cow_src, int32_t* cow_dst, int32_t* n_cow, int32_t* lens_out, void* stream);
+
+// kvp_verify_step_device_io: one speculative-decoding verify step with the
+// page bookkeeping on the device and host buffers in and out ("Week 3 Day 3:
+// Paged KV Cache" of tiny-llm: rewind(n) drops the rejected drafts). The M
+// drafts of every request are appended on the device (new pages popped, a
+// shared tail page copied first), stored and verified at once, layer by
+// layer; then each request's rejected drafts are rewound on the device, and
+// with a window the pages it no longer reaches are released. The inputs
+// travel on the page state's copy stream while the append runs; layer l's
+// store and verify wait for layer l's copies only. One native call per step.
+extern "C" int kvp_verify_step_device_io(kvp_dev_pages* d, const kvp_pool* pool, int32_t* table,
+                                         int table_rows_total, int table_cols, int table_mode, const int32_t* rids,
+                                         int n, int num_q_tokens, int window, int sinks, int num_q_heads, float scale,
+                                         const void* const* q_host, const void* const* k_host,
+                                         const void* const* v_host, const int32_t* n_back_host,
+                                         void* const* out_host, void* const* q_dev, void* const* k_dev,
+                                         void* const* v_dev, void* const* out_dev, int32_t* scratch, int may_share,
+                                         void* workspace, size_t workspace_bytes, void* stream) {
+  const int M = num_q_tokens;
+  if (!d || !pool || !table || !rids || n <= 0 || M < 1 || num_q_heads <= 0 || !q_host || !k_host || !v_host ||
+      !n_back_host || !out_host || !q_dev || !k_dev || !v_dev || !out_dev || !scratch)
+    return KVP_ERR_INVALID_ARG;
+  if (sinks < 0 || (window > 0 && sinks >= window)) return KVP_ERR_INVALID_ARG;
+  if (window <= 0) sinks = 0;
+  for (int i = 0; i < n; ++i)
+    if (n_back_host[i] < 0 || n_back_host[i] > M) return KVP_ERR_INVALID_ARG;  // only this step's drafts go back
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int layers = pool->num_layers;
+  void* io = nullptr;
+  void** ev = nullptr;
+  int rc = kvp_dev_io_resources(d, layers + 1, &io, &ev);
+  if (rc != KVP_OK) return rc;
+  const cudaStream_t cs = static_cast<cudaStream_t>(io);
+  int32_t* out_loc = scratch;             // n * M slots, request-major
+  int32_t* lens = scratch + n * M;        // n
+  int32_t* cow_src = lens + n;            // n
+  int32_t* cow_dst = cow_src + n;         // n
+  int32_t* n_cow = cow_dst + n;           // 1
+  int32_t* n_back = n_cow + 1;            // n
+  const size_t qbytes = (size_t)n * M * num_q_heads * pool->head_dim * pool->elem;
+  const size_t kvbytes = (size_t)n * M * pool->row_bytes;
+  if (cudaEventRecord(static_cast<cudaEvent_t>(ev[0]), st) != cudaSuccess ||
+      cudaStreamWaitEvent(cs, static_cast<cudaEvent_t>(ev[0]), 0) != cudaSuccess)
+    return KVP_ERR_CUDA;
+  for (int l = 0; l < layers; ++l) {
+    if (cudaMemcpyAsync(q_dev[l], q_host[l], qbytes, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
+        cudaMemcpyAsync(k_dev[l], k_host[l], kvbytes, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
+        cudaMemcpyAsync(v_dev[l], v_host[l], kvbytes, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
+        (l == 0 && cudaMemcpyAsync(n_back, n_back_host, sizeof(int32_t) * n, cudaMemcpyHostToDevice, cs) !=
+                       cudaSuccess) ||
+        cudaEventRecord(static_cast<cudaEvent_t>(ev[1 + l]), cs) != cudaSuccess)
+      return KVP_ERR_CUDA;
+  }
+  rc = kvp_dev_append_uniform(d, rids, M, n, out_loc, n * M, cow_src, cow_dst, n_cow, lens, stream);
+  if (rc == KVP_OK && may_share) rc = copy_pages_device_count(pool, cow_src, cow_dst, n_cow, n, stream);
+  for (int l = 0; rc == KVP_OK && l < layers; ++l) {
+    if (cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(ev[1 + l]), 0) != cudaSuccess) {
+      rc = KVP_ERR_CUDA;
+      break;
+    }
+    rc = store_cache(pool, l, k_dev[l], v_dev[l], out_loc, n * M, stream);
+    if (rc == KVP_OK)
+      rc = paged_verify_attention(pool, l, q_dev[l], n, M, num_q_heads, table, table_rows_total, table_cols,
+                                  table_mode, rids, lens, window, sinks, scale, out_dev[l], workspace,
+                                  workspace_bytes, stream);
+  }
+  // the rejected drafts go back (n_back was copied with layer 0's inputs), then the window's releases
+  if (rc == KVP_OK) rc = kvp_dev_rewind(d, rids, n_back, n, stream);
+  if (rc == KVP_OK && window > 0) rc = kvp_dev_trim(d, rids, nullptr, n, window, sinks, stream);
+  if (rc != KVP_OK) {
+    cudaStreamSynchronize(cs);  // the host buffers stay in use until the copies are done
+    return rc;
+  }
+  for (int l = 0; l < layers; ++l)
+    if (cudaMemcpyAsync(out_host[l], out_dev[l], qbytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+      return KVP_ERR_CUDA;
+  return cudaStreamSynchronize(st) == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
+}

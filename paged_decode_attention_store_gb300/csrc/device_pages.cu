@@ -126,12 +126,13 @@ __global__ void dev_new_kernel(DevState s, const int32_t* rids, int n) {
   s.len[r] = s.dropped[r] = s.sinkp[r] = 0;
 }
 
-// One token row per request by default; counts[i] rows for request i
-// otherwise (a verify step's drafts). Request-major slots in out_loc.
+// ``uniform`` token rows per request when counts is NULL; counts[i] rows for
+// request i otherwise (a verify step's drafts). Request-major slots in out_loc.
 __global__ void __launch_bounds__(kDevThreads) dev_append_kernel(DevState s, const int32_t* rids,
-                                                                  const int32_t* counts, int n, int32_t* out_loc,
-                                                                  int max_tokens, int32_t* cow_src, int32_t* cow_dst,
-                                                                  int32_t* n_cow, int32_t* lens_out) {
+                                                                  const int32_t* counts, int uniform, int n,
+                                                                  int32_t* out_loc, int max_tokens, int32_t* cow_src,
+                                                                  int32_t* cow_dst, int32_t* n_cow,
+                                                                  int32_t* lens_out) {
   __shared__ int s_tail[kDevThreads];
   __shared__ int s_rid[kDevThreads];
   const int i = threadIdx.x;
@@ -142,7 +143,7 @@ __global__ void __launch_bounds__(kDevThreads) dev_append_kernel(DevState s, con
   griddep_launch_dependents();
   if (i < n) {
     r = rids[i];
-    c = counts ? counts[i] : 1;
+    c = counts ? counts[i] : uniform;
     if ((unsigned)r >= (unsigned)s.max_requests || r >= s.rows || c < 0) {
       ok = false;
     } else {
@@ -220,8 +221,11 @@ __global__ void __launch_bounds__(kDevThreads) dev_append_kernel(DevState s, con
 
 // Trim (mode 0): release the pages after the sink pages that lie wholly
 // below keep_from[i]; release (mode 1): let go of every live page and end
-// the request. Pages go back in call order, each pushed by the release that
-// drops its count to zero (that is the host's order).
+// the request; rewind (mode 2): drop the newest keep_from[i] rows and let go
+// of the pages past the new length, tail first (the host's rewind, so that
+// the stack hands them back in logical order). Pages go back in call order,
+// each pushed by the release that drops its count to zero (that is the
+// host's order).
 __global__ void __launch_bounds__(kDevThreads) dev_release_kernel(DevState s, const int32_t* rids,
                                                                    const int32_t* keep_from, int window, int sinks,
                                                                    int n, int mode) {
@@ -231,7 +235,7 @@ __global__ void __launch_bounds__(kDevThreads) dev_release_kernel(DevState s, co
   const int i = threadIdx.x;
   const int P = s.P;
   bool ok = true;
-  int r = -1, cnt = 0, lo = 0, sp = 0, d = 0, pages = 0;
+  int r = -1, cnt = 0, lo = 0, sp = 0, d = 0, pages = 0, keep_len = 0;
   griddep_wait();
   griddep_launch_dependents();
   if (i < n) {
@@ -250,9 +254,17 @@ __global__ void __launch_bounds__(kDevThreads) dev_release_kernel(DevState s, co
         const int hi = min(kf > 0 ? kf / P : 0, pages);
         lo = sp + d;
         cnt = max(0, hi - lo);
-      } else {
+      } else if (mode == 1) {
         sp = s.sinkp[r];
         cnt = pages - d;  // every live page: the sink pages, then the ones after the holes
+      } else {
+        const int back = keep_from[i];
+        keep_len = L - back;
+        sp = s.sinkp[r];
+        // no rewind into the rows a window or its sinks released
+        if (back < 0 || back > L || (d > 0 && (long long)keep_len < (long long)(sp + d) * P)) ok = false;
+        lo = ceil_div_d(keep_len, P);  // first logical page let go
+        cnt = ok ? pages - lo : 0;
       }
     }
   }
@@ -272,8 +284,9 @@ __global__ void __launch_bounds__(kDevThreads) dev_release_kernel(DevState s, co
     return;
   }
   for (int k = 0; k < cnt; ++k) {
-    // logical page of the k-th release: trim [lo, lo + cnt); release skips the holes [sp, sp + d)
-    const int lp = mode == 0 ? lo + k : (d > 0 && k >= sp ? k + d : k);
+    // logical page of the k-th release: trim [lo, lo + cnt); release skips the
+    // holes [sp, sp + d); rewind goes from the tail down to lo
+    const int lp = mode == 0 ? lo + k : mode == 1 ? (d > 0 && k >= sp ? k + d : k) : pages - 1 - k;
     const int p = page_at(s, r, lp);
     s_page[o + k] = p;
     s_ref0[o + k] = (unsigned)p < (unsigned)s.num_pages ? s.ref[p] : 0;
@@ -313,8 +326,11 @@ __global__ void __launch_bounds__(kDevThreads) dev_release_kernel(DevState s, co
       for (int k = 0; k < cnt; ++k) set_page(s, r, lo + k, -1);
       s.dropped[r] = d + cnt;
       s.sinkp[r] = sp;
-    } else {
+    } else if (mode == 1) {
       s.len[r] = s.dropped[r] = s.sinkp[r] = 0;
+    } else {
+      for (int k = 0; k < cnt; ++k) set_page(s, r, lo + k, -1);
+      s.len[r] = keep_len;
     }
   }
   __syncthreads();
@@ -470,7 +486,29 @@ extern "C" int kvp_dev_append(kvp_dev_pages* d, const int32_t* rids, const int32
   if (n == 0) return KVP_OK;
   if (!rids || !out_loc || !cow_src || !cow_dst) return KVP_ERR_INVALID_ARG;
   const cudaError_t e = launch_one_block(dev_append_kernel, static_cast<cudaStream_t>(stream), state_of(d), rids,
-                                         counts, n, out_loc, max_tokens, cow_src, cow_dst, n_cow, lens_out);
+                                         counts, 1, n, out_loc, max_tokens, cow_src, cow_dst, n_cow, lens_out);
+  return e == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
+}
+
+// kvp_dev_append with the same number of rows (``count``) for every request,
+// without a device array of counts (the verify step's drafts).
+int kvp_dev_append_uniform(kvp_dev_pages* d, const int32_t* rids, int count, int n, int32_t* out_loc, int max_tokens,
+                           int32_t* cow_src, int32_t* cow_dst, int32_t* n_cow, int32_t* lens_out, void* stream) {
+  if (!d || n < 0 || n > kDevThreads || max_tokens < 0 || count < 0) return KVP_ERR_INVALID_ARG;
+  if (n == 0) return KVP_OK;
+  if (!rids || !out_loc || !cow_src || !cow_dst) return KVP_ERR_INVALID_ARG;
+  const cudaError_t e = launch_one_block(dev_append_kernel, static_cast<cudaStream_t>(stream), state_of(d), rids,
+                                         static_cast<const int32_t*>(nullptr), count, n, out_loc, max_tokens, cow_src,
+                                         cow_dst, n_cow, lens_out);
+  return e == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
+}
+
+extern "C" int kvp_dev_rewind(kvp_dev_pages* d, const int32_t* rids, const int32_t* n_back, int n, void* stream) {
+  if (!d || n < 0 || n > kDevThreads) return KVP_ERR_INVALID_ARG;
+  if (n == 0) return KVP_OK;
+  if (!rids || !n_back) return KVP_ERR_INVALID_ARG;
+  const cudaError_t e = launch_one_block(dev_release_kernel, static_cast<cudaStream_t>(stream), state_of(d), rids,
+                                         n_back, 0, 0, n, 2);
   return e == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
 }
 

@@ -406,11 +406,23 @@ class DevicePagedKVCache:
     def release(self, rids):
         self.pages.release(self._i32(rids))
 
-    def workspace(self, batch, num_q_heads):
-        key = (batch, num_q_heads)
+    def rewind(self, rids, n_back):
+        """Drop the newest n_back[i] rows of each request (rejected drafts)."""
+        self.pages.rewind(self._i32(rids), self._i32(n_back))
+
+    def workspace(self, batch, num_q_heads, num_q_tokens=1):
+        key = (batch, num_q_heads, num_q_tokens)
         if key not in self._ws:
-            self._ws[key] = kb.alloc_workspace(self.pool, batch, num_q_heads, device=self.dev)
+            self._ws[key] = (kb.alloc_workspace(self.pool, batch, num_q_heads, device=self.dev) if num_q_tokens == 1
+                             else kb.alloc_verify_workspace(self.pool, batch, num_q_tokens, num_q_heads,
+                                                            device=self.dev))
         return self._ws[key]
+
+    def verify(self, layer, q, context_lens, window, scale, out, table_rows=None, sinks=0):
+        """Multi-token verify attention: q/out [B, M, Hq, D] (the M newest tokens, stored)."""
+        ws = self.workspace(q.shape[0], q.shape[2], q.shape[1])
+        kb.paged_verify_attention(self.pool, layer, q, self.table, self.table_mode, context_lens, window, scale,
+                                  out, ws, table_rows=table_rows, sinks=sinks)
 
     def attend(self, layer, q, context_lens, window, scale, out, table_rows=None, sinks=0):
         ws = self.workspace(q.shape[0], q.shape[1])
@@ -469,6 +481,36 @@ class DevicePagedKVCache:
             self.table_mode, vp(rids.data_ptr()), n, int(window or 0), int(sinks), Hq, float(scale), pa(q), pa(k),
             pa(v), pa(out), pa(qd), pa(kd), pa(vd), pa(od), vp(scratch.data_ptr()), int(self.may_share),
             vp(ws.data_ptr()), ws.numel(), vp(stream.cuda_stream)), "kvp_decode_step_device_io")
+
+    def verify_step_host(self, rids, q, k, v, n_back, out, window, scale, sinks=0):
+        """One speculative-decoding verify step with HOST buffers (pinned),
+        the page bookkeeping on the device: the M drafts of every request are
+        appended, stored and verified at once, then each request's rejected
+        drafts (``n_back``: host int32 [B], 0..M) are rewound. ``q``/``out``
+        per-layer host tensors [B, M, Hq, D], ``k``/``v`` [B * M, Hkv, D]
+        (request-major); ``rids``: device int32 [B]. One native call
+        (kvp_verify_step_device_io); returns when ``out`` holds the results."""
+        n, M, Hq = rids.numel(), q[0].shape[1], q[0].shape[2]
+        key = ("verify", n, M, Hq)
+        stage = self._staging.get(key)
+        if stage is None:
+            mk = lambda t: torch.empty(t.shape, dtype=t.dtype, device=self.dev)  # noqa: E731
+            stage = self._staging[key] = ([mk(t) for t in q], [mk(t) for t in k], [mk(t) for t in v],
+                                          [mk(t) for t in out], torch.zeros(n * M + 4 * n + 1, dtype=torch.int32,
+                                                                            device=self.dev))
+        qd, kd, vd, od, scratch = stage
+        ws = self.workspace(n, Hq, M)
+        nb = np.ascontiguousarray(n_back, dtype=np.int32)
+        if nb.shape != (n,):
+            raise ValueError("n_back must hold one count per request")
+        vp = ctypes.c_void_p
+        pa = self._ptr_array
+        stream = torch.cuda.current_stream(self.dev)
+        kb._check(kb.lib().kvp_verify_step_device_io(
+            self.pages.handle, self.pool.handle, vp(self.table.data_ptr()), self.table.shape[0], self.table.shape[1],
+            self.table_mode, vp(rids.data_ptr()), n, M, int(window or 0), int(sinks), Hq, float(scale), pa(q), pa(k),
+            pa(v), nb.ctypes.data_as(vp), pa(out), pa(qd), pa(kd), pa(vd), pa(od), vp(scratch.data_ptr()),
+            int(self.may_share), vp(ws.data_ptr()), ws.numel(), vp(stream.cuda_stream)), "kvp_verify_step_device_io")
 
     def check(self):
         """Raise if a device-side error was recorded since the last check."""

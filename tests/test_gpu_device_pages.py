@@ -1,7 +1,7 @@
 """Device-side page allocation (kvp_dev_*) against the oracle's page table.
 
 Random batches of new / append (several rows per request) / fork / trim
-(with sink pages) / release run on the device and on the oracle
+(with sink pages) / rewind / release run on the device and on the oracle
 (chapter 15's page table, restated in oracle/pagetable.py) from the same
 free-list order. After every batch the device state read back must equal
 the oracle's bit for bit: the free list, every reference count, lengths,
@@ -67,7 +67,7 @@ def test_device_pages_match_the_oracle(kb, seed):
     cd = torch.empty(max_req, dtype=torch.int32, device=DEV)
     nc = torch.zeros(1, dtype=torch.int32, device=DEV)
     for step in range(160):
-        op = R.choice(["append"] * 5 + ["new", "fork", "trim", "trim", "release"])
+        op = R.choice(["append"] * 5 + ["new", "fork", "trim", "trim", "rewind", "rewind", "release"])
         free = [r for r in range(max_req) if r not in live]
         if op == "new" and free:
             rids = free[:R.randrange(1, min(3, len(free)) + 1)]
@@ -117,6 +117,15 @@ def test_device_pages_match_the_oracle(kb, seed):
                     opt.trim(r, k, sink_rows=S)
                 else:
                     opt.trim(r, k)
+        elif op == "rewind" and live:
+            rids = R.sample(live, R.randrange(1, len(live) + 1))
+            back = []
+            for r in rids:  # no rewind into released rows (the oracle refuses it)
+                floor = (opt.sinks[r] + opt.dropped[r]) * P if opt.dropped[r] else 0
+                back.append(R.randrange(0, min(opt.length[r] - floor, 2 * P + 3) + 1))
+            dev.rewind(_i32(rids), _i32(back))
+            for r, nb in zip(rids, back):
+                opt.rewind(r, nb)
         elif op == "release" and live:
             rids = R.sample(live, R.randrange(1, min(3, len(live)) + 1))
             dev.release(_i32(rids))
@@ -147,3 +156,26 @@ def test_device_append_refuses_bad_calls(kb):
     assert dev.sync_error() == kb.KVP_ERR_OUT_OF_PAGES and dev.snapshot() == before
     dev.append(_i32([0, 1]), out, cs, cd, nc, counts=_i32([16, 16]))  # exactly the pool
     assert dev.sync_error() == 0 and dev.snapshot()[0] == []
+
+
+def test_device_rewind_refuses_released_rows(kb):
+    """A rewind below the rows a window released, or of more rows than a
+    request holds, fails whole and changes nothing."""
+    P, n_pages = 4, 16
+    table = torch.full((2, 16), -1, dtype=torch.int32, device=DEV)
+    dev = kb.DevicePages(n_pages, P, 2, table, kb.KVP_BLOCK_TABLE, device=DEV)
+    dev.new(_i32([0, 1]))
+    out = torch.empty(64, dtype=torch.int32, device=DEV)
+    cs, cd, nc = (torch.zeros(2, dtype=torch.int32, device=DEV) for _ in range(3))
+    dev.append(_i32([0, 1]), out, cs, cd, nc, counts=_i32([14, 6]))
+    dev.trim(_i32([0]), _i32([9]))  # request 0 lets go of pages 0 and 1 (rows 0..7)
+    assert dev.sync_error() == 0
+    before = dev.snapshot()
+    dev.rewind(_i32([1, 0]), _i32([1, 7]))  # request 0 would keep 7 rows, inside its released pages
+    assert dev.sync_error() == kb.KVP_ERR_INVALID_ARG and dev.snapshot() == before
+    dev.rewind(_i32([1]), _i32([7]))  # request 1 holds 6 rows
+    assert dev.sync_error() == kb.KVP_ERR_INVALID_ARG and dev.snapshot() == before
+    dev.rewind(_i32([0, 1]), _i32([6, 6]))  # down to row 8 and to nothing: allowed
+    assert dev.sync_error() == 0
+    _, _, lens, _, _ = dev.snapshot()
+    assert lens[:2] == [8, 0]

@@ -148,3 +148,69 @@ def test_device_bookkeeping_decode_step_matches_the_oracle(kb, window, sinks, ho
         row = orc.table_row(b)
         assert tab[b, :len(row)].tolist() == row
     cache.check()
+
+
+@pytest.mark.parametrize("M,mode", [(4, "block"), (3, "raw")])
+def test_device_verify_step_matches_the_oracle(kb, M, mode):
+    """DevicePagedKVCache.verify_step_host: the M drafts of every request
+    appended, stored and verified with the page bookkeeping on the device,
+    then the rejected drafts rewound, in one native call with host buffers.
+    Outputs of every query against the oracle's verify positions; slots,
+    tables and the device free list bit-exact after every step."""
+    import random
+
+    import oracle.attention as OA
+    from paged_decode_attention_store_gb300.engine import DevicePagedKVCache
+
+    Hq, Hkv, D, P, seed = 32, 8, 128, 16, 79
+    lengths = [300, 17, 64, 5, 1000]
+    B, steps = len(lengths), 8
+    num_pages = sum(-(-(L + steps * M) // P) for L in lengths) + 8
+    order = wl.free_stack_for_order(wl.permutation(seed, num_pages))
+    w = wl.Workload("devverify", "bf16", Hq, Hkv, D, P, 1, num_pages, order, lengths, scale=1.0 / math.sqrt(D))
+    cache = DevicePagedKVCache(num_pages, P, Hkv, D, 1, "bf16", max_requests=B, table_mode=mode,
+                               max_seq_len=1200, free_stack=order, device=DEV)
+    orc = OracleSession(w, B, seed=seed, mode=mode, raw_from_pages=True)
+    cache.new(range(B))
+    for b in range(B):
+        orc.new(b)
+    slots = cache.append(list(range(B)), counts=lengths)
+    rr = [b for b in range(B) for _ in range(lengths[b])]
+    pp = [t for L in lengths for t in range(L)]
+    k, v = wl.kv_rows(seed, 0, rr, pp, Hkv, D, device=DEV)
+    cache.store(0, k, v, slots)
+    assert slots.cpu().tolist() == orc.append(rr, pp)
+    rids = torch.arange(B, dtype=torch.int32, device=DEV)
+    R = random.Random(seed)
+    lens = list(lengths)
+    for step in range(1, steps + 1):
+        rr = [b for b in range(B) for _ in range(M)]
+        pos = [L + j for L in lens for j in range(M)]
+        q = torch.stack([wl.q_rows(seed, step * M + j, 0, list(range(B)), Hq, D) for j in range(M)], dim=1)
+        k, v = wl.kv_rows(seed, 0, rr, pos, Hkv, D)
+        qh, kh, vh = (x.contiguous().pin_memory() for x in (q, k, v))
+        out = torch.empty((B, M, Hq, D), dtype=torch.bfloat16, pin_memory=True)
+        back = [R.randrange(0, M + 1) for _ in range(B)]
+        cache.verify_step_host(rids, [qh], [kh], [vh], back, [out], 0, w.scale)
+        want_slots = orc.append(rr, pos)
+        scratch = cache._staging[("verify", B, M, Hq)][4]
+        assert scratch[:B * M].cpu().tolist() == want_slots, f"step {step}: slots"
+        ctx = [L + M for L in lens]
+        got = out.float().numpy()
+        for b in range(B):
+            for j, ps in enumerate(OA.verify_positions(ctx[b], M, None)):
+                ref = OA.attend_request(orc.stores[0], q[b, j].float().numpy(),
+                                        [s for p in ps for s in orc.slots(b, p, p + 1)], w.scale)
+                close(got[b, j], ref, "bf16", f"step {step} request {b} query {j}")
+        for b in range(B):
+            orc.pt.rewind(b, back[b])
+        lens = [c - nb for c, nb in zip(ctx, back)]
+    torch.cuda.synchronize()
+    free, ref, lens_d, _, _ = cache.pages.snapshot()
+    assert free == orc.pt.free and ref == orc.pt.ref
+    assert lens_d[:B] == lens
+    tab = cache.table.cpu().numpy()
+    for b in range(B):
+        row = orc.table_row(b)
+        assert tab[b, :len(row)].tolist() == row
+    cache.check()
