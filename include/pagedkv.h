@@ -565,9 +565,10 @@ int kvp_decode_step_device(kvp_dev_pages* d, const kvp_pool* pool,
  * stream is synchronised). One call per step.
  * The input copies run on a copy stream of the page state, after the work
  * already queued on ``stream``, while the page append runs on ``stream``;
- * layer l's attention waits for layer l's copies only. The first call
- * creates that stream and num_layers + 1 events; kvp_dev_pages_destroy
- * releases them (no device memory is allocated). */
+ * layer l's attention waits for layer l's copies only, and layer l's output
+ * goes back on a second copy stream as soon as the layer is done. The first
+ * call creates the two streams and 2 * num_layers + 1 events;
+ * kvp_dev_pages_destroy releases them (no device memory is allocated). */
 int kvp_decode_step_device_io(kvp_dev_pages* d, const kvp_pool* pool,
                               int32_t* table, int table_rows_total,
                               int table_cols, int table_mode,
@@ -596,7 +597,8 @@ int kvp_decode_step_device_io(kvp_dev_pages* d, const kvp_pool* pool,
  *      lengths;
  *   4. kvp_dev_rewind of n_back[i] rows per request (the rejected drafts),
  *      then with a window kvp_dev_trim to L + 1 - (window - sinks);
- *   5. out_dev[l] -> out_host[l]; returns once the outputs are on the host.
+ *   5. out_dev[l] -> out_host[l] on a second copy stream as soon as layer l
+ *      is done; returns once the outputs are on the host.
  * scratch: device int32 [n * M + 4 n + 1]; workspace as
  * paged_verify_attention_workspace_size(pool, n, M, Hq). Host buffers
  * should be pinned for the copies to be asynchronous. Errors as the calls

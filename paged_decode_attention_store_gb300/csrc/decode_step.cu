@@ -173,15 +173,18 @@ extern "C" int kvp_decode_step_device(kvp_dev_pages* d, const kvp_pool* pool, in
   return KVP_OK;
 }
 
-// The page state's copy stream and events (device_pages.cu).
-int kvp_dev_io_resources(kvp_dev_pages* d, int nevents, void** stream, void*** events);
+// The page state's two copy streams and its events (device_pages.cu).
+int kvp_dev_io_resources(kvp_dev_pages* d, int nevents, void** stream, void** stream2, void*** events);
 
 // kvp_decode_step_device_io: kvp_decode_step_device with host buffers in and
 // out. Each layer's q, k, v are copied from host memory into the caller's
-// device staging on the state's copy stream, while the page append runs on
-// ``stream``; layer l's attention waits for layer l's copies only. Each
-// layer's output is copied back on ``stream`` and the call returns once the
+// device staging on the state's first copy stream, while the page append
+// runs on ``stream``; layer l's attention waits for layer l's copies only.
+// Each layer's output goes back on the second copy stream as soon as that
+// layer is done, while the next layers run. The call returns once the
 // outputs are on the host. One native call per step.
+// Events: [0] the step's start, [1 + l] layer l's inputs in, [1 + L + l]
+// layer l done.
 extern "C" int kvp_decode_step_device_io(kvp_dev_pages* d, const kvp_pool* pool, int32_t* table,
                                          int table_rows_total, int table_cols, int table_mode, const int32_t* rids,
                                          int n, int window, int sinks, int num_q_heads, float scale,
@@ -196,10 +199,11 @@ extern "C" int kvp_decode_step_device_io(kvp_dev_pages* d, const kvp_pool* pool,
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int layers = pool->num_layers;
   void* io = nullptr;
+  void* io2 = nullptr;
   void** ev = nullptr;
-  int rc = kvp_dev_io_resources(d, layers + 1, &io, &ev);
+  int rc = kvp_dev_io_resources(d, 2 * layers + 1, &io, &io2, &ev);
   if (rc != KVP_OK) return rc;
-  const cudaStream_t cs = static_cast<cudaStream_t>(io);
+  const cudaStream_t cs = static_cast<cudaStream_t>(io), ds = static_cast<cudaStream_t>(io2);
   const size_t qbytes = (size_t)n * num_q_heads * pool->head_dim * pool->elem;
   const size_t kvbytes = (size_t)n * pool->row_bytes;
   // the copies start after the work already on ``stream`` (the staging may still be read there)
@@ -214,16 +218,18 @@ extern "C" int kvp_decode_step_device_io(kvp_dev_pages* d, const kvp_pool* pool,
       return KVP_ERR_CUDA;
   }
   rc = kvp_decode_step_device(d, pool, table, table_rows_total, table_cols, table_mode, rids, n, window, sinks,
-                              num_q_heads, scale, q_dev, k_dev, v_dev, out_dev, ev + 1, nullptr, scratch, may_share,
-                              workspace, workspace_bytes, stream);
+                              num_q_heads, scale, q_dev, k_dev, v_dev, out_dev, ev + 1, ev + 1 + layers, scratch,
+                              may_share, workspace, workspace_bytes, stream);
   if (rc != KVP_OK) {
     cudaStreamSynchronize(cs);  // the host buffers stay in use until the copies are done
     return rc;
   }
   for (int l = 0; l < layers; ++l)
-    if (cudaMemcpyAsync(out_host[l], out_dev[l], qbytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    if (cudaStreamWaitEvent(ds, static_cast<cudaEvent_t>(ev[1 + layers + l]), 0) != cudaSuccess ||
+        cudaMemcpyAsync(out_host[l], out_dev[l], qbytes, cudaMemcpyDeviceToHost, ds) != cudaSuccess)
       return KVP_ERR_CUDA;
-  return cudaStreamSynchronize(st) == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
+  return cudaStreamSynchronize(ds) == cudaSuccess && cudaStreamSynchronize(st) == cudaSuccess ? KVP_OK
+                                                                                               : KVP_ERR_CUDA;
 }
 
 // kvp_dev_append for ``count`` rows of every request (device_pages.cu).
@@ -237,8 +243,10 @@ int kvp_dev_append_uniform(kvp_dev_pages* d, const int32_t* rids, int count, int
 // shared tail page copied first), stored and verified at once, layer by
 // layer; then each request's rejected drafts are rewound on the device, and
 // with a window the pages it no longer reaches are released. The inputs
-// travel on the page state's copy stream while the append runs; layer l's
-// store and verify wait for layer l's copies only. One native call per step.
+// travel on the page state's first copy stream while the append runs; layer
+// l's store and verify wait for layer l's copies only, and its output goes
+// back on the second copy stream as soon as it is done. One native call per
+// step.
 extern "C" int kvp_verify_step_device_io(kvp_dev_pages* d, const kvp_pool* pool, int32_t* table,
                                          int table_rows_total, int table_cols, int table_mode, const int32_t* rids,
                                          int n, int num_q_tokens, int window, int sinks, int num_q_heads, float scale,
@@ -258,10 +266,11 @@ extern "C" int kvp_verify_step_device_io(kvp_dev_pages* d, const kvp_pool* pool,
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int layers = pool->num_layers;
   void* io = nullptr;
+  void* io2 = nullptr;
   void** ev = nullptr;
-  int rc = kvp_dev_io_resources(d, layers + 1, &io, &ev);
+  int rc = kvp_dev_io_resources(d, 2 * layers + 1, &io, &io2, &ev);
   if (rc != KVP_OK) return rc;
-  const cudaStream_t cs = static_cast<cudaStream_t>(io);
+  const cudaStream_t cs = static_cast<cudaStream_t>(io), ds = static_cast<cudaStream_t>(io2);
   int32_t* out_loc = scratch;             // n * M slots, request-major
   int32_t* lens = scratch + n * M;        // n
   int32_t* cow_src = lens + n;            // n
@@ -294,16 +303,21 @@ extern "C" int kvp_verify_step_device_io(kvp_dev_pages* d, const kvp_pool* pool,
       rc = paged_verify_attention(pool, l, q_dev[l], n, M, num_q_heads, table, table_rows_total, table_cols,
                                   table_mode, rids, lens, window, sinks, scale, out_dev[l], workspace,
                                   workspace_bytes, stream);
+    // layer l's output goes back while the next layers run
+    if (rc == KVP_OK &&
+        (cudaEventRecord(static_cast<cudaEvent_t>(ev[1 + layers + l]), st) != cudaSuccess ||
+         cudaStreamWaitEvent(ds, static_cast<cudaEvent_t>(ev[1 + layers + l]), 0) != cudaSuccess ||
+         cudaMemcpyAsync(out_host[l], out_dev[l], qbytes, cudaMemcpyDeviceToHost, ds) != cudaSuccess))
+      rc = KVP_ERR_CUDA;
   }
   // the rejected drafts go back (n_back was copied with layer 0's inputs), then the window's releases
   if (rc == KVP_OK) rc = kvp_dev_rewind(d, rids, n_back, n, stream);
   if (rc == KVP_OK && window > 0) rc = kvp_dev_trim(d, rids, nullptr, n, window, sinks, stream);
   if (rc != KVP_OK) {
     cudaStreamSynchronize(cs);  // the host buffers stay in use until the copies are done
+    cudaStreamSynchronize(ds);
     return rc;
   }
-  for (int l = 0; l < layers; ++l)
-    if (cudaMemcpyAsync(out_host[l], out_dev[l], qbytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
-      return KVP_ERR_CUDA;
-  return cudaStreamSynchronize(st) == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
+  return cudaStreamSynchronize(ds) == cudaSuccess && cudaStreamSynchronize(st) == cudaSuccess ? KVP_OK
+                                                                                               : KVP_ERR_CUDA;
 }

@@ -33,9 +33,10 @@ struct kvp_dev_pages {
   int32_t* sinkp;
   int32_t* table;
   int rows, cols, raw;
-  // host-to-device copy stream and events of kvp_decode_step_device_io,
-  // created on its first call: [0] the step's start, [1 + l] layer l's inputs
+  // copy streams (host to device, device to host) and events of the
+  // host-buffer steps, created on their first call
   void* io_stream;
+  void* io_stream2;
   void** io_events;
   int io_nevents;
 };
@@ -422,6 +423,7 @@ extern "C" int kvp_dev_pages_create(int num_pages, int page_size, int max_reques
   d->cols = table_cols;
   d->raw = table_mode == KVP_RAW_LOCATIONS;
   d->io_stream = nullptr;
+  d->io_stream2 = nullptr;
   d->io_events = nullptr;
   d->io_nevents = 0;
   *out = d;
@@ -434,17 +436,23 @@ extern "C" int kvp_dev_pages_destroy(kvp_dev_pages* d) {
     if (d->io_events[i]) cudaEventDestroy(static_cast<cudaEvent_t>(d->io_events[i]));
   delete[] d->io_events;
   if (d->io_stream) cudaStreamDestroy(static_cast<cudaStream_t>(d->io_stream));
+  if (d->io_stream2) cudaStreamDestroy(static_cast<cudaStream_t>(d->io_stream2));
   delete d;
   return KVP_OK;
 }
 
-// The copy stream and ``nevents`` events of the host-buffer step (created
-// once, kept until kvp_dev_pages_destroy).
-int kvp_dev_io_resources(kvp_dev_pages* d, int nevents, void** stream, void*** events) {
+// The two copy streams and ``nevents`` events of the host-buffer steps
+// (created once, kept until kvp_dev_pages_destroy).
+int kvp_dev_io_resources(kvp_dev_pages* d, int nevents, void** stream, void** stream2, void*** events) {
   if (!d->io_stream) {
     cudaStream_t s;
     if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return KVP_ERR_CUDA;
     d->io_stream = s;
+  }
+  if (!d->io_stream2) {
+    cudaStream_t s;
+    if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return KVP_ERR_CUDA;
+    d->io_stream2 = s;
   }
   if (d->io_nevents < nevents) {
     void** ev = new (std::nothrow) void*[nevents];
@@ -460,6 +468,7 @@ int kvp_dev_io_resources(kvp_dev_pages* d, int nevents, void** stream, void*** e
     }
   }
   *stream = d->io_stream;
+  *stream2 = d->io_stream2;
   *events = d->io_events;
   return KVP_OK;
 }
