@@ -9,46 +9,44 @@
 // attends (causal, the same window and sinks; chapter 15, "The model", and
 // its exercise "Attention sinks"), reading K/V in place through the table.
 //
-// How (one CTA of eleven warps per pair of 128-row query tiles):
+// How (one CTA of 22 warps per 128-row query tile):
 // * A tile is 128 / G consecutive query tokens of one request times the G
 //   query heads of one KV head: 128 rows of Q, loaded once by TMA (128-byte
-//   swizzle, two 64-element halves of head_dim). A CTA takes two adjacent
-//   tiles (A and B) of the same request and KV head, so every K/V block it
-//   loads serves 256 query rows.
-// * The keys the pair needs (the union of its queries' spans) stream in
+//   swizzle, two 64-element halves of head_dim). The tiles of one request
+//   and KV head are adjacent in the grid, so L2 serves their shared K/V.
+// * The keys the tile needs (the union of its queries' spans) stream in
 //   blocks of 128. A 16-slot group whose slots are contiguous and 16-aligned
-//   comes by TMA copies (4 KB of K or V), any other key row is copied by the
-//   loader warp into the same layout. K lies half-major (each half of d is
-//   128 key rows of 128 B, 8-row atoms 1 KB apart: two copies per group), so
-//   that S = Q K^T of a block is eight MMAs of N 128; V lies group-major
-//   (one copy per group), the B operand of O += P V.
-// * The tensor cores take the same time per MMA instruction for any N up to
-//   256 (measured), so the kernel keeps N large: S_X = Q_X K^T (M 128, N 128,
-//   K 128, both operands K-major) accumulates in the tile's 128-column TMEM
-//   S buffer, column c holding key c of the block. Each softmax thread owns
-//   one query row: it reads its 128 scores from TMEM (one wait for all) and
-//   keeps an online softmax in log2 units. A block that no row of the warp
-//   masks (causal, window, sinks, block end) skips the mask;
-//   the row maximum is taken on unscaled scores and P = 2^(s * scale - m) is
-//   one FMA and one ex2 per score. O is rescaled (read, scaled, written back
-//   in TMEM) only when the row maximum grows by more than 8, so P <= 256
-//   always fits bf16 (numerator and denominator use the same m; the row sum
-//   adds the fp32 exponentials, P V their bf16 roundings).
-// * P (bf16, two per 32-bit column, keys in order) is written back into the
-//   first 64 columns of S_X and is the A operand, read from TMEM, of O += P V
-//   (V the MN-major operand in shared memory, one 16-key group per K step).
-//   The epilogue divides by the row sum and stores bf16.
-// * Warp-specialised pipeline: two loader warps fill a three-stage K ring
-//   and a two-stage V ring (a K stage is free once both tiles' S have read
-//   it, a V stage once both P V have), each resolving its own slots; an MMA
-//   warp per tile issues S_X(0), then per block i: P_X(i) V and S_X(i + 1)
-//   (one issuing thread cannot keep the tensor core busy: measured); two
-//   groups of four softmax warps turn each tile's scores into P. S_X(i + 1)
-//   overwrites P_X(i), so it is issued once P_X(i) V is done. mbarriers carry
-//   every hand-off.
-// * The softmax is bound by instruction issue: the scale-and-shift of a pair
-//   of scores is one packed fma.rn.f32x2, their row sum one packed
-//   add.rn.f32x2 (of the fp32 exponentials, before the bf16 rounding of P).
+//   comes by TMA copies (4 KB of K or V), any other key row is copied by a
+//   loader warp into the same layout. With a block table whose page size is
+//   a multiple of 16, a 16-aligned group needs one table read. K lies
+//   half-major (each half of d is 128 key rows of 128 B, 8-row atoms 1 KB
+//   apart: two copies per group), so that S = Q K^T of a block is eight MMAs
+//   of N 128; V lies group-major (one copy per group), the B operand of
+//   O += P V.
+// * A chain of MMAs into one accumulator runs at 60-100 ns per MMA
+//   (measured), well below the tensor cores' rate, so the kernel keeps two
+//   chains in flight: S(i + 1) = Q K(i + 1)^T (M 128, N 128, K 128, both
+//   operands K-major) goes into one of two 128-column TMEM S buffers while
+//   O += P(i) V(i) accumulates in the 128-column O, each from its own
+//   issuing warp, and the softmax works on S(i) meanwhile. P (bf16, two per
+//   32-bit column, keys in order) goes to one of two 64-column TMEM P
+//   buffers and is the A operand, read from TMEM, of O += P V (V the
+//   MN-major operand in shared memory, one 16-key group per K step).
+// * Four softmax threads per query row, each on 32 keys of the block: they
+//   read their scores from TMEM (then the S buffer is free for S(i + 2)),
+//   agree on the row maximum through shared memory, and keep an online
+//   softmax in log2 units. A part that no row of the warp masks (causal,
+//   window, sinks, block end) skips the mask; the maximum is taken on
+//   unscaled scores and P = 2^(s * scale - m) is one packed fma.rn.f32x2 per
+//   pair of scores and one ex2 per score; each part's row sum adds the fp32
+//   exponentials (packed add.rn.f32x2), P V their bf16 roundings. O is
+//   rescaled (read, scaled, written back in TMEM) only when the row maximum
+//   grows by more than 8, so P <= 256 always fits bf16. The epilogue adds
+//   the parts' row sums, divides and stores bf16.
+// * Warp-specialised pipeline: two K loader warps (even and odd blocks) fill
+//   a three-stage K ring and two V loader warps a two-stage V ring, each
+//   resolving its own slots; the S issuer, the P V issuer and the softmax
+//   hand off through mbarriers.
 // * Every wait is bounded (2 s): on timeout the CTA records KVP_ERR_TIMEOUT,
 //   issues nothing more, waits (bounded) for what it issued and frees TMEM.
 #include <cudaTypedefs.h>
@@ -62,9 +60,15 @@ namespace {
 constexpr int kPM = 128;  // query rows per tile
 constexpr int kPN = 128;  // keys per block
 constexpr int kPD = 128;  // head_dim
-constexpr int kPThreads = 384;  // warps: K loader, MMA (tile A), 4 softmax (tile A), 4 softmax (tile B), V loader, MMA (tile B)
-constexpr int kVWarp = 10;
-constexpr int kMmaWarpB = 11;
+// warps: 0 and 1 K loaders (even and odd blocks; 0 also loads Q), 2 and 3 V
+// loaders, 4 S issuer, 5 P V issuer, 6..21 softmax (four warps per TMEM lane
+// quadrant, each on 32 of a block's 128 keys)
+constexpr int kPThreads = 704;
+constexpr int kVWarp = 2;
+constexpr int kSWarp = 4;
+constexpr int kPVWarp = 5;
+constexpr int kSoftWarp0 = 6;
+constexpr int kParts = 4;  // softmax threads per query row
 constexpr int kKS = 3;  // K ring stages
 constexpr int kVS = 2;  // V ring stages
 constexpr uint32_t kHalf = 16384;  // one 64-element half of a 128-row operand: 128 rows x 128 B
@@ -201,6 +205,13 @@ __device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1) {
       : "f"(a0), "f"(a1));
 }
 
+// max(a, b, c) in one instruction (sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // 2^x by the PTX approximate base-2 exponential (flush-to-zero; 2^-inf = +0).
 __device__ __forceinline__ float ex2_ftz(float x) {
   float y;
@@ -212,21 +223,24 @@ __device__ __forceinline__ float ex2_ftz(float x) {
 // Byte offset of 16-byte chunk c (0..7) of row r in a 128-byte-swizzled operand half.
 __device__ __forceinline__ uint32_t sw128(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
 
-// Barriers and flags of one CTA (static shared memory). Per-tile barriers
-// are indexed by the tile (0: A, 1: B) and complete once per key block.
+// Barriers and flags of one CTA (static shared memory). Block i uses S and
+// P buffer i % 2; the barriers of a buffer complete once per block using it.
 struct PrefillBars {
   uint64_t q_full;
-  uint64_t k_full[kKS];   // loader -> MMA: K block in K stage s (TMA bytes and thread copies)
-  uint64_t k_empty[kKS];  // MMA (one commit per tile) -> loader: both tiles' S have read K stage s
-  uint64_t v_full[kVS];   // loader -> MMA: V block in V stage s
-  uint64_t v_empty[kVS];  // MMA (one commit per tile) -> loader: both tiles' P V have read V stage s
-  uint64_t s_full[2];     // MMA -> softmax of tile X: S_X = Q_X K^T of the block in TMEM
-  uint64_t p_full[2];     // softmax of tile X (4 warps) -> MMA: P_X of the block in TMEM
-  uint64_t pv_done[2];    // MMA -> all: O_X += P_X V of the block done (S_X's columns free again)
-  uint64_t drain;         // MMA (one commit per tile) -> all: everything issued is done
+  uint64_t k_full[kKS];   // K loaders -> S issuer: K block in K stage s (TMA bytes and thread copies)
+  uint64_t k_empty[kKS];  // S issuer (commit) -> K loader: S has read K stage s
+  uint64_t v_full[kVS];   // V loaders -> P V issuer: V block in V stage s
+  uint64_t v_empty[kVS];  // P V issuer (commit) -> V loader: P V has read V stage s
+  uint64_t s_full[2];     // S issuer (commit) -> softmax: S = Q K^T of the block in S buffer b
+  uint64_t s_free[2];     // softmax (16 warps) -> S issuer: S buffer b read into registers
+  uint64_t p_full[2];     // softmax (16 warps) -> P V issuer: P of the block in P buffer b
+  uint64_t pv_done[2];    // P V issuer (commit) -> softmax: O += P V of the block done, P buffer b free
+  uint64_t drain;         // both issuers (commit) -> all: everything issued is done
+  uint64_t xbar[4];       // the four softmax warps of a row quadrant: their partials are in xch
   uint32_t taddr;
   int abort;
-  int slots[2][kPN];      // the K and the V loader's slots of the block being loaded
+  int slots[4][kPN];      // each loader's slots of the block it is loading
+  float xch[2][kParts][kPM];  // [block % 2][part][row]: the part's row maximum (the row sum at the end)
 };
 
 // Wait for phase ``k`` of ``bar`` (parity k & 1), bounded.
@@ -272,7 +286,9 @@ __device__ __forceinline__ void load_rows(const PrefillArgs& a, unsigned char* d
       *reinterpret_cast<uint4*>(dst + off) = val;
     }
   }
-  fence_proxy_async_smem();
+  // the thread copies' writes are visible to the tensor cores' (async proxy)
+  // reads; a block copied by TMA alone has none to order
+  if (tm != 0xFFu) fence_proxy_async_smem();
   __syncwarp();
   if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)__popc(tm) * kGroupBytes);
   __syncwarp();
@@ -286,72 +302,72 @@ __device__ __forceinline__ void load_rows(const PrefillArgs& a, unsigned char* d
   __syncwarp();
 }
 
-// Warp roles: 0 loads Q once, then K blocks into a three-stage ring; 10
-// loads V blocks into a two-stage ring; 1 issues tile A's MMAs and 11 tile
-// B's (lane 0 each: one issuing thread cannot keep the tensor core busy);
-// 2..5 run the softmax of tile A and 6..9 that of tile B, one query row per
-// thread (TMEM lane quadrant = warp % 4), and their epilogues.
+// Warp roles: 0 and 1 load K blocks (even, odd) into a three-stage ring, 0
+// loads Q first; 2 and 3 load V blocks into a two-stage ring; 4 issues the
+// S MMAs and 5 the P V MMAs (lane 0 each); 6..21 run the softmax and the
+// epilogue, four threads per query row (TMEM lane quadrant = warp % 4, part
+// = (warp - 6) / 4: keys 32 part .. 32 part + 31 of each block).
 __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_constant__ PrefillArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ PrefillBars sb;
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  unsigned char* sQ = smem;                   // tile X's Q at X * 2 kHalf: [2 halves][128 rows][128 B]
-  unsigned char* sK = smem + 4 * kHalf;       // K stage s at s * 2 kHalf
-  unsigned char* sV = sK + kKS * 2 * kHalf;   // V stage s at s * 2 kHalf
+  unsigned char* sQ = smem;                  // Q: [2 halves][128 rows][128 B]
+  unsigned char* sK = smem + 2 * kHalf;      // K stage s at s * 2 kHalf
+  unsigned char* sV = sK + kKS * 2 * kHalf;  // V stage s at s * 2 kHalf
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   volatile int* abort_flag = &sb.abort;
 
-  // CTA order: request and KV head major, the pair with the most keys first,
-  // so that the pairs reading the same K/V run side by side (L2 serves all
+  // CTA order: request and KV head major, the tile with the most keys first,
+  // so that the tiles reading the same K/V run side by side (L2 serves all
   // but the first of them).
-  const int pairs = (a.tiles + 1) >> 1;
-  const int pair = pairs - 1 - (int)(blockIdx.x % pairs);
-  const int bg = (int)(blockIdx.x / pairs);
+  const int tile = a.tiles - 1 - (int)(blockIdx.x % a.tiles);
+  const int bg = (int)(blockIdx.x / a.tiles);
   const int b = bg / a.Hkv, g = bg % a.Hkv;
   const int TT = kPM / a.G;  // query tokens per tile
-  const int j0 = 2 * pair * TT;  // first token of tile A; tile B starts at j0 + TT
+  const int j0 = tile * TT;  // first query token of the tile
   const int L = a.context_lens[b];
   const int ql = a.q_lens ? a.q_lens[b] : a.C;
   const int row = a.table_rows ? a.table_rows[b] : b;
   const bool valid = ql >= 1 && ql <= a.C && ql <= L && L <= table_capacity(a.T) && row >= 0 && row < a.T.rows_total;
-  // softmax threads: tile X = (warp - 2) / 4, query row r = 32 * (warp % 4) + lane: token j0 + X TT + r / G,
-  // head r % G of the group (the MMA warps: tile X = warp == kMmaWarpB)
-  const int X = warp >= 6 ? (warp == kVWarp ? 0 : 1) : 0;
+  // softmax threads: query row r = 32 * (warp % 4) + lane (token j0 + r / G,
+  // head r % G of the group), keys 32 part .. 32 part + 31 of each block
+  const bool soft = warp >= kSoftWarp0;
+  const int part = soft ? (warp - kSoftWarp0) >> 2 : 0;
   const int r = 32 * (warp & 3) + lane;
-  const int rt = X * TT + r / a.G, hh = r % a.G;  // token offset from j0, head in the group
-  __nv_bfloat16* orow = a.out + (((size_t)b * a.C + j0 + rt) * a.Hq + (size_t)g * a.G + hh) * kPD;
+  const int rt = r / a.G, hh = r % a.G;
+  __nv_bfloat16* orow = a.out + (((size_t)b * a.C + j0 + rt) * a.Hq + (size_t)g * a.G + hh) * kPD + 32 * part;
   if (!valid) {
-    if (tid == 0 && g == 0 && pair == 0) set_error(a.err, KVP_ERR_BAD_INDEX);
-    if (warp >= 2 && warp < kVWarp && j0 + rt < a.C)
-      for (int d = 0; d < kPD; d += 8) *reinterpret_cast<uint4*>(orow + d) = make_uint4(0u, 0u, 0u, 0u);
+    if (tid == 0 && g == 0 && tile == 0) set_error(a.err, KVP_ERR_BAD_INDEX);
+    if (soft && j0 + rt < a.C)
+      for (int d = 0; d < 32; d += 8) *reinterpret_cast<uint4*>(orow + d) = make_uint4(0u, 0u, 0u, 0u);
     return;
   }
-  if (j0 >= ql) return;  // no query of this request falls in the pair
-  const int jn = min(2 * TT, ql - j0);  // query tokens of the pair
-  const bool has_b = jn > TT;
+  if (j0 >= ql) return;  // no query of this request falls in the tile
+  const int jn = min(TT, ql - j0);  // query tokens of the tile
   const int p_first = L - ql + j0, p_last = p_first + jn - 1;
-  // the union of the pair's spans: the first query reaches furthest back
+  // the union of the tile's spans: the first query reaches furthest back
   const Span u = attend_span(p_last + 1, a.window > 0 ? a.window + (p_last - p_first) : 0, a.sinks);
   const int n_keys = u.se + (p_last + 1 - u.lo);
   const int nblk = (n_keys + kPN - 1) / kPN;
 
   if (tid == 0) {
     mbar_init(&sb.q_full, 1);
-    const uint32_t ntile = has_b ? 2 : 1;
     for (int s2 = 0; s2 < kKS; ++s2) {
       mbar_init(&sb.k_full[s2], 1);
-      mbar_init(&sb.k_empty[s2], ntile);
+      mbar_init(&sb.k_empty[s2], 1);
     }
     for (int s2 = 0; s2 < kVS; ++s2) {
       mbar_init(&sb.v_full[s2], 1);
-      mbar_init(&sb.v_empty[s2], ntile);
+      mbar_init(&sb.v_empty[s2], 1);
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(&sb.s_full[x], 1);
-      mbar_init(&sb.p_full[x], 4);
+      mbar_init(&sb.s_free[x], 4 * kParts);
+      mbar_init(&sb.p_full[x], 4 * kParts);
       mbar_init(&sb.pv_done[x], 1);
     }
-    mbar_init(&sb.drain, ntile);
+    for (int qd = 0; qd < 4; ++qd) mbar_init(&sb.xbar[qd], kParts);
+    mbar_init(&sb.drain, 2);
     sb.abort = 0;
     fence_mbar_init();
   }
@@ -363,50 +379,69 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_c
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // TMEM: S_A at columns 0, S_B at 128, O_A at 256, O_B at 384; P_X in the
-  // first 64 columns of S_X
+  // TMEM: S buffers at columns 0 and 128, O at 256, P buffers (bf16, two
+  // keys per column) at 384 and 448
   const uint32_t tbase = sb.taddr;
+  const uint32_t tO = tbase + 256u;
 
-  if (warp == 0 || warp == kVWarp) {
+  if (warp < kSWarp) {
     // ======================= loaders ==========================================
-    // Warp 0 loads Q, then K(i) once both S of block i - kKS have read its
-    // stage; warp kVWarp loads V(i) once both P V of block i - kVS have. Each
-    // resolves its own slots, so neither waits on the other's ring.
-    const bool is_v = warp == kVWarp;
+    // Warps 0 and 1 load K(i) (i even, odd) once S(i - kKS) has read its
+    // stage, warp 0 Q first; warps 2 and 3 load V(i) once P V(i - kVS) has.
+    // Each resolves its own slots; one loader's table reads overlap the
+    // other's copies.
+    const bool is_v = warp >= kVWarp;
     const int NS = is_v ? kVS : kKS;
-    if (!is_v && lane == 0) {
-      mbar_arrive_expect_tx(&sb.q_full, (has_b ? 4u : 2u) * kHalf);
+    const int par = warp & 1;
+    if (warp == 0 && lane == 0) {
+      mbar_arrive_expect_tx(&sb.q_full, 2u * kHalf);
       tma_load_4d(sQ, &a.qmap, 0, g * a.G, j0, b, &sb.q_full);
       tma_load_4d(sQ + kHalf, &a.qmap, 64, g * a.G, j0, b, &sb.q_full);
-      if (has_b) {
-        tma_load_4d(sQ + 2 * kHalf, &a.qmap, 0, g * a.G, j0 + TT, b, &sb.q_full);
-        tma_load_4d(sQ + 3 * kHalf, &a.qmap, 64, g * a.G, j0 + TT, b, &sb.q_full);
-      }
     }
-    int* slots = sb.slots[is_v ? 1 : 0];
-    for (int i = 0; i < nblk; ++i) {
+    int* slots = sb.slots[warp];
+    // A block table whose page size is a multiple of 16 keeps every
+    // 16-aligned run of 16 positions in one page: such a group needs one
+    // table read (lane gi reads group gi's) and goes by TMA.
+    const bool group_reads = a.use_kvmap && !a.T.raw && (a.T.page_size & 15) == 0;
+    for (int i = par; i < nblk; i += 2) {
       const int st = i % NS;
       const int o0 = i * kPN;
-      // lane l resolves keys 4l .. 4l+3 (four independent table reads); group
-      // gi (lanes 4gi .. 4gi+3) goes by one TMA copy when its 16 slots are
-      // contiguous and 16-aligned
-      int sl[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int o = o0 + 4 * lane + k;
-        sl[k] = o < n_keys ? resolve_slot(a.T, row, span_pos(u, o), a.err) : -1;
-      }
-      __syncwarp();  // the previous block's copies have read the slot list
-#pragma unroll
-      for (int k = 0; k < 4; ++k) slots[4 * lane + k] = sl[k];
-      const int g0 = __shfl_sync(0xffffffffu, sl[0], lane & ~3);
-      const bool mine = a.use_kvmap && sl[0] >= 0 && sl[1] == sl[0] + 1 && sl[2] == sl[0] + 2 &&
-                        sl[3] == sl[0] + 3 && sl[0] == g0 + 4 * (lane & 3) && (g0 & 15) == 0;
-      const unsigned okb = __ballot_sync(0xffffffffu, mine);
       unsigned tm = 0;
+      bool whole = false;  // every group of the block resolved by its one read
+      if (group_reads) {
+        const int og = o0 + 16 * lane;
+        int s0 = -1;
+        if (lane < 8 && og + 15 < n_keys && (og + 15 < u.se || og >= u.se)) {
+          const int p = span_pos(u, og);
+          if ((p & 15) == 0) s0 = resolve_slot(a.T, row, p, a.err);
+        }
+        const unsigned okb = __ballot_sync(0xffffffffu, s0 >= 0);
+        whole = (okb & 0xFFu) == 0xFFu;
+        __syncwarp();  // this warp's previous copies have read the slot list
+        if (whole && lane < 8) slots[16 * lane] = s0;
+        tm = whole ? 0xFFu : 0u;
+      }
+      if (!whole) {
+        // lane l resolves keys 4l .. 4l+3 (four independent table reads);
+        // group gi (lanes 4gi .. 4gi+3) goes by TMA when its 16 slots are
+        // contiguous and 16-aligned
+        int sl[4];
 #pragma unroll
-      for (int gi = 0; gi < 8; ++gi)
-        if (((okb >> (4 * gi)) & 0xFu) == 0xFu) tm |= 1u << gi;
+        for (int k = 0; k < 4; ++k) {
+          const int o = o0 + 4 * lane + k;
+          sl[k] = o < n_keys ? resolve_slot(a.T, row, span_pos(u, o), a.err) : -1;
+        }
+        __syncwarp();  // this warp's previous copies have read the slot list
+#pragma unroll
+        for (int k = 0; k < 4; ++k) slots[4 * lane + k] = sl[k];
+        const int g0 = __shfl_sync(0xffffffffu, sl[0], lane & ~3);
+        const bool mine = a.use_kvmap && sl[0] >= 0 && sl[1] == sl[0] + 1 && sl[2] == sl[0] + 2 &&
+                          sl[3] == sl[0] + 3 && sl[0] == g0 + 4 * (lane & 3) && (g0 & 15) == 0;
+        const unsigned okb = __ballot_sync(0xffffffffu, mine);
+#pragma unroll
+        for (int gi = 0; gi < 8; ++gi)
+          if (((okb >> (4 * gi)) & 0xFu) == 0xFu) tm |= 1u << gi;
+      }
       __syncwarp();
       if (i >= NS && !__all_sync(0xffffffffu, pwait(is_v ? &sb.v_empty[st] : &sb.k_empty[st], (i - NS) / NS,
                                                     abort_flag, a.err)))
@@ -414,178 +449,196 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_c
       load_rows(a, (is_v ? sV : sK) + st * 2 * kHalf, slots, tm, g, is_v, is_v ? &sb.v_full[st] : &sb.k_full[st],
                 lane);
     }
-  } else if (warp == 1 || warp == kMmaWarpB) {
-    // ======================= MMA issuers (one per tile) ========================
-    // S_X(i) = Q_X K(i)^T is eight N 128 MMAs (one per 16-wide K step of d),
-    // so S column c is key c of the block. S_X(i + 1) overwrites P_X(i), so
-    // it waits for P_X(i) V. Per block i: P_X(i) V, then S_X(i + 1); the two
-    // tiles' issuers run side by side, so while one tile's softmax runs the
-    // tensor core works on the other tile. The whole warp walks the schedule
-    // and waits (no divergent spin beside the issuing lane); lane 0 alone
-    // issues the MMAs and the commits. A K (V) stage is free once both
-    // tiles' issuers have committed their S (P V) of it.
-    if (X == 0 || has_b) {
-      const bool issuer = lane == 0;
-      const uint32_t id_n128 = umma_idesc(0, kPN), id_o = umma_idesc(1, kPN);
-      const uint32_t tS = tbase + (uint32_t)X * 128u, tO = tbase + 256u + (uint32_t)X * 128u;
-      // descriptors of the operands' starts; a K step adds its byte offset >> 4
-      const uint64_t dq = umma_desc(smem_u32(sQ + X * 2 * kHalf), 16, 1024);
-      const uint64_t dk0 = umma_desc(smem_u32(sK), 16, 1024);
-      const uint64_t dv0 = umma_desc(smem_u32(sV), kGroupBytes / 2, 1024);
-      auto issue_s = [&](int blk) {
-        const uint64_t dk = dk0 + (uint64_t)(((blk % kKS) * 2 * kHalf) >> 4);
-        if (issuer) {
+  } else if (warp == kSWarp) {
+    // ======================= S issuer ==========================================
+    // S(i) = Q K(i)^T into S buffer i % 2: eight N 128 MMAs (one per 16-wide
+    // K step of d), column c holding key c of the block. It needs K(i) and the
+    // softmax's read of S(i - 2), so it runs while the softmax works on
+    // S(i - 1). The whole warp walks the schedule; lane 0 issues.
+    const bool issuer = lane == 0;
+    const uint32_t id_n128 = umma_idesc(0, kPN);
+    const uint64_t dq = umma_desc(smem_u32(sQ), 16, 1024);
+    const uint64_t dk0 = umma_desc(smem_u32(sK), 16, 1024);
+    bool ok = __all_sync(0xffffffffu, pwait(&sb.q_full, 0, abort_flag, a.err));
+    for (int i = 0; ok && i < nblk; ++i) {
+      const int ks = i % kKS, sbuf = i & 1;
+      ok = __all_sync(0xffffffffu, pwait(&sb.k_full[ks], i / kKS, abort_flag, a.err));
+      if (ok && i >= 2) ok = __all_sync(0xffffffffu, pwait(&sb.s_free[sbuf], (i - 2) >> 1, abort_flag, a.err));
+      if (!ok) break;
+      tc_fence_after();
+      const uint64_t dk = dk0 + (uint64_t)((ks * 2 * kHalf) >> 4);
+      if (issuer) {
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint64_t off = (uint64_t)((((ks >> 2) * kHalf) + (ks & 3) * 32) >> 4);
-            umma_f16(tS, dq + off, dk + off, id_n128, ks > 0);
-          }
-          umma_commit(&sb.s_full[X]);
-          umma_commit(&sb.k_empty[blk % kKS]);
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t off = (uint64_t)((((kk >> 2) * kHalf) + (kk & 3) * 32) >> 4);
+          umma_f16(tbase + 128u * (uint32_t)sbuf, dq + off, dk + off, id_n128, kk > 0);
         }
-        __syncwarp();
-      };
-      bool ok = __all_sync(0xffffffffu, pwait(&sb.q_full, 0, abort_flag, a.err));
-      if (ok) ok = __all_sync(0xffffffffu, pwait(&sb.k_full[0], 0, abort_flag, a.err));
-      if (ok) {
-        tc_fence_after();
-        issue_s(0);
+        umma_commit(&sb.s_full[sbuf]);
+        umma_commit(&sb.k_empty[ks]);
       }
-      for (int i = 0; ok && i < nblk; ++i) {
-        const int sv = i % kVS;
-        ok = __all_sync(0xffffffffu, pwait(&sb.v_full[sv], i / kVS, abort_flag, a.err));
-        if (ok) ok = __all_sync(0xffffffffu, pwait(&sb.p_full[X], i, abort_flag, a.err));
-        if (!ok) break;
-        tc_fence_after();
-        // O_X += P_X(i) V(i): P_X from TMEM (8 columns per 16 keys), V group m
-        // the MN-major B operand of K step m (halves of d 2 KB apart, 8-key atoms 1 KB)
-        const uint64_t dv = dv0 + (uint64_t)((sv * 2 * kHalf) >> 4);
-        if (issuer) {
-#pragma unroll
-          for (int m = 0; m < 8; ++m)
-            umma_f16_ts(tO, tS + (uint32_t)m * 8u, dv + (uint64_t)((m * kGroupBytes) >> 4), id_o,
-                        (i > 0 || m > 0) ? 1u : 0u);
-          umma_commit(&sb.pv_done[X]);
-          umma_commit(&sb.v_empty[sv]);
-        }
-        __syncwarp();
-        if (i + 1 < nblk) {
-          ok = __all_sync(0xffffffffu, pwait(&sb.k_full[(i + 1) % kKS], (i + 1) / kKS, abort_flag, a.err));
-          if (ok) ok = __all_sync(0xffffffffu, pwait(&sb.pv_done[X], i, abort_flag, a.err));
-          if (!ok) break;
-          tc_fence_after();
-          issue_s(i + 1);
-        }
-      }
-      if (issuer) umma_commit(&sb.drain);  // arrives once everything this warp issued is done
       __syncwarp();
     }
-  } else if (warp < kVWarp && (X == 0 || has_b)) {
-    // ======================= softmax warps (tile X) ============================
+    if (issuer) umma_commit(&sb.drain);  // arrives once everything this warp issued is done
+    __syncwarp();
+  } else if (warp == kPVWarp) {
+    // ======================= P V issuer ========================================
+    // O += P(i) V(i): P from TMEM (8 columns per 16 keys), V group m the
+    // MN-major B operand of K step m (halves of d 2 KB apart, 8-key atoms 1 KB).
+    const bool issuer = lane == 0;
+    const uint32_t id_o = umma_idesc(1, kPN);
+    const uint64_t dv0 = umma_desc(smem_u32(sV), kGroupBytes / 2, 1024);
+    bool ok = true;
+    for (int i = 0; ok && i < nblk; ++i) {
+      const int vs = i % kVS, pbuf = i & 1;
+      ok = __all_sync(0xffffffffu, pwait(&sb.v_full[vs], i / kVS, abort_flag, a.err));
+      if (ok) ok = __all_sync(0xffffffffu, pwait(&sb.p_full[pbuf], i >> 1, abort_flag, a.err));
+      if (!ok) break;
+      tc_fence_after();
+      const uint64_t dv = dv0 + (uint64_t)((vs * 2 * kHalf) >> 4);
+      const uint32_t tP = tbase + 384u + 64u * (uint32_t)pbuf;
+      if (issuer) {
+#pragma unroll
+        for (int m = 0; m < 8; ++m)
+          umma_f16_ts(tO, tP + (uint32_t)m * 8u, dv + (uint64_t)((m * kGroupBytes) >> 4), id_o,
+                      (i > 0 || m > 0) ? 1u : 0u);
+        umma_commit(&sb.pv_done[pbuf]);
+        umma_commit(&sb.v_empty[vs]);
+      }
+      __syncwarp();
+    }
+    if (issuer) umma_commit(&sb.drain);
+    __syncwarp();
+  } else {
+    // ======================= softmax warps =====================================
+    // Four threads per query row, each on 32 of a block's keys. They read
+    // their scores (then free the S buffer for S(i + 2)), agree on the row
+    // maximum through xch (an mbarrier per quadrant, bounded wait), write P
+    // of their keys into P buffer i % 2 once P V(i - 2) has read it, and keep
+    // their part of the row sum, added at the end. O is rescaled (each
+    // thread its 32 columns) only when the row maximum grows by more than 8.
     const bool rv = rt < jn;
     const int pr = p_first + rt;
     const Span sr0 = attend_span(pr + 1, a.window, a.sinks);
-    // In key offsets of the pair's span u: the row's sink rows are offsets
+    // In key offsets of the tile's span u: the row's sink rows are offsets
     // [0, sr.se) (when u keeps a sink segment its width is the row's; when it
     // does not, u starts at position 0 and offsets are positions), and its
     // window [sr.lo, pr] starts at or after u.lo. Rows past the chunk keep nothing.
     const Span sr = rv ? sr0 : Span{0, 0};
     const int wb0 = rv ? u.se + (sr.lo - u.lo) : 1 << 30, we0 = rv ? u.se + (pr - u.lo) : -1;
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-    const uint32_t tS = tbase + (uint32_t)X * 128u + lane_base, tO = tbase + 256u + (uint32_t)X * 128u + lane_base;
+    const uint32_t tOp = tO + lane_base + 32u * (uint32_t)part;
+    uint64_t* xbar = &sb.xbar[warp & 3];
+    // hand this thread's partial to the row's other parts (phase k) and
+    // combine the four with ``op``
+    auto exchange = [&](float v, int k, bool use_max, float& res) -> bool {
+      volatile float* xc = &sb.xch[k & 1][0][0];
+      xc[part * kPM + r] = v;
+      __threadfence_block();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(xbar);
+      if (!__all_sync(0xffffffffu, pwait(xbar, k, abort_flag, a.err))) return false;
+      const float v0 = xc[r], v1 = xc[kPM + r], v2 = xc[2 * kPM + r], v3 = xc[3 * kPM + r];
+      res = use_max ? fmaxf(fmaxf(v0, v1), fmaxf(v2, v3)) : (v0 + v1) + (v2 + v3);
+      return true;
+    };
     const float sl2 = a.scale_log2;
-    float m_used = -INFINITY, lsum = 0.f;  // m in scaled log2 units
+    float m_used = -INFINITY, lsum = 0.f;  // m in scaled log2 units; lsum over this part's keys
     bool ok = true;
     for (int i = 0; i < nblk; ++i) {
-      ok = __all_sync(0xffffffffu, pwait(&sb.s_full[X], i, abort_flag, a.err));
+      const int sbuf = i & 1;
+      ok = __all_sync(0xffffffffu, pwait(&sb.s_full[sbuf], i >> 1, abort_flag, a.err));
       if (!ok) break;
       tc_fence_after();
-      // The row attends key offsets [0, ea) (its sink rows) and [wb, we] (its
-      // window), relative to this block's first offset; S column c is key c.
-      const int o0 = i * kPN;
-      const int ea = sr.se - o0, wb = wb0 - o0, we = we0 - o0;
-      const bool unmasked = __all_sync(0xffffffffu, wb <= 0 && we >= kPN - 1);  // no row of the warp masks
-      // The row's 128 scores, read from TMEM once (one wait for four loads).
-      float sv[128];
-#pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) tmem_ld16_nowait(tS + 16 * c8, sv + 16 * c8);
+      // the part's 32 scores, read from TMEM once; then S buffer sbuf is free
+      float sv[32];
+      const uint32_t tS = tbase + 128u * (uint32_t)sbuf + lane_base + 32u * (uint32_t)part;
+      tmem_ld16_nowait(tS, sv);
+      tmem_ld16_nowait(tS + 16, sv + 16);
       tmem_wait_ld();
-      if (!unmasked) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sb.s_free[sbuf]);
+      // The row attends key offsets [0, ea) (its sink rows) and [wb, we] (its
+      // window), relative to this part's first key; column c of the part is key c.
+      const int o0 = i * kPN + 32 * part;
+      const int ea = sr.se - o0, wb = wb0 - o0, we = we0 - o0;
+      if (!__all_sync(0xffffffffu, wb <= 0 && we >= 31)) {  // some row of the warp masks
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
+        for (int c = 0; c < 32; ++c)
           if (!(c < ea || (c >= wb && c <= we))) sv[c] = -INFINITY;
       }
-      // the row maximum, taken on unscaled scores (scale > 0) and scaled once
-      float rmax = -INFINITY;
+      // the part's maximum on unscaled scores (scale > 0)
+      float mx[4];
 #pragma unroll
-      for (int c = 0; c < 128; ++c) rmax = fmaxf(rmax, sv[c]);
-      rmax *= sl2;
+      for (int t = 0; t < 4; ++t)
+        mx[t] = fmax3(fmax3(sv[8 * t], sv[8 * t + 1], sv[8 * t + 2]), fmax3(sv[8 * t + 3], sv[8 * t + 4], sv[8 * t + 5]),
+                      fmaxf(sv[8 * t + 6], sv[8 * t + 7]));
+      float rmax;
+      if (!(ok = exchange(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2, i, true, rmax))) break;
       const bool grow = rmax > m_used + 8.f;  // also when nothing was kept before
-      const bool scale_o = grow && lsum > 0.f;
+      const bool scale_o = grow && m_used > -INFINITY;  // O and lsum hold kept keys
       const float f = scale_o ? exp2f(m_used - rmax) : 1.f;
       if (grow) m_used = rmax;
       const float msub = m_used == -INFINITY ? 0.f : m_used;  // masked scores give 2^-inf = 0 either way
-      // P_X(i), keys in order, two per 32-bit column, over the first 64
-      // columns of S_X (S_X(i + 1) is issued only after P_X(i) V(i) is done)
-      float ps0 = 0.f, ps1 = 0.f;  // the row sum, two lanes of a packed add
+      // P of the part's keys, in order, two per 32-bit column, into P buffer
+      // sbuf (columns 16 part .. 16 part + 15) once P V(i - 2) has read it
+      uint32_t w[16];
+      float ps0 = 0.f, ps1 = 0.f;  // the part's row sum, two lanes of a packed add
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t w[16];
-#pragma unroll
-        for (int x = 0; x < 16; ++x) {
-          float x0, x1;
-          fma2_bc(x0, x1, sv[32 * q + 2 * x], sv[32 * q + 2 * x + 1], sl2, -msub);
-          const float p0 = ex2_ftz(x0), p1 = ex2_ftz(x1);
-          w[x] = pack_bf16(p0, p1);
-          add2(ps0, ps1, p0, p1);
-        }
-        tmem_st16(tS + 16 * q, w);
+      for (int x = 0; x < 16; ++x) {
+        float x0, x1;
+        fma2_bc(x0, x1, sv[2 * x], sv[2 * x + 1], sl2, -msub);
+        const float p0 = ex2_ftz(x0), p1 = ex2_ftz(x1);
+        w[x] = pack_bf16(p0, p1);
+        add2(ps0, ps1, p0, p1);
       }
-      lsum = lsum * f + (ps0 + ps1);
-      if (__any_sync(0xffffffffu, scale_o)) {
-        // O_X holds blocks < i in the old maximum: rescale it once P V(i - 1) is
-        // in, before P V(i) may start (a warp-wide TMEM read and write)
-        ok = __all_sync(0xffffffffu, pwait(&sb.pv_done[X], i - 1, abort_flag, a.err));
+      if (i >= 2) {
+        ok = __all_sync(0xffffffffu, pwait(&sb.pv_done[sbuf], (i - 2) >> 1, abort_flag, a.err));
         if (!ok) break;
         tc_fence_after();
+      }
+      tmem_st16(tbase + 384u + 64u * (uint32_t)sbuf + lane_base + 16u * (uint32_t)part, w);
+      lsum = lsum * f + (ps0 + ps1);
+      if (__any_sync(0xffffffffu, scale_o)) {
+        // O holds blocks < i in the old maximum: rescale this part's columns
+        // once P V(i - 1) is in (P V(i) waits for this block's P)
+        ok = __all_sync(0xffffffffu, pwait(&sb.pv_done[(i - 1) & 1], (i - 1) >> 1, abort_flag, a.err));
+        if (!ok) break;
+        tc_fence_after();
+        float ov[32];
+        tmem_ld32(tOp, ov);
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          float ov[32];
-          tmem_ld32(tO + c4 * 32, ov);
-#pragma unroll
-          for (int x = 0; x < 32; ++x) ov[x] *= f;
-          tmem_st32(tO + c4 * 32, ov);
-        }
+        for (int x = 0; x < 32; ++x) ov[x] *= f;
+        tmem_st32(tOp, ov);
       }
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sb.p_full[X]);
+      if (lane == 0) mbar_arrive(&sb.p_full[sbuf]);
     }
-    // ---- epilogue: O / l -> bf16, once the last P V is in O ------------------
-    if (ok) ok = __all_sync(0xffffffffu, pwait(&sb.pv_done[X], nblk - 1, abort_flag, a.err));
+    // ---- epilogue: O / l -> bf16 (this part's 32 columns), once the last P V is in O
+    float tot = 0.f;
+    if (ok) ok = __all_sync(0xffffffffu, pwait(&sb.pv_done[(nblk - 1) & 1], (nblk - 1) >> 1, abort_flag, a.err));
+    if (ok) ok = exchange(lsum, nblk, false, tot);
     if (ok) {
       tc_fence_after();
-      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+      const float inv = tot > 0.f ? 1.f / tot : 0.f;
+      float ov[32];
+      tmem_ld32(tOp, ov);
+      if (rv) {
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        float ov[32];
-        tmem_ld32(tO + c4 * 32, ov);
-        if (rv) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint4 w;
-            w.x = pack_bf16(ov[8 * q + 0] * inv, ov[8 * q + 1] * inv);
-            w.y = pack_bf16(ov[8 * q + 2] * inv, ov[8 * q + 3] * inv);
-            w.z = pack_bf16(ov[8 * q + 4] * inv, ov[8 * q + 5] * inv);
-            w.w = pack_bf16(ov[8 * q + 6] * inv, ov[8 * q + 7] * inv);
-            *reinterpret_cast<uint4*>(orow + c4 * 32 + q * 8) = w;
-          }
+        for (int q = 0; q < 4; ++q) {
+          uint4 w;
+          w.x = pack_bf16(ov[8 * q + 0] * inv, ov[8 * q + 1] * inv);
+          w.y = pack_bf16(ov[8 * q + 2] * inv, ov[8 * q + 3] * inv);
+          w.z = pack_bf16(ov[8 * q + 4] * inv, ov[8 * q + 5] * inv);
+          w.w = pack_bf16(ov[8 * q + 6] * inv, ov[8 * q + 7] * inv);
+          *reinterpret_cast<uint4*>(orow + q * 8) = w;
         }
       }
     }
   }
-  // Everything the MMA lane issued is done (bounded) before TMEM goes back.
+  // Everything the issuers issued is done (bounded) before TMEM goes back.
   {
     const uint64_t t0 = global_timer_ns();
     while (!mbar_try_wait(&sb.drain, 0u))
@@ -644,7 +697,7 @@ bool encode_qmap(const void* q, int B, int C, int Hq, int G, CUtensorMap* out) {
 
 }  // namespace
 
-constexpr size_t kPrefillSmem = (4 + 2 * kKS + 2 * kVS) * kHalf + 1024;  // two Q tiles, the K and V rings
+constexpr size_t kPrefillSmem = (2 + 2 * kKS + 2 * kVS) * kHalf + 1024;  // Q, the K and V rings
 
 bool prefill_tc_eligible(const kvp_pool* pool, int Hq, int C, float scale) {
   // the row maximum is taken on unscaled scores, which needs scale > 0
@@ -697,7 +750,7 @@ int launch_prefill_tc(const kvp_pool* pool, int layer, const void* q, int batch,
       return KVP_ERR_CUDA;
     attr = true;
   }
-  const long long grid = (long long)((a.tiles + 1) / 2) * batch * pool->kv_heads;
+  const long long grid = (long long)a.tiles * batch * pool->kv_heads;
   if (grid <= 0 || grid > 0x7fffffffLL) return KVP_ERR_INVALID_ARG;
   prefill_tc_kernel<<<(unsigned)grid, kPThreads, kPrefillSmem, stream>>>(a);
   return cudaGetLastError() == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
