@@ -270,8 +270,26 @@ __device__ __forceinline__ void tma_load_5d(void* dst, const void* tmap, int c0,
 //    of O += P V, one group per 16-key K step). A group is one copy.
 __device__ __forceinline__ void load_rows(const PrefillArgs& a, unsigned char* dst, const int* slots, unsigned tm,
                                           int g, bool is_v, uint64_t* bar, int lane) {
-  const size_t base = is_v ? a.kv_bytes : 0;
   const int kvl = is_v ? a.kvl_v : a.kvl_k;
+  if (tm == 0xFFu) {  // every group by TMA (the common case): one lane issues all copies
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar, 8u * kGroupBytes);
+      if (is_v) {
+#pragma unroll
+        for (int gi = 0; gi < 8; ++gi) tma_load_5d(dst + gi * kGroupBytes, &a.kvmap, 0, slots[16 * gi], 0, g, kvl, bar);
+      } else {
+#pragma unroll
+        for (int gi = 0; gi < 8; ++gi) {
+          const int s0 = slots[16 * gi];
+          tma_load_5d(dst + gi * (kGroupBytes / 2), &a.kmap, 0, s0, 0, g, kvl, bar);
+          tma_load_5d(dst + kHalf + gi * (kGroupBytes / 2), &a.kmap, 0, s0, 1, g, kvl, bar);
+        }
+      }
+    }
+    __syncwarp();
+    return;
+  }
+  const size_t base = is_v ? a.kv_bytes : 0;
   for (int gi = 0; gi < 8; ++gi) {
     if ((tm >> gi) & 1) continue;
     for (int x = lane; x < 16 * 16; x += 32) {
@@ -286,9 +304,8 @@ __device__ __forceinline__ void load_rows(const PrefillArgs& a, unsigned char* d
       *reinterpret_cast<uint4*>(dst + off) = val;
     }
   }
-  // the thread copies' writes are visible to the tensor cores' (async proxy)
-  // reads; a block copied by TMA alone has none to order
-  if (tm != 0xFFu) fence_proxy_async_smem();
+  // the thread copies' writes are visible to the tensor cores' (async proxy) reads
+  fence_proxy_async_smem();
   __syncwarp();
   if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)__popc(tm) * kGroupBytes);
   __syncwarp();
