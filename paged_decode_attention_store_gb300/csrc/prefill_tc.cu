@@ -236,6 +236,7 @@ struct PrefillBars {
   uint64_t p_full[2];     // softmax (16 warps) -> P V issuer: P of the block in P buffer b
   uint64_t pv_done[2];    // P V issuer (commit) -> softmax: O += P V of the block done, P buffer b free
   uint64_t drain;         // both issuers (commit) -> all: everything issued is done
+  uint64_t vtail;         // TMA -> V loader: the last block's partial group landed (used once)
   uint64_t xbar[4];       // the four softmax warps of a row quadrant: their partials are in xch
   uint32_t taddr;
   int abort;
@@ -258,36 +259,60 @@ __device__ __forceinline__ void tma_load_5d(void* dst, const void* tmap, int c0,
       : "memory");
 }
 
-// The loader warp fills one 128-key operand from ``slots``: 16-slot groups
-// flagged in ``tm`` by TMA copies, the others by plain 16-byte copies (zeros
-// for slots < 0); ``bar`` (count 1) gets the arrival and the TMA byte count.
-// Both layouts use the 128-byte swizzle with 8-row atoms of 1 KB.
-//  - K (``is_v`` false), half-major: half h of d at h * 16 KB, key row k at
-//    + k * 128 B, so the 128 keys of a half are 16 evenly spaced atoms (the
-//    N 128 B operand of S = Q K^T). A group is two copies (one per half).
-//  - V, group-major: group gi (keys 16 gi .. 16 gi + 15) at gi * 4 KB, its
-//    half h at + h * 2 KB, key row r at + r * 128 B (the MN-major B operand
-//    of O += P V, one group per 16-key K step). A group is one copy.
-__device__ __forceinline__ void load_rows(const PrefillArgs& a, unsigned char* dst, const int* slots, unsigned tm,
-                                          int g, bool is_v, uint64_t* bar, int lane) {
+// tx bytes for ``bar``'s current phase, without an arrival.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t tx) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(tx) : "memory");
+}
+
+// The paths of load_rows for a block with a partial or empty groups (the
+// last block of a CTA) or groups that are not 16-aligned in one page.
+__device__ __forceinline__ bool load_rows_slow(const PrefillArgs& a, unsigned char* dst, const int* slots, unsigned tm,
+                                            unsigned tp, int kp, unsigned te, int g, bool is_v, uint64_t* bar,
+                                            uint64_t* vtail, int lane, volatile int* abort_flag) {
   const int kvl = is_v ? a.kvl_v : a.kvl_k;
-  if (tm == 0xFFu) {  // every group by TMA (the common case): one lane issues all copies
+  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+  if ((tm | tp | te) == 0xFFu && !is_v) {  // K with a partial or empty groups: TMA alone
     if (lane == 0) {
-      mbar_arrive_expect_tx(bar, 8u * kGroupBytes);
-      if (is_v) {
-#pragma unroll
-        for (int gi = 0; gi < 8; ++gi) tma_load_5d(dst + gi * kGroupBytes, &a.kvmap, 0, slots[16 * gi], 0, g, kvl, bar);
-      } else {
-#pragma unroll
-        for (int gi = 0; gi < 8; ++gi) {
-          const int s0 = slots[16 * gi];
-          tma_load_5d(dst + gi * (kGroupBytes / 2), &a.kmap, 0, s0, 0, g, kvl, bar);
-          tma_load_5d(dst + kHalf + gi * (kGroupBytes / 2), &a.kmap, 0, s0, 1, g, kvl, bar);
-        }
+      const unsigned tt = tm | tp;
+      mbar_arrive_expect_tx(bar, (uint32_t)__popc(tt) * kGroupBytes);
+      for (int gi = 0; gi < 8; ++gi) {
+        if (!((tt >> gi) & 1)) continue;
+        const int s0 = slots[16 * gi];
+        tma_load_5d(dst + gi * (kGroupBytes / 2), &a.kmap, 0, s0, 0, g, kvl, bar);
+        tma_load_5d(dst + kHalf + gi * (kGroupBytes / 2), &a.kmap, 0, s0, 1, g, kvl, bar);
       }
     }
     __syncwarp();
-    return;
+    return true;
+  }
+  if ((tm | tp | te) == 0xFFu) {  // V with a partial or empty groups
+    const int gp = tp ? __ffs(tp) - 1 : -1;
+    if (lane == 0) {
+      if (gp >= 0) {
+        mbar_arrive_expect_tx(vtail, kGroupBytes);
+        tma_load_5d(dst + gp * kGroupBytes, &a.kvmap, 0, slots[16 * gp], 0, g, kvl, vtail);
+      }
+      mbar_expect_tx(bar, (uint32_t)__popc(tm) * kGroupBytes);
+#pragma unroll
+      for (int gi = 0; gi < 8; ++gi)
+        if ((tm >> gi) & 1) tma_load_5d(dst + gi * kGroupBytes, &a.kvmap, 0, slots[16 * gi], 0, g, kvl, bar);
+    }
+    for (int gi = 0; gi < 8; ++gi)
+      if ((te >> gi) & 1)
+        for (int x = lane; x < kGroupBytes / 16; x += 32) reinterpret_cast<uint4*>(dst + gi * kGroupBytes)[x] = z;
+    if (gp >= 0) {
+      if (!__all_sync(0xffffffffu, pwait(vtail, 0, abort_flag, a.err))) return false;
+      // rows kp .. 15 of both halves: 16 B chunk c of row r at h * 2 KB + r * 128 B
+      for (int x = kp * 16 + lane; x < 16 * 16; x += 32) {
+        const int r = x >> 4, c = x & 15;
+        *reinterpret_cast<uint4*>(dst + gp * kGroupBytes + (c >> 3) * (kGroupBytes / 2) + r * 128 + (c & 7) * 16) = z;
+      }
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar);
+    __syncwarp();
+    return true;
   }
   const size_t base = is_v ? a.kv_bytes : 0;
   for (int gi = 0; gi < 8; ++gi) {
@@ -295,7 +320,7 @@ __device__ __forceinline__ void load_rows(const PrefillArgs& a, unsigned char* d
     for (int x = lane; x < 16 * 16; x += 32) {
       const int key = 16 * gi + x / 16, c = x % 16;
       const int sl = slots[key];
-      uint4 val = make_uint4(0u, 0u, 0u, 0u);
+      uint4 val = z;
       if (sl >= 0)
         val = __ldg(reinterpret_cast<const uint4*>(a.kv_layer + base + (size_t)sl * a.row_bytes +
                                                    (size_t)g * kPD * 2) + c);
@@ -317,7 +342,54 @@ __device__ __forceinline__ void load_rows(const PrefillArgs& a, unsigned char* d
     tma_load_5d(dst + h * kHalf + gi * (kGroupBytes / 2), &a.kmap, 0, slots[16 * gi], h, g, kvl, bar);
   }
   __syncwarp();
+  return true;
 }
+
+// The loader warp fills one 128-key operand; ``bar`` (count 1) gets the
+// arrival and the TMA byte count. Both layouts use the 128-byte swizzle with
+// 8-row atoms of 1 KB.
+//  - K (``is_v`` false), half-major: half h of d at h * 16 KB, key row k at
+//    + k * 128 B, so the 128 keys of a half are 16 evenly spaced atoms (the
+//    N 128 B operand of S = Q K^T). A group is two copies (one per half).
+//  - V, group-major: group gi (keys 16 gi .. 16 gi + 15) at gi * 4 KB, its
+//    half h at + h * 2 KB, key row r at + r * 128 B (the MN-major B operand
+//    of O += P V, one group per 16-key K step). A group is one copy.
+// Groups in ``tm`` go by TMA from the 16 slots starting at slots[16 gi]. When
+// the other groups are all in ``tp`` (the block's last group with keys, whose
+// first ``kp`` keys are in the span and whose 16 slots lie in one page) or
+// ``te`` (no key in the span), they are handled without thread copies: K's
+// partial group goes by TMA whole and its empty groups stay as they are (the
+// scores of keys past the span are masked); V's empty groups are zeroed, and
+// its partial group goes by TMA on ``vtail`` and has its rows from kp on
+// zeroed once it has landed (P is 0 there, and 0 times what the page holds
+// past the span must stay 0). Otherwise the groups outside ``tm`` are copied
+// by the threads from ``slots`` (zeros for slots < 0). Returns false when a
+// wait gave up.
+__device__ __forceinline__ bool load_rows(const PrefillArgs& a, unsigned char* dst, const int* slots, unsigned tm,
+                                          unsigned tp, int kp, unsigned te, int g, bool is_v, uint64_t* bar,
+                                          uint64_t* vtail, int lane, volatile int* abort_flag) {
+  const int kvl = is_v ? a.kvl_v : a.kvl_k;
+  if (tm == 0xFFu) {  // every group full, by TMA (the common case): one lane issues all copies
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar, 8u * kGroupBytes);
+      if (is_v) {
+#pragma unroll
+        for (int gi = 0; gi < 8; ++gi) tma_load_5d(dst + gi * kGroupBytes, &a.kvmap, 0, slots[16 * gi], 0, g, kvl, bar);
+      } else {
+#pragma unroll
+        for (int gi = 0; gi < 8; ++gi) {
+          const int s0 = slots[16 * gi];
+          tma_load_5d(dst + gi * (kGroupBytes / 2), &a.kmap, 0, s0, 0, g, kvl, bar);
+          tma_load_5d(dst + kHalf + gi * (kGroupBytes / 2), &a.kmap, 0, s0, 1, g, kvl, bar);
+        }
+      }
+    }
+    __syncwarp();
+    return true;
+  }
+  return load_rows_slow(a, dst, slots, tm, tp, kp, te, g, is_v, bar, vtail, lane, abort_flag);
+}
+
 
 // Warp roles: 0 and 1 load K blocks (even, odd) into a three-stage ring, 0
 // loads Q first; 2 and 3 load V blocks into a two-stage ring; 4 issues the
@@ -385,6 +457,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_c
     }
     for (int qd = 0; qd < 4; ++qd) mbar_init(&sb.xbar[qd], kParts);
     mbar_init(&sb.drain, 2);
+    mbar_init(&sb.vtail, 1);
     sb.abort = 0;
     fence_mbar_init();
   }
@@ -423,20 +496,36 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_c
     for (int i = par; i < nblk; i += 2) {
       const int st = i % NS;
       const int o0 = i * kPN;
-      unsigned tm = 0;
-      bool whole = false;  // every group of the block resolved by its one read
+      unsigned tm = 0, tp = 0, te = 0;
+      int kp = 0;
+      bool whole = false;  // every group of the block full, partial or empty by its one read
       if (group_reads) {
+        // lane gi < 8: group gi is full (its 16 keys in the span, in one
+        // segment, 16-aligned positions), partial (the span ends inside it,
+        // in the window segment, aligned) or empty (past the span)
         const int og = o0 + 16 * lane;
         int s0 = -1;
-        if (lane < 8 && og + 15 < n_keys && (og + 15 < u.se || og >= u.se)) {
-          const int p = span_pos(u, og);
-          if ((p & 15) == 0) s0 = resolve_slot(a.T, row, p, a.err);
+        bool empty = false;
+        if (lane < 8) {
+          if (og >= n_keys) {
+            empty = true;
+          } else if (og >= u.se || og + 15 < u.se) {
+            const int p = span_pos(u, og);
+            if ((p & 15) == 0) s0 = resolve_slot(a.T, row, p, a.err);
+          }
         }
-        const unsigned okb = __ballot_sync(0xffffffffu, s0 >= 0);
-        whole = (okb & 0xFFu) == 0xFFu;
+        const unsigned full = __ballot_sync(0xffffffffu, s0 >= 0 && og + 15 < n_keys) & 0xFFu;
+        tp = __ballot_sync(0xffffffffu, s0 >= 0 && og + 15 >= n_keys) & 0xFFu;
+        te = __ballot_sync(0xffffffffu, empty) & 0xFFu;
+        whole = (full | tp | te) == 0xFFu;
         __syncwarp();  // this warp's previous copies have read the slot list
-        if (whole && lane < 8) slots[16 * lane] = s0;
-        tm = whole ? 0xFFu : 0u;
+        if (whole && lane < 8 && s0 >= 0) slots[16 * lane] = s0;
+        if (whole) {
+          tm = full;
+          kp = tp ? n_keys - (o0 + 16 * (__ffs(tp) - 1)) : 0;
+        } else {
+          tp = te = 0;
+        }
       }
       if (!whole) {
         // lane l resolves keys 4l .. 4l+3 (four independent table reads);
@@ -463,8 +552,9 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_c
       if (i >= NS && !__all_sync(0xffffffffu, pwait(is_v ? &sb.v_empty[st] : &sb.k_empty[st], (i - NS) / NS,
                                                     abort_flag, a.err)))
         break;
-      load_rows(a, (is_v ? sV : sK) + st * 2 * kHalf, slots, tm, g, is_v, is_v ? &sb.v_full[st] : &sb.k_full[st],
-                lane);
+      if (!load_rows(a, (is_v ? sV : sK) + st * 2 * kHalf, slots, tm, tp, kp, te, g, is_v,
+                     is_v ? &sb.v_full[st] : &sb.k_full[st], &sb.vtail, lane, abort_flag))
+        break;
     }
   } else if (warp == kSWarp) {
     // ======================= S issuer ==========================================
