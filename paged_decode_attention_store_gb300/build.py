@@ -3,6 +3,9 @@
 Objects go to ``_build/`` next to this file; the library to
 ``libpagedkv.so`` next to this file. Translation units compile in parallel
 and only when a source or header is newer than the library.
+``build_traced()`` builds the tracing variant of the prefill kernel
+(``-DKVP_PREFILL_TRACE``) as ``libpagedkv_trace.so`` from objects in
+``_build/trace/``; it is a measuring tool, never the product.
 """
 
 from __future__ import annotations
@@ -20,6 +23,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpagedkv.so")
+TRACE_LIB = os.path.join(HERE, "libpagedkv_trace.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -39,10 +43,10 @@ def _deps():
     return _sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h")) + [__file__]
 
 
-def needs_build() -> bool:
-    if not os.path.exists(LIB):
+def needs_build(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(p) > t for p in _deps())
 
 
@@ -53,18 +57,20 @@ def _run(cmd):
     return r.stdout + r.stderr
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile every translation unit and link libpagedkv.so; returns its path."""
-    if not force and not needs_build():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, lib: str = LIB, objdir: str = BUILD,
+          defines: tuple = ()) -> str:
+    """Compile every translation unit and link ``lib`` (libpagedkv.so by
+    default); returns its path."""
+    if not force and not needs_build(lib):
+        return lib
+    os.makedirs(objdir, exist_ok=True)
     nvcc = _nvcc()
     jobs = []
     for src in _sources():
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        obj = os.path.join(objdir, os.path.basename(src) + ".o")
         if src.endswith(".cu"):
             cmd = [nvcc, *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE,
-                   "-Xptxas", "-v", "-c", src, "-o", obj]
+                   *[f"-D{d}" for d in defines], "-Xptxas", "-v", "-c", src, "-o", obj]
         else:
             cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-Wall", "-I", INCLUDE, "-c", src, "-o", obj]
         jobs.append((cmd, obj))
@@ -73,10 +79,15 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if verbose:
         for log in logs:
             sys.stdout.write(log)
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     _run([nvcc, *ARCH, "-shared", "-Xcompiler", "-fPIC", *[o for _, o in jobs], "-o", tmp])
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
+
+
+def build_traced(force: bool = False) -> str:
+    """The tracing variant of the library (the prefill kernel's stamps on)."""
+    return build(force=force, lib=TRACE_LIB, objdir=os.path.join(BUILD, "trace"), defines=("KVP_PREFILL_TRACE",))
 
 
 if __name__ == "__main__":

@@ -264,6 +264,43 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t tx) {
   asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(tx) : "memory");
 }
 
+// Tracing build (-DKVP_PREFILL_TRACE; paged_decode_attention_store_gb300.
+// trace_prefill builds it beside the library): every CTA records its entry
+// and exit times, SM and key blocks, and one armed CTA the global-timer time
+// of each pipeline event of its first kTraceBlocks blocks. The product build
+// compiles none of it.
+enum PrefillTraceEvent {
+  kTrKResolved,  // K loader: the block's slots resolved (before its stage wait)
+  kTrKIssued,    // K loader: the block's copies issued
+  kTrVResolved,
+  kTrVIssued,
+  kTrSFull,      // S issuer: K(i) landed
+  kTrSIssued,    // S issuer: S(i) issued and committed
+  kTrPvV,        // P V issuer: V(i) landed
+  kTrPvP,        // P V issuer: P(i) written
+  kTrPvIssued,   // P V issuer: P V(i) issued and committed
+  kTrSmS,        // softmax (first warp, lane 0): S(i) in TMEM
+  kTrSmMax,      // softmax: the row maximum agreed
+  kTrSmP,        // softmax: P(i) computed (before waiting for its P buffer)
+  kTrSmArrive,   // softmax: P(i) written and handed to the P V issuer
+  kTrEvents
+};
+#ifdef KVP_PREFILL_TRACE
+constexpr int kTraceBlocks = 128;
+constexpr int kTraceCtas = 4096;
+__device__ unsigned long long g_ptrace_ev[kTrEvents][kTraceBlocks];
+__device__ unsigned long long g_ptrace_cta[kTraceCtas][4];  // entry, SM, exit, blocks
+__device__ int g_ptrace_target = -1;
+#define PTRACE(e, i)                                                                \
+  do {                                                                              \
+    if (traced && (i) < kTraceBlocks) g_ptrace_ev[e][i] = global_timer_ns();        \
+  } while (0)
+#else
+#define PTRACE(e, i) \
+  do {               \
+  } while (0)
+#endif
+
 // The paths of load_rows for a block with a partial or empty groups (the
 // last block of a CTA) or groups that are not 16-aligned in one page.
 __device__ __forceinline__ bool load_rows_slow(const PrefillArgs& a, unsigned char* dst, const int* slots, unsigned tm,
@@ -405,6 +442,10 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_c
   unsigned char* sV = sK + kKS * 2 * kHalf;  // V stage s at s * 2 kHalf
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   volatile int* abort_flag = &sb.abort;
+#ifdef KVP_PREFILL_TRACE
+  const unsigned long long t_entry = global_timer_ns();
+  const bool traced = (int)blockIdx.x == g_ptrace_target;
+#endif
 
   // CTA order: request and KV head major, the tile with the most keys first,
   // so that the tiles reading the same K/V run side by side (L2 serves all
@@ -438,6 +479,15 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_c
   const Span u = attend_span(p_last + 1, a.window > 0 ? a.window + (p_last - p_first) : 0, a.sinks);
   const int n_keys = u.se + (p_last + 1 - u.lo);
   const int nblk = (n_keys + kPN - 1) / kPN;
+#ifdef KVP_PREFILL_TRACE
+  if (tid == 0 && blockIdx.x < kTraceCtas) {
+    unsigned smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    g_ptrace_cta[blockIdx.x][0] = t_entry;
+    g_ptrace_cta[blockIdx.x][1] = smid;
+    g_ptrace_cta[blockIdx.x][3] = (unsigned long long)nblk;
+  }
+#endif
 
   if (tid == 0) {
     mbar_init(&sb.q_full, 1);
@@ -549,12 +599,14 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_c
           if (((okb >> (4 * gi)) & 0xFu) == 0xFu) tm |= 1u << gi;
       }
       __syncwarp();
+      if (lane == 0) PTRACE(is_v ? kTrVResolved : kTrKResolved, i);
       if (i >= NS && !__all_sync(0xffffffffu, pwait(is_v ? &sb.v_empty[st] : &sb.k_empty[st], (i - NS) / NS,
                                                     abort_flag, a.err)))
         break;
       if (!load_rows(a, (is_v ? sV : sK) + st * 2 * kHalf, slots, tm, tp, kp, te, g, is_v,
                      is_v ? &sb.v_full[st] : &sb.k_full[st], &sb.vtail, lane, abort_flag))
         break;
+      if (lane == 0) PTRACE(is_v ? kTrVIssued : kTrKIssued, i);
     }
   } else if (warp == kSWarp) {
     // ======================= S issuer ==========================================
@@ -570,6 +622,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_c
     for (int i = 0; ok && i < nblk; ++i) {
       const int ks = i % kKS, sbuf = i & 1;
       ok = __all_sync(0xffffffffu, pwait(&sb.k_full[ks], i / kKS, abort_flag, a.err));
+      if (lane == 0) PTRACE(kTrSFull, i);
       if (ok && i >= 2) ok = __all_sync(0xffffffffu, pwait(&sb.s_free[sbuf], (i - 2) >> 1, abort_flag, a.err));
       if (!ok) break;
       tc_fence_after();
@@ -582,6 +635,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_c
         }
         umma_commit(&sb.s_full[sbuf]);
         umma_commit(&sb.k_empty[ks]);
+        PTRACE(kTrSIssued, i);
       }
       __syncwarp();
     }
@@ -598,7 +652,9 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_c
     for (int i = 0; ok && i < nblk; ++i) {
       const int vs = i % kVS, pbuf = i & 1;
       ok = __all_sync(0xffffffffu, pwait(&sb.v_full[vs], i / kVS, abort_flag, a.err));
+      if (lane == 0) PTRACE(kTrPvV, i);
       if (ok) ok = __all_sync(0xffffffffu, pwait(&sb.p_full[pbuf], i >> 1, abort_flag, a.err));
+      if (lane == 0) PTRACE(kTrPvP, i);
       if (!ok) break;
       tc_fence_after();
       const uint64_t dv = dv0 + (uint64_t)((vs * 2 * kHalf) >> 4);
@@ -610,6 +666,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_c
                       (i > 0 || m > 0) ? 1u : 0u);
         umma_commit(&sb.pv_done[pbuf]);
         umma_commit(&sb.v_empty[vs]);
+        PTRACE(kTrPvIssued, i);
       }
       __syncwarp();
     }
@@ -655,6 +712,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_c
       const int sbuf = i & 1;
       ok = __all_sync(0xffffffffu, pwait(&sb.s_full[sbuf], i >> 1, abort_flag, a.err));
       if (!ok) break;
+      if (lane == 0 && warp == kSoftWarp0) PTRACE(kTrSmS, i);
       tc_fence_after();
       // the part's 32 scores, read from TMEM once; then S buffer sbuf is free
       float sv[32];
@@ -682,6 +740,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_c
                       fmaxf(sv[8 * t + 6], sv[8 * t + 7]));
       float rmax;
       if (!(ok = exchange(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2, i, true, rmax))) break;
+      if (lane == 0 && warp == kSoftWarp0) PTRACE(kTrSmMax, i);
       const bool grow = rmax > m_used + 8.f;  // also when nothing was kept before
       const bool scale_o = grow && m_used > -INFINITY;  // O and lsum hold kept keys
       const float f = scale_o ? exp2f(m_used - rmax) : 1.f;
@@ -699,6 +758,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_c
         w[x] = pack_bf16(p0, p1);
         add2(ps0, ps1, p0, p1);
       }
+      if (lane == 0 && warp == kSoftWarp0) PTRACE(kTrSmP, i);
       if (i >= 2) {
         ok = __all_sync(0xffffffffu, pwait(&sb.pv_done[sbuf], (i - 2) >> 1, abort_flag, a.err));
         if (!ok) break;
@@ -722,6 +782,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_c
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sb.p_full[sbuf]);
+      if (lane == 0 && warp == kSoftWarp0) PTRACE(kTrSmArrive, i);
     }
     // ---- epilogue: O / l -> bf16 (this part's 32 columns), once the last P V is in O
     float tot = 0.f;
@@ -757,6 +818,9 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_tc_kernel(const __grid_c
   tc_fence_before();
   __syncthreads();
   if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tbase) : "memory");
+#ifdef KVP_PREFILL_TRACE
+  if (tid == 0 && blockIdx.x < kTraceCtas) g_ptrace_cta[blockIdx.x][2] = global_timer_ns();
+#endif
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
@@ -803,6 +867,27 @@ bool encode_qmap(const void* q, int B, int C, int Hq, int G, CUtensorMap* out) {
 }
 
 }  // namespace
+
+#ifdef KVP_PREFILL_TRACE
+// Tracing build only: arm CTA ``cta`` for the per-block events (-1: none).
+extern "C" int kvp_prefill_trace_arm(int cta) {
+  return cudaMemcpyToSymbol(g_ptrace_target, &cta, sizeof(int)) == cudaSuccess ? KVP_OK : KVP_ERR_CUDA;
+}
+
+// Tracing build only: copy the records out. ``events`` gets kTrEvents x
+// kTraceBlocks global-timer times (ns) of the armed CTA, ``ctas`` kTraceCtas x 4
+// (entry ns, SM, exit ns, key blocks) of every CTA; ``dims`` gets kTrEvents,
+// kTraceBlocks and kTraceCtas. Synchronous.
+extern "C" int kvp_prefill_trace_read(unsigned long long* events, unsigned long long* ctas, int32_t* dims) {
+  if (!events || !ctas || !dims) return KVP_ERR_INVALID_ARG;
+  dims[0] = kTrEvents;
+  dims[1] = kTraceBlocks;
+  dims[2] = kTraceCtas;
+  if (cudaMemcpyFromSymbol(events, g_ptrace_ev, sizeof(g_ptrace_ev)) != cudaSuccess) return KVP_ERR_CUDA;
+  if (cudaMemcpyFromSymbol(ctas, g_ptrace_cta, sizeof(g_ptrace_cta)) != cudaSuccess) return KVP_ERR_CUDA;
+  return KVP_OK;
+}
+#endif
 
 constexpr size_t kPrefillSmem = (2 + 2 * kKS + 2 * kVS) * kHalf + 1024;  // Q, the K and V rings
 
