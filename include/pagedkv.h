@@ -215,7 +215,9 @@ int paged_verify_attention(const kvp_pool* pool, int layer, const void* q,
  * 128 % (num_q_heads / kv_heads) == 0 and scale > 0 run on the tcgen05
  * tensor cores (TMEM accumulators), others on the general kernel. The
  * tcgen05 kernel keeps the pool's tensor map (built on first use) in the
- * pool descriptor; ``q`` is mapped per call.
+ * pool descriptor; ``q`` is mapped per call. It may read the rows of a
+ * request's last page past the attended span (they lie in the same page of
+ * the pool); whatever they hold never reaches the output.
  *   q    device [batch, chunk, num_q_heads, head_dim], pool dtype,
  *        16-byte aligned.
  *   out  device, the same shape; rows j >= q_lens[b] are not written.

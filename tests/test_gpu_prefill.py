@@ -43,6 +43,8 @@ CASES = [
     ("bf16", 32, 8, 128, 16, "raw", 200, [500, 33], [200, 150], 0, 0),                    # raw table, page 16 (TMA)
     ("bf16", 32, 8, 128, 16, "block", 300, [1000, 0], [300, 300], 128, 0),                # window, no sinks
     ("bf16", 16, 8, 128, 16, "block", 96, [70, 0], [96, 5], 0, 0),                        # GQA 2: 64 tokens per tile
+    ("bf16", 32, 8, 128, 32, "block", 200, [300, 45], [200, 190], 0, 0),                  # page 32: two groups a page
+    ("bf16", 32, 8, 128, 64, "block", 160, [1000, 7], [160, 160], 256, 16),               # page 64, a whole sink group
 ]
 
 
