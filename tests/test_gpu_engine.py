@@ -87,11 +87,14 @@ def test_decode_step_matches_the_oracle(kb, window, host_io, sinks):
 
 
 @pytest.mark.parametrize("window,sinks,host_io,mode", [(0, 0, True, "block"), (40, 2, True, "block"),
-                                                        (0, 0, False, "raw"), (40, 0, False, "block")])
+                                                        (0, 0, False, "raw"), (40, 0, False, "block"),
+                                                        (0, 0, "reuse", "block"), (40, 2, "reuse", "raw")])
 def test_device_bookkeeping_decode_step_matches_the_oracle(kb, window, sinks, host_io, mode):
     """DevicePagedKVCache: pages chosen on the device each step (one native
     call with host or device buffers); outputs, slots, tables and the device
-    free list against the oracle."""
+    free list against the oracle. With ``reuse`` the steps alternate between
+    two fixed sets of pinned buffers, refilled each step, as a caller reuses
+    its staging buffers."""
     from paged_decode_attention_store_gb300.engine import DevicePagedKVCache
 
     Hq, Hkv, D, P, seed = 32, 8, 128, 16, 73
@@ -119,10 +122,17 @@ def test_device_bookkeeping_decode_step_matches_the_oracle(kb, window, sinks, ho
             orc.trim(b, max(0, lengths[b] + 1 - (window - sinks)), sinks=sinks)
     rids = torch.arange(B, dtype=torch.int32, device=DEV)
     lens = list(lengths)
+    sets = [[torch.empty(shape, dtype=torch.bfloat16, pin_memory=True) for shape in
+             ((B, Hq, D), (B, Hkv, D), (B, Hkv, D), (B, Hq, D))] for _ in range(2)]
     for step in range(1, steps + 1):
         q = wl.q_rows(seed, step, 0, list(range(B)), Hq, D, device=DEV)
         k, v = wl.kv_rows(seed, 0, list(range(B)), lens, Hkv, D, device=DEV)
-        if host_io:
+        if host_io == "reuse":
+            qh, kh, vh, out = sets[step % 2]
+            for dst, src in ((qh, q), (kh, k), (vh, v)):
+                dst.copy_(src)
+            cache.decode_step_host(rids, [qh], [kh], [vh], [out], window, w.scale, sinks=sinks)
+        elif host_io:
             qh, kh, vh = (x.cpu().pin_memory() for x in (q, k, v))
             out = torch.empty((B, Hq, D), dtype=torch.bfloat16, pin_memory=True)
             cache.decode_step_host(rids, [qh], [kh], [vh], [out], window, w.scale, sinks=sinks)
