@@ -71,3 +71,20 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(kb, "LIB_PATH", str(tmp_path / "nope.so"))
     with pytest.raises(RuntimeError):
         kb.lib()
+
+
+def test_tracing_accessors_live_only_in_the_tracing_build():
+    """The prefill kernel's tracing build (KVP_PREFILL_TRACE) exports its two
+    accessors; the product library exports neither, and neither library is
+    the other."""
+    kb = ensure_built()
+    from paged_decode_attention_store_gb300 import build as kbuild
+
+    traced = kbuild.build_traced()
+    assert os.path.abspath(traced) != os.path.abspath(kb.LIB_PATH)
+    t = ctypes.CDLL(traced)
+    for name in ("kvp_prefill_trace_arm", "kvp_prefill_trace_read"):
+        assert hasattr(t, name), f"the tracing build lacks {name}"
+        assert not hasattr(kb.lib(), name), f"the product library exports {name}"
+    for name in declared_functions():  # the tracing build is the whole library besides
+        assert hasattr(t, name), f"the tracing build lacks {name}"
