@@ -68,8 +68,8 @@ class PagedKVCache:
     def _to_device(self, flat):
         # A fresh pinned block per call: torch's caching host allocator does
         # not hand it out again before the asynchronous copy has completed.
-        host = torch.tensor(flat, dtype=torch.int32).pin_memory()
-        self.h2d_bytes += 4 * len(flat)
+        host = torch.from_numpy(np.ascontiguousarray(flat, dtype=np.int32)).pin_memory()
+        self.h2d_bytes += 4 * host.numel()
         return host.to(self.dev, non_blocking=True)
 
     def _write_table(self, writes):
@@ -106,18 +106,14 @@ class PagedKVCache:
 
         Also leaves the counts of this call's table writes and copies in
         ``last_writes`` / ``last_copies``."""
-        slots, writes, cows = self.host.append(rids)
-        np.add.at(self.lengths, np.asarray(rids, np.int64), 1)
-        self.last_writes, self.last_copies = len(writes), len(cows)
-        n, nw, nc = len(slots), len(writes), len(cows)
-        flat = list(slots)
-        if nw:
-            r, c, v = zip(*writes)
-            flat += list(r) + list(c) + list(v)
-        if nc:
-            s, d = zip(*cows)
-            flat += list(s) + list(d)
-        dev = self._to_device(flat)
+        r = np.ascontiguousarray(rids, dtype=np.int32)
+        n = int(r.shape[0])
+        buf = np.empty(6 * max(n, 1), np.int32)  # slots, table writes (rows, cols, values), copy pairs
+        slots, tw, cow = buf[:n], buf[n:4 * n].reshape(3, n), buf[4 * n:6 * n].reshape(2, n)
+        nw, nc = self.host.append_into(r, slots, tw, cow)
+        self.lengths += np.bincount(r, minlength=self.lengths.shape[0])
+        self.last_writes, self.last_copies = nw, nc
+        dev = self._to_device(np.concatenate((slots, tw[:, :nw].ravel(), cow[:, :nc].ravel())))
         if nw:
             kb.page_table_write(self.table, dev[n:n + nw], dev[n + nw:n + 2 * nw], dev[n + 2 * nw:n + 3 * nw],
                                 expand=self.P if self.raw else 1, error_word=self.pool.error_word)
@@ -196,11 +192,11 @@ class PagedKVCache:
 
     def _multi_step(self, kind, rids, q, k, v, out, window, scale, sinks):
         B, M = q[0].shape[0], q[0].shape[1]
-        rr = [int(r) for r in rids for _ in range(M)]
-        ctx = [int(self.lengths[r]) + M for r in rids]
-        out_loc = self.append(rr)
+        r = np.ascontiguousarray(rids, dtype=np.int32)
+        ctx = self.lengths[r] + M
+        out_loc = self.append(np.repeat(r, M))
         lens = self._to_device(ctx)
-        rows = self._to_device([int(r) for r in rids])
+        rows = self._to_device(r)
         host_out = not out[0].is_cuda
         for layer in range(self.layers):
             qd, kd, vd = (x[layer].to(self.dev, non_blocking=True) for x in (q, k, v))

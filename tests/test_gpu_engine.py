@@ -224,3 +224,58 @@ def test_device_verify_step_matches_the_oracle(kb, M, mode):
         row = orc.table_row(b)
         assert tab[b, :len(row)].tolist() == row
     cache.check()
+
+
+@pytest.mark.parametrize("window,sinks", [(0, 0), (100, 4)])
+def test_prefill_step_matches_the_oracle(kb, window, sinks):
+    """PagedKVCache.prefill_step (the per-step driver of chunked prefill, host
+    bookkeeping) with pinned host buffers: each request's chunk is appended,
+    stored and attended at once; every query's output against the oracle
+    (query j of a chunk attends what a one-token step with context
+    prefix + j + 1 attends), slots and table rows bit-exact. Two chunks, so
+    the second attends the first."""
+    import oracle.attention as OA
+    from paged_decode_attention_store_gb300.engine import PagedKVCache
+
+    Hq, Hkv, D, P, seed, C = 32, 8, 128, 16, 83, 48
+    prefixes = [100, 0, 37]
+    B, chunks = len(prefixes), 2
+    num_pages = sum(-(-(L + chunks * C) // P) for L in prefixes) + 8
+    order = wl.free_stack_for_order(wl.permutation(seed, num_pages))
+    w = wl.Workload("prefillstep", "bf16", Hq, Hkv, D, P, 1, num_pages, order, prefixes, window=window, sinks=sinks,
+                    scale=1.0 / math.sqrt(D))
+    cache = PagedKVCache(num_pages, P, Hkv, D, 1, "bf16", max_requests=B, max_seq_len=512, free_stack=order,
+                         device=DEV)
+    orc = OracleSession(w, B, seed=seed)
+    for b in range(B):
+        cache.new(b)
+        orc.new(b)
+        if prefixes[b]:
+            slots = cache.append([b] * prefixes[b])
+            k, v = wl.kv_rows(seed, 0, b, list(range(prefixes[b])), Hkv, D, device=DEV)
+            cache.store(0, k, v, slots)
+            assert slots.cpu().tolist() == orc.append([b] * prefixes[b], list(range(prefixes[b])))
+    lens = list(prefixes)
+    rids = np.arange(B, dtype=np.int32)
+    for step in range(1, chunks + 1):
+        rr = [b for b in range(B) for _ in range(C)]
+        pos = [L + j for L in lens for j in range(C)]
+        q = torch.stack([wl.q_rows(seed, step * C + j, 0, list(range(B)), Hq, D) for j in range(C)], dim=1)
+        k, v = wl.kv_rows(seed, 0, rr, pos, Hkv, D)
+        qh, kh, vh = (x.contiguous().pin_memory() for x in (q, k, v))
+        out = torch.empty((B, C, Hq, D), dtype=torch.bfloat16, pin_memory=True)
+        cache.prefill_step(rids, [qh], [kh], [vh], [out], window, w.scale, sinks=sinks)
+        assert orc.append(rr, pos) is not None
+        lens = [L + C for L in lens]
+        assert cache.lengths[:B].tolist() == lens
+        got = out.float().numpy()
+        for b in range(B):
+            for j, ps in enumerate(OA.verify_positions(lens[b], C, window if window > 0 else None, sinks)):
+                ref = OA.attend_request(orc.stores[0], q[b, j].float().numpy(),
+                                        [s for p in ps for s in orc.slots(b, p, p + 1)], w.scale)
+                close(got[b, j], ref, "bf16", f"chunk {step} request {b} query {j}")
+    tab = cache.table.cpu().numpy()
+    for b in range(B):
+        row = orc.table_row(b)
+        assert tab[b, :len(row)].tolist() == row
+    cache.check()
