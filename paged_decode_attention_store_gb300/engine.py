@@ -192,6 +192,26 @@ class PagedKVCache:
 
     def _multi_step(self, kind, rids, q, k, v, out, window, scale, sinks):
         B, M = q[0].shape[0], q[0].shape[1]
+        main = torch.cuda.current_stream(self.dev)
+        staged = None
+        if not q[0].is_cuda:
+            # host inputs: every layer's q/k/v go up on a side stream right away,
+            # while the host bookkeeping below runs; layer l's store waits for
+            # layer l's copies only
+            side = self._steps.get("multi_h2d")
+            if side is None:
+                side = self._steps["multi_h2d"] = torch.cuda.Stream(self.dev)
+            side.wait_stream(main)
+            staged = []
+            with torch.cuda.stream(side):
+                for layer in range(self.layers):
+                    xs = tuple(x[layer].to(self.dev, non_blocking=True) for x in (q, k, v))
+                    for t in xs:
+                        t.record_stream(main)
+                    ev = torch.cuda.Event()
+                    ev.record(side)
+                    staged.append((xs, ev))
+                    self.h2d_bytes += sum(x[layer].numel() * x[layer].element_size() for x in (q, k, v))
         r = np.ascontiguousarray(rids, dtype=np.int32)
         ctx = self.lengths[r] + M
         out_loc = self.append(np.repeat(r, M))
@@ -199,9 +219,11 @@ class PagedKVCache:
         rows = self._to_device(r)
         host_out = not out[0].is_cuda
         for layer in range(self.layers):
-            qd, kd, vd = (x[layer].to(self.dev, non_blocking=True) for x in (q, k, v))
-            if not q[0].is_cuda:
-                self.h2d_bytes += sum(x[layer].numel() * x[layer].element_size() for x in (q, k, v))
+            if staged is None:
+                qd, kd, vd = (x[layer] for x in (q, k, v))
+            else:
+                (qd, kd, vd), ev = staged[layer]
+                main.wait_event(ev)
             self.store(layer, kd, vd, out_loc)
             od = torch.empty_like(qd) if host_out else out[layer]
             if kind == "verify":
